@@ -1,0 +1,133 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module is shared by the CUDA path's tests/benchmark and by the CPU
+oracle's tests. It holds no attention arithmetic: it only draws numbers.
+
+Recipe (the pages measure on synthetic shapes only -- FlashAttention-4 paper,
+Section 5, Figs. 4-8 sweep sequence length and head dim):
+  * every tensor is drawn i.i.d. N(0, 1) in fp32 from ``torch.Generator('cpu')``
+    and rounded to bf16 (round-to-nearest-even); the same bf16 bits go to the
+    GPU and (widened exactly) to the oracle;
+  * a workload with seed ``s`` draws Q, K, V, dO from seeds ``10*s + 0..3``;
+  * the head-dim sweep multiplies K by 4 on a random 5% of sequence positions
+    (seed ``10*s + 4``; the same positions for every head of a batch entry) so
+    that the running row maximum jumps and conditional rescaling is exercised;
+  * the variable-length batch draws its sequence lengths uniformly from
+    ``[lo, hi]`` (seed ``10*s + 5``) and packs the sequences back to back.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem shape. ``lengths`` set => packed variable-length."""
+    name: str
+    B: int
+    H: int
+    L: int
+    d: int
+    causal: bool
+    seed: int
+    kspike_frac: float = 0.0          # fraction of positions whose K rows are scaled
+    kspike: float = 4.0
+    lengths: Optional[tuple] = None   # varlen: per-sequence lengths
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d), rounded to fp32 (the C ABI takes a 32-bit float)."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def varlen(self) -> bool:
+        return self.lengths is not None
+
+    @property
+    def total(self) -> int:
+        return sum(self.lengths) if self.varlen else self.B * self.L
+
+    def pairs(self) -> int:
+        """Number of unmasked (query, key) pairs summed over batch and heads."""
+        def per_seq(L):
+            return L * (L + 1) // 2 if self.causal else L * L
+        if self.varlen:
+            return self.H * sum(per_seq(L) for L in self.lengths)
+        return self.B * self.H * per_seq(self.L)
+
+    def fwd_flops(self) -> int:
+        """Algorithmic forward FLOPs: two GEMMs of 2*d FLOPs per unmasked pair."""
+        return 4 * self.d * self.pairs()
+
+    def bwd_flops(self) -> int:
+        """Algorithmic backward FLOPs: five GEMMs, i.e. 2.5x the forward."""
+        return 10 * self.d * self.pairs()
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    g = torch.Generator("cpu").manual_seed(10 * seed + 5)
+    return tuple(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g))
+
+
+def cu_seqlens(lengths) -> torch.Tensor:
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+# The five workloads. Names describe the shape.
+TINY = Workload("tiny_b1h2l128d64", B=1, H=2, L=128, d=64, causal=False, seed=1)
+MHA4K = Workload("b4h16l4096d128", B=4, H=16, L=4096, d=128, causal=True, seed=2)
+HDSWEEP = Workload("b2h16l8192", B=2, H=16, L=8192, d=128, causal=True, seed=3, kspike_frac=0.05)
+VARLEN = Workload("varlen32_h16d128", B=32, H=16, L=16384, d=128, causal=True, seed=4,
+                  lengths=varlen_lengths(32, 256, 16384, 4))
+LONG = Workload("b1h32l32768d128", B=1, H=32, L=32768, d=128, causal=True, seed=5)
+
+
+def _randn(shape, seed: int) -> torch.Tensor:
+    g = torch.Generator("cpu").manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float32)
+
+
+def make(w: Workload, with_grad: bool = True) -> dict:
+    """Draw q, k, v (and dO) for a workload as CPU bf16 tensors.
+
+    Dense layout ``[B, L, H, d]``; varlen ``[T, H, d]`` plus ``cu_seqlens``.
+    """
+    shape = (w.total, w.H, w.d) if w.varlen else (w.B, w.L, w.H, w.d)
+    q = _randn(shape, 10 * w.seed + 0)
+    k = _randn(shape, 10 * w.seed + 1)
+    v = _randn(shape, 10 * w.seed + 2)
+    if w.kspike_frac > 0:
+        g = torch.Generator("cpu").manual_seed(10 * w.seed + 4)
+        n = max(1, int(round(w.kspike_frac * w.L)))
+        if w.varlen:
+            raise ValueError("K spikes are defined for dense workloads only")
+        for b in range(w.B):
+            pos = torch.randperm(w.L, generator=g)[:n]
+            k[b, pos] *= w.kspike
+    out = {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+    if with_grad:
+        out["do"] = _randn(shape, 10 * w.seed + 3).to(torch.bfloat16)
+    if w.varlen:
+        out["cu_seqlens"] = cu_seqlens(w.lengths)
+    return out
+
+
+def small(B=1, H=2, L=128, d=64, causal=False, seed=1, Lk=None) -> dict:
+    """Small dense problem with possibly different query and key lengths."""
+    Lk = L if Lk is None else Lk
+    return {
+        "q": _randn((B, L, H, d), 10 * seed + 0).to(torch.bfloat16),
+        "k": _randn((B, Lk, H, d), 10 * seed + 1).to(torch.bfloat16),
+        "v": _randn((B, Lk, H, d), 10 * seed + 2).to(torch.bfloat16),
+        "do": _randn((B, L, H, d), 10 * seed + 3).to(torch.bfloat16),
+    }

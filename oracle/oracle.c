@@ -1,0 +1,356 @@
+/*
+ * fp64 CPU oracle for exact multi-head scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do. It shares no code, header, table or helper with the CUDA
+ * library, and it includes nothing from it.
+ *
+ * What it computes is the plain textbook definition (FlashAttention-4 paper,
+ * "Abstract" and Section 1: the method is *exact* attention; Section 2.1
+ * "Multi-head attention" is empty in the page, so the standard definition is
+ * used). Per batch b and head h, with s_ij = scale * <q_i, k_j>:
+ *
+ *     allowed(i, j) = j < Lk                       (non-causal)
+ *                   = j <= i + (Lk - Lq)           (causal, bottom-right aligned)
+ *     LSE_i = m_i + ln sum_j exp(s_ij - m_i),  m_i = max_j s_ij   (allowed j)
+ *     P_ij  = exp(s_ij - LSE_i)
+ *     O_i   = sum_j P_ij v_j
+ *
+ * Backward, for the scalar loss L = sum(O * dO) (FlashAttention-4 paper,
+ * Section 3.2.2: five products -- S recomputed, dP = dO V^T, dV = P^T dO,
+ * dQ = dS K, dK = dS^T Q):
+ *
+ *     dP_ij = <dO_i, v_j>,   D_i = <dO_i, O_i>,   dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij k_j
+ *     dK_j  = scale * sum_i dS_ij q_i
+ *     dV_j  = sum_i P_ij dO_i
+ *
+ * A row with no allowed key (only possible when causal and Lq > Lk) has
+ * O_i = 0, LSE_i = -inf, and contributes nothing to any gradient.
+ *
+ * Every output element is evaluated directly from its formula, with a single
+ * running accumulator per sum in index order; there is no blocking, tiling,
+ * online softmax or reordering. Threads only split the set of independent
+ * outputs (rows of O / dQ, rows of dK / dV) between them.
+ *
+ * Layouts (row-major, element counts):
+ *   dense  : q, o, dq  [B, Lq, H, d];  k, v, dk, dv [B, Lk, H, d];  lse [B, H, Lq]
+ *   varlen : cu_seqlens[B+1] (host, int32) packs B sequences; sequence b has
+ *            Lq_b = Lk_b = cu[b+1]-cu[b] rows; q,k,v,o,...  [T, H, d]; lse [H, T]
+ *            (T = cu[B]); Lq and Lk are then ignored.
+ *
+ * Row subsets: `rows` (nrows entries) lists query-row indices, relative to
+ * each sequence, whose O / LSE / dQ are wanted; `krows` lists key-row indices
+ * whose dK / dV are wanted. NULL means every row. Entries out of range for a
+ * sequence are skipped. Outputs outside the subset are left untouched.
+ *
+ * Return value: 0 on success, -1 on a bad argument, -2 on allocation failure.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdatomic.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *o, *lse, *dq, *dk, *dv;
+    int B, H, Lq, Lk, d, causal;
+    double scale;
+    const int *cu;          /* NULL for dense */
+    /* per (b, h, row) statistics used by the backward pass */
+    double *lse_all;        /* [B*H*Lq_max] or varlen [H*T] */
+    double *D_all;
+    /* work list */
+    const int *items;       /* (b, h, row) triples, flattened */
+    long n_items;
+    atomic_long next;
+    int phase;
+} job_t;
+
+/* ---- sequence geometry ------------------------------------------------- */
+
+static int seq_lq(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lq; }
+static int seq_lk(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lk; }
+
+/* element offset of row i of sequence b, head h, in a [.., L, H, d] tensor */
+static long row_off(const job_t *J, int b, int i, int h, int L) {
+    if (J->cu) return ((long)(J->cu[b] + i) * J->H + h) * J->d;
+    return (((long)b * L + i) * J->H + h) * J->d;
+}
+
+/* index of (b, h, i) into an lse-shaped array */
+static long stat_off(const job_t *J, int b, int h, int i) {
+    if (J->cu) return (long)h * J->cu[J->B] + J->cu[b] + i;
+    return ((long)b * J->H + h) * J->Lq + i;
+}
+
+static int allowed(const job_t *J, int b, int i, int j) {
+    int lq = seq_lq(J, b), lk = seq_lk(J, b);
+    if (j < 0 || j >= lk) return 0;
+    if (J->causal) return j <= i + (lk - lq);
+    return 1;
+}
+
+static double dot(const double *a, const double *b, int n) {
+    double s = 0.0;
+    for (int c = 0; c < n; c++) s += a[c] * b[c];
+    return s;
+}
+
+static double score(const job_t *J, int b, int h, int i, int j) {
+    const double *qi = J->q + row_off(J, b, i, h, J->Lq);
+    const double *kj = J->k + row_off(J, b, j, h, J->Lk);
+    return J->scale * dot(qi, kj, J->d);
+}
+
+/* LSE_i by the definition: max, then ln of the shifted sum of exponentials. */
+static double row_lse(const job_t *J, int b, int h, int i) {
+    int lk = seq_lk(J, b);
+    double m = -INFINITY;
+    for (int j = 0; j < lk; j++)
+        if (allowed(J, b, i, j)) {
+            double s = score(J, b, h, i, j);
+            if (s > m) m = s;
+        }
+    if (m == -INFINITY) return -INFINITY;
+    double sum = 0.0;
+    for (int j = 0; j < lk; j++)
+        if (allowed(J, b, i, j)) sum += exp(score(J, b, h, i, j) - m);
+    return m + log(sum);
+}
+
+/* O_i = sum_j exp(s_ij - LSE_i) v_j  (written into out[0..d)) */
+static void row_out(const job_t *J, int b, int h, int i, double lse, double *out) {
+    int d = J->d, lk = seq_lk(J, b);
+    for (int c = 0; c < d; c++) out[c] = 0.0;
+    if (lse == -INFINITY) return;
+    for (int j = 0; j < lk; j++) {
+        if (!allowed(J, b, i, j)) continue;
+        double p = exp(score(J, b, h, i, j) - lse);
+        const double *vj = J->v + row_off(J, b, j, h, J->Lk);
+        for (int c = 0; c < d; c++) out[c] += p * vj[c];
+    }
+}
+
+/* dS_ij = P_ij (<dO_i, v_j> - D_i) */
+static double dscore(const job_t *J, int b, int h, int i, int j) {
+    long st = stat_off(J, b, h, i);
+    double p = exp(score(J, b, h, i, j) - J->lse_all[st]);
+    const double *doi = J->dout + row_off(J, b, i, h, J->Lq);
+    const double *vj = J->v + row_off(J, b, j, h, J->Lk);
+    return p * (dot(doi, vj, J->d) - J->D_all[st]);
+}
+
+/* ---- work items -------------------------------------------------------- */
+/* items are (b, h, i) triples; the phase decides what is computed for them */
+
+enum { PH_FWD = 0, PH_STATS = 1, PH_DQ = 2, PH_DKV = 3 };
+
+static void do_item(job_t *J, int b, int h, int i) {
+    int d = J->d;
+    if (J->phase == PH_FWD) {
+        double lse = row_lse(J, b, h, i);
+        J->lse[stat_off(J, b, h, i)] = lse;
+        row_out(J, b, h, i, lse, J->o + row_off(J, b, i, h, J->Lq));
+    } else if (J->phase == PH_STATS) {
+        long st = stat_off(J, b, h, i);
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+        double lse = row_lse(J, b, h, i);
+        row_out(J, b, h, i, lse, tmp);
+        J->lse_all[st] = lse;
+        J->D_all[st] = dot(J->dout + row_off(J, b, i, h, J->Lq), tmp, d);
+        free(tmp);
+    } else if (J->phase == PH_DQ) {
+        double *dqi = J->dq + row_off(J, b, i, h, J->Lq);
+        int lk = seq_lk(J, b);
+        for (int c = 0; c < d; c++) dqi[c] = 0.0;
+        if (J->lse_all[stat_off(J, b, h, i)] == -INFINITY) return;
+        for (int j = 0; j < lk; j++) {
+            if (!allowed(J, b, i, j)) continue;
+            double ds = dscore(J, b, h, i, j);
+            const double *kj = J->k + row_off(J, b, j, h, J->Lk);
+            for (int c = 0; c < d; c++) dqi[c] += ds * kj[c];
+        }
+        for (int c = 0; c < d; c++) dqi[c] *= J->scale;
+    } else { /* PH_DKV: item row index is a key row j */
+        int j = i, lq = seq_lq(J, b);
+        double *dkj = J->dk + row_off(J, b, j, h, J->Lk);
+        double *dvj = J->dv + row_off(J, b, j, h, J->Lk);
+        for (int c = 0; c < d; c++) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        for (int r = 0; r < lq; r++) {
+            if (!allowed(J, b, r, j)) continue;
+            long st = stat_off(J, b, h, r);
+            double p = exp(score(J, b, h, r, j) - J->lse_all[st]);
+            const double *dor = J->dout + row_off(J, b, r, h, J->Lq);
+            const double *qr = J->q + row_off(J, b, r, h, J->Lq);
+            double ds = p * (dot(dor, J->v + row_off(J, b, j, h, J->Lk), d) - J->D_all[st]);
+            for (int c = 0; c < d; c++) {
+                dkj[c] += ds * qr[c];
+                dvj[c] += p * dor[c];
+            }
+        }
+        for (int c = 0; c < d; c++) dkj[c] *= J->scale;
+    }
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    for (;;) {
+        long t = atomic_fetch_add(&J->next, 1);
+        if (t >= J->n_items) break;
+        const int *it = J->items + 3 * t;
+        do_item(J, it[0], it[1], it[2]);
+    }
+    return NULL;
+}
+
+static void run_items(job_t *J, int phase, const int *items, long n, int nthreads) {
+    J->phase = phase;
+    J->items = items;
+    J->n_items = n;
+    atomic_store(&J->next, 0);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads == 1 || n < 2) { worker(J); return; }
+    pthread_t th[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; t++)
+        if (pthread_create(&th[t], NULL, worker, J) == 0) started++;
+        else break;
+    if (started == 0) worker(J);
+    for (int t = 0; t < started; t++) pthread_join(th[t], NULL);
+}
+
+/* Build the (b, h, i) list for a row subset; kind 0 = query rows, 1 = key rows. */
+static int *make_items(const job_t *J, const int *rows, int nrows, int kind, long *n_out) {
+    long cap = 0;
+    for (int b = 0; b < J->B; b++) {
+        int L = kind ? seq_lk(J, b) : seq_lq(J, b);
+        cap += (long)J->H * (rows ? nrows : L);
+    }
+    int *items = (int *)malloc(sizeof(int) * 3 * (size_t)(cap > 0 ? cap : 1));
+    if (!items) return NULL;
+    long n = 0;
+    for (int b = 0; b < J->B; b++) {
+        int L = kind ? seq_lk(J, b) : seq_lq(J, b);
+        int cnt = rows ? nrows : L;
+        for (int h = 0; h < J->H; h++)
+            for (int t = 0; t < cnt; t++) {
+                int i = rows ? rows[t] : t;
+                if (i < 0 || i >= L) continue;
+                items[3 * n] = b; items[3 * n + 1] = h; items[3 * n + 2] = i;
+                n++;
+            }
+    }
+    *n_out = n;
+    return items;
+}
+
+static int check_args(int B, int H, int Lq, int Lk, int d, const int *cu) {
+    if (B < 0 || H < 1 || d < 1) return -1;
+    if (!cu && (Lq < 0 || Lk < 0)) return -1;
+    if (cu) {
+        if (cu[0] != 0) return -1;
+        for (int b = 0; b < B; b++) if (cu[b + 1] < cu[b]) return -1;
+    }
+    return 0;
+}
+
+static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
+                     int B, int H, int Lq, int Lk, int d, double scale, int causal, const int *cu) {
+    memset(J, 0, sizeof(*J));
+    J->q = q; J->k = k; J->v = v; J->dout = dout;
+    J->B = B; J->H = H; J->Lq = Lq; J->Lk = Lk; J->d = d;
+    J->scale = scale; J->causal = causal != 0; J->cu = cu;
+}
+
+int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
+               int B, int H, int Lq, int Lk, int d, double scale, int causal,
+               const int *cu_seqlens, const int *rows, int nrows, int nthreads) {
+    if (!q || !k || !v || !o || !lse) return -1;
+    if (check_args(B, H, Lq, Lk, d, cu_seqlens)) return -1;
+    job_t J;
+    init_job(&J, q, k, v, NULL, B, H, Lq, Lk, d, scale, causal, cu_seqlens);
+    J.o = o; J.lse = lse;
+    long n;
+    int *items = make_items(&J, rows, nrows, 0, &n);
+    if (!items) return -2;
+    run_items(&J, PH_FWD, items, n, nthreads);
+    free(items);
+    return 0;
+}
+
+int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
+               double *dq, double *dk, double *dv,
+               int B, int H, int Lq, int Lk, int d, double scale, int causal,
+               const int *cu_seqlens, const int *qrows, int nqrows,
+               const int *krows, int nkrows, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
+    if (check_args(B, H, Lq, Lk, d, cu_seqlens)) return -1;
+    if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
+    job_t J;
+    init_job(&J, q, k, v, dout, B, H, Lq, Lk, d, scale, causal, cu_seqlens);
+    J.dq = dq; J.dk = dk; J.dv = dv;
+
+    /* longest sequence, the range of relative row indices */
+    int lmax = cu_seqlens ? 0 : Lq;
+    if (cu_seqlens)
+        for (int b = 0; b < B; b++) if (cu_seqlens[b + 1] - cu_seqlens[b] > lmax) lmax = cu_seqlens[b + 1] - cu_seqlens[b];
+    long nstat = cu_seqlens ? (long)H * cu_seqlens[B] : (long)B * H * Lq;
+    J.lse_all = (double *)malloc(sizeof(double) * (size_t)(nstat > 0 ? nstat : 1));
+    J.D_all = (double *)malloc(sizeof(double) * (size_t)(nstat > 0 ? nstat : 1));
+    unsigned char *need = (unsigned char *)calloc((size_t)(lmax > 0 ? lmax : 1), 1);
+    int *list = (int *)malloc(sizeof(int) * (size_t)(lmax > 0 ? lmax : 1));
+    if (!J.lse_all || !J.D_all || !need || !list) {
+        free(J.lse_all); free(J.D_all); free(need); free(list);
+        return -2;
+    }
+
+    /* Query rows whose LSE_i and D_i are needed: the requested dQ rows, plus
+       every row that can see a requested key row (for a dense causal problem
+       key j is seen by rows i >= j - (Lk - Lq); otherwise by all rows). */
+    int want_dq = !(qrows && nqrows == 0);
+    int want_dkv = !(krows && nkrows == 0);
+    if (want_dq) {
+        if (!qrows) memset(need, 1, (size_t)lmax);
+        else for (int t = 0; t < nqrows; t++) if (qrows[t] >= 0 && qrows[t] < lmax) need[qrows[t]] = 1;
+    }
+    if (want_dkv) {
+        int i0 = 0;
+        if (krows && causal && !cu_seqlens) {
+            int jmin = Lk;
+            for (int t = 0; t < nkrows; t++) if (krows[t] >= 0 && krows[t] < jmin) jmin = krows[t];
+            i0 = jmin - (Lk - Lq);
+            if (i0 < 0) i0 = 0;
+        }
+        for (int i = i0; i < lmax; i++) need[i] = 1;
+    }
+    int nlist = 0;
+    for (int i = 0; i < lmax; i++) if (need[i]) list[nlist++] = i;
+
+    long n;
+    int rc = 0;
+    int *items = make_items(&J, list, nlist, 0, &n);
+    if (!items) { rc = -2; goto done; }
+    run_items(&J, PH_STATS, items, n, nthreads);
+    free(items);
+
+    if (want_dq) {
+        items = make_items(&J, qrows, nqrows, 0, &n);
+        if (!items) { rc = -2; goto done; }
+        run_items(&J, PH_DQ, items, n, nthreads);
+        free(items);
+    }
+    if (want_dkv) {
+        items = make_items(&J, krows, nkrows, 1, &n);
+        if (!items) { rc = -2; goto done; }
+        run_items(&J, PH_DKV, items, n, nthreads);
+        free(items);
+    }
+done:
+    free(J.lse_all); free(J.D_all); free(need); free(list);
+    return rc;
+}

@@ -1,0 +1,89 @@
+"""Plausible mistakes planted in the oracle (on the CPU) must fail a pin.
+
+Each mutant is a one-line edit of a temporary copy of oracle/oracle.c: a
+dropped scale, a wrong mask boundary, a wrong operand, a sign flip, a wrong
+varlen offset. The copy is compiled and bound in place of the real oracle, and
+the pin battery from test_oracle_pins.py is run against it; at least one pin
+must fail. The real oracle must pass the same battery.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = [
+    ("drop scale in scores", "return J->scale * dot(qi, kj, J->d);", "return dot(qi, kj, J->d);"),
+    ("strict causal boundary", "return j <= i + (lk - lq);", "return j < i + (lk - lq);"),
+    ("top-left causal alignment", "return j <= i + (lk - lq);", "return j <= i;"),
+    ("LSE without the max", "return m + log(sum);", "return log(sum);"),
+    ("base-2 exponential", "sum += exp(score(J, b, h, i, j) - m);", "sum += exp2(score(J, b, h, i, j) - m);"),
+    ("O sums keys instead of values", "const double *vj = J->v + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < d; c++) out[c]",
+     "const double *vj = J->k + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < d; c++) out[c]"),
+    ("score uses key row i", "const double *kj = J->k + row_off(J, b, j, h, J->Lk);\n    return",
+     "const double *kj = J->k + row_off(J, b, i < J->Lk ? i : 0, h, J->Lk);\n    return"),
+    ("dS sign flip", "return p * (dot(doi, vj, J->d) - J->D_all[st]);", "return p * (dot(doi, vj, J->d) + J->D_all[st]);"),
+    ("D dropped", "J->D_all[st] = dot(", "J->D_all[st] = 0.0 * dot("),
+    ("dQ without scale", "for (int c = 0; c < d; c++) dqi[c] *= J->scale;", ""),
+    ("dK without scale", "for (int c = 0; c < d; c++) dkj[c] *= J->scale;", ""),
+    ("dV weighted by dS", "dvj[c] += p * dor[c];", "dvj[c] += ds * dor[c];"),
+    ("dK from dO instead of Q", "dkj[c] += ds * qr[c];", "dkj[c] += ds * dor[c];"),
+    ("varlen row offset ignores start", "if (J->cu) return ((long)(J->cu[b] + i) * J->H + h) * J->d;",
+     "if (J->cu) return ((long)(i) * J->H + h) * J->d;"),
+    ("varlen LSE offset ignores start", "if (J->cu) return (long)h * J->cu[J->B] + J->cu[b] + i;",
+     "if (J->cu) return (long)h * J->cu[J->B] + i;"),
+]
+
+BATTERY = [
+    (pins.test_golden_hand_example, (False,)),
+    (pins.test_golden_hand_example, (True,)),
+    (pins.test_fwd_matches_textbook_softmax, (2, 3, 5, 5, 4, False)),
+    (pins.test_fwd_matches_textbook_softmax, (1, 2, 7, 11, 8, True)),
+    (pins.test_causal_first_row_returns_v0, ()),
+    (pins.test_bottom_right_causal_with_more_queries, ()),
+    (pins.test_varlen_is_per_sequence_attention, ()),
+    (pins.test_bwd_finite_differences, (3, 4, False)),
+    (pins.test_bwd_finite_differences, (7, 8, True)),
+    (pins.test_bwd_finite_differences_rectangular_and_varlen, ()),
+    (pins.test_bwd_column_sums, ()),
+]
+
+
+def run_battery():
+    failed = []
+    for fn, args in BATTERY:
+        try:
+            fn(*args)
+        except (AssertionError, RuntimeError, ValueError, FloatingPointError) as e:
+            failed.append(f"{fn.__name__}{args}: {type(e).__name__}")
+    return failed
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    with open(SRC) as f:
+        return f.read()
+
+
+def test_real_oracle_passes_battery():
+    assert run_battery() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, src_text, tmp_path, monkeypatch):
+    assert src_text.count(old) == 1, f"mutation site for '{name}' not unique"
+    mutated = src_text.replace(old, new)
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated)
+    so_path = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so_path),
+                           str(c_path), "-lm", "-lpthread"])
+    monkeypatch.setattr(oracle, "_lib", oracle.bind(str(so_path)))
+    failed = run_battery()
+    assert failed, f"mutant '{name}' passed every pin"
+    shutil.rmtree(tmp_path, ignore_errors=True)

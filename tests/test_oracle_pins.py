@@ -1,0 +1,320 @@
+"""Pins for the fp64 oracle, independent of the oracle itself.
+
+Each check ties the oracle to something other than its own formulas: a
+hand-derived example (tests/golden/hand_2x2.txt), closed forms of special
+cases, a textbook softmax written with scipy on tiny inputs, invariants of
+softmax attention, and central finite differences for the backward pass.
+The mutant test (test_oracle_mutants.py) shows that plausible mistakes in the
+oracle source fail at least one of these.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import oracle
+from exact_attention_blackwell_tma_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- golden file
+
+def load_golden(name):
+    consts = {"LN2": math.log(2.0), "LN3": math.log(3.0)}
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = (s.strip() for s in line.split("=", 1))
+            nums = []
+            for tok in val.split(","):
+                tok = tok.strip()
+                if not tok:
+                    continue
+                factor = 1.0
+                if "*" in tok:
+                    a, b = tok.split("*")
+                    tok, factor = a.strip(), consts[b.strip()]
+                nums.append((consts[tok] if tok in consts else float(tok)) * factor)
+            out[key] = np.array(nums)
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_hand_example(causal):
+    g = load_golden("hand_2x2.txt")
+    shp = (1, 2, 1, 2)
+    q, k, v, do = (g[n].reshape(shp) for n in ("q", "k", "v", "do"))
+    scale = float(g["scale"][0])
+    tag = "causal" if causal else "noncausal"
+    o, lse = oracle.fwd(q, k, v, scale, causal)
+    np.testing.assert_allclose(o.reshape(-1), g[f"{tag}.o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.reshape(-1), g[f"{tag}.lse"], rtol=0, atol=1e-12)
+    dq, dk, dv = oracle.bwd(q, k, v, do, scale, causal)
+    np.testing.assert_allclose(dq.reshape(-1), g[f"{tag}.dq"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.reshape(-1), g[f"{tag}.dk"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv.reshape(-1), g[f"{tag}.dv"], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------- forward pins
+
+def textbook(q, k, v, scale, causal):
+    """softmax(scale Q K^T [+ bottom-right causal mask]) V with scipy, tiny sizes."""
+    B, Lq, H, d = q.shape
+    Lk = k.shape[1]
+    s = np.einsum("bihc,bjhc->bhij", q, k) * scale
+    if causal:
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        s = np.where(j <= i + (Lk - Lq), s, -np.inf)
+    with np.errstate(invalid="ignore"):
+        lse = logsumexp(s, axis=-1)
+        p = softmax(s, axis=-1)
+    p = np.nan_to_num(p, nan=0.0)
+    o = np.einsum("bhij,bjhc->bihc", p, v)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Lq,Lk,d", [(1, 1, 1, 1, 1), (2, 3, 5, 5, 4), (1, 2, 7, 11, 8),
+                                         (2, 1, 9, 4, 3), (1, 2, 16, 16, 16)])
+def test_fwd_matches_textbook_softmax(B, H, Lq, Lk, d, causal):
+    q, k, v = rnd((B, Lq, H, d), 1), rnd((B, Lk, H, d), 2), rnd((B, Lk, H, d), 3)
+    scale = 0.7
+    o, lse = oracle.fwd(q, k, v, scale, causal)
+    o_ref, lse_ref = textbook(q, k, v, scale, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_single_key_returns_v():
+    q, k, v = rnd((2, 6, 3, 8), 4), rnd((2, 1, 3, 8), 5), rnd((2, 1, 3, 8), 6)
+    s = 0.3 * np.einsum("bihc,bhc->bhi", q, k[:, 0])
+    o, lse = oracle.fwd(q, k, v, 0.3, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, s, rtol=1e-13, atol=1e-13)   # LSE of one score is it
+    # causal, bottom-right aligned: only the last query row sees the single key
+    o, lse = oracle.fwd(q, k, v, 0.3, True)
+    np.testing.assert_allclose(o[:, -1], v[:, 0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[:, :, -1], s[:, :, -1], rtol=1e-13, atol=1e-13)
+    assert np.all(o[:, :-1] == 0) and np.all(np.isneginf(lse[:, :, :-1]))
+
+
+def test_identical_keys_give_mean_of_v():
+    L, d = 9, 5
+    q = rnd((1, L, 2, d), 7)
+    k = np.broadcast_to(rnd((1, 1, 2, d), 8), (1, L, 2, d)).copy()
+    v = rnd((1, L, 2, d), 9)
+    o, lse = oracle.fwd(q, k, v, 0.5, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=1, keepdims=True), o.shape),
+                               rtol=1e-12, atol=1e-12)
+    s = 0.5 * np.einsum("bihc,bhc->bhi", q, k[:, 0])
+    np.testing.assert_allclose(lse, s + math.log(L), rtol=1e-12, atol=1e-12)
+
+
+def test_zero_query_gives_column_mean():
+    q = np.zeros((1, 4, 1, 6))
+    k, v = rnd((1, 10, 1, 6), 10), rnd((1, 10, 1, 6), 11)
+    o, lse = oracle.fwd(q, k, v, 1.0, False)
+    np.testing.assert_allclose(o[0, :, 0], np.broadcast_to(v[0, :, 0].mean(0), (4, 6)), atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(10), atol=1e-13)
+
+
+def test_identity_values_expose_probabilities():
+    """With V = I (d = Lk), O_i is the probability row P_i: rows sum to 1."""
+    L = 12
+    q, k = rnd((1, L, 1, L), 12), rnd((1, L, 1, L), 13)
+    v = np.eye(L).reshape(1, L, 1, L)
+    for causal in (False, True):
+        o, _ = oracle.fwd(q, k, v, 0.4, causal)
+        p = o[0, :, 0, :]
+        np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-12)
+        assert (p >= 0).all()
+        if causal:
+            assert np.all(np.triu(p, 1) == 0)
+
+
+def test_causal_first_row_returns_v0():
+    q, k, v = rnd((2, 8, 3, 4), 14), rnd((2, 8, 3, 4), 15), rnd((2, 8, 3, 4), 16)
+    o, lse = oracle.fwd(q, k, v, 0.9, True)
+    np.testing.assert_allclose(o[:, 0], v[:, 0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[:, :, 0], 0.9 * np.einsum("bhc,bhc->bh", q[:, 0], k[:, 0]),
+                               atol=1e-13)
+
+
+def test_key_permutation_invariance():
+    q, k, v = rnd((1, 6, 2, 4), 17), rnd((1, 10, 2, 4), 18), rnd((1, 10, 2, 4), 19)
+    perm = np.random.default_rng(0).permutation(10)
+    o1, l1 = oracle.fwd(q, k, v, 0.6, False)
+    o2, l2 = oracle.fwd(q, k[:, perm], v[:, perm], 0.6, False)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_causal_row_equals_prefix_attention():
+    L = 9
+    q, k, v = rnd((1, L, 2, 4), 20), rnd((1, L, 2, 4), 21), rnd((1, L, 2, 4), 22)
+    o, lse = oracle.fwd(q, k, v, 0.8, True)
+    for i in range(L):
+        oi, li = oracle.fwd(q[:, i:i + 1], k[:, :i + 1], v[:, :i + 1], 0.8, False)
+        np.testing.assert_allclose(o[:, i], oi[:, 0], atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], li[:, :, 0], atol=1e-13)
+
+
+def test_bottom_right_causal_with_more_queries():
+    """Lq > Lk: rows i < Lq - Lk see no key (O = 0, LSE = -inf)."""
+    q, k, v = rnd((1, 7, 1, 3), 23), rnd((1, 4, 1, 3), 24), rnd((1, 4, 1, 3), 25)
+    o, lse = oracle.fwd(q, k, v, 1.0, True)
+    assert np.all(o[0, :3] == 0) and np.all(np.isneginf(lse[0, 0, :3]))
+    assert np.all(np.isfinite(lse[0, 0, 3:]))
+    # the last Lk rows behave like square causal attention with the last queries
+    o2, l2 = oracle.fwd(q[:, 3:], k, v, 1.0, True)
+    np.testing.assert_allclose(o[:, 3:], o2, atol=1e-13)
+
+
+def test_shift_invariance_of_keys():
+    """Adding a vector u to every key shifts row i's scores by scale<q_i,u>:
+    probabilities (so O) are unchanged and LSE moves by exactly that amount."""
+    q, k, v = rnd((1, 5, 1, 4), 26), rnd((1, 8, 1, 4), 27), rnd((1, 8, 1, 4), 28)
+    u = 3.0 * rnd((4,), 29)
+    o1, l1 = oracle.fwd(q, k, v, 0.5, False)
+    o2, l2 = oracle.fwd(q, k + u, v, 0.5, False)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, 0.5 * np.einsum("bihc,c->bhi", q, u), atol=1e-12)
+
+
+def test_large_scores_do_not_overflow():
+    q, k, v = rnd((1, 4, 1, 8), 30), rnd((1, 6, 1, 8), 31), rnd((1, 6, 1, 8), 32)
+    o, lse = oracle.fwd(q, k, v, 300.0, False)
+    o_ref, lse_ref = textbook(q, k, v, 300.0, False)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12)
+
+
+def test_varlen_is_per_sequence_attention():
+    lens = [3, 1, 6, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, H, d = cu[-1], 2, 4
+    q, k, v = rnd((T, H, d), 33), rnd((T, H, d), 34), rnd((T, H, d), 35)
+    for causal in (False, True):
+        o, lse = oracle.fwd(q, k, v, 0.7, causal, cu_seqlens=cu)
+        for b, L in enumerate(lens):
+            a = cu[b]
+            ob, lb = textbook(q[None, a:a + L], k[None, a:a + L], v[None, a:a + L], 0.7, causal)
+            np.testing.assert_allclose(o[a:a + L], ob[0], atol=1e-12)
+            np.testing.assert_allclose(lse[:, a:a + L], lb[0], atol=1e-12)
+
+
+def test_row_subset_matches_full():
+    q, k, v = rnd((2, 10, 2, 4), 36), rnd((2, 10, 2, 4), 37), rnd((2, 10, 2, 4), 38)
+    full_o, full_l = oracle.fwd(q, k, v, 0.5, True)
+    rows = [0, 3, 9]
+    o, lse = oracle.fwd(q, k, v, 0.5, True, rows=rows)
+    np.testing.assert_array_equal(o[:, rows], full_o[:, rows])
+    np.testing.assert_array_equal(lse[:, :, rows], full_l[:, :, rows])
+    assert np.isnan(o[:, 1]).all()
+
+
+def test_workload_inputs_roundtrip_through_oracle():
+    """The seeded bf16 inputs widen exactly and the tiny workload runs."""
+    t = inputs.make(inputs.TINY)
+    q = t["q"].float().numpy()
+    assert np.array_equal(q.astype(np.float64).astype(np.float32), q)
+    o, lse = oracle.fwd(q, t["k"].float().numpy(), t["v"].float().numpy(),
+                        inputs.TINY.scale, False)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------- backward pins
+
+def loss(q, k, v, do, scale, causal, cu=None):
+    o, _ = oracle.fwd(q, k, v, scale, causal, cu_seqlens=cu)
+    return float(np.sum(o * do))
+
+
+def finite_diff(q, k, v, do, scale, causal, cu=None, h=1e-6):
+    grads = []
+    for which in range(3):
+        arrs = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(arrs[which])
+        it = np.nditer(g, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [a.copy() for a in arrs]
+            minus = [a.copy() for a in arrs]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            g[idx] = (loss(*plus, do, scale, causal, cu) - loss(*minus, do, scale, causal, cu)) / (2 * h)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L,d", [(1, 4), (3, 4), (7, 8)])
+def test_bwd_finite_differences(L, d, causal):
+    q, k, v, do = rnd((1, L, 1, d), 40), rnd((1, L, 1, d), 41), rnd((1, L, 1, d), 42), rnd((1, L, 1, d), 43)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.6, causal)
+    fq, fk, fv = finite_diff(q, k, v, do, 0.6, causal)
+    for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+        err = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert err < 1e-6 or np.abs(got - ref).max() < 1e-8, err
+
+
+def test_bwd_finite_differences_rectangular_and_varlen():
+    q, k, v, do = rnd((1, 5, 2, 3), 44), rnd((1, 3, 2, 3), 45), rnd((1, 3, 2, 3), 46), rnd((1, 5, 2, 3), 47)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.9, True)
+    fq, fk, fv = finite_diff(q, k, v, do, 0.9, True)
+    for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.abs(got - ref).max() < 1e-7
+    lens = [2, 3]
+    cu = np.array([0, 2, 5], dtype=np.int32)
+    q, k, v, do = rnd((5, 1, 3), 48), rnd((5, 1, 3), 49), rnd((5, 1, 3), 50), rnd((5, 1, 3), 51)
+    for causal in (False, True):
+        dq, dk, dv = oracle.bwd(q, k, v, do, 0.8, causal, cu_seqlens=cu)
+        fq, fk, fv = finite_diff(q, k, v, do, 0.8, causal, cu=cu)
+        for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+            assert np.abs(got - ref).max() < 1e-7
+    assert sum(lens) == 5
+
+
+def test_bwd_column_sums():
+    """sum_j dS_ij = 0 gives sum_j dK_j = 0; rows of P sum to 1 give
+    sum_j dV_j = sum_i dO_i (per batch and head)."""
+    q, k, v, do = (rnd((2, 12, 3, 5), s) for s in (52, 53, 54, 55))
+    for causal in (False, True):
+        dq, dk, dv = oracle.bwd(q, k, v, do, 0.7, causal)
+        np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+        np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), atol=1e-12)
+
+
+def test_bwd_single_key():
+    """One key: P = 1, so dS = 0 => dQ = dK = 0, and dV_0 = sum_i dO_i."""
+    q, k, v, do = rnd((1, 6, 2, 4), 56), rnd((1, 1, 2, 4), 57), rnd((1, 1, 2, 4), 58), rnd((1, 6, 2, 4), 59)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.5, False)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-13)
+    np.testing.assert_allclose(dv[:, 0], do.sum(axis=1), atol=1e-13)
+
+
+def test_bwd_row_subsets_match_full():
+    q, k, v, do = (rnd((1, 16, 2, 4), s) for s in (60, 61, 62, 63))
+    for causal in (False, True):
+        fq, fk, fv = oracle.bwd(q, k, v, do, 0.5, causal)
+        dq, dk, dv = oracle.bwd(q, k, v, do, 0.5, causal, qrows=[2, 15], krows=[0, 7, 14])
+        np.testing.assert_array_equal(dq[:, [2, 15]], fq[:, [2, 15]])
+        np.testing.assert_array_equal(dk[:, [0, 7, 14]], fk[:, [0, 7, 14]])
+        np.testing.assert_array_equal(dv[:, [0, 7, 14]], fv[:, [0, 7, 14]])
+        dq, dk, dv = oracle.bwd(q, k, v, do, 0.5, causal, qrows=[], krows=[13])
+        np.testing.assert_array_equal(dk[:, 13], fk[:, 13])
+        assert np.isnan(dq).all()
