@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the attention hot path on GB300.
+
+A step is one pass of the whole path over one batch of synthetic input: for
+each mask variant of the workload, the forward (attn_fwd) and the backward
+(attn_bwd: preprocess, main kernel, dQ conversion). The default workload is
+B=4, H=16, L=4096, d=128 (bf16), causal and non-causal. Throughput is
+algorithmic FLOPs / time: forward 4*d per unmasked (query, key) pair,
+backward 2.5x that.
+
+  python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). Under torchrun each rank runs the same
+workload on its own GPU (independent replicas, no collective on the data
+path: weak scaling); the timed region is bracketed by a barrier and a device
+synchronise, and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_attention_blackwell_tma_gb300 import binding, inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, causal+non-causal) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+
+WORKLOADS = {
+    "b4h16l4096d128": (inputs.MHA4K, (True, False)),
+    "b2h16l8192d128": (inputs.HDSWEEP, (True,)),
+    "b2h16l8192d64": (inputs.HDSWEEP.with_(d=64), (True,)),
+    "varlen32_h16d128": (inputs.VARLEN, (True,)),
+    "b1h32l32768d128": (inputs.LONG, (True, False)),
+}
+DEFAULT_WORKLOAD = "b4h16l4096d128"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16": float(pk["bf16_tflops"]), "bf16_sustained": float(pk["bf16_tflops_sustained"]),
+                "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class Problem:
+    """Device buffers for one workload."""
+
+    def __init__(self, w, device):
+        t = inputs.make(w)
+        self.w = w
+        self.host = t
+        self.q, self.k, self.v, self.do = (t[n].to(device) for n in ("q", "k", "v", "do"))
+        self.cu = t["cu_seqlens"].to(device) if w.varlen else None
+        self.o = torch.empty_like(self.q)
+        self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
+        if w.varlen:
+            self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.total, w.total, w.d
+            self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=device)
+        else:
+            self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.L, w.L, w.d
+            self.lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=device)
+        ws = max(binding.attn_bwd_workspace_size(self.B, self.H, self.Lq, self.Lk, self.d, 1, 0), 1)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+
+    def fwd(self, causal):
+        rc = binding.attn_fwd(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Lq, self.Lk, self.d,
+                              self.w.scale, causal, self.cu)
+        if rc:
+            raise binding.AttnError(rc, binding.last_error())
+
+    def bwd(self, causal):
+        rc = binding.attn_bwd(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
+                              self.B, self.H, self.Lq, self.Lk, self.d, self.w.scale, causal, self.cu, 0,
+                              self.ws, self.ws.numel())
+        if rc:
+            raise binding.AttnError(rc, binding.last_error())
+
+
+def flops(w, causal, which):
+    ww = w.with_(causal=causal)
+    return ww.fwd_flops() if which == "fwd" else ww.bwd_flops()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return world, rank, local, dist
+    torch.cuda.set_device(local)
+    return 1, 0, local, None
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------------------------------ oracle
+def oracle_sample(w, variants, nthreads=None):
+    """fp64 oracle (forward + backward) on one head of batch entry 0 for each
+    variant; returns (algorithmic flops of the sample, seconds, threads)."""
+    import numpy as np
+    import oracle
+    t = inputs.make(w)
+    total_flops, secs = 0, 0.0
+    nthreads = nthreads or oracle.default_threads()
+    if w.varlen:
+        cu = t["cu_seqlens"]
+        L = int(cu[1] - cu[0])
+        sl = {n: t[n][int(cu[0]):int(cu[1]), :1].unsqueeze(0) for n in ("q", "k", "v", "do")}
+        sub_w = w.with_(lengths=None, B=1, H=1, L=L)
+    else:
+        sl = {n: t[n][:1, :, :1] for n in ("q", "k", "v", "do")}
+        sub_w = w.with_(B=1, H=1)
+    f64 = {n: x.float().numpy().astype(np.float64) for n, x in sl.items()}
+    for causal in variants:
+        t0 = time.perf_counter()
+        oracle.fwd(f64["q"], f64["k"], f64["v"], w.scale, causal, nthreads=nthreads)
+        oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads)
+        secs += time.perf_counter() - t0
+        total_flops += flops(sub_w, causal, "fwd") + flops(sub_w, causal, "bwd")
+    return total_flops, secs, nthreads
+
+
+def run_reference(args, world, rank, dist):
+    if rank != 0:
+        return 0
+    w, variants = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(w, variants)
+    fl, secs = 0, 0.0
+    threads = None
+    for _ in range(args.steps):
+        f, s, threads = oracle_sample(w, variants)
+        fl += f
+        secs += s
+    value = fl / secs / 1e12
+    sample = f"one head (batch 0, head 0) of {w.name}, forward+backward for {'/'.join('causal' if c else 'non-causal' for c in variants)}, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "variants": ["causal" if c else "non-causal" for c in variants]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------ ours
+def run_ours(args, world, rank, local, dist):
+    w, variants = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    pk = load_peaks()
+    prob = Problem(w, dev)
+    step_flops = sum(flops(w, c, "fwd") + flops(w, c, "bwd") for c in variants)
+    input_bytes = sum(x.numel() * x.element_size() for x in (prob.q, prob.k, prob.v, prob.do))
+
+    def step(ev=None):
+        for c in variants:
+            if ev is not None:
+                ev[("fwd", c)][0].record()
+            prob.fwd(c)
+            if ev is not None:
+                ev[("fwd", c)][1].record()
+                ev[("bwd", c)][0].record()
+            prob.bwd(c)
+            if ev is not None:
+                ev[("bwd", c)][1].record()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    binding.check_status()
+
+    # ---- timed region: K steps, per-call events on the launching stream
+    evs = [{(k, c): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for k in ("fwd", "bwd") for c in variants} for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        t0.record()
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record()
+        barrier(dist)
+    binding.check_status()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dist)
+    value = world * step_flops / (ms * 1e-3) / 1e12
+
+    # per-kernel-call durations -> rooflines
+    per_call = {}
+    for key in evs[0]:
+        per_call[key] = statistics.mean(e[key][0].elapsed_time(e[key][1]) for e in evs)
+    rooflines = []
+    for (kind, c), t_ms in per_call.items():
+        fl = flops(w, c, kind)
+        ach = fl / (t_ms * 1e-3) / 1e12
+        rooflines.append({"kernel": f"attn_{kind}", "variant": "causal" if c else "non-causal",
+                          "ms": t_ms, "achieved": ach, "bound": "tensor", "unit": "TFLOP/s",
+                          "peak": pk["bf16"], "frac": ach / pk["bf16"], "traffic": None})
+    dom = max(rooflines, key=lambda r: r["ms"])
+    roofline = {"bound": "tensor", "achieved": dom["achieved"], "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": dom["achieved"] / pk["bf16"], "traffic": None,
+                "kernel": f"{dom['kernel']} ({dom['variant']})",
+                "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"}
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {n: prob.host[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                for n, x in (("o", prob.o), ("lse", prob.lse), ("dq", prob.dq), ("dk", prob.dk),
+                             ("dv", prob.dv))}
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = len(variants) * sum(x.numel() * x.element_size() for x in outs.values())
+
+        def e2e_step():
+            prob.q.copy_(host["q"], non_blocking=True)
+            prob.k.copy_(host["k"], non_blocking=True)
+            prob.v.copy_(host["v"], non_blocking=True)
+            prob.do.copy_(host["do"], non_blocking=True)
+            for c in variants:
+                prob.fwd(c)
+                prob.bwd(c)
+                for n, dst in outs.items():
+                    dst.copy_(getattr(prob, n), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier(dist)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        barrier(dist)
+        e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist)
+        e2e = {"value": world * step_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---- oracle on the host cores (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, secs, threads = oracle_sample(w, variants)
+        cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"one head (batch 0, head 0) of {w.name}, forward+backward per variant; "
+                         f"{secs:.1f} s", "seconds": secs}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                           "variants": ["causal" if c else "non-causal" for c in variants],
+                           "flops_per_step": step_flops,
+                           "l2": f"inputs {input_bytes / 2**20:.0f} MiB > 129 MiB L2; no flush between steps",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "frac_of_peak": value / world / pk["bf16"],
+                "roofline": roofline, "roofline_calls": rooflines,
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * len(variants) * 4,
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local, dist = dist_setup() if args.impl == "ours" else (
+        int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None)
+    if args.impl == "reference":
+        return run_reference(args, world, rank, dist)
+    rc = run_ours(args, world, rank, local, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,184 @@
+"""Python binding of libattn.so: the C entry points under the same names.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. PyTorch supplies device memory and the current stream. If the
+library has not been built, ``load()`` raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+_selftest = None
+
+c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_ALIGN, ATTN_ERR_LAUNCH, ATTN_ERR_WORKSPACE, ATTN_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"attn error {code}: {msg}")
+        self.code = code
+
+
+def _declare(lib):
+    lib.attn_fwd.restype = c_int
+    lib.attn_fwd.argtypes = [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_void_p, c_void_p]
+    lib.attn_bwd_workspace_size.restype = c_size_t
+    lib.attn_bwd_workspace_size.argtypes = [c_int] * 7
+    lib.attn_bwd.restype = c_int
+    lib.attn_bwd.argtypes = ([c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p, c_size_t,
+                                                               c_void_p])
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_last_error.argtypes = []
+    lib.attn_check_status.restype = c_int
+    lib.attn_check_status.argtypes = [c_void_p]
+    lib.attn_version.restype = c_int
+    lib.attn_version.argtypes = []
+    return lib
+
+
+def library_path() -> str:
+    return _build.lib_path("libattn.so")
+
+
+def load():
+    """Load libattn.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: run exact_attention_blackwell_tma_gb300.build.build() "
+                                   "(or __graft_entry__.build()) first; there is no CPU fallback")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def load_selftest():
+    global _selftest
+    with _lock:
+        if _selftest is None:
+            path = _build.lib_path("libattn_selftest.so")
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build first")
+            lib = ctypes.CDLL(path)
+            lib.attn_selftest_mma.restype = c_int
+            lib.attn_selftest_mma.argtypes = [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+            lib.attn_selftest_wait_timeout.restype = c_int
+            lib.attn_selftest_wait_timeout.argtypes = [c_void_p, ctypes.c_ulonglong, c_void_p]
+            _selftest = lib
+    return _selftest
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def last_error() -> str:
+    return load().attn_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != ATTN_OK:
+        raise AttnError(rc, last_error())
+
+
+# ---------------------------------------------------------------- C entry points, same names
+
+def attn_fwd(q, k, v, o, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens=None, stream=None) -> int:
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, scale, int(causal),
+                           _ptr(cu_seqlens), _stream(stream))
+
+
+def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
+    return load().attn_bwd_workspace_size(B, H, Lq, Lk, d, int(causal), int(deterministic))
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens, deterministic,
+             workspace, ws_bytes, stream=None) -> int:
+    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, H, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens), int(deterministic),
+                           _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def attn_last_error() -> str:
+    return last_error()
+
+
+def attn_check_status(stream=None) -> int:
+    return load().attn_check_status(_stream(stream))
+
+
+# ---------------------------------------------------------------- tensor-level helpers
+
+def _dims(q, k, cu_seqlens):
+    if cu_seqlens is None:
+        B, Lq, H, d = q.shape
+        return B, H, Lq, k.shape[1], d
+    T, H, d = q.shape
+    return cu_seqlens.numel() - 1, H, T, k.shape[0], d
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
+            stream=None):
+    """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens)."""
+    _check_tensors(q, k, v, cu_seqlens)
+    B, H, Lq, Lk, d = _dims(q, k, cu_seqlens)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
+    _check(attn_fwd(q, k, v, out, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens, stream))
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu_seqlens=None,
+             deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV (bf16) for the loss sum(O * dO)."""
+    _check_tensors(q, k, v, o, lse, dout, cu_seqlens)
+    B, H, Lq, Lk, d = _dims(q, k, cu_seqlens)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
+                    deterministic, workspace, workspace.numel() * workspace.element_size(), stream))
+    return dq, dk, dv
+
+
+def check_status(stream=None):
+    _check(attn_check_status(stream))

@@ -1,0 +1,297 @@
+// C-ABI host layer of libattn.so: argument checks, TMA descriptors, launches.
+// The operation and the layouts are specified in include/attn.h.
+#include <attn.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace attn {
+
+// Device status word: kernels set it (atomically) when a bounded wait runs
+// out; attn_check_status reads and clears it.
+__device__ int g_attn_status;
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows, H, d] bf16 viewed as 3-D (d innermost); boxes of 128 rows x 1 head x
+// 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect.
+// Rows past `rows` read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+    int sms = 0;
+    int* status = nullptr;
+};
+
+bool device_info(DevInfo* out) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    DevInfo& di = cache[dev];
+    if (di.sms == 0) {
+        int sms = 0;
+        void* st = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&st, g_attn_status) != cudaSuccess) return false;
+        di.status = static_cast<int*>(st);
+        di.sms = sms;
+    }
+    *out = di;
+    return true;
+}
+
+uint64_t wait_budget_ns() {
+    static uint64_t ns = [] {
+        const char* e = getenv("ATTN_WAIT_BUDGET_MS");
+        double ms = e ? atof(e) : 2000.0;
+        if (!(ms > 0)) ms = 2000.0;
+        return (uint64_t)(ms * 1e6);
+    }();
+    return ns;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Heads per L2 section for the LPT walk: K and V of a section should fit in
+// about half of the 129 MB L2 (FlashAttention-4 paper, Section 3.3).
+int head_section(int H, long keys, int d) {
+    const double budget = 64.0 * 1024 * 1024;
+    double per_head = 2.0 * 2.0 * (double)keys * d;   // K and V, bf16
+    int hs = per_head > 0 ? (int)(budget / per_head) : H;
+    if (hs < 1) hs = 1;
+    if (hs > H) hs = H;
+    return hs;
+}
+
+int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu, bool bwd) {
+    if (B < 0 || H <= 0 || Lq < 0 || Lk < 0) return fail(ATTN_ERR_ARG, "bad sizes B=%d H=%d Lq=%d Lk=%d", B, H, Lq, Lk);
+    if (d != 64 && d != 128)
+        return fail(ATTN_ERR_ARG, "head dim %d not supported by the %s pass (64, 128)", d, bwd ? "backward" : "forward");
+    if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_ARG, "scale must be finite and > 0");
+    if (cu) {
+        if (Lq != Lk) return fail(ATTN_ERR_ARG, "varlen: Lq and Lk must both be the packed row count T");
+        if (B < 1 || B > kMaxVarlenBatch) return fail(ATTN_ERR_ARG, "varlen: B must be in [1, %d]", kMaxVarlenBatch);
+    }
+    long rows_q = cu ? (long)Lq : (long)B * Lq, rows_k = cu ? (long)Lk : (long)B * Lk;
+    if (rows_q >= (1L << 31) || rows_k >= (1L << 31)) return fail(ATTN_ERR_ARG, "too many rows");
+    return ATTN_OK;
+}
+
+}  // namespace
+
+int* device_status_word() {
+    DevInfo di;
+    return device_info(&di) ? di.status : nullptr;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
+                        int Lk, int d, float scale, int causal, const int* cu_seqlens, cudaStream_t stream) {
+    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, false);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+    const long rows_q = cu_seqlens ? (long)Lq : (long)B * Lq;
+    const long rows_k = cu_seqlens ? (long)Lk : (long)B * Lk;
+    if (rows_q == 0) return ok();
+    DevInfo di;
+    if (!device_info(&di)) return fail(ATTN_ERR_LAUNCH, "cannot query the current device");
+    FwdParams p{};
+    p.g.B = B;
+    p.g.H = H;
+    p.g.Lq = Lq;
+    p.g.Lk = Lk;
+    p.g.d = d;
+    p.g.cu_seqlens = cu_seqlens;
+    p.g.causal = causal ? 1 : 0;
+    p.g.scale = scale;
+    p.g.scale_log2 = scale * kLog2e;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.nm = (Lq + 255) / 256;
+    p.n_tiles = cu_seqlens ? 0 : B * H * p.nm;
+    p.head_section = head_section(H, cu_seqlens ? (rows_k / B) : Lk, d);
+    p.status = di.status;
+    p.wait_budget_ns = wait_budget_ns();
+    CUtensorMap tq, tk, tv;
+    // a problem with no keys still needs valid descriptors: point them at q
+    const long krows = rows_k > 0 ? rows_k : rows_q;
+    const void* kp = rows_k > 0 ? k : q;
+    const void* vp = rows_k > 0 ? v : q;
+    if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, H, d) || !make_map(&tv, vp, krows, H, d))
+        return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    cudaError_t e = launch_fwd(tq, tk, tv, p, di.sms, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+namespace {
+
+struct BwdWorkspace {
+    size_t dq_off, delta_off, sem_off, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+BwdWorkspace bwd_layout(int B, int H, int Lq, int d, bool varlen) {
+    BwdWorkspace w{};
+    const size_t rows_q = varlen ? (size_t)Lq : (size_t)B * Lq;
+    const size_t n_dq_tiles = varlen ? (size_t)H * ((size_t)Lq / 128 + (size_t)B + 1)
+                                     : (size_t)B * H * (((size_t)Lq + 127) / 128);
+    w.dq_off = 0;
+    w.delta_off = align256(rows_q * H * d * sizeof(float));
+    w.sem_off = w.delta_off + align256(rows_q * H * sizeof(float));
+    w.total = w.sem_off + align256(n_dq_tiles * sizeof(int)) + align256(sizeof(VarlenMap));
+    return w;
+}
+
+}  // namespace
+
+extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, int deterministic) {
+    (void)Lk;
+    (void)causal;
+    (void)deterministic;
+    if (B < 0 || H <= 0 || Lq < 0 || d <= 0) return 0;
+    // varlen and dense share the formula when Lq is the packed count; the
+    // varlen semaphore bound is the larger one, so take the maximum.
+    BwdWorkspace a = bwd_layout(B, H, Lq, d, false), b = bwd_layout(B, H, Lq, d, true);
+    return a.total > b.total ? a.total : b.total;
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                        float scale, int causal, const int* cu_seqlens, int deterministic, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, true);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+        return fail(ATTN_ERR_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+    const bool varlen = cu_seqlens != nullptr;
+    const long rows_q = varlen ? (long)Lq : (long)B * Lq;
+    const long rows_k = varlen ? (long)Lk : (long)B * Lk;
+    if (rows_q == 0 && rows_k == 0) return ok();
+    const size_t need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic);
+    if (!workspace || ws_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
+    DevInfo di;
+    if (!device_info(&di)) return fail(ATTN_ERR_LAUNCH, "cannot query the current device");
+    BwdWorkspace wl = bwd_layout(B, H, Lq, d, varlen);
+    char* ws = static_cast<char*>(workspace);
+    BwdParams p{};
+    p.g.B = B;
+    p.g.H = H;
+    p.g.Lq = Lq;
+    p.g.Lk = Lk;
+    p.g.d = d;
+    p.g.cu_seqlens = cu_seqlens;
+    p.g.causal = causal ? 1 : 0;
+    p.g.scale = scale;
+    p.g.scale_log2 = scale * kLog2e;
+    p.o = static_cast<const __nv_bfloat16*>(o);
+    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.lse = lse;
+    p.dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
+    p.delta = reinterpret_cast<float*>(ws + wl.delta_off);
+    p.semaphores = reinterpret_cast<int*>(ws + wl.sem_off);
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.deterministic = deterministic ? 1 : 0;
+    p.nm = (Lk + 127) / 128;
+    p.nq = (Lq + 127) / 128;
+    p.n_tiles = varlen ? 0 : B * H * p.nm;
+    p.head_section = head_section(H, varlen ? (rows_q / B) : Lq, d);
+    p.status = di.status;
+    p.wait_budget_ns = wait_budget_ns();
+    CUtensorMap tq, tk, tv, tdo;
+    const long qrows = rows_q > 0 ? rows_q : rows_k;
+    const long krows = rows_k > 0 ? rows_k : rows_q;
+    if (!make_map(&tq, rows_q > 0 ? q : k, qrows, H, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, H, d) ||
+        !make_map(&tv, rows_k > 0 ? v : q, krows, H, d) || !make_map(&tdo, rows_q > 0 ? dout : k, qrows, H, d))
+        return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    cudaError_t e = launch_bwd(tq, tk, tv, tdo, p, di.sms, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+extern "C" const char* attn_last_error(void) { return g_err; }
+
+extern "C" int attn_check_status(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "stream error: %s", cudaGetErrorString(e));
+    int st = 0;
+    e = cudaMemcpyFromSymbol(&st, g_attn_status, sizeof(int));
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cannot read the status word: %s", cudaGetErrorString(e));
+    if (st != kStatusOk) {
+        int zero = 0;
+        cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
+        if (st == kStatusMisaligned)
+            return fail(ATTN_ERR_LAUNCH, "dynamic shared memory was not 1024-byte aligned");
+        return fail(ATTN_ERR_TIMEOUT, "a kernel gave up waiting (status %d)", st);
+    }
+    return ok();
+}
+
+extern "C" int attn_version(void) { return 100; }

@@ -1,0 +1,706 @@
+// Backward pass: dQ, dK, dV of L = sum(O * dO).
+//
+// FlashAttention-4 paper, Section 3.2.2: the backward pass runs five MMAs --
+// S recomputed, dP = dO V^T, dV += P^T dO, dK += dS^T Q, dQ += dS K -- and
+// iterates along the K/V sequence dimension, computing transposed tiles
+// (S^T, P^T, dP^T, dS^T) so that the dV product can read P^T from tensor
+// memory; dQ is accumulated with global atomics. Tensor memory holds four
+// 128-column blocks: S^T (P^T written over it), dP^T (the dQ tile reuses it),
+// dV and dK. Section 3.2.4: a deterministic mode serialises every dQ tile's
+// accumulation behind a semaphore in a fixed order.
+//
+// Kernels (all on the caller's stream):
+//   bwd_prep     D_i = <dO_i, O_i> (fp32), zero the fp32 dQ accumulator and the
+//                semaphores, build the longest-first varlen map;
+//   bwd_kernel   persistent, one work tile = one 128-key block of one
+//                (batch, head); warp 0 TMA, warp 1 MMA, warps 4-11 two compute
+//                warpgroups (query columns 0-63 / 64-127 of each tile, one key
+//                row per thread), warps 12-15 read dQ tiles out of tensor
+//                memory and add them to the fp32 accumulator;
+//   bwd_convert  dQ = scale * accumulator -> bf16.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;              // query rows per Q block
+constexpr int kBN = 128;              // keys per K/V block (work tile)
+constexpr int kThreads = 512;         // 16 warps
+constexpr uint32_t kFullMask = 0xffffffffu;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBox = 16384;           // 128 rows x 64 bf16 columns
+
+template <int HD>
+struct BwdLayout {
+    static constexpr int kHalves = HD / 64;
+    static constexpr int kTileBytes = kBM * HD * 2;
+    static constexpr int kStages = HD == 64 ? 3 : 2;               // Q/dO ring
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kTileBytes;
+    static constexpr int kQOff = 2 * kTileBytes;                   // stage s: Q at +2s*tile, dO at +(2s+1)*tile
+    static constexpr int kDSOff = kQOff + kStages * 2 * kTileBytes;  // dS^T, 128 x 128 bf16
+    static constexpr int kStatOff = kDSOff + 2 * kBox;             // stage s: lse2[128], D[128]
+    static constexpr int kBarOff = kStatOff + kStages * 1024;
+    static constexpr int kKVFull = 0, kKVEmpty = 1, kQFull = 2, kQEmpty = 2 + kStages,
+                         kSFull = 2 + 2 * kStages, kSRead = kSFull + 1, kDPFull = kSRead + 1,
+                         kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,
+                         kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
+                         kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kDrain = kSemDone + 1,
+                         kNumBars = kDrain + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16;
+    // tensor memory columns
+    static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + HD;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * HD <= (int)kTmemCols, "tensor memory budget");
+};
+
+struct BwdTile {
+    int b, h, n;       // batch, head, 128-key block
+    int lq, lk;
+    int q_row0;        // packed row of query 0 of the sequence
+    int k_row0;        // packed row of key 0 of the sequence
+    int m_begin, m_end;  // 128-row query blocks that see this key block
+};
+
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+__device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
+    const Geometry& g = p.g;
+    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.H, kBN, p.head_section, false)
+                 : sched_dense(t, g.H, p.nm, p.head_section, false);
+    BwdTile f;
+    f.b = ti.b;
+    f.h = ti.h;
+    f.n = ti.m;   // ascending: for causal the smallest key blocks carry the most work
+    if (vm) {
+        const int s0 = vm->start[ti.b];
+        f.lq = f.lk = vm->start[ti.b + 1] - s0;
+        f.q_row0 = f.k_row0 = s0;
+    } else {
+        f.lq = g.Lq;
+        f.lk = g.Lk;
+        f.q_row0 = ti.b * g.Lq;
+        f.k_row0 = ti.b * g.Lk;
+    }
+    f.m_end = (f.lq + kBM - 1) / kBM;
+    f.m_begin = 0;
+    if (g.causal) {
+        // query i sees key j iff j <= i + (lk - lq): the first query block that
+        // sees the block's first key holds row n*kBN - (lk - lq)
+        f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
+    }
+    if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
+    return f;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+    return __shfl_sync(kFullMask, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    uint64_t start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - start > budget_ns) return;
+    }
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Bounded spin until *sem == target (deterministic dQ order). Acquire on success.
+__device__ __forceinline__ bool sem_wait(const int* sem, int target, const WaitCtx& w) {
+    uint64_t start = 0;
+    for (uint32_t it = 0;; ++it) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+        if (v == target) return true;
+        if ((it & 63u) == 63u) {
+            if (*w.abort_flag) return false;
+            if (*(volatile int*)w.status != kStatusOk) {
+                *w.abort_flag = 1;
+                return false;
+            }
+            uint64_t now = global_timer_ns();
+            if (start == 0) start = now;
+            else if (now - start > w.budget_ns) {
+                *w.abort_flag = 1;
+                atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Preprocess: D = rowsum(dO * O), zero the dQ accumulator and semaphores,
+// build the varlen map (block 0). One thread per (row, head).
+__global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc4, int n_sem) {
+    const Geometry& g = p.g;
+    const long stride = (long)gridDim.x * blockDim.x;
+    const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int d = g.d;
+    for (long i = tid; i < rows_q * g.H; i += stride) {
+        const long row = i / g.H;
+        const int h = (int)(i - row * g.H);
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.o + i * d);
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + i * d);
+        float acc = 0.f;
+        for (int c = 0; c < d / 8; ++c) {
+            uint4 a = o4[c], b = d4[c];
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+        }
+        long di;
+        if (g.cu_seqlens) {
+            di = (long)h * g.Lq + row;
+        } else {
+            const long b = row / g.Lq, r = row - b * g.Lq;
+            di = (b * g.H + h) * g.Lq + r;
+        }
+        p.delta[di] = acc;
+    }
+    float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+    for (long i = tid; i < n_acc4; i += stride) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = tid; i < n_sem; i += stride) p.semaphores[i] = 0;
+    if (g.cu_seqlens && blockIdx.x == 0) {
+        // longest-first map of the sequences (FlashAttention-4 paper, Section 3.3, varlen LPT)
+        const int B = g.B;
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) vm_out->start[i] = g.cu_seqlens[i];
+        __syncthreads();
+        for (int i = threadIdx.x; i < B; i += blockDim.x) {
+            const int li = vm_out->start[i + 1] - vm_out->start[i];
+            int rank = 0;
+            for (int j = 0; j < B; ++j) {
+                const int lj = vm_out->start[j + 1] - vm_out->start[j];
+                rank += (lj > li) || (lj == li && j < i);
+            }
+            vm_out->order[rank] = i;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int k = 0; k < B; ++k) {
+                vm_out->pre[k] = acc;
+                const int b = vm_out->order[k];
+                const int L = vm_out->start[b + 1] - vm_out->start[b];
+                acc += g.H * ((L + kBN - 1) / kBN);
+            }
+            vm_out->pre[B] = acc;
+        }
+    }
+}
+
+// dQ = scale * accumulator, fp32 -> bf16, 8 elements per step.
+__global__ void bwd_convert(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n8, float scale) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16x2(a.x * scale, a.y * scale);
+        o.y = pack_bf16x2(a.z * scale, a.w * scale);
+        o.z = pack_bf16x2(b.x * scale, b.y * scale);
+        o.w = pack_bf16x2(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4*>(dq)[i] = o;
+    }
+}
+
+// ----------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+           const BwdParams p, const VarlenMap* vm) {
+    using Lay = BwdLayout<HD>;
+    constexpr int NST = Lay::kStages;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t base = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Geometry& g = p.g;
+    if (base & 1023u) {   // the swizzled operand tiles need 1024-byte alignment
+        if (tid == 0) atomicCAS(p.status, kStatusOk, kStatusMisaligned);
+        return;
+    }
+    auto bar = [&](int i) -> uint32_t { return base + Lay::kBarOff + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
+
+    if (tid == 0) {
+        mbar_init(bar(Lay::kKVFull), 1);
+        mbar_init(bar(Lay::kKVEmpty), 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar(Lay::kQFull + s), 1);
+            mbar_init(bar(Lay::kQEmpty + s), 1);
+        }
+        mbar_init(bar(Lay::kSFull), 1);
+        mbar_init(bar(Lay::kSRead), 256);
+        mbar_init(bar(Lay::kDPFull), 1);
+        mbar_init(bar(Lay::kPFull), 256);
+        mbar_init(bar(Lay::kDSFull), 256);
+        mbar_init(bar(Lay::kDSEmpty), 1);
+        mbar_init(bar(Lay::kDQFull), 1);
+        mbar_init(bar(Lay::kDQFree), 128);
+        mbar_init(bar(Lay::kDKVFull), 1);
+        mbar_init(bar(Lay::kSemGo), 1);
+        mbar_init(bar(Lay::kSemDone), 128);
+        mbar_init(bar(Lay::kDrain), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmDO);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
+    const bool varlen = g.cu_seqlens != nullptr;
+    const VarlenMap* vmp = varlen ? vm : nullptr;
+    const int n_tiles = varlen ? vm->pre[g.B] : p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t tile_it = 0, qc = 0;
+        bool ok = true;
+        float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const BwdTile f = bwd_tile(t, p, vmp);
+            if (f.m_begin >= f.m_end) continue;
+            ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_expect_tx(bar(Lay::kKVFull), 2 * Lay::kTileBytes);
+                for (int hf = 0; hf < Lay::kHalves; ++hf) {
+                    tma_load_3d(base + Lay::kKOff + hf * kBox, &tmK, bar(Lay::kKVFull), hf * 64, f.h,
+                                f.k_row0 + f.n * kBN);
+                    tma_load_3d(base + Lay::kVOff + hf * kBox, &tmV, bar(Lay::kKVFull), hf * 64, f.h,
+                                f.k_row0 + f.n * kBN);
+                }
+            }
+            __syncwarp();
+            ++tile_it;
+            for (int m = f.m_begin; m < f.m_end && ok; ++m) {
+                const uint32_t st = qc % NST;
+                ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NST) & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                // row statistics for this query block: lse in log2 units and D
+                float* lse2 = stats + st * 256;
+                float* dd = lse2 + 128;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = m * kBM + lane * 4 + e;
+                    float lv = INFINITY, dv = 0.f;   // rows past the end: P = 0
+                    if (r < f.lq) {
+                        long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
+                                         : ((long)f.b * g.H + f.h) * g.Lq + r;
+                        lv = p.lse[si] * kLog2e;
+                        dv = p.delta[si];
+                    }
+                    lse2[lane * 4 + e] = lv;
+                    dd[lane * 4 + e] = dv;
+                }
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_expect_tx(bar(Lay::kQFull + st), 2 * Lay::kTileBytes);
+                    const uint32_t qa = base + Lay::kQOff + st * 2 * Lay::kTileBytes;
+                    for (int hf = 0; hf < Lay::kHalves; ++hf) {
+                        tma_load_3d(qa + hf * kBox, &tmQ, bar(Lay::kQFull + st), hf * 64, f.h, f.q_row0 + m * kBM);
+                        tma_load_3d(qa + Lay::kTileBytes + hf * kBox, &tmDO, bar(Lay::kQFull + st), hf * 64, f.h,
+                                    f.q_row0 + m * kBM);
+                    }
+                }
+                __syncwarp();
+                ++qc;
+            }
+        }
+        if (lane == 0) {
+            if (tile_it) drain_wait(bar(Lay::kKVFull), (tile_it - 1) & 1u, p.wait_budget_ns);
+            for (uint32_t i = 0; i < (uint32_t)NST && i < qc; ++i) {
+                const uint32_t n = qc - 1 - i;
+                drain_wait(bar(Lay::kQFull + n % NST), (n / NST) & 1u, p.wait_budget_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t kIdSq = idesc_bf16_f32(kBN, kBM, false, false);    // S^T, dP^T: 128 x 128
+        constexpr uint32_t kIdKV = idesc_bf16_f32(kBN, HD, false, true);      // dV, dK: 128 x d, B MN-major
+        constexpr uint32_t kIdDQ = idesc_bf16_f32(kBM, HD, true, true);       // dQ: A (dS) MN-major
+        const uint32_t k_s = base + Lay::kKOff, v_s = base + Lay::kVOff, ds_s = base + Lay::kDSOff;
+        // D[128 x 128] = A[128 x d] * B[128 x d]^T, both K-major (d contiguous)
+        auto mma_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t b) {
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {
+                const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
+                mma_ss(d_tmem, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), kIdSq, k > 0);
+            }
+        };
+        uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const BwdTile f = bwd_tile(t, p, vmp);
+            if (f.m_begin >= f.m_end) continue;
+            ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
+            if (!ok) break;
+            ++tile_it;
+            uint32_t st = qc % NST;
+            ok = warp_wait(bar(Lay::kQFull + st), (qc / NST) & 1u, w, lane);
+            if (!ok) break;
+            tc_fence_after_sync();
+            if (lane == 0) {   // S^T for the first query block
+                mma_nt(tmem + Lay::kTS, k_s, base + Lay::kQOff + st * 2 * Lay::kTileBytes);
+                tc_commit(bar(Lay::kSFull));
+            }
+            __syncwarp();
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                const uint32_t qa = base + Lay::kQOff + st * 2 * Lay::kTileBytes;
+                const uint32_t doa = qa + Lay::kTileBytes;
+                // dP^T = V dO^T into the dP/dQ block once the previous dQ tile is read out
+                ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                ++dqf;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    mma_nt(tmem + Lay::kTDP, v_s, doa);
+                    tc_commit(bar(Lay::kDPFull));
+                }
+                __syncwarp();
+                // dV += P^T dO (P^T from tensor memory)
+                ok = warp_wait(bar(Lay::kPFull), pc & 1u, w, lane);
+                if (!ok) break;
+                ++pc;
+                tc_fence_after_sync();
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < kBM / 16; ++k)
+                        mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + k * 8, sdesc_sw128(doa + k * 2048, kBox, 1024),
+                               kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                // S^T for the next query block overlaps the dS computation
+                const bool more = m + 1 < f.m_end;
+                uint32_t st_next = st;
+                if (more) {
+                    st_next = (qc + 1) % NST;
+                    ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NST) & 1u, w, lane);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
+                // the compute warps must have read S^T before it is overwritten
+                if (more) {
+                    if (lane == 0) {
+                        mma_nt(tmem + Lay::kTS, k_s, base + Lay::kQOff + st_next * 2 * Lay::kTileBytes);
+                        tc_commit(bar(Lay::kSFull));
+                    }
+                    __syncwarp();
+                }
+                // dK += dS^T Q and dQ = dS K once dS^T is in shared memory
+                ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
+                if (!ok) break;
+                ++dsc;
+                tc_fence_after_sync();
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < kBM / 16; ++k) {
+                        const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
+                        mma_ss(tmem + Lay::kTDK, sdesc_sw128(ds_s + off, 16, 1024),
+                               sdesc_sw128(qa + k * 2048, kBox, 1024), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        mma_ss(tmem + Lay::kTDP, sdesc_sw128(ds_s + k * 2048, kBox, 1024),
+                               sdesc_sw128(k_s + k * 2048, kBox, 1024), kIdDQ, k > 0 ? 1u : 0u);
+                    tc_commit(bar(Lay::kDQFull));
+                    tc_commit(bar(Lay::kQEmpty + st));
+                    tc_commit(bar(Lay::kDSEmpty));
+                    if (!more) {
+                        tc_commit(bar(Lay::kDKVFull));
+                        tc_commit(bar(Lay::kKVEmpty));
+                    }
+                }
+                __syncwarp();
+                ++qc;
+                st = st_next;
+            }
+        }
+        if (lane == 0) {
+            tc_commit(bar(Lay::kDrain));
+            drain_wait(bar(Lay::kDrain), 0, p.wait_budget_ns);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ compute warpgroups
+        const int wg = (warp - 4) >> 2;            // query columns [64*wg, 64*wg + 64)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;         // key row inside the block
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = g.scale_log2;
+        uint8_t* ds_tile = smem + Lay::kDSOff + wg * kBox;   // this warpgroup's 64 query columns
+        const float* stats = reinterpret_cast<const float*>(smem + Lay::kStatOff);
+        uint32_t sc = 0, qc = 0, dpc = 0, dsw = 0, srd = 0, tile_it = 0;
+        bool ok = true;
+        uint32_t rr[32];
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const BwdTile f = bwd_tile(t, p, vmp);
+            const int key = f.n * kBN + r;
+            const bool key_ok = key < f.lk;
+            const long krow = (long)f.k_row0 + key;
+            __nv_bfloat16* dv_ptr = p.dv + (krow * g.H + f.h) * HD + wg * (HD / 2);
+            __nv_bfloat16* dk_ptr = p.dk + (krow * g.H + f.h) * HD + wg * (HD / 2);
+            if (f.m_begin >= f.m_end) {   // no query sees this key block
+                if (key_ok) {
+#pragma unroll
+                    for (int c = 0; c < HD / 16; ++c) {
+                        reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
+                        reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                continue;
+            }
+            // query q (inside the sequence) is allowed for this key iff q_lo <= q < lq
+            const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                const uint32_t st = qc % NST;
+                ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
+                if (!ok) break;
+                ++sc;
+                ok = warp_wait(bar(Lay::kQFull + st), (qc / NST) & 1u, w, lane);   // stats visibility
+                if (!ok) break;
+                ++qc;
+                tc_fence_after_sync();
+                float pv[64];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTS + wg * 64 + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pv[c * 32 + i] = u2f(rr[i]);
+                }
+                // both warpgroups must hold their S^T columns before P^T overwrites them
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kSRead));
+                ok = warp_wait(bar(Lay::kSRead), srd & 1u, w, lane);
+                if (!ok) break;
+                ++srd;
+                tc_fence_after_sync();
+                const float* lse2 = stats + st * 256 + wg * 64;
+                const float* dd = stats + st * 256 + 128 + wg * 64;
+                const int q0 = m * kBM + wg * 64;
+                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float e = ex2_mufu(fmaf(pv[c], sl2, -lse2[c]));
+                    if (!full) {
+                        const int q = q0 + c;
+                        e = (key_ok && q >= q_lo && q < f.lq) ? e : 0.f;
+                    }
+                    pv[c] = e;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32(tmem + lane_off + Lay::kTS + wg * 32, rr);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kPFull));
+                // dS^T = P^T * (dP^T - D)
+                ok = warp_wait(bar(Lay::kDPFull), dpc & 1u, w, lane);
+                if (!ok) break;
+                ++dpc;
+                tc_fence_after_sync();
+                ok = warp_wait(bar(Lay::kDSEmpty), (dsw & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                ++dsw;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTDP + wg * 64 + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int cc = c * 32 + i + 2 * e;
+                            const float d0 = pv[cc] * (u2f(rr[i + 2 * e]) - dd[cc]);
+                            const float d1 = pv[cc + 1] * (u2f(rr[i + 2 * e + 1]) - dd[cc + 1]);
+                            w4[e] = pack_bf16x2(d0, d1);
+                        }
+                        // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)
+                        const int chunk = (c * 32 + i) >> 3;
+                        uint8_t* dst = ds_tile + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kDSFull));
+            }
+            if (!ok) break;
+            // epilogue: this warpgroup writes d/2 columns of dV and of dK for its key row
+            ok = warp_wait(bar(Lay::kDKVFull), tile_it & 1u, w, lane);
+            if (!ok) break;
+            ++tile_it;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col0 = (which ? Lay::kTDK : Lay::kTDV) + wg * (HD / 2);
+                const float mul = which ? g.scale : 1.f;
+                __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c) {
+                    tmem_ld32(tmem + lane_off + col0 + c * 32, rr);
+                    if (key_ok) {
+                        uint32_t o2[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o2[i] = pack_bf16x2(u2f(rr[2 * i]) * mul, u2f(rr[2 * i + 1]) * mul);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            d4[v4] = make_uint4(o2[4 * v4], o2[4 * v4 + 1], o2[4 * v4 + 2], o2[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ dQ read-out warpgroup
+        const int quarter = warp & 3;
+        const int rq = quarter * 32 + lane;        // query row inside the block
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const bool leader = warp == 12 && lane == 0;
+        uint32_t dqc = 0, sgo = 0, sdone = 0;
+        bool ok = true;
+        uint32_t rr[32];
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const BwdTile f = bwd_tile(t, p, vmp);
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
+                if (!ok) break;
+                ++dqc;
+                tc_fence_after_sync();
+                const int q = m * kBM + rq;
+                const bool q_ok = q < f.lq;
+                float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD;
+                int* sem = nullptr;
+                if (p.deterministic) {
+                    // dQ tile (b, h, m) takes its key blocks' contributions in ascending
+                    // block order: block n waits until n blocks have added theirs. Every
+                    // block below n also sees query block m (causal or not).
+                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    sem = p.semaphores + tile;
+                    if (leader) {
+                        sem_wait(sem, f.n, w);
+                        mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
+                    }
+                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                    ++sgo;
+                    ok = ok && !*abort_flag;
+                }
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
+                    if (q_ok && ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            red_add_v4(dst + c * 32 + i, u2f(rr[i]), u2f(rr[i + 1]), u2f(rr[i + 2]), u2f(rr[i + 3]));
+                    }
+                }
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kDQFree));
+                if (p.deterministic) {
+                    __threadfence();
+                    mbar_arrive(bar(Lay::kSemDone));
+                    if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                    ++sdone;
+                }
+                if (!ok) break;
+            }
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int HD>
+cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream) {
+    using Lay = BwdLayout<HD>;
+    const Geometry& g = p.g;
+    const bool varlen = g.cu_seqlens != nullptr;
+    const long rows_q = varlen ? (long)g.Lq : (long)g.B * g.Lq;
+    const long n_acc4 = rows_q * g.H * HD / 4;
+    const int n_sem = varlen ? g.H * ((g.Lq + kBM - 1) / kBM + g.B + 1) : g.B * g.H * p.nq;
+    // the varlen map lives right after the semaphores
+    VarlenMap* vm = reinterpret_cast<VarlenMap*>(
+        reinterpret_cast<char*>(p.semaphores) + (((size_t)n_sem * sizeof(int) + 255) & ~(size_t)255));
+    {
+        const long work = rows_q * g.H;
+        int blocks = (int)((work + 255) / 256);
+        if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+        if (blocks < 1) blocks = 1;
+        bwd_prep<<<blocks, 256, 0, stream>>>(p, vm, rows_q, n_acc4, n_sem);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    auto kern = bwd_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
+    if (grid > 0) {
+        kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, p, vm);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const long n8 = rows_q * g.H * HD / 8;
+        int blocks = (int)((n8 + 255) / 256);
+        if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+        if (blocks < 1) blocks = 1;
+        bwd_convert<<<blocks, 256, 0, stream>>>(p.dq_acc, p.dq, n8, g.scale);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace
+
+size_t bwd_varlen_map_bytes() { return sizeof(VarlenMap); }
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream) {
+    switch (p.g.d) {
+        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, p, num_sms, stream);
+        case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, p, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

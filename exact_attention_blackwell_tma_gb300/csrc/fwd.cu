@@ -1,0 +1,462 @@
+// Forward kernel: O = softmax(scale * Q K^T [+ causal mask]) V and the row
+// log-sum-exp, tile by tile, with the score tile S kept in tensor memory.
+//
+// Design (FlashAttention-4 paper, Section 3.1.2 "New pipeline for overlapping
+// MMA and softmax", Section 3.1.4 "Skipping online softmax rescaling"; blog
+// post on FA4, "Tile life cycle" and "Warp specialisation"):
+//  * each work tile is two 128-row Q tiles of one (batch, head); the MMA of one
+//    tile overlaps the softmax of the other (ping-pong);
+//  * warp roles: warp 0 issues TMA loads (Q once per tile, K/V blocks through
+//    a ring of shared-memory stages), warp 1 issues tcgen05 MMAs from one
+//    thread, warps 4-7 and 8-11 are the two softmax warpgroups (one query row
+//    per thread, so the row max needs no shuffles);
+//  * tensor memory holds S_0, S_1 (fp32, 128 columns each) and O_0, O_1
+//    (fp32, d columns each); P is written as bf16 over the first half of its
+//    S tile and read by the PV MMA straight from tensor memory;
+//  * the running max is only moved when it grows by more than kTau (log2
+//    units); the decision is warp-uniform (if any row of a warp needs it, the
+//    warp rescales). Results are unchanged because the final normalisation
+//    uses the same stale max for the sum and the output.
+// Every wait is bounded (see ptx.cuh); on a timeout the kernel records an
+// error, stops issuing work, waits (bounded) for its own copies and MMAs in
+// flight, frees its tensor memory and returns.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;            // query rows per Q tile
+constexpr int kBN = 128;            // keys per K/V block
+constexpr int kRowsPerTile = 2 * kBM;
+constexpr int kThreads = 384;       // 12 warps
+constexpr float kTau = 8.0f;        // rescale threshold, log2 units (a factor of 256)
+constexpr uint32_t kFullMask = 0xffffffffu;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBox = 16384;         // one 128-row x 64-column bf16 TMA box
+
+template <int HD>
+struct FwdLayout {
+    static constexpr int kHalves = HD / 64;             // 64-column boxes per row
+    static constexpr int kTileBytes = kBM * HD * 2;     // one 128 x HD bf16 tile
+    static constexpr int kStages = HD == 64 ? 8 : 4;    // K/V ring depth (tiles)
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    // barrier indices
+    static constexpr int kQFull = 0, kQEmpty = 1, kKVFull = 2, kKVEmpty = 2 + kStages,
+                         kSFull = 2 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2,
+                         kDrain = kOFull + 2, kNumBars = kDrain + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort flag
+    static constexpr int kMapOff = (kMiscOff + 16 + 15) / 16 * 16;
+    static constexpr int kSmemBytes = kMapOff + (int)sizeof(VarlenMap) + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemO0 = 256, kTmemO1 = 256 + HD;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * HD <= (int)kTmemCols, "tensor memory budget");
+};
+
+struct FwdTile {
+    int b, h, mp;      // batch, head, 256-row query block
+    int lq, lk;        // sequence lengths
+    int q_row0;        // packed row of the first query row of the tile
+    int k_row0;        // packed row of the first key of the sequence
+    int n_kv;          // K/V blocks to visit (0: every row is fully masked)
+};
+
+__device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
+    const Geometry& g = p.g;
+    Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0)
+                     : sched_dense(t, g.H, p.nm, p.head_section, g.causal != 0);
+    FwdTile f;
+    f.b = ti.b;
+    f.h = ti.h;
+    f.mp = ti.m;
+    if (varlen) {
+        int s0 = vm.start[ti.b];
+        f.lq = f.lk = vm.start[ti.b + 1] - s0;
+        f.q_row0 = s0 + ti.m * kRowsPerTile;
+        f.k_row0 = s0;
+    } else {
+        f.lq = g.Lq;
+        f.lk = g.Lk;
+        f.q_row0 = ti.b * g.Lq + ti.m * kRowsPerTile;
+        f.k_row0 = ti.b * g.Lk;
+    }
+    int keys = f.lk;
+    if (g.causal) {
+        int row_last = min(ti.m * kRowsPerTile + kRowsPerTile - 1, f.lq - 1);
+        keys = min(f.lk, row_last + 1 + f.lk - f.lq);   // bottom-right aligned mask
+    }
+    f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
+    return f;
+}
+
+// Lane 0 polls the barrier; the verdict is broadcast so the warp stays uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+    return __shfl_sync(kFullMask, ok, 0) != 0;
+}
+
+// Bounded wait that ignores the abort flag: used only on the way out, to let
+// copies and MMAs already issued finish before the CTA releases its memory.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    uint64_t start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - start > budget_ns) return;
+    }
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using Lay = FwdLayout<HD>;
+    constexpr int S = Lay::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Geometry& g = p.g;
+    const bool varlen = g.cu_seqlens != nullptr;
+
+    auto bar = [&](int i) -> uint32_t { return base + Lay::kBarOff + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
+    VarlenMap& vm = *reinterpret_cast<VarlenMap*>(smem + Lay::kMapOff);
+
+    if (tid == 0) {
+        mbar_init(bar(Lay::kQFull), 1);
+        mbar_init(bar(Lay::kQEmpty), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(Lay::kKVFull + s), 1);
+            mbar_init(bar(Lay::kKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(Lay::kSFull + t), 1);
+            mbar_init(bar(Lay::kPFull + t), 4 * 32);
+            mbar_init(bar(Lay::kOFull + t), 1);
+        }
+        mbar_init(bar(Lay::kDrain), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    int n_tiles = p.n_tiles;
+    if (varlen) {
+        sched_varlen_build(vm, g.cu_seqlens, g.B, g.H, kRowsPerTile, tid, kThreads);
+        n_tiles = vm.pre[g.B];
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t kv_cnt = 0, it = 0, q_issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            if (f.n_kv == 0) continue;
+            ok = warp_wait(bar(Lay::kQEmpty), (it & 1u) ^ 1u, w, lane);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_expect_tx(bar(Lay::kQFull), 2 * Lay::kTileBytes);
+                for (int tq = 0; tq < 2; ++tq)
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
+                        tma_load_3d(base + Lay::kQOff + tq * Lay::kTileBytes + hf * kBox, &tmQ,
+                                    bar(Lay::kQFull), hf * 64, f.h, f.q_row0 + tq * kBM);
+            }
+            __syncwarp();
+            ++q_issued;
+            for (int j = 0; j < f.n_kv && ok; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t slot = kv_cnt % S, ph = (kv_cnt / S) & 1u;
+                    ok = warp_wait(bar(Lay::kKVEmpty + slot), ph ^ 1u, w, lane);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_expect_tx(bar(Lay::kKVFull + slot), Lay::kTileBytes);
+                        for (int hf = 0; hf < Lay::kHalves; ++hf)
+                            tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox,
+                                        kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.h,
+                                        f.k_row0 + j * kBN);
+                    }
+                    __syncwarp();
+                    ++kv_cnt;
+                }
+            }
+            ++it;
+        }
+        if (lane == 0) {   // let issued copies land before the CTA can exit
+            if (q_issued) drain_wait(bar(Lay::kQFull), (q_issued - 1) & 1u, p.wait_budget_ns);
+            for (uint32_t i = 0; i < (uint32_t)S && i < kv_cnt; ++i) {
+                const uint32_t n = kv_cnt - 1 - i;
+                drain_wait(bar(Lay::kKVFull + n % S), (n / S) & 1u, p.wait_budget_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, HD, false, true);
+        // S_tq = Q_tq K^T: both operands K-major; 16-column K steps inside a 64-column box.
+        auto issue_s = [&](int tq, uint32_t slot) {
+            const uint32_t qa = base + Lay::kQOff + tq * Lay::kTileBytes;
+            const uint32_t ka = base + Lay::kKVOff + slot * Lay::kTileBytes;
+            const uint32_t d_tmem = tmem + (tq ? 128u : 0u);
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {
+                const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
+                mma_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdescS,
+                       k > 0);
+            }
+        };
+        // O_tq (+)= P_tq V: P (bf16, 2 per column) from tensor memory, V MN-major in shared memory.
+        auto issue_pv = [&](int tq, uint32_t slot, bool acc) {
+            const uint32_t va = base + Lay::kKVOff + slot * Lay::kTileBytes;
+            const uint32_t d_tmem = tmem + (tq ? Lay::kTmemO1 : Lay::kTmemO0);
+            const uint32_t p_tmem = tmem + (tq ? 128u : 0u);
+#pragma unroll
+            for (int k = 0; k < kBN / 16; ++k)
+                mma_ts(d_tmem, p_tmem + k * 8, sdesc_sw128(va + k * 2048, kBox, 1024), kIdescPV,
+                       (acc || k > 0) ? 1u : 0u);
+        };
+        uint32_t kv_cnt = 0, it = 0, pc0 = 0, pc1 = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            if (f.n_kv == 0) continue;
+            ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
+            if (!ok) break;
+            uint32_t slot_k = kv_cnt % S;
+            ok = warp_wait(bar(Lay::kKVFull + slot_k), (kv_cnt / S) & 1u, w, lane);
+            if (!ok) break;
+            ++kv_cnt;
+            tc_fence_after_sync();
+            if (lane == 0) {
+                issue_s(0, slot_k);
+                tc_commit(bar(Lay::kSFull + 0));
+                issue_s(1, slot_k);
+                tc_commit(bar(Lay::kSFull + 1));
+                tc_commit(bar(Lay::kKVEmpty + slot_k));
+            }
+            __syncwarp();
+            for (int j = 0; j < f.n_kv; ++j) {
+                const uint32_t slot_v = kv_cnt % S;
+                ok = warp_wait(bar(Lay::kKVFull + slot_v), (kv_cnt / S) & 1u, w, lane);
+                if (!ok) break;
+                ++kv_cnt;
+                const bool more = j + 1 < f.n_kv;
+                // tile 0: PV for block j, then S for block j+1
+                ok = warp_wait(bar(Lay::kPFull + 0), pc0 & 1u, w, lane);
+                if (!ok) break;
+                ++pc0;
+                tc_fence_after_sync();
+                if (lane == 0) issue_pv(0, slot_v, j > 0);
+                __syncwarp();
+                if (more) {
+                    slot_k = kv_cnt % S;
+                    ok = warp_wait(bar(Lay::kKVFull + slot_k), (kv_cnt / S) & 1u, w, lane);
+                    if (!ok) break;
+                    ++kv_cnt;
+                    tc_fence_after_sync();
+                    if (lane == 0) {
+                        issue_s(0, slot_k);
+                        tc_commit(bar(Lay::kSFull + 0));
+                    }
+                } else if (lane == 0) {
+                    tc_commit(bar(Lay::kOFull + 0));
+                }
+                __syncwarp();
+                // tile 1
+                ok = warp_wait(bar(Lay::kPFull + 1), pc1 & 1u, w, lane);
+                if (!ok) break;
+                ++pc1;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    issue_pv(1, slot_v, j > 0);
+                    tc_commit(bar(Lay::kKVEmpty + slot_v));
+                    if (more) {
+                        issue_s(1, slot_k);
+                        tc_commit(bar(Lay::kSFull + 1));
+                        tc_commit(bar(Lay::kKVEmpty + slot_k));
+                    } else {
+                        tc_commit(bar(Lay::kOFull + 1));
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(bar(Lay::kQEmpty));
+            __syncwarp();
+            ++it;
+        }
+        if (lane == 0) {   // every MMA issued so far must finish before tensor memory is freed
+            tc_commit(bar(Lay::kDrain));
+            drain_wait(bar(Lay::kDrain), 0, p.wait_budget_ns);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int tq = (warp - 4) >> 2;
+        const int quarter = warp & 3;                 // tensor-memory lane quarter of this warp
+        const int row_in_tile = quarter * 32 + lane;
+        const uint32_t t_s = tmem_at(tmem, quarter * 32, tq ? 128u : 0u);
+        const uint32_t t_o = tmem_at(tmem, quarter * 32, tq ? Lay::kTmemO1 : Lay::kTmemO0);
+        const float sl2 = g.scale_log2;
+        uint32_t sc = 0, it = 0;
+        bool ok = true;
+        uint32_t rr[32];
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            const int r = f.mp * kRowsPerTile + tq * kBM + row_in_tile;   // row inside the sequence
+            const bool valid = r < f.lq;
+            const long prow = (long)f.q_row0 + tq * kBM + row_in_tile;   // packed row
+            __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * HD;
+            float* lptr = varlen ? p.lse + (long)f.h * g.Lq + prow
+                                 : p.lse + ((long)f.b * g.H + f.h) * g.Lq + r;
+            if (f.n_kv == 0) {
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(optr);
+#pragma unroll
+                    for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                    *lptr = -INFINITY;
+                }
+                continue;
+            }
+            const int col_limit = g.causal ? min(f.lk, r + 1 + f.lk - f.lq) : f.lk;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < f.n_kv; ++j) {
+                ok = warp_wait(bar(Lay::kSFull + tq), sc & 1u, w, lane);
+                if (!ok) break;
+                ++sc;
+                tc_fence_after_sync();
+                float s[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    tmem_ld32(t_s + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = u2f(rr[i]);
+                }
+                const int c0 = j * kBN;
+                if (c0 + kBN > col_limit) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c0 + c >= col_limit) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < kBN; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                const bool need = m_new > m_run + kTau;
+                if (__any_sync(kFullMask, need)) {
+                    const float alpha = (m_new == -INFINITY) ? 1.f : ex2_mufu(m_run - m_new);
+                    if (j > 0) {   // O holds blocks 0..j-1 (their MMAs completed before S_j did)
+#pragma unroll
+                        for (int c = 0; c < HD / 32; ++c) {
+                            tmem_ld32(t_o + c * 32, rr);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) rr[i] = f2u(u2f(rr[i]) * alpha);
+                            tmem_st32(t_o + c * 32, rr);
+                        }
+                    }
+                    l_run *= alpha;
+                    m_run = m_new;
+                }
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {   // P columns [32*hf, 32*hf+32) hold keys [64*hf, 64*hf+64)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = ex2_mufu(fmaf(s[64 * hf + 2 * i], sl2, neg_m));
+                        const float p1 = ex2_mufu(fmaf(s[64 * hf + 2 * i + 1], sl2, neg_m));
+                        l0 += p0;
+                        l1 += p1;
+                        rr[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(t_s + 32 * hf, rr);
+                }
+                l_run += l0 + l1;
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kPFull + tq));
+            }
+            if (!ok) break;
+            ok = warp_wait(bar(Lay::kOFull + tq), it & 1u, w, lane);
+            if (!ok) break;
+            ++it;
+            tc_fence_after_sync();
+            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                tmem_ld32(t_o + c * 32, rr);
+                if (valid) {
+                    uint32_t o2[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o2[i] = pack_bf16x2(u2f(rr[2 * i]) * inv_l, u2f(rr[2 * i + 1]) * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(o2[4 * v4], o2[4 * v4 + 1], o2[4 * v4 + 2], o2[4 * v4 + 3]);
+                }
+            }
+            if (valid) *lptr = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            tc_fence_before_sync();
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int HD>
+cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FwdParams& p, int num_sms, cudaStream_t stream) {
+    using Lay = FwdLayout<HD>;
+    auto kern = fwd_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.g.cu_seqlens ? num_sms : min(p.n_tiles, num_sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int num_sms, cudaStream_t stream) {
+    switch (p.g.d) {
+        case 64: return launch_fwd_hd<64>(tq, tk, tv, p, num_sms, stream);
+        case 128: return launch_fwd_hd<128>(tq, tk, tv, p, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI host layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Problem geometry as the kernels see it. Rows are "packed": a dense tensor
+// [B, L, H, d] is viewed as [B*L, H, d], batch b starting at packed row b*L;
+// a varlen tensor [T, H, d] has sequence b starting at cu_seqlens[b].
+struct Geometry {
+    int B, H, Lq, Lk, d;      // dense: sizes; varlen: Lq = Lk = T (packed rows)
+    const int* cu_seqlens;    // device, B+1 entries, or null (dense)
+    int causal;
+    float scale;              // softmax scale (> 0)
+    float scale_log2;         // scale * log2(e)
+};
+
+struct FwdParams {
+    Geometry g;
+    __nv_bfloat16* o;         // same layout as q
+    float* lse;               // dense [B, H, Lq]; varlen [H, T]
+    int n_tiles;              // dense: exact count; varlen: computed on device
+    int nm;                   // dense: 256-row query blocks per (b, h)
+    int head_section;         // heads per L2 section (LPT walk)
+    int* status;
+    uint64_t wait_budget_ns;
+};
+
+struct BwdParams {
+    Geometry g;
+    const __nv_bfloat16* o;
+    const __nv_bfloat16* dout;
+    const float* lse;         // natural-log LSE from the forward, layout as FwdParams::lse
+    float* dq_acc;            // fp32 accumulator, layout of q
+    float* delta;             // D_i = rowsum(dO * O), layout of lse
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int* semaphores;          // deterministic mode: one counter per dQ tile, zeroed by preprocess
+    int deterministic;
+    int n_tiles;
+    int nm;                   // dense: 128-row K/V blocks per (b, h)
+    int nq;                   // dense: 128-row Q blocks per (b, h)
+    int head_section;
+    int* status;
+    uint64_t wait_budget_ns;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream);
+
+int* device_status_word();   // address of the module's device status word
+
+}  // namespace attn

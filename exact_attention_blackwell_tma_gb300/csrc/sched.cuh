@@ -1,0 +1,103 @@
+// Persistent tile scheduling: longest-processing-time-first (LPT) orders.
+//
+// FlashAttention-4 paper, Section 3.3 "Scheduling":
+//  * causal LPT: the batch is the outermost dimension; heads are split into
+//    sections whose K/V fit in L2; within a section the scheduler walks the
+//    m-blocks in reverse (longest causal rows first), and within an m-block
+//    the heads of the section;
+//  * varlen LPT: sequences are sorted by the cost of their longest work tile
+//    (descending) into a virtual-to-real batch map that the kernel walks.
+// Blog post on FA4 (qian.cx), "StaticPersistentTileScheduler": at most one
+// CTA per SM; CTA c takes tiles c, c + grid, c + 2*grid, ...
+//
+// A work tile is (b, h, m) where m indexes a block of query rows (forward:
+// a pair of 128-row Q tiles; backward: one 128-row K/V block). The same
+// closed-form walk is used for dense problems; varlen problems walk the
+// sorted sequence map built in shared memory by sched_varlen_build().
+#pragma once
+
+#include <cstdint>
+
+namespace attn {
+
+constexpr int kMaxVarlenBatch = 1024;   // sequences per varlen call (shared-memory map)
+
+struct Tile {
+    int b, h, m;   // batch (real sequence index), head, row-block index
+};
+
+// Walk position `rem` inside one batch entry with `nm` row blocks and H heads,
+// heads grouped `hs` at a time; `reverse` walks row blocks from the last.
+__device__ __forceinline__ void sched_within_batch(int rem, int nm, int H, int hs, bool reverse,
+                                                   int& h, int& m) {
+    int s = rem / (hs * nm);
+    int h0 = s * hs;
+    int sec_h = min(hs, H - h0);
+    int idx = rem - s * hs * nm;
+    int mi = idx / sec_h;
+    h = h0 + (idx - mi * sec_h);
+    m = reverse ? nm - 1 - mi : mi;
+}
+
+__device__ __forceinline__ Tile sched_dense(int t, int H, int nm, int hs, bool reverse) {
+    Tile ti;
+    int per_b = H * nm;
+    ti.b = t / per_b;
+    sched_within_batch(t - ti.b * per_b, nm, H, hs, reverse, ti.h, ti.m);
+    return ti;
+}
+
+// Shared-memory tables for a varlen problem.
+struct VarlenMap {
+    int start[kMaxVarlenBatch + 1];   // cu_seqlens copy
+    int order[kMaxVarlenBatch];       // virtual -> real sequence (longest first)
+    int pre[kMaxVarlenBatch + 1];     // prefix count of tiles in virtual order
+};
+
+// Build the map with all `nthreads` threads of the CTA; ends with __syncthreads.
+// rows_per_block: query rows per work tile; the tile count of a sequence of
+// length L is H * ceil(L / rows_per_block).
+__device__ __forceinline__ void sched_varlen_build(VarlenMap& vm, const int* cu, int B, int H,
+                                                   int rows_per_block, int tid, int nthreads) {
+    for (int i = tid; i <= B; i += nthreads) vm.start[i] = cu[i];
+    __syncthreads();
+    for (int i = tid; i < B; i += nthreads) {
+        int li = vm.start[i + 1] - vm.start[i];
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            int lj = vm.start[j + 1] - vm.start[j];
+            rank += (lj > li) || (lj == li && j < i);
+        }
+        vm.order[rank] = i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int k = 0; k < B; ++k) {
+            vm.pre[k] = acc;
+            int b = vm.order[k];
+            int L = vm.start[b + 1] - vm.start[b];
+            acc += H * ((L + rows_per_block - 1) / rows_per_block);
+        }
+        vm.pre[B] = acc;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ Tile sched_varlen(const VarlenMap& vm, int t, int B, int H, int rows_per_block,
+                                             int hs, bool reverse) {
+    int lo = 0, hi = B - 1;   // largest k with pre[k] <= t
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (vm.pre[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    Tile ti;
+    ti.b = vm.order[lo];
+    int L = vm.start[ti.b + 1] - vm.start[ti.b];
+    int nm = (L + rows_per_block - 1) / rows_per_block;
+    sched_within_batch(t - vm.pre[lo], nm, H, hs, reverse, ti.h, ti.m);
+    return ti;
+}
+
+}  // namespace attn

@@ -1,0 +1,113 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact multi-head scaled-dot-product attention
+ * (forward and backward) on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation (FlashAttention-4 paper: Abstract and Section 1 -- exact
+ * attention; Section 2.1 "Multi-head attention", empty in the page, read as the
+ * textbook definition; Section 3.2.2 -- the five backward products). For each
+ * batch entry b and head h, with s_ij = scale * <q_i, k_j>:
+ *
+ *   allowed(i, j) = j < Lk                     (causal == 0)
+ *                 = j <= i + (Lk - Lq)         (causal != 0, bottom-right aligned)
+ *   LSE_i = ln sum_{allowed j} exp(s_ij)        (natural log; -inf if no j allowed)
+ *   O_i   = sum_j exp(s_ij - LSE_i) v_j         (0 if no j allowed)
+ *   with loss L = sum(O * dO):
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i,
+ *   dS_ij = P_ij (<dO_i, v_j> - <dO_i, O_i>),   P_ij = exp(s_ij - LSE_i).
+ *
+ * Layouts (row-major, contiguous, element types given):
+ *   dense  (cu_seqlens == NULL): q, o, dq, dO  bf16 [B, Lq, H, d];
+ *                                k, v, dk, dv  bf16 [B, Lk, H, d];
+ *                                lse           fp32 [B, H, Lq].
+ *   varlen (cu_seqlens != NULL): B sequences packed back to back; Lq and Lk
+ *          are BOTH the packed row count T (they must be equal: one
+ *          cu_seqlens serves queries and keys); cu_seqlens is a DEVICE int32
+ *          array of B+1 nondecreasing offsets with cu_seqlens[0] = 0 and
+ *          cu_seqlens[B] = T; tensors are [T, H, d], lse is fp32 [H, T].
+ *          Sequence b covers rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends
+ *          only within itself. 1 <= B <= 1024.
+ *
+ * Arguments common to all calls:
+ *   d       head dimension: forward 64 or 128; backward 64 or 128.
+ *   scale   softmax scale, finite and > 0 (typically 1/sqrt(d)).
+ *   causal  0 or 1.
+ *   stream  CUDA stream the work is enqueued on; calls are asynchronous and
+ *           never synchronise the host (except attn_check_status).
+ *
+ * Ownership: every pointer is caller-owned device memory, 16-byte aligned.
+ * The library allocates no device memory; the backward pass takes a caller-
+ * provided workspace. Inputs are read-only; outputs are fully overwritten.
+ *
+ * Errors: 0 on success, else a negative code; attn_last_error() returns a
+ * thread-local message describing the last failure on the calling thread.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_OK 0
+#define ATTN_ERR_ARG (-1)          /* null pointer, unsupported d, bad sizes or scale */
+#define ATTN_ERR_ALIGN (-2)        /* a pointer is not 16-byte aligned */
+#define ATTN_ERR_LAUNCH (-3)       /* a CUDA call or kernel launch failed */
+#define ATTN_ERR_WORKSPACE (-4)    /* workspace missing or too small */
+#define ATTN_ERR_TIMEOUT (-5)      /* a kernel gave up waiting (reported by attn_check_status) */
+
+/*
+ * Forward pass: writes o and lse (see the definitions above).
+ * Tiles of 2x128 query rows run on a persistent grid (one CTA per SM) in a
+ * longest-first order (FlashAttention-4 paper, Section 3.3 "Scheduling");
+ * varlen batches are sorted longest-first on the device.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Lq, int Lk, int d, float scale, int causal,
+             const int* cu_seqlens, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this problem (same size
+ * arguments as attn_bwd; for varlen pass Lq = Lk = T). The workspace holds the
+ * fp32 dQ accumulator, the row terms D_i = <dO_i, O_i>, and the semaphores of
+ * the deterministic mode. Its contents need not be initialised.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, int deterministic);
+
+/*
+ * Backward pass: given q, k, v, the forward's o and lse, and dO, writes dq,
+ * dk, dv (bf16, layouts of q, k, v). FlashAttention-4 paper, Section 3.2:
+ * the kernel iterates over K/V blocks, recomputes S^T, keeps P^T and the
+ * dK/dV accumulators in tensor memory, and accumulates dQ with fp32 global
+ * atomics (Section 3.2.2). deterministic != 0 serialises each dQ tile's
+ * accumulation in a fixed order with semaphores so repeated calls are
+ * bit-identical (Section 3.2.4). workspace/ws_bytes: caller-owned device
+ * memory of at least attn_bwd_workspace_size(...) bytes, 256-byte aligned,
+ * not used concurrently by another call.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv,
+             int B, int H, int Lq, int Lk, int d, float scale, int causal,
+             const int* cu_seqlens, int deterministic, void* workspace, size_t ws_bytes,
+             cudaStream_t stream);
+
+/* Message for the last nonzero return code on this thread ("" if none). */
+const char* attn_last_error(void);
+
+/*
+ * Synchronises `stream`, then reports (and clears) the device status word the
+ * kernels set when a bounded wait ran out: 0 if clean, ATTN_ERR_TIMEOUT if a
+ * kernel gave up, ATTN_ERR_LAUNCH if the stream reports a CUDA error.
+ */
+int attn_check_status(cudaStream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

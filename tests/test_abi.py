@@ -1,0 +1,76 @@
+"""The C ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_blackwell_tma_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    return build.build()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_last_error",
+                     "attn_check_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    lib = ctypes.CDLL(binding.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in attn.h but not exported"
+
+
+def test_error_codes_match_header(built):
+    text = open(HEADER).read()
+    codes = dict(re.findall(r"#define (ATTN_\w+) \(?(-?\d+)\)?", text))
+    assert int(codes["ATTN_OK"]) == binding.ATTN_OK
+    assert int(codes["ATTN_ERR_ARG"]) == binding.ATTN_ERR_ARG
+    assert int(codes["ATTN_ERR_ALIGN"]) == binding.ATTN_ERR_ALIGN
+    assert int(codes["ATTN_ERR_LAUNCH"]) == binding.ATTN_ERR_LAUNCH
+    assert int(codes["ATTN_ERR_WORKSPACE"]) == binding.ATTN_ERR_WORKSPACE
+    assert int(codes["ATTN_ERR_TIMEOUT"]) == binding.ATTN_ERR_TIMEOUT
+
+
+def test_argument_errors_need_no_gpu(built):
+    """Host-side validation returns before touching the device."""
+    lib = binding.load()
+    dummy = 1 << 20   # never dereferenced: validation fails first
+    # unsupported head dim
+    assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 96, 0.1, 0, None, None) == -1
+    assert "head dim" in binding.last_error()
+    # non-positive scale
+    assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 64, 0.0, 0, None, None) == -1
+    # null pointer
+    assert lib.attn_fwd(None, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 64, 0.1, 0, None, None) == -1
+    # misaligned pointer
+    assert lib.attn_fwd(dummy + 2, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 64, 0.1, 0, None, None) == -2
+    # varlen requires Lq == Lk (both the packed row count)
+    assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 2, 1, 128, 64, 64, 0.1, 0, dummy, None) == -1
+    # backward: workspace too small
+    ws = lib.attn_bwd_workspace_size(1, 1, 128, 128, 64, 0, 0)
+    assert ws > 0
+    rc = lib.attn_bwd(*([dummy] * 9), 1, 1, 128, 128, 64, 0.1, 0, None, 0, dummy, ws - 1, None)
+    assert rc == -4
+
+
+def test_workspace_size_grows_with_problem(built):
+    lib = binding.load()
+    a = lib.attn_bwd_workspace_size(1, 16, 4096, 4096, 128, 1, 0)
+    b = lib.attn_bwd_workspace_size(4, 16, 4096, 4096, 128, 1, 0)
+    assert b > a > 4 * 16 * 4096 * 128 // 4   # at least the fp32 dQ accumulator
+    assert lib.attn_bwd_workspace_size(-1, 1, 1, 1, 64, 0, 0) == 0

@@ -1,0 +1,172 @@
+"""Backward parity: dQ, dK, dV from the CUDA path (through the C ABI) vs the
+fp64 oracle, plus the deterministic mode's bit-reproducibility.
+
+The backward consumes the forward's O and LSE from the CUDA path (as a user
+would); the oracle recomputes everything from q, k, v, dO by the definition.
+Small problems are compared over every element; the workload shapes on
+sampled query rows (dQ) and key rows (dK, dV), and over whole tensors through
+two identities that hold at any size: sum_j dV_j = sum_i dO_i and
+sum_j dK_j = 0 (rows of P sum to one; rows of dS sum to zero).
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_blackwell_tma_gb300 import binding, inputs
+from _util import assert_grad_close, oracle_bwd_subset, rel_l2, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_dense(t, causal, scale, deterministic=False):
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = binding.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=causal, scale=scale, deterministic=deterministic)
+    binding.check_status()
+    return dq, dk, dv
+
+
+def check_all(t, causal, scale, heads, what, deterministic=False):
+    dq, dk, dv = run_dense(t, causal, scale, deterministic)
+    rq, rk, rv = oracle_bwd_subset(t, scale, causal, heads=heads)
+    assert_grad_close(to64(dq[:, :, heads]), rq, f"{what} dQ")
+    assert_grad_close(to64(dk[:, :, heads]), rk, f"{what} dK")
+    assert_grad_close(to64(dv[:, :, heads]), rv, f"{what} dV")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload_full(causal, deterministic):
+    w = inputs.TINY
+    check_all(inputs.make(w), causal, w.scale, list(range(w.H)), f"tiny causal={causal}", deterministic)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [1, 77, 129, 300])
+def test_ragged_lengths_full(L, causal, d):
+    t = inputs.small(B=2, H=2, L=L, d=d, seed=21)
+    check_all(t, causal, float(np.float32(1 / np.sqrt(d))), [0, 1], f"L={L} causal={causal} d={d}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lk", [(200, 77), (77, 300), (384, 129)])
+def test_rectangular(Lq, Lk, causal):
+    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=64, seed=22)
+    check_all(t, causal, 0.125, [0, 1], f"Lq={Lq} Lk={Lk} causal={causal}")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_varlen_small_full(deterministic):
+    lens = [1, 128, 200, 513, 77, 256]
+    cu = inputs.cu_seqlens(lens)
+    T, H, d = int(cu[-1]), 2, 128
+    g = torch.Generator("cpu").manual_seed(23)
+    t = {n: torch.randn(T, H, d, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
+    cud = cu.cuda()
+    o, lse = binding.forward(q, k, v, causal=True, scale=0.1, cu_seqlens=cud)
+    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=True, scale=0.1, cu_seqlens=cud,
+                                  deterministic=deterministic)
+    binding.check_status()
+    rq, rk, rv = oracle_bwd_subset(t, 0.1, True, heads=[0, 1], cu=cu.numpy())
+    assert_grad_close(to64(dq), rq, "varlen dQ")
+    assert_grad_close(to64(dk), rk, "varlen dK")
+    assert_grad_close(to64(dv), rv, "varlen dV")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_is_bit_identical(causal):
+    t = inputs.small(B=2, H=4, L=1024, d=128, seed=24)
+    ref = run_dense(t, causal, 0.088, deterministic=True)
+    for _ in range(4):
+        again = run_dense(t, causal, 0.088, deterministic=True)
+        for a, b in zip(ref, again):
+            assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ workload shapes
+
+def _rows(L, n, seed, tail=None):
+    rng = np.random.default_rng(seed)
+    if tail is None:
+        rows = set(rng.choice(L, size=min(n, L), replace=False).tolist()) | {0, 127, 128, L - 1}
+    else:
+        rows = set((L - 1 - rng.choice(tail, size=min(n, tail), replace=False)).tolist()) | {L - 1, L - tail}
+    return sorted(r for r in rows if 0 <= r < L)
+
+
+def _identities(t, dk, dv, what):
+    """sum_j dV_j = sum_i dO_i and sum_j dK_j = 0, per batch and head, over whole tensors."""
+    sdv = dv.float().sum(dim=1)
+    sdo = t["do"].cuda().float().sum(dim=1)
+    e = rel_l2(sdv.double().cpu().numpy(), sdo.double().cpu().numpy())
+    assert e < 2e-2, f"{what}: sum dV vs sum dO rel {e:.3e}"
+    sdk = dk.float().sum(dim=1)
+    scale = dk.float().pow(2).sum(dim=1).sqrt()
+    ratio = float((sdk.norm() / scale.norm()).item())
+    assert ratio < 5e-2, f"{what}: |sum dK| / |dK| = {ratio:.3e}"
+
+
+def _workload_check(w, causal, heads, deterministic=False, tail_keys=None, kv_rows=True):
+    t = inputs.make(w)
+    dq, dk, dv = run_dense(t, causal, w.scale, deterministic)
+    qrows = _rows(w.L, 16, w.seed)
+    krows = _rows(w.L, 12, w.seed + 1, tail=tail_keys) if kv_rows else []
+    bsel = sorted({0, w.B - 1})   # first and last batch entries
+    sub = {n: t[n][bsel] for n in ("q", "k", "v", "do")}
+    rq, rk, rv = oracle_bwd_subset(sub, w.scale, causal, heads=heads, qrows=qrows, krows=krows)
+    assert_grad_close(to64(dq[bsel][:, qrows][:, :, heads]), rq[:, qrows], f"{w.name} dQ")
+    if kv_rows:
+        assert_grad_close(to64(dk[bsel][:, krows][:, :, heads]), rk[:, krows], f"{w.name} dK")
+        assert_grad_close(to64(dv[bsel][:, krows][:, :, heads]), rv[:, krows], f"{w.name} dV")
+    _identities(t, dk, dv, w.name)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_workload_b4h16l4096(causal, deterministic):
+    _workload_check(inputs.MHA4K, causal, heads=[0, 15], deterministic=deterministic)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_workload_hdsweep(d):
+    _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_workload_long(causal):
+    # causal: dK/dV sampled among the last 256 keys (cheap for the oracle);
+    # non-causal: dQ rows exactly, dK/dV through the identities over all keys
+    _workload_check(inputs.LONG, causal, heads=[7], tail_keys=256 if causal else None, kv_rows=causal)
+
+
+def test_workload_long_deterministic_repeatable():
+    w = inputs.LONG
+    t = inputs.make(w)
+    a = run_dense(t, True, w.scale, deterministic=True)
+    b = run_dense(t, True, w.scale, deterministic=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_workload_varlen():
+    w = inputs.VARLEN
+    t = inputs.make(w)
+    cu = t["cu_seqlens"]
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
+    cud = cu.cuda()
+    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale, cu_seqlens=cud)
+    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=True, scale=w.scale, cu_seqlens=cud)
+    binding.check_status()
+    lens = np.diff(cu.numpy())
+    order = np.argsort(lens)
+    for b in [int(order[0]), int(order[-1]), 5]:
+        a, L = int(cu[b]), int(lens[b])
+        sub = {n: t[n][a:a + L].unsqueeze(0) for n in ("q", "k", "v", "do")}
+        qrows = _rows(L, 10, b)
+        krows = _rows(L, 8, b + 1, tail=min(256, L))
+        rq, rk, rv = oracle_bwd_subset(sub, w.scale, True, heads=[0, 9], qrows=qrows, krows=krows)
+        assert_grad_close(to64(dq[a:a + L][qrows][:, [0, 9]])[None], rq[:, qrows], f"varlen seq {b} dQ")
+        assert_grad_close(to64(dk[a:a + L][krows][:, [0, 9]])[None], rk[:, krows], f"varlen seq {b} dK")
+        assert_grad_close(to64(dv[a:a + L][krows][:, [0, 9]])[None], rv[:, krows], f"varlen seq {b} dV")
