@@ -145,12 +145,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
                         int Lk, int d, float scale, int causal, const int* cu_seqlens, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, false);
     if (rc) return rc;
-    if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_ARG, "null tensor pointer");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
     const long rows_q = cu_seqlens ? (long)Lq : (long)B * Lq;
     const long rows_k = cu_seqlens ? (long)Lk : (long)B * Lk;
-    if (rows_q == 0) return ok();
+    if (rows_q == 0) return ok();   // nothing to compute; pointers may be null
+    if (!q || !o || !lse || (rows_k > 0 && (!k || !v))) return fail(ATTN_ERR_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
     DevInfo di;
     if (!device_info(&di)) return fail(ATTN_ERR_LAUNCH, "cannot query the current device");
     FwdParams p{};
@@ -221,15 +221,15 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                         size_t ws_bytes, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, true);
     if (rc) return rc;
+    const bool varlen = cu_seqlens != nullptr;
+    const long rows_q = varlen ? (long)Lq : (long)B * Lq;
+    const long rows_k = varlen ? (long)Lk : (long)B * Lk;
+    if (rows_q == 0 && rows_k == 0) return ok();   // nothing to compute; pointers may be null
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
         return fail(ATTN_ERR_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
-    const bool varlen = cu_seqlens != nullptr;
-    const long rows_q = varlen ? (long)Lq : (long)B * Lq;
-    const long rows_k = varlen ? (long)Lk : (long)B * Lk;
-    if (rows_q == 0 && rows_k == 0) return ok();
     const size_t need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic);
     if (!workspace || ws_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
