@@ -38,6 +38,8 @@ def _declare(lib):
     lib.attn_bwd.restype = c_int
     lib.attn_bwd.argtypes = ([c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p, c_size_t,
                                                                c_void_p])
+    lib.attn_bwd_noalloc.restype = c_int
+    lib.attn_bwd_noalloc.argtypes = [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_check_status.restype = c_int
@@ -121,6 +123,15 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, 
     return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                            _ptr(dv), B, H, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens), int(deterministic),
                            _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
+                     deterministic, stream=None) -> int:
+    """attn_bwd without a workspace: scratch comes from a fixed array inside the
+    library (for callers that cannot allocate device memory; see include/attn.h)."""
+    return load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), B, H, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens),
+                                   int(deterministic), _stream(stream))
 
 
 def attn_last_error() -> str:

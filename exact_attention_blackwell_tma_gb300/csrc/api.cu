@@ -276,6 +276,61 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return ok();
 }
 
+// ---------------------------------------------------------------- backward without allocation
+// Scratch memory for attn_bwd_noalloc: the fp32 dQ accumulator, the D_i terms,
+// the semaphores and the varlen map of one backward call. It lives in a
+// file-scope device array, so every GPU that loads this library holds it
+// until the process exits, and every call on a device shares it.
+namespace {
+
+static __device__ __align__(256) unsigned char g_bwd_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_bwd_scratch on the current device, looked up once per
+// device. The name g_bwd_scratch in host code is only a host-side stand-in,
+// never a device address, so the address must come from the runtime.
+bool scratch_address(void** out, cudaError_t* err) {
+    static std::mutex mu;
+    static void* cache[64] = {};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return false;
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_bwd_scratch);
+        if (*err != cudaSuccess) return false;
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return true;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+                                int d, float scale, int causal, const int* cu_seqlens, int deterministic,
+                                cudaStream_t stream) {
+    const size_t need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic);
+    if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
+        return fail(ATTN_ERR_WORKSPACE,
+                    "attn_bwd_noalloc: this problem needs %zu bytes of scratch but the built-in array holds %zu; "
+                    "call attn_bwd with a workspace instead",
+                    need, (size_t)ATTN_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (!scratch_address(&scratch, &e))
+        return fail(ATTN_ERR_LAUNCH, "attn_bwd_noalloc: cannot get the scratch array's device address: %s",
+                    cudaGetErrorString(e));
+    // the backward's preprocess kernel zeroes the accumulator and the semaphores on every call
+    return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens, deterministic,
+                    scratch, (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 extern "C" const char* attn_last_error(void) { return g_err; }
 
 extern "C" int attn_check_status(cudaStream_t stream) {

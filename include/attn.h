@@ -93,6 +93,34 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              const int* cu_seqlens, int deterministic, void* workspace, size_t ws_bytes,
              cudaStream_t stream);
 
+/*
+ * Backward pass that allocates nothing: the same operation, arguments and
+ * results as attn_bwd, minus the workspace. It is meant for callers that
+ * cannot hand the library device memory of its own -- for instance code
+ * running inside a host framework or serving runtime that owns the whole
+ * device memory pool (allocations outside its planner are forbidden once it
+ * runs), or a plugin that only receives the input and output pointers.
+ * (The FlashAttention-4 paper has no counterpart to this entry point.)
+ *
+ * Its scratch memory is a fixed array of ATTN_NOALLOC_SCRATCH_BYTES inside
+ * this library, which every GPU that loads the library holds until the
+ * process exits. Problems whose attn_bwd_workspace_size(...) exceeds it are
+ * rejected with ATTN_ERR_WORKSPACE (use attn_bwd with a workspace for them).
+ * It calls no cudaMalloc/cudaFree and no allocating library routine.
+ *
+ * The first call on each device looks up the array's device address (set-up
+ * done once per device, with that device current); make that first call
+ * before any stream capture. All calls on a device share the one array and
+ * it keeps the previous call's contents: each call clears what must start at
+ * zero itself, but calls that overlap on the GPU (e.g. on two streams at
+ * once) race on the array and must be serialised by the caller.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv,
+                     int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                     const int* cu_seqlens, int deterministic, cudaStream_t stream);
+
 /* Message for the last nonzero return code on this thread ("" if none). */
 const char* attn_last_error(void);
 
