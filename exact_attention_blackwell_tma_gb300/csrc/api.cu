@@ -69,6 +69,21 @@ bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d) {
     return r == CUDA_SUCCESS;
 }
 
+// The fp32 dQ accumulator [rows, H, d] for TMA reduce-adds: boxes of 128 rows x
+// 32 columns (128 bytes) with the 128-byte swizzle. Rows past `rows` are skipped.
+bool make_map_f32(CUtensorMap* m, void* ptr, long rows, int H, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct DevInfo {
     int sms = 0;
     int* status = nullptr;
@@ -265,13 +280,14 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.head_section = head_section(H, varlen ? (rows_q / B) : Lq, d);
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     const long qrows = rows_q > 0 ? rows_q : rows_k;
     const long krows = rows_k > 0 ? rows_k : rows_q;
     if (!make_map(&tq, rows_q > 0 ? q : k, qrows, H, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, H, d) ||
-        !make_map(&tv, rows_k > 0 ? v : q, krows, H, d) || !make_map(&tdo, rows_q > 0 ? dout : k, qrows, H, d))
+        !make_map(&tv, rows_k > 0 ? v : q, krows, H, d) || !make_map(&tdo, rows_q > 0 ? dout : k, qrows, H, d) ||
+        !make_map_f32(&tdq, p.dq_acc, qrows, H, d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = launch_bwd(tq, tk, tv, tdo, p, di.sms, stream);
+    cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

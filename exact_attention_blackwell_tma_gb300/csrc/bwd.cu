@@ -47,8 +47,8 @@ struct BwdLayout {
                          kSFull = 2 + 2 * kStages, kSRead = kSFull + 1, kDPFull = kSRead + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,
                          kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
-                         kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kDrain = kSemDone + 1,
-                         kNumBars = kDrain + 1;
+                         kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kStageReady = kSemDone + 1,
+                         kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory columns
@@ -225,7 +225,7 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-           const BwdParams p, const VarlenMap* vm) {
+           const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, const VarlenMap* vm) {
     using Lay = BwdLayout<HD>;
     constexpr int NST = Lay::kStages;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -258,6 +258,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
         mbar_init(bar(Lay::kSemDone), 128);
+        mbar_init(bar(Lay::kStageReady), 128);
+        mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -267,6 +269,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmDQ);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -436,7 +439,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                sdesc_sw128(k_s + k * 2048, kBox, 1024), kIdDQ, k > 0 ? 1u : 0u);
                     tc_commit(bar(Lay::kDQFull));
                     tc_commit(bar(Lay::kQEmpty + st));
-                    tc_commit(bar(Lay::kDSEmpty));
                     if (!more) {
                         tc_commit(bar(Lay::kDKVFull));
                         tc_commit(bar(Lay::kKVEmpty));
@@ -585,11 +587,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ read-out warpgroup
+        // Each dQ tile (128 query rows x d, fp32) goes from tensor memory to the
+        // global accumulator. Default: staged through shared memory (the dS^T
+        // tile, idle at this point) in 128-row x 32-column swizzled boxes and
+        // added by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic
+        // mode: per-thread vector atomics under the tile's semaphore, in key-
+        // block order. Either way the dS^T tile is handed back afterwards.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, sgo = 0, sdone = 0;
+        uint8_t* stage = smem + Lay::kDSOff;
+        const uint32_t stage_s = base + Lay::kDSOff;
+        uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -599,25 +609,62 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (!ok) break;
                 ++dqc;
                 tc_fence_after_sync();
+                if (!p.deterministic) {
+                    for (int rnd = 0; rnd < HD / 64; ++rnd) {
+                        if (rnd > 0) {
+                            ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
+                            ++sfree;
+                            if (!ok) break;
+                        }
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            tmem_ld32(tmem + lane_off + Lay::kTDP + rnd * 64 + c2 * 32, rr);
+                            uint8_t* row = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)   // 128-byte swizzle: chunk j at j ^ (row % 8)
+                                *reinterpret_cast<uint4*>(row + ((j ^ (rq & 7)) << 4)) =
+                                    make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]);
+                        }
+                        if (rnd == HD / 64 - 1) {   // tensor-memory reads done: dP^T may be overwritten
+                            tc_fence_before_sync();
+                            mbar_arrive(bar(Lay::kDQFree));
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(Lay::kStageReady));
+                        if (leader) {
+                            if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
+                                // rows past the query block's sequence carry exact zeros (P = 0 there)
+                                for (int c2 = 0; c2 < 2; ++c2)
+                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, f.h,
+                                                      f.q_row0 + m * kBM);
+                                bulk_commit_group();
+                                bulk_wait_group_read0();
+                            }
+                            mbar_arrive(bar(rnd == HD / 64 - 1 ? Lay::kDSEmpty : Lay::kStageFree));
+                        }
+                        ++srdy;
+                    }
+                    if (!ok) break;
+                    continue;
+                }
+                // deterministic: ordered per-thread atomics; the dS^T tile is not used here
+                if (leader) mbar_arrive(bar(Lay::kDSEmpty));
                 const int q = m * kBM + rq;
                 const bool q_ok = q < f.lq;
                 float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD;
-                int* sem = nullptr;
-                if (p.deterministic) {
-                    // dQ tile (b, h, m) takes its key blocks' contributions in ascending
-                    // block order: block n waits until n blocks have added theirs. Every
-                    // block below n also sees query block m (causal or not).
-                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + f.h) * p.nq + m;
-                    sem = p.semaphores + tile;
-                    if (leader) {
-                        sem_wait(sem, f.n, w);
-                        mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
-                    }
-                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
-                    ++sgo;
-                    ok = ok && !*abort_flag;
+                // dQ tile (b, h, m) takes its key blocks' contributions in ascending
+                // block order: block n waits until n blocks have added theirs. Every
+                // block below n also sees query block m (causal or not).
+                const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                         : ((long)f.b * g.H + f.h) * p.nq + m;
+                int* sem = p.semaphores + tile;
+                if (leader) {
+                    sem_wait(sem, f.n, w);
+                    mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
                 }
+                ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                ++sgo;
+                ok = ok && !*abort_flag;
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
@@ -629,16 +676,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-                if (p.deterministic) {
-                    __threadfence();
-                    mbar_arrive(bar(Lay::kSemDone));
-                    if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
-                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                    ++sdone;
-                }
+                __threadfence();
+                mbar_arrive(bar(Lay::kSemDone));
+                if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                ++sdone;
                 if (!ok) break;
             }
         }
+        if (leader) bulk_wait_group0();   // the last reduce-adds complete before the CTA exits
     }
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
@@ -651,7 +697,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
 template <int HD>
 cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
+                          cudaStream_t stream) {
     using Lay = BwdLayout<HD>;
     const Geometry& g = p.g;
     const bool varlen = g.cu_seqlens != nullptr;
@@ -675,7 +722,7 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (e != cudaSuccess) return e;
     const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
     if (grid > 0) {
-        kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, p, vm);
+        kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -695,10 +742,11 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 size_t bwd_varlen_map_bytes() { return sizeof(VarlenMap); }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
+                       cudaStream_t stream) {
     switch (p.g.d) {
-        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, p, num_sms, stream);
-        case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, p, num_sms, stream);
+        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
+        case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

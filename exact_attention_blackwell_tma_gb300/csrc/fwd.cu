@@ -35,6 +35,13 @@ constexpr float kTau = 8.0f;        // rescale threshold, log2 units (a factor o
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;         // one 128-row x 64-column bf16 TMA box
+// Register split: the kernel is compiled for 168 registers per thread
+// (384 threads, one CTA per SM); the load/MMA warpgroup gives registers up
+// and the two softmax warpgroups, which hold a 128-column score row each,
+// take them.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kRegsLoadMma = 88, kRegsSoftmax = 208;
+static_assert((kRegsLoadMma + 2 * kRegsSoftmax) * 128 <= kLaunchRegs * kThreads, "register split");
 
 template <int HD>
 struct FwdLayout {
@@ -168,6 +175,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<kRegsLoadMma>();
         uint32_t kv_cnt = 0, it = 0, q_issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -212,6 +220,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<kRegsLoadMma>();
         constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
         constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, HD, false, true);
         // S_tq = Q_tq K^T: both operands K-major; 16-column K steps inside a 64-column box.
@@ -311,8 +320,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             drain_wait(bar(Lay::kDrain), 0, p.wait_budget_ns);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        setmaxnreg_dec<kRegsLoadMma>();   // idle warps of the load/MMA warpgroup
+    } else {
         // ------------------------------------------------------------ softmax warpgroups
+        setmaxnreg_inc<kRegsSoftmax>();
         const int tq = (warp - 4) >> 2;
         const int quarter = warp & 3;                 // tensor-memory lane quarter of this warp
         const int row_in_tile = quarter * 32 + lane;
@@ -347,11 +359,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 ++sc;
                 tc_fence_after_sync();
                 float s[kBN];
+                {
+                    uint32_t r128[kBN];
+                    tmem_ld128(t_s, r128);
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    tmem_ld32(t_s + c * 32, rr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = u2f(rr[i]);
+                    for (int i = 0; i < kBN; ++i) s[i] = u2f(r128[i]);
                 }
                 const int c0 = j * kBN;
                 if (c0 + kBN > col_limit) {
@@ -442,6 +454,11 @@ cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     auto kern = fwd_kernel<HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    // the register split re-distributes exactly the registers the CTA launches with
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
     const int grid = p.g.cu_seqlens ? num_sms : min(p.n_tiles, num_sms);
     if (grid <= 0) return cudaSuccess;
     kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p);

@@ -57,7 +57,8 @@ struct BwdParams {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int num_sms, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p, int num_sms,
+                       cudaStream_t stream);
 
 int* device_status_word();   // address of the module's device status word
 
