@@ -31,6 +31,16 @@ constexpr int kThreads = 512;         // 16 warps
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;           // 128 rows x 64 bf16 columns
+// Register split: 512 threads launch with 128 registers each; the load/MMA
+// warpgroup gives 56 up and the dQ warpgroup (which holds a whole 128-column
+// dQ row) takes them; the compute warpgroups keep their 128.
+constexpr int kLaunchRegs = 128;
+constexpr uint32_t kRegsLoadMma = 72, kRegsCompute = 128, kRegsDq = 184;
+static_assert((kRegsLoadMma + 2 * kRegsCompute + kRegsDq) * 128 <= kLaunchRegs * kThreads, "register split");
+
+// TMEM column of the bf16 operand (P^T or dS^T) for the k-th 16-query step:
+// queries [64 wg, 64 wg + 64) sit in the first 32 columns of the block at 64 wg.
+__device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
 
 template <int HD>
 struct BwdLayout {
@@ -44,14 +54,17 @@ struct BwdLayout {
     static constexpr int kStatOff = kDSOff + 2 * kBox;             // stage s: lse2[128], D[128]
     static constexpr int kBarOff = kStatOff + kStages * 1024;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kQFull = 2, kQEmpty = 2 + kStages,
-                         kSFull = 2 + 2 * kStages, kSRead = kSFull + 1, kDPFull = kSRead + 1,
+                         kSFull = 2 + 2 * kStages, kDPFull = kSFull + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,
                          kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
                          kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kStageReady = kSemDone + 1,
                          kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
-    // tensor memory columns
+    // tensor memory columns. Compute warpgroup wg owns query columns
+    // [64 wg, 64 wg + 64) of the S^T and dP^T blocks and writes its bf16 P^T and
+    // dS^T (two per column) into the first 32 columns of that range, so neither
+    // warpgroup ever overwrites a column the other has yet to read.
     static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + HD;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * HD <= (int)kTmemCols, "tensor memory budget");
@@ -248,7 +261,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             mbar_init(bar(Lay::kQEmpty + s), 1);
         }
         mbar_init(bar(Lay::kSFull), 1);
-        mbar_init(bar(Lay::kSRead), 256);
         mbar_init(bar(Lay::kDPFull), 1);
         mbar_init(bar(Lay::kPFull), 256);
         mbar_init(bar(Lay::kDSFull), 256);
@@ -286,6 +298,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<kRegsLoadMma>();
         uint32_t tile_it = 0, qc = 0;
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
@@ -350,6 +363,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<kRegsLoadMma>();
         constexpr uint32_t kIdSq = idesc_bf16_f32(kBN, kBM, false, false);    // S^T, dP^T: 128 x 128
         constexpr uint32_t kIdKV = idesc_bf16_f32(kBN, HD, false, true);      // dV, dK: 128 x d, B MN-major
         constexpr uint32_t kIdDQ = idesc_bf16_f32(kBM, HD, true, true);       // dQ: A (dS) MN-major
@@ -400,8 +414,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (lane == 0) {
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
-                        mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + k * 8, sdesc_sw128(doa + k * 2048, kBox, 1024),
-                               kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
+                               sdesc_sw128(doa + k * 2048, kBox, 1024), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
                 }
                 __syncwarp();
                 // S^T for the next query block overlaps the dS computation
@@ -421,18 +435,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     }
                     __syncwarp();
                 }
-                // dK += dS^T Q and dQ = dS K once dS^T is in shared memory
+                // dK += dS^T Q (dS^T from tensor memory) and dQ = dS K (dS from shared memory)
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
                 if (!ok) break;
                 ++dsc;
                 tc_fence_after_sync();
                 if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < kBM / 16; ++k) {
-                        const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
-                        mma_ss(tmem + Lay::kTDK, sdesc_sw128(ds_s + off, 16, 1024),
+                    for (int k = 0; k < kBM / 16; ++k)
+                        mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(k),
                                sdesc_sw128(qa + k * 2048, kBox, 1024), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
-                    }
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k)
                         mma_ss(tmem + Lay::kTDP, sdesc_sw128(ds_s + k * 2048, kBox, 1024),
@@ -454,7 +466,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             drain_wait(bar(Lay::kDrain), 0, p.wait_budget_ns);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp < 4) {
+        setmaxnreg_dec<kRegsLoadMma>();   // idle warps of the load/MMA warpgroup
+    } else if (warp < 12) {
         // ------------------------------------------------------------ compute warpgroups
         const int wg = (warp - 4) >> 2;            // query columns [64*wg, 64*wg + 64)
         const int quarter = warp & 3;
@@ -463,7 +477,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const float sl2 = g.scale_log2;
         uint8_t* ds_tile = smem + Lay::kDSOff + wg * kBox;   // this warpgroup's 64 query columns
         const float* stats = reinterpret_cast<const float*>(smem + Lay::kStatOff);
-        uint32_t sc = 0, qc = 0, dpc = 0, dsw = 0, srd = 0, tile_it = 0;
+        uint32_t sc = 0, qc = 0, dpc = 0, dsw = 0, tile_it = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -501,13 +515,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int i = 0; i < 32; ++i) pv[c * 32 + i] = u2f(rr[i]);
                 }
-                // both warpgroups must hold their S^T columns before P^T overwrites them
-                tc_fence_before_sync();
-                mbar_arrive(bar(Lay::kSRead));
-                ok = warp_wait(bar(Lay::kSRead), srd & 1u, w, lane);
-                if (!ok) break;
-                ++srd;
-                tc_fence_after_sync();
                 const float* lse2 = stats + st * 256 + wg * 64;
                 const float* dd = stats + st * 256 + 128 + wg * 64;
                 const int q0 = m * kBM + wg * 64;
@@ -523,7 +530,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
-                tmem_st32(tmem + lane_off + Lay::kTS + wg * 32, rr);
+                tmem_st32(tmem + lane_off + Lay::kTS + wg * 64, rr);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kPFull));
@@ -535,25 +542,29 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 ok = warp_wait(bar(Lay::kDSEmpty), (dsw & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dsw;
+                uint32_t ds2[32];   // dS^T, two bf16 per word
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     tmem_ld32(tmem + lane_off + Lay::kTDP + wg * 64 + c * 32, rr);
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
-                        uint32_t w4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int cc = c * 32 + i + 2 * e;
                             const float d0 = pv[cc] * (u2f(rr[i + 2 * e]) - dd[cc]);
                             const float d1 = pv[cc + 1] * (u2f(rr[i + 2 * e + 1]) - dd[cc + 1]);
-                            w4[e] = pack_bf16x2(d0, d1);
+                            ds2[cc >> 1] = pack_bf16x2(d0, d1);
                         }
                         // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)
                         const int chunk = (c * 32 + i) >> 3;
                         uint8_t* dst = ds_tile + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        const int b = (c * 32 + i) >> 1;
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(ds2[b], ds2[b + 1], ds2[b + 2], ds2[b + 3]);
                     }
                 }
+                // dS^T also into tensor memory (over this warpgroup's dP^T columns, already read) for dK
+                tmem_st32(tmem + lane_off + Lay::kTDP + wg * 64, ds2);
+                tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDSFull));
@@ -585,7 +596,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             tc_fence_before_sync();
         }
-    } else if (warp >= 12) {
+    } else {
         // ------------------------------------------------------------ dQ read-out warpgroup
         // Each dQ tile (128 query rows x d, fp32) goes from tensor memory to the
         // global accumulator. Default: staged through shared memory (the dS^T
@@ -596,6 +607,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
         uint8_t* stage = smem + Lay::kDSOff;
         const uint32_t stage_s = base + Lay::kDSOff;
@@ -610,6 +622,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 ++dqc;
                 tc_fence_after_sync();
                 if (!p.deterministic) {
+                    // the whole dQ row leaves tensor memory at once, so the next dP^T can start
+                    uint32_t row[HD];
+                    if constexpr (HD == 128) {
+                        tmem_ld128(tmem + lane_off + Lay::kTDP, row);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < HD / 32; ++c) {
+                            tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
+                        }
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(Lay::kDQFree));
+#pragma unroll
                     for (int rnd = 0; rnd < HD / 64; ++rnd) {
                         if (rnd > 0) {
                             ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
@@ -618,16 +645,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         }
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2) {
-                            tmem_ld32(tmem + lane_off + Lay::kTDP + rnd * 64 + c2 * 32, rr);
-                            uint8_t* row = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+                            uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+                            const int c0 = rnd * 64 + c2 * 32;
 #pragma unroll
                             for (int j = 0; j < 8; ++j)   // 128-byte swizzle: chunk j at j ^ (row % 8)
-                                *reinterpret_cast<uint4*>(row + ((j ^ (rq & 7)) << 4)) =
-                                    make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]);
-                        }
-                        if (rnd == HD / 64 - 1) {   // tensor-memory reads done: dP^T may be overwritten
-                            tc_fence_before_sync();
-                            mbar_arrive(bar(Lay::kDQFree));
+                                *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
+                                    make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
+                                               row[c0 + 4 * j + 3]);
                         }
                         fence_proxy_async_smem();
                         mbar_arrive(bar(Lay::kStageReady));
@@ -720,6 +744,11 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     auto kern = bwd_kernel<HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    // the register split re-distributes exactly the registers the CTA launches with
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
     const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
     if (grid > 0) {
         kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
