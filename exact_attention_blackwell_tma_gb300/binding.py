@@ -76,6 +76,8 @@ def load_selftest():
             lib = ctypes.CDLL(path)
             lib.attn_selftest_mma.restype = c_int
             lib.attn_selftest_mma.argtypes = [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+            lib.attn_selftest_exp2.restype = c_int
+            lib.attn_selftest_exp2.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_void_p]
             lib.attn_selftest_wait_timeout.restype = c_int
             lib.attn_selftest_wait_timeout.argtypes = [c_void_p, ctypes.c_ulonglong, c_void_p]
             _selftest = lib

@@ -367,13 +367,26 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         constexpr uint32_t kIdSq = idesc_bf16_f32(kBN, kBM, false, false);    // S^T, dP^T: 128 x 128
         constexpr uint32_t kIdKV = idesc_bf16_f32(kBN, HD, false, true);      // dV, dK: 128 x d, B MN-major
         constexpr uint32_t kIdDQ = idesc_bf16_f32(kBM, HD, true, true);       // dQ: A (dS) MN-major
-        const uint32_t k_s = base + Lay::kKOff, v_s = base + Lay::kVOff, ds_s = base + Lay::kDSOff;
+        // Descriptors are built once; each MMA adds a compile-time offset to the low half.
+        // K-major views (d contiguous along K) and MN-major views of the same tiles.
+        const SmemDesc k_km = sdesc_sw128_split(base + Lay::kKOff, 16, 1024);
+        const SmemDesc v_km = sdesc_sw128_split(base + Lay::kVOff, 16, 1024);
+        const SmemDesc k_mn = sdesc_sw128_split(base + Lay::kKOff, kBox, 1024);
+        const SmemDesc ds_mn = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
+        const SmemDesc q_km0 = sdesc_sw128_split(base + Lay::kQOff, 16, 1024);
+        const SmemDesc q_mn0 = sdesc_sw128_split(base + Lay::kQOff, kBox, 1024);
+        constexpr uint32_t kStageStep = desc_step(2 * Lay::kTileBytes);   // next Q/dO stage
+        constexpr uint32_t kDoStep = desc_step(Lay::kTileBytes);           // dO follows Q in a stage
+        auto at_stage = [&](SmemDesc d, uint32_t stage, uint32_t extra) {
+            d.lo += stage * kStageStep + extra;
+            return d;
+        };
         // D[128 x 128] = A[128 x d] * B[128 x d]^T, both K-major (d contiguous)
-        auto mma_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t b) {
+        auto mma_nt = [&](uint32_t d_tmem, SmemDesc a, SmemDesc b) {
 #pragma unroll
             for (int k = 0; k < HD / 16; ++k) {
-                const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
-                mma_ss(d_tmem, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), kIdSq, k > 0);
+                const uint32_t off = desc_step((k >> 2) * kBox + (k & 3) * 32);
+                mma_ss(d_tmem, a, off, b, off, kIdSq, k > 0);
             }
         };
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
@@ -389,20 +402,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!ok) break;
             tc_fence_after_sync();
             if (lane == 0) {   // S^T for the first query block
-                mma_nt(tmem + Lay::kTS, k_s, base + Lay::kQOff + st * 2 * Lay::kTileBytes);
+                mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st, 0));
                 tc_commit(bar(Lay::kSFull));
             }
             __syncwarp();
             for (int m = f.m_begin; m < f.m_end; ++m) {
-                const uint32_t qa = base + Lay::kQOff + st * 2 * Lay::kTileBytes;
-                const uint32_t doa = qa + Lay::kTileBytes;
+                const SmemDesc do_km = at_stage(q_km0, st, kDoStep), do_mn = at_stage(q_mn0, st, kDoStep);
+                const SmemDesc q_mn = at_stage(q_mn0, st, 0);
                 // dP^T = V dO^T into the dP/dQ block once the previous dQ tile is read out
                 ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dqf;
                 tc_fence_after_sync();
                 if (lane == 0) {
-                    mma_nt(tmem + Lay::kTDP, v_s, doa);
+                    mma_nt(tmem + Lay::kTDP, v_km, do_km);
                     tc_commit(bar(Lay::kDPFull));
                 }
                 __syncwarp();
@@ -415,7 +428,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
                         mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
-                               sdesc_sw128(doa + k * 2048, kBox, 1024), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                               do_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
                 }
                 __syncwarp();
                 // S^T for the next query block overlaps the dS computation
@@ -430,7 +443,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 // the compute warps must have read S^T before it is overwritten
                 if (more) {
                     if (lane == 0) {
-                        mma_nt(tmem + Lay::kTS, k_s, base + Lay::kQOff + st_next * 2 * Lay::kTileBytes);
+                        mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next, 0));
                         tc_commit(bar(Lay::kSFull));
                     }
                     __syncwarp();
@@ -444,11 +457,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
                         mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(k),
-                               sdesc_sw128(qa + k * 2048, kBox, 1024), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                               q_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k)
-                        mma_ss(tmem + Lay::kTDP, sdesc_sw128(ds_s + k * 2048, kBox, 1024),
-                               sdesc_sw128(k_s + k * 2048, kBox, 1024), kIdDQ, k > 0 ? 1u : 0u);
+                        mma_ss(tmem + Lay::kTDP, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
+                               k > 0 ? 1u : 0u);
                     tc_commit(bar(Lay::kDQFull));
                     tc_commit(bar(Lay::kQEmpty + st));
                     if (!more) {

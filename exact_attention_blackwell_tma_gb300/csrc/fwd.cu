@@ -63,6 +63,40 @@ struct FwdLayout {
     static_assert(256 + 2 * HD <= (int)kTmemCols, "tensor memory budget");
 };
 
+// Partial exp2 emulation (FlashAttention-4 paper, Section 3.1.3): one pair of
+// score columns in every kPolyEvery is exponentiated by the FMA polynomial
+// instead of the MUFU unit, off on the last K/V block of each row (FA4 blog,
+// "关键实现技术"). 0 disables it, which is the default on GB300: its MUFU unit
+// runs ex2 at twice the B200 rate (31.6/clk/SM measured), and in this kernel
+// one pair in 8 emulated was 2-4% slower, one in 4 was 8-11% slower.
+#ifndef ATTN_POLY_EVERY
+#define ATTN_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = ATTN_POLY_EVERY;
+
+// P = 2^(s * sl2 - m) for one 128-column row, packed to bf16 pairs into tensor
+// memory at t_p (64 columns); the fp32 sum goes to l0 + l1.
+template <bool kEmulate>
+__device__ __forceinline__ void exp_row_to_tmem(const float (&s)[128], float sl2, float neg_m, uint32_t t_p,
+                                                float& l0, float& l1) {
+    uint32_t rr[32];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {   // P columns [32*hf, 32*hf+32) hold keys [64*hf, 64*hf+64)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float x0 = fmaf(s[64 * hf + 2 * i], sl2, neg_m);
+            const float x1 = fmaf(s[64 * hf + 2 * i + 1], sl2, neg_m);
+            const bool poly = kEmulate && kPolyEvery > 0 && (i % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
+            const float p0 = poly ? ex2_poly3(x0) : ex2_mufu(x0);
+            const float p1 = poly ? ex2_poly3(x1) : ex2_mufu(x1);
+            l0 += p0;
+            l1 += p1;
+            rr[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(t_p + 32 * hf, rr);
+    }
+}
+
 struct FwdTile {
     int b, h, mp;      // batch, head, 256-row query block
     int lq, lk;        // sequence lengths
@@ -223,27 +257,32 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         setmaxnreg_dec<kRegsLoadMma>();
         constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
         constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, HD, false, true);
+        // Descriptors are built once; each MMA adds a compile-time offset to the low half.
+        const SmemDesc q_desc[2] = {sdesc_sw128_split(base + Lay::kQOff, 16, 1024),
+                                    sdesc_sw128_split(base + Lay::kQOff + Lay::kTileBytes, 16, 1024)};
+        const SmemDesc k_desc0 = sdesc_sw128_split(base + Lay::kKVOff, 16, 1024);     // K-major
+        const SmemDesc v_desc0 = sdesc_sw128_split(base + Lay::kKVOff, kBox, 1024);   // MN-major
         // S_tq = Q_tq K^T: both operands K-major; 16-column K steps inside a 64-column box.
         auto issue_s = [&](int tq, uint32_t slot) {
-            const uint32_t qa = base + Lay::kQOff + tq * Lay::kTileBytes;
-            const uint32_t ka = base + Lay::kKVOff + slot * Lay::kTileBytes;
+            const SmemDesc qd = q_desc[tq];
+            SmemDesc kd = k_desc0;
+            kd.lo += slot * desc_step(Lay::kTileBytes);
             const uint32_t d_tmem = tmem + (tq ? 128u : 0u);
 #pragma unroll
             for (int k = 0; k < HD / 16; ++k) {
-                const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
-                mma_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdescS,
-                       k > 0);
+                const uint32_t off = desc_step((k >> 2) * kBox + (k & 3) * 32);
+                mma_ss(d_tmem, qd, off, kd, off, kIdescS, k > 0);
             }
         };
         // O_tq (+)= P_tq V: P (bf16, 2 per column) from tensor memory, V MN-major in shared memory.
         auto issue_pv = [&](int tq, uint32_t slot, bool acc) {
-            const uint32_t va = base + Lay::kKVOff + slot * Lay::kTileBytes;
+            SmemDesc vd = v_desc0;
+            vd.lo += slot * desc_step(Lay::kTileBytes);
             const uint32_t d_tmem = tmem + (tq ? Lay::kTmemO1 : Lay::kTmemO0);
             const uint32_t p_tmem = tmem + (tq ? 128u : 0u);
 #pragma unroll
             for (int k = 0; k < kBN / 16; ++k)
-                mma_ts(d_tmem, p_tmem + k * 8, sdesc_sw128(va + k * 2048, kBox, 1024), kIdescPV,
-                       (acc || k > 0) ? 1u : 0u);
+                mma_ts(d_tmem, p_tmem + k * 8, vd, desc_step(k * 2048), kIdescPV, (acc || k > 0) ? 1u : 0u);
         };
         uint32_t kv_cnt = 0, it = 0, pc0 = 0, pc1 = 0;
         bool ok = true;
@@ -263,6 +302,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 issue_s(1, slot_k);
                 tc_commit(bar(Lay::kSFull + 1));
                 tc_commit(bar(Lay::kKVEmpty + slot_k));
+                if (f.n_kv == 1) tc_commit(bar(Lay::kQEmpty));   // Q is no longer read: the next tile's may land
             }
             __syncwarp();
             for (int j = 0; j < f.n_kv; ++j) {
@@ -304,6 +344,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         issue_s(1, slot_k);
                         tc_commit(bar(Lay::kSFull + 1));
                         tc_commit(bar(Lay::kKVEmpty + slot_k));
+                        if (j + 2 == f.n_kv) tc_commit(bar(Lay::kQEmpty));   // that was the tile's last S
                     } else {
                         tc_commit(bar(Lay::kOFull + 1));
                     }
@@ -311,8 +352,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(bar(Lay::kQEmpty));
-            __syncwarp();
             ++it;
         }
         if (lane == 0) {   // every MMA issued so far must finish before tensor memory is freed
@@ -397,18 +436,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {   // P columns [32*hf, 32*hf+32) hold keys [64*hf, 64*hf+64)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2_mufu(fmaf(s[64 * hf + 2 * i], sl2, neg_m));
-                        const float p1 = ex2_mufu(fmaf(s[64 * hf + 2 * i + 1], sl2, neg_m));
-                        l0 += p0;
-                        l1 += p1;
-                        rr[i] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32(t_s + 32 * hf, rr);
-                }
+                if (j + 1 < f.n_kv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
+                else exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
                 l_run += l0 + l1;
                 tmem_st_wait();
                 tc_fence_before_sync();

@@ -208,6 +208,46 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The same descriptor split into 32-bit halves. The high half (SBO, version,
+// swizzle) is loop-invariant; the low half holds the start address (>> 4) and
+// LBO, so stepping along an operand adds (bytes >> 4) to the low half only --
+// valid while the address stays inside the 256 KB shared window, which it
+// always does. Keeping per-instruction work to one integer add matters: one
+// thread issues every MMA, and rebuilding 64-bit descriptors per instruction
+// made issue, not the tensor pipe, the limit.
+struct SmemDesc {
+    uint32_t lo, hi;
+};
+__host__ __device__ __forceinline__ SmemDesc sdesc_sw128_split(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    SmemDesc d;
+    d.lo = ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+    d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+    return d;
+}
+// Byte offset -> low-half increment.
+__host__ __device__ constexpr uint32_t desc_step(uint32_t bytes) { return bytes >> 4; }
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SmemDesc a, uint32_t a_step, SmemDesc b, uint32_t b_step,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo + a_step), "r"(a.hi), "r"(b.lo + b_step), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t b_step,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo + b_step), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // TMEM address of (lane, column).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
@@ -296,6 +336,25 @@ __device__ __forceinline__ float ex2_mufu(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x on the FMA and integer pipes, no MUFU (FlashAttention-4 paper, Section
+// 3.1.3: Cody-Waite range reduction, then a polynomial by Horner's rule).
+// x = n + f with n = floor(x), f in [0, 1): adding 1.5 * 2^23 with rounding
+// toward -inf leaves floor(x) in the low mantissa bits of t; p(f) ~ 2^f is a
+// degree-3 polynomial with p(0) = 1 (coefficients from our own relative-error
+// minimax fit, csrc/fit_exp2_poly.py; max relative error 8.6e-5); 2^n is applied
+// by adding n to the exponent field (t's low bits shifted by 23). Inputs are
+// clamped at -127, where f = 0, p = 1 and the result is exactly +0. Valid for
+// x < 128.
+__device__ __forceinline__ float ex2_poly3(float x) {
+    constexpr float kC1 = 6.951167583e-01f, kC2 = 2.276449949e-01f, kC3 = 7.706703991e-02f;
+    x = fmaxf(x, -127.f);
+    float t;
+    asm("add.rm.f32 %0, %1, %2;" : "=f"(t) : "f"(x), "f"(12582912.0f));
+    const float f = x - (t - 12582912.0f);
+    const float p = fmaf(fmaf(fmaf(kC3, f, kC2), f, kC1), f, 1.0f);
+    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
 }
 
 // Two floats to a bf16x2 word, round to nearest even; `lo` goes to the low half.

@@ -136,6 +136,14 @@ __global__ void selftest_timeout_kernel(int* status, unsigned long long budget_n
     __syncthreads();
 }
 
+// Both exp2 paths of the softmax on an array of inputs.
+__global__ void selftest_exp2_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        y_poly[i] = ex2_poly3(x[i]);
+        y_mufu[i] = ex2_mufu(x[i]);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -183,5 +191,12 @@ extern "C" int attn_selftest_mma(int mode, const void* A, const void* B, float* 
 
 extern "C" int attn_selftest_wait_timeout(int* status_dev, unsigned long long budget_ns, cudaStream_t stream) {
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(status_dev, budget_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+// y_poly = FMA-polynomial exp2(x), y_mufu = hardware exp2(x), n elements (device pointers).
+extern "C" int attn_selftest_exp2(const float* x, float* y_poly, float* y_mufu, int n, cudaStream_t stream) {
+    if (n <= 0) return 0;
+    selftest_exp2_kernel<<<(n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024, 256, 0, stream>>>(x, y_poly, y_mufu, n);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
