@@ -83,7 +83,7 @@ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b :
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
     Tile ti = vm ? sched_varlen(*vm, t, g.B, g.H, kBN, p.head_section, false)
-                 : sched_dense(t, g.H, p.nm, p.head_section, false);
+                 : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, false) : sched_dense(t, g.H, p.nm, p.head_section, false));
     BwdTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -302,7 +302,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t tile_it = 0, qc = 0;
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const BwdTile f = bwd_tile(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
@@ -391,7 +391,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         };
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const BwdTile f = bwd_tile(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
@@ -493,7 +493,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t sc = 0, qc = 0, dpc = 0, dsw = 0, tile_it = 0;
         bool ok = true;
         uint32_t rr[32];
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const BwdTile f = bwd_tile(t, p, vmp);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
@@ -627,7 +627,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const BwdTile f = bwd_tile(t, p, vmp);
             for (int m = f.m_begin; m < f.m_end; ++m) {
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);

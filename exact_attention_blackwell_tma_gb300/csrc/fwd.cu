@@ -108,7 +108,7 @@ struct FwdTile {
 __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
     const Geometry& g = p.g;
     Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0)
-                     : sched_dense(t, g.H, p.nm, p.head_section, g.causal != 0);
+                     : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, true) : sched_dense(t, g.H, p.nm, p.head_section, false));
     FwdTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -212,7 +212,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         setmaxnreg_dec<kRegsLoadMma>();
         uint32_t kv_cnt = 0, it = 0, q_issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const FwdTile f = fwd_tile(t, p, vm, varlen);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQEmpty), (it & 1u) ^ 1u, w, lane);
@@ -286,7 +286,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         };
         uint32_t kv_cnt = 0, it = 0, pc0 = 0, pc1 = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const FwdTile f = fwd_tile(t, p, vm, varlen);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
@@ -373,7 +373,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t sc = 0, it = 0;
         bool ok = true;
         uint32_t rr[32];
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const FwdTile f = fwd_tile(t, p, vm, varlen);
             const int r = f.mp * kRowsPerTile + tq * kBM + row_in_tile;   // row inside the sequence
             const bool valid = r < f.lq;
