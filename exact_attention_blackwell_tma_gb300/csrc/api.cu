@@ -133,8 +133,9 @@ int head_section(int H, long keys, int d) {
 
 int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu, bool bwd) {
     if (B < 0 || H <= 0 || Lq < 0 || Lk < 0) return fail(ATTN_ERR_ARG, "bad sizes B=%d H=%d Lq=%d Lk=%d", B, H, Lq, Lk);
-    if (d != 64 && d != 128)
-        return fail(ATTN_ERR_ARG, "head dim %d not supported by the %s pass (64, 128)", d, bwd ? "backward" : "forward");
+    if (bwd ? (d != 64 && d != 128) : (d != 64 && d != 128 && d != 192 && d != 256))
+        return fail(ATTN_ERR_ARG, "head dim %d not supported by the %s pass (%s)", d, bwd ? "backward" : "forward",
+                    bwd ? "64, 128" : "64, 128, 192, 256");
     if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_ARG, "scale must be finite and > 0");
     if (cu) {
         if (Lq != Lk) return fail(ATTN_ERR_ARG, "varlen: Lq and Lk must both be the packed row count T");
@@ -180,7 +181,10 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.g.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
-    p.nm = (Lq + 255) / 256;
+    // d <= 128: a work tile is two 128-row Q tiles; wider heads: one
+    const bool wide = d > 128;
+    const int rows_per_tile = wide ? 128 : 256;
+    p.nm = (Lq + rows_per_tile - 1) / rows_per_tile;
     p.n_tiles = cu_seqlens ? 0 : B * H * p.nm;
     p.head_section = head_section(H, cu_seqlens ? (rows_k / B) : Lk, d);
     p.status = di.status;
@@ -192,7 +196,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     const void* vp = rows_k > 0 ? v : q;
     if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, H, d) || !make_map(&tv, vp, krows, H, d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = launch_fwd(tq, tk, tv, p, di.sms, stream);
+    cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream) : launch_fwd(tq, tk, tv, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

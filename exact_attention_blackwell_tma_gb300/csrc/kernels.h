@@ -27,7 +27,7 @@ struct FwdParams {
     __nv_bfloat16* o;         // same layout as q
     float* lse;               // dense [B, H, Lq]; varlen [H, T]
     int n_tiles;              // dense: exact count; varlen: computed on device
-    int nm;                   // dense: 256-row query blocks per (b, h)
+    int nm;                   // dense: query blocks per (b, h): 256 rows (d <= 128) or 128 rows
     int head_section;         // heads per L2 section (LPT walk)
     int* status;
     uint64_t wait_budget_ns;
@@ -56,6 +56,9 @@ struct BwdParams {
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int num_sms, cudaStream_t stream);
+// Head dims 192 and 256: one 128-row Q tile per work tile (nm counts 128-row blocks).
+cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p, int num_sms,
                        cudaStream_t stream);

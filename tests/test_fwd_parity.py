@@ -32,7 +32,7 @@ def test_tiny_workload_full(causal):
     assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"tiny causal={causal}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 192, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("L", [1, 77, 128, 129, 300, 513])
 def test_ragged_lengths_full(L, causal, d):
@@ -43,39 +43,42 @@ def test_ragged_lengths_full(L, causal, d):
     assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"L={L} causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Lq,Lk", [(200, 77), (77, 300), (256, 1), (1, 256), (384, 129)])
-def test_rectangular(Lq, Lk, causal):
-    t = inputs.small(B=2, H=2, L=Lq, Lk=Lk, d=128, seed=8)
+def test_rectangular(Lq, Lk, causal, d):
+    t = inputs.small(B=2, H=2, L=Lq, Lk=Lk, d=d, seed=8)
     scale = float(np.float32(0.088))
     o, lse = run_dense(t, causal, scale)
     o_ref, lse_ref = oracle_fwd_subset(t, scale, causal, heads=[0, 1])
-    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"Lq={Lq} Lk={Lk} causal={causal}")
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"Lq={Lq} Lk={Lk} causal={causal} d={d}")
 
 
-def test_large_scores_and_rescaling():
+@pytest.mark.parametrize("d", [64, 192])
+def test_large_scores_and_rescaling(d):
     """Scores far larger than the rescale threshold, growing along the keys."""
-    t = inputs.small(B=1, H=2, L=640, d=64, seed=9)
+    t = inputs.small(B=1, H=2, L=640, d=d, seed=9)
     ramp = torch.linspace(0.2, 6.0, 640).view(1, 640, 1, 1)
     t["k"] = (t["k"].float() * ramp).to(torch.bfloat16)
     for causal in (False, True):
         o, lse = run_dense(t, causal, 0.5)
         o_ref, lse_ref = oracle_fwd_subset(t, 0.5, causal, heads=[0, 1])
-        assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"spiky causal={causal}")
+        assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"spiky causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_varlen_small_full(causal):
+def test_varlen_small_full(causal, d):
     lens = [1, 128, 200, 513, 77, 256]
     cu = inputs.cu_seqlens(lens)
-    T, H, d = int(cu[-1]), 3, 128
+    T, H = int(cu[-1]), 3
     g = torch.Generator("cpu").manual_seed(11)
     t = {n: torch.randn(T, H, d, generator=g).to(torch.bfloat16) for n in ("q", "k", "v")}
     q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
     o, lse = binding.forward(q, k, v, causal=causal, scale=0.1, cu_seqlens=cu.cuda())
     binding.check_status()
     o_ref, lse_ref = oracle_fwd_subset(t, 0.1, causal, heads=[0, 1, 2], cu=cu.numpy())
-    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"varlen causal={causal}")
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"varlen causal={causal} d={d}")
 
 
 def test_empty_batch_is_a_no_op():
@@ -85,8 +88,9 @@ def test_empty_batch_is_a_no_op():
     assert o.shape == q.shape
 
 
-def test_repeated_calls_are_identical():
-    t = inputs.small(B=1, H=2, L=700, d=128, seed=12)
+@pytest.mark.parametrize("d", [128, 192])
+def test_repeated_calls_are_identical(d):
+    t = inputs.small(B=1, H=2, L=700, d=d, seed=12)
     o1, l1 = run_dense(t, True, 0.09)
     o2, l2 = run_dense(t, True, 0.09)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
@@ -118,7 +122,7 @@ def test_workload_b4h16l4096(causal):
     _workload_check(inputs.MHA4K, causal, heads=[0, 15])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 192, 256])
 def test_workload_hdsweep(d):
     _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
 
