@@ -41,6 +41,8 @@ WORKLOADS = {
     "b4h16l4096d128": (inputs.MHA4K, (True, False)),
     "b2h16l8192d128": (inputs.HDSWEEP, (True,)),
     "b2h16l8192d64": (inputs.HDSWEEP.with_(d=64), (True,)),
+    "b2h16l8192d192": (inputs.HDSWEEP.with_(d=192), (True,)),
+    "b2h16l8192d256": (inputs.HDSWEEP.with_(d=256), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
     "b1h32l32768d128": (inputs.LONG, (True, False)),
 }

@@ -133,9 +133,9 @@ int head_section(int H, long keys, int d) {
 
 int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu, bool bwd) {
     if (B < 0 || H <= 0 || Lq < 0 || Lk < 0) return fail(ATTN_ERR_ARG, "bad sizes B=%d H=%d Lq=%d Lk=%d", B, H, Lq, Lk);
-    if (bwd ? (d != 64 && d != 128) : (d != 64 && d != 128 && d != 192 && d != 256))
-        return fail(ATTN_ERR_ARG, "head dim %d not supported by the %s pass (%s)", d, bwd ? "backward" : "forward",
-                    bwd ? "64, 128" : "64, 128, 192, 256");
+    (void)bwd;
+    if (d != 64 && d != 128 && d != 192 && d != 256)
+        return fail(ATTN_ERR_ARG, "head dim %d not supported (64, 128, 192, 256)", d);
     if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_ARG, "scale must be finite and > 0");
     if (cu) {
         if (Lq != Lk) return fail(ATTN_ERR_ARG, "varlen: Lq and Lk must both be the packed row count T");
@@ -212,12 +212,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 BwdWorkspace bwd_layout(int B, int H, int Lq, int d, bool varlen) {
     BwdWorkspace w{};
     const size_t rows_q = varlen ? (size_t)Lq : (size_t)B * Lq;
-    const size_t n_dq_tiles = varlen ? (size_t)H * ((size_t)Lq / 128 + (size_t)B + 1)
-                                     : (size_t)B * H * (((size_t)Lq + 127) / 128);
+    const size_t n_sem = (size_t)bwd_semaphore_count(B, H, Lq, varlen);
     w.dq_off = 0;
     w.delta_off = align256(rows_q * H * d * sizeof(float));
     w.sem_off = w.delta_off + align256(rows_q * H * sizeof(float));
-    w.total = w.sem_off + align256(n_dq_tiles * sizeof(int)) + align256(sizeof(VarlenMap));
+    w.total = w.sem_off + align256(n_sem * sizeof(int)) + align256(sizeof(VarlenMap));
     return w;
 }
 

@@ -28,7 +28,6 @@ namespace {
 constexpr int kBM = 128;              // query rows per Q block
 constexpr int kBN = 128;              // keys per K/V block (work tile)
 constexpr int kThreads = 512;         // 16 warps
-constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;           // 128 rows x 64 bf16 columns
 // Register split: 512 threads launch with 128 registers each; the load/MMA
@@ -107,50 +106,6 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
     }
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
     return f;
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
-    return __shfl_sync(kFullMask, ok, 0) != 0;
-}
-
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
-    uint64_t start = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - start > budget_ns) return;
-    }
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
-// Bounded spin until *sem == target (deterministic dQ order). Acquire on success.
-__device__ __forceinline__ bool sem_wait(const int* sem, int target, const WaitCtx& w) {
-    uint64_t start = 0;
-    for (uint32_t it = 0;; ++it) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
-        if (v == target) return true;
-        if ((it & 63u) == 63u) {
-            if (*w.abort_flag) return false;
-            if (*(volatile int*)w.status != kStatusOk) {
-                *w.abort_flag = 1;
-                return false;
-            }
-            uint64_t now = global_timer_ns();
-            if (start == 0) start = now;
-            else if (now - start > w.budget_ns) {
-                *w.abort_flag = 1;
-                atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
-                return false;
-            }
-        }
-    }
 }
 
 // ----------------------------------------------------------------------------
@@ -736,12 +691,11 @@ template <int HD>
 cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
                           cudaStream_t stream) {
-    using Lay = BwdLayout<HD>;
     const Geometry& g = p.g;
     const bool varlen = g.cu_seqlens != nullptr;
     const long rows_q = varlen ? (long)g.Lq : (long)g.B * g.Lq;
     const long n_acc4 = rows_q * g.H * HD / 4;
-    const int n_sem = varlen ? g.H * ((g.Lq + kBM - 1) / kBM + g.B + 1) : g.B * g.H * p.nq;
+    const int n_sem = (int)bwd_semaphore_count(g.B, g.H, g.Lq, varlen);
     // the varlen map lives right after the semaphores
     VarlenMap* vm = reinterpret_cast<VarlenMap*>(
         reinterpret_cast<char*>(p.semaphores) + (((size_t)n_sem * sizeof(int) + 255) & ~(size_t)255));
@@ -754,19 +708,26 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    auto kern = bwd_kernel<HD>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    // the register split re-distributes exactly the registers the CTA launches with
-    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
-    if (grid > 0) {
-        kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
-        e = cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    if constexpr (HD > 128) {
+        e = launch_bwd_wide(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
+    } else {
+        using Lay = BwdLayout<HD>;
+        auto kern = bwd_kernel<HD>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        // the register split re-distributes exactly the registers the CTA launches with
+        if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+        const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
+        if (grid > 0) {
+            kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
     }
     {
         const long n8 = rows_q * g.H * HD / 8;
@@ -789,6 +750,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     switch (p.g.d) {
         case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
         case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
+        case 192: return launch_bwd_hd<192>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
+        case 256: return launch_bwd_hd<256>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

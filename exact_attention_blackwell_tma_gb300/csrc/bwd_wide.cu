@@ -1,0 +1,668 @@
+// Backward main kernel for head dims 192 and 256.
+//
+// The same five MMAs, warp roles and dQ path as the d <= 128 kernel in bwd.cu
+// (FlashAttention-4 paper, Section 3.2.2), with two changes forced by the
+// on-chip budgets at these head dims:
+//  * tensor memory (512 columns) cannot hold S^T, dP^T and full-width dK and
+//    dV (2 x 128 + 2 x d > 512). A work tile is one 128-key block AND one
+//    column chunk c of dK, dV and dQ: columns [128c, 128c + CW), CW = 128, or
+//    64 for the second chunk at d = 192. Both chunks of a key block recompute
+//    the full-d contractions S^T and dP^T (1.4x the algorithmic MMA work);
+//  * shared memory (227 KB) cannot hold 128 x d tiles of K, V, Q and dO at
+//    once when d = 256. K and V stay resident for the work tile; Q and dO
+//    stream through a ring of 128-row x 128-column pieces, five per query
+//    block in consumption order: Q[o], Q[c] (S^T), dO[o], dO[c] (dP^T; dO[c]
+//    is kept for dV), then Q[c] again for dK (o = the other chunk).
+// Tensor memory: S^T at 0 (P^T over it), dP^T at 128 (dS^T over it, then the
+// dQ chunk), dV chunk at 256, dK chunk at 384. Every wait is bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;              // query rows per Q block
+constexpr int kBN = 128;              // keys per K/V block
+constexpr int kThreads = 512;         // 16 warps, roles as in bwd.cu
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBox = 16384;           // 128 rows x 64 bf16 columns
+constexpr int kPieceBytes = 2 * kBox; // 128 rows x 128 columns
+constexpr int kItemsPerBlock = 5;     // ring items per query block
+constexpr int kLaunchRegs = 128;
+constexpr uint32_t kRegsLoadMma = 72, kRegsCompute = 128, kRegsDq = 184;
+static_assert((kRegsLoadMma + 2 * kRegsCompute + kRegsDq) * 128 <= kLaunchRegs * kThreads, "register split");
+
+__device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
+
+template <int HD>
+struct WideBwdLayout {
+    static constexpr int kHalves = HD / 64;                       // 64-column boxes per row
+    static constexpr int kSlots = HD == 192 ? 3 : 2;              // Q/dO piece ring
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kHalves * kBox;
+    static constexpr int kRingOff = 2 * kHalves * kBox;
+    static constexpr int kDSOff = kRingOff + kSlots * kPieceBytes;  // dS, 128 x 128 bf16 (also dQ staging)
+    static constexpr int kStatOff = kDSOff + 2 * kBox;              // 2 stages: lse2[128], D[128]
+    static constexpr int kBarOff = kStatOff + 2 * 1024;
+    static constexpr int kKVFull = 0, kKVEmpty = 1, kRFull = 2, kREmpty = 2 + kSlots, kStatFull = 2 + 2 * kSlots,
+                         kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
+                         kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1,
+                         kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1,
+                         kStageReady = kSemDone + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
+                         kNumBars = kDrain + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16;
+    static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 384;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// 64-column boxes in piece p (128-column piece p covers boxes 2p, 2p+1).
+template <int HD>
+__device__ __forceinline__ int piece_boxes(int p) { return min(2, HD / 64 - 2 * p); }
+
+// Chunk width: columns of dK/dV/dQ that a work tile owns.
+template <int HD>
+__device__ __forceinline__ int chunk_width(int c) { return min(128, HD - 128 * c); }
+
+struct WideBwdTile {
+    int b, h, n, c;      // batch, head, 128-key block, column chunk
+    int lq, lk;
+    int q_row0, k_row0;  // packed rows of query 0 / key 0 of the sequence
+    int m_begin, m_end;  // query blocks that see this key block
+};
+
+__device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Tile t: key-block tile t/2 of the d <= 128 walk, chunk t%2 (the two chunks of
+// a key block run at the same time on neighbouring CTAs and share its loads in L2).
+__device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
+    const Geometry& g = p.g;
+    const int u = t >> 1;
+    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.H, kBN, p.head_section, false)
+                 : (g.causal ? sched_dense_lpt(u, g.B, g.H, p.nm, false)
+                             : sched_dense(u, g.H, p.nm, p.head_section, false));
+    WideBwdTile f;
+    f.b = ti.b;
+    f.h = ti.h;
+    f.n = ti.m;
+    f.c = t & 1;
+    if (vm) {
+        const int s0 = vm->start[ti.b];
+        f.lq = f.lk = vm->start[ti.b + 1] - s0;
+        f.q_row0 = f.k_row0 = s0;
+    } else {
+        f.lq = g.Lq;
+        f.lk = g.Lk;
+        f.q_row0 = ti.b * g.Lq;
+        f.k_row0 = ti.b * g.Lk;
+    }
+    f.m_end = (f.lq + kBM - 1) / kBM;
+    f.m_begin = 0;
+    if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
+    if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
+    return f;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, const VarlenMap* vm) {
+    using Lay = WideBwdLayout<HD>;
+    constexpr int NS = Lay::kSlots;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t base = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Geometry& g = p.g;
+    if (base & 1023u) {
+        if (tid == 0) atomicCAS(p.status, kStatusOk, kStatusMisaligned);
+        return;
+    }
+    auto bar = [&](int i) -> uint32_t { return base + Lay::kBarOff + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
+
+    if (tid == 0) {
+        mbar_init(bar(Lay::kKVFull), 1);
+        mbar_init(bar(Lay::kKVEmpty), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(Lay::kRFull + s), 1);
+            mbar_init(bar(Lay::kREmpty + s), 1);
+        }
+        mbar_init(bar(Lay::kStatFull + 0), 1);
+        mbar_init(bar(Lay::kStatFull + 1), 1);
+        mbar_init(bar(Lay::kSFull), 1);
+        mbar_init(bar(Lay::kDPFull), 1);
+        mbar_init(bar(Lay::kPFull), 256);
+        mbar_init(bar(Lay::kDSFull), 256);
+        mbar_init(bar(Lay::kDSEmpty), 1);
+        mbar_init(bar(Lay::kDQFull), 1);
+        mbar_init(bar(Lay::kDQFree), 128);
+        mbar_init(bar(Lay::kDKVFull), 1);
+        mbar_init(bar(Lay::kSemGo), 1);
+        mbar_init(bar(Lay::kSemDone), 128);
+        mbar_init(bar(Lay::kStageReady), 128);
+        mbar_init(bar(Lay::kStageFree), 1);
+        mbar_init(bar(Lay::kDrain), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmDQ);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
+    const bool varlen = g.cu_seqlens != nullptr;
+    const VarlenMap* vmp = varlen ? vm : nullptr;
+    const int n_tiles = 2 * (varlen ? vm->pre[g.B] : p.n_tiles);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<kRegsLoadMma>();
+        uint32_t tile_it = 0, ic = 0, qb = 0;
+        bool ok = true;
+        float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
+            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            if (f.m_begin >= f.m_end) continue;
+            ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_expect_tx(bar(Lay::kKVFull), 2 * Lay::kHalves * kBox);
+                for (int hf = 0; hf < Lay::kHalves; ++hf) {
+                    tma_load_3d(base + Lay::kKOff + hf * kBox, &tmK, bar(Lay::kKVFull), hf * 64, f.h,
+                                f.k_row0 + f.n * kBN);
+                    tma_load_3d(base + Lay::kVOff + hf * kBox, &tmV, bar(Lay::kKVFull), hf * 64, f.h,
+                                f.k_row0 + f.n * kBN);
+                }
+            }
+            __syncwarp();
+            ++tile_it;
+            const int pc = f.c, po = 1 - f.c;
+            for (int m = f.m_begin; m < f.m_end && ok; ++m) {
+                for (int item = 0; item < kItemsPerBlock; ++item) {
+                    const uint32_t slot = ic % NS;
+                    ok = warp_wait(bar(Lay::kREmpty + slot), ((ic / NS) & 1u) ^ 1u, w, lane);
+                    if (!ok) break;
+                    if (item == 0) {
+                        // row statistics of this query block (lse in log2 units, D); the
+                        // stage is free: its previous block's dS was consumed before the
+                        // ring slot just acquired could be released
+                        float* lse2 = stats + (qb & 1u) * 256;
+                        float* dd = lse2 + 128;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = m * kBM + lane * 4 + e;
+                            float lv = INFINITY, dv = 0.f;   // rows past the end: P = 0
+                            if (r < f.lq) {
+                                const long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
+                                                       : ((long)f.b * g.H + f.h) * g.Lq + r;
+                                lv = p.lse[si] * kLog2e;
+                                dv = p.delta[si];
+                            }
+                            lse2[lane * 4 + e] = lv;
+                            dd[lane * 4 + e] = dv;
+                        }
+                        __threadfence_block();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(Lay::kStatFull + (qb & 1u)));
+                    }
+                    const int piece = (item == 0 || item == 2) ? po : pc;
+                    const int nb = piece_boxes<HD>(piece);
+                    const CUtensorMap* src = (item == 2 || item == 3) ? &tmDO : &tmQ;
+                    if (lane == 0) {
+                        mbar_expect_tx(bar(Lay::kRFull + slot), nb * kBox);
+                        for (int bb = 0; bb < nb; ++bb)
+                            tma_load_3d(base + Lay::kRingOff + slot * kPieceBytes + bb * kBox, src,
+                                        bar(Lay::kRFull + slot), (2 * piece + bb) * 64, f.h, f.q_row0 + m * kBM);
+                    }
+                    __syncwarp();
+                    ++ic;
+                }
+                ++qb;
+            }
+        }
+        if (lane == 0) {
+            if (tile_it) drain_wait(bar(Lay::kKVFull), (tile_it - 1) & 1u, p.wait_budget_ns);
+            for (uint32_t i = 0; i < (uint32_t)NS && i < ic; ++i) {
+                const uint32_t n = ic - 1 - i;
+                drain_wait(bar(Lay::kRFull + n % NS), (n / NS) & 1u, p.wait_budget_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<kRegsLoadMma>();
+        constexpr uint32_t kIdSq = idesc_bf16_f32(kBN, kBM, false, false);
+        constexpr uint32_t kIdKV128 = idesc_bf16_f32(kBN, 128, false, true);
+        constexpr uint32_t kIdKV64 = idesc_bf16_f32(kBN, 64, false, true);
+        constexpr uint32_t kIdDQ128 = idesc_bf16_f32(kBM, 128, true, true);
+        constexpr uint32_t kIdDQ64 = idesc_bf16_f32(kBM, 64, true, true);
+        const SmemDesc k_km = sdesc_sw128_split(base + Lay::kKOff, 16, 1024);
+        const SmemDesc v_km = sdesc_sw128_split(base + Lay::kVOff, 16, 1024);
+        const SmemDesc k_mn = sdesc_sw128_split(base + Lay::kKOff, kBox, 1024);
+        const SmemDesc ds_mn = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
+        const SmemDesc r_km0 = sdesc_sw128_split(base + Lay::kRingOff, 16, 1024);
+        const SmemDesc r_mn0 = sdesc_sw128_split(base + Lay::kRingOff, kBox, 1024);
+        auto at_slot = [&](SmemDesc d, uint32_t slot) {
+            d.lo += slot * desc_step(kPieceBytes);
+            return d;
+        };
+        // wait for ring item `item` (global index) to land; returns its slot
+        auto item_wait = [&](uint32_t item, uint32_t& slot) -> bool {
+            slot = item % NS;
+            return warp_wait(bar(Lay::kRFull + slot), (item / NS) & 1u, w, lane);
+        };
+        // D[128 x 128] (+)= A[128 x 128c'] B^T over one piece: A = K or V boxes
+        // 2*piece.., B = the piece in ring slot `slot`; both K-major
+        auto mma_piece = [&](uint32_t d_tmem, SmemDesc a, int piece, uint32_t slot, bool acc) {
+            const SmemDesc b = at_slot(r_km0, slot);
+            const int nb = piece_boxes<HD>(piece);
+            for (int bb = 0; bb < nb; ++bb) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t a_off = desc_step((2 * piece + bb) * kBox + k * 32);
+                    const uint32_t b_off = desc_step(bb * kBox + k * 32);
+                    mma_ss(d_tmem, a, a_off, b, b_off, kIdSq, (acc || bb > 0 || k > 0) ? 1u : 0u);
+                }
+            }
+        };
+        uint32_t tile_it = 0, qb = 0, pcnt = 0, dsc = 0, dqf = 0;
+        bool ok = true;
+        // S^T of query block `blk` (its items 0 and 1)
+        auto issue_s = [&](uint32_t blk, int pc, int po) -> bool {
+            const uint32_t i0 = blk * kItemsPerBlock;
+            uint32_t s0, s1;
+            if (!item_wait(i0, s0) || !item_wait(i0 + 1, s1)) return false;
+            tc_fence_after_sync();
+            if (lane == 0) {
+                mma_piece(tmem + Lay::kTS, k_km, po, s0, false);
+                mma_piece(tmem + Lay::kTS, k_km, pc, s1, true);
+                tc_commit(bar(Lay::kSFull));
+                tc_commit(bar(Lay::kREmpty + s0));
+                tc_commit(bar(Lay::kREmpty + s1));
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
+            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            if (f.m_begin >= f.m_end) continue;
+            const int pc = f.c, po = 1 - f.c;
+            const bool narrow = chunk_width<HD>(f.c) == 64;
+            const uint32_t id_kv = narrow ? kIdKV64 : kIdKV128;
+            const uint32_t id_dq = narrow ? kIdDQ64 : kIdDQ128;
+            const SmemDesc kc_mn = [&] {   // K columns of this chunk, MN-major (B of dQ)
+                SmemDesc d = k_mn;
+                d.lo += desc_step(2 * f.c * kBox);
+                return d;
+            }();
+            ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
+            if (!ok) break;
+            ++tile_it;
+            tc_fence_after_sync();
+            ok = issue_s(qb, pc, po);
+            if (!ok) break;
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                const uint32_t i0 = qb * kItemsPerBlock;
+                const bool more = m + 1 < f.m_end;
+                // dP^T = V dO^T once the previous dQ chunk has left tensor memory
+                ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                ++dqf;
+                uint32_t s2, s3, s4;
+                ok = item_wait(i0 + 2, s2) && item_wait(i0 + 3, s3);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    mma_piece(tmem + Lay::kTDP, v_km, po, s2, false);
+                    mma_piece(tmem + Lay::kTDP, v_km, pc, s3, true);
+                    tc_commit(bar(Lay::kDPFull));
+                    tc_commit(bar(Lay::kREmpty + s2));
+                }
+                __syncwarp();
+                // dV[:, chunk] += P^T dO[:, chunk] (P^T from tensor memory)
+                ok = warp_wait(bar(Lay::kPFull), pcnt & 1u, w, lane);
+                if (!ok) break;
+                ++pcnt;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    const SmemDesc do_mn = at_slot(r_mn0, s3);
+#pragma unroll
+                    for (int kk = 0; kk < kBM / 16; ++kk)
+                        mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(kk), do_mn, desc_step(kk * 2048), id_kv,
+                               (m > f.m_begin || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(Lay::kREmpty + s3));
+                }
+                __syncwarp();
+                // with three ring slots the next S^T can overlap the dS computation
+                if (NS >= 3 && more) {
+                    ok = issue_s(qb + 1, pc, po);
+                    if (!ok) break;
+                }
+                // dK[:, chunk] += dS^T Q[:, chunk]; dQ[:, chunk] = dS K[:, chunk]
+                ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
+                if (!ok) break;
+                ++dsc;
+                ok = item_wait(i0 + 4, s4);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    const SmemDesc q_mn = at_slot(r_mn0, s4);
+#pragma unroll
+                    for (int kk = 0; kk < kBM / 16; ++kk)
+                        mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(kk), q_mn, desc_step(kk * 2048), id_kv,
+                               (m > f.m_begin || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ss(tmem + Lay::kTDP, ds_mn, desc_step(kk * 2048), kc_mn, desc_step(kk * 2048), id_dq,
+                               kk > 0 ? 1u : 0u);
+                    tc_commit(bar(Lay::kDQFull));
+                    tc_commit(bar(Lay::kREmpty + s4));
+                    if (!more) {
+                        tc_commit(bar(Lay::kDKVFull));
+                        tc_commit(bar(Lay::kKVEmpty));
+                    }
+                }
+                __syncwarp();
+                ++qb;
+                if (NS < 3 && more) {
+                    ok = issue_s(qb, pc, po);
+                    if (!ok) break;
+                }
+            }
+        }
+        if (lane == 0) {
+            tc_commit(bar(Lay::kDrain));
+            drain_wait(bar(Lay::kDrain), 0, p.wait_budget_ns);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        setmaxnreg_dec<kRegsLoadMma>();
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ compute warpgroups
+        const int wg = (warp - 4) >> 2;            // query columns [64*wg, 64*wg + 64)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;         // key row inside the block
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = g.scale_log2;
+        uint8_t* ds_tile = smem + Lay::kDSOff + wg * kBox;
+        const float* stats = reinterpret_cast<const float*>(smem + Lay::kStatOff);
+        uint32_t sc = 0, qb = 0, dpc = 0, dsw = 0, tile_it = 0;
+        bool ok = true;
+        uint32_t rr[32];
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
+            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const int cw = chunk_width<HD>(f.c);
+            const int key = f.n * kBN + r;
+            const bool key_ok = key < f.lk;
+            const long krow = (long)f.k_row0 + key;
+            const int col0 = 128 * f.c + wg * (cw / 2);   // this warpgroup's dK/dV columns
+            __nv_bfloat16* dv_ptr = p.dv + (krow * g.H + f.h) * HD + col0;
+            __nv_bfloat16* dk_ptr = p.dk + (krow * g.H + f.h) * HD + col0;
+            if (f.m_begin >= f.m_end) {   // no query sees this key block
+                if (key_ok) {
+                    for (int c = 0; c < cw / 16; ++c) {
+                        reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
+                        reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                continue;
+            }
+            const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
+                if (!ok) break;
+                ++sc;
+                ok = warp_wait(bar(Lay::kStatFull + (qb & 1u)), (qb >> 1) & 1u, w, lane);
+                if (!ok) break;
+                const uint32_t stage = qb & 1u;
+                ++qb;
+                tc_fence_after_sync();
+                float pv[64];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTS + wg * 64 + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pv[c * 32 + i] = u2f(rr[i]);
+                }
+                const float* lse2 = stats + stage * 256 + wg * 64;
+                const float* dd = stats + stage * 256 + 128 + wg * 64;
+                const int q0 = m * kBM + wg * 64;
+                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float e = ex2_mufu(fmaf(pv[c], sl2, -lse2[c]));
+                    if (!full) {
+                        const int q = q0 + c;
+                        e = (key_ok && q >= q_lo && q < f.lq) ? e : 0.f;
+                    }
+                    pv[c] = e;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32(tmem + lane_off + Lay::kTS + wg * 64, rr);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kPFull));
+                // dS^T = P^T * (dP^T - D)
+                ok = warp_wait(bar(Lay::kDPFull), dpc & 1u, w, lane);
+                if (!ok) break;
+                ++dpc;
+                tc_fence_after_sync();
+                ok = warp_wait(bar(Lay::kDSEmpty), (dsw & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                ++dsw;
+                uint32_t ds2[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTDP + wg * 64 + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int cc = c * 32 + i + 2 * e;
+                            const float d0 = pv[cc] * (u2f(rr[i + 2 * e]) - dd[cc]);
+                            const float d1 = pv[cc + 1] * (u2f(rr[i + 2 * e + 1]) - dd[cc + 1]);
+                            ds2[cc >> 1] = pack_bf16x2(d0, d1);
+                        }
+                        // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)
+                        const int chunk = (c * 32 + i) >> 3;
+                        uint8_t* dst = ds_tile + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+                        const int b = (c * 32 + i) >> 1;
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(ds2[b], ds2[b + 1], ds2[b + 2], ds2[b + 3]);
+                    }
+                }
+                tmem_st32(tmem + lane_off + Lay::kTDP + wg * 64, ds2);
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kDSFull));
+            }
+            if (!ok) break;
+            // epilogue: cw/2 columns of the dV and dK chunks for this key row
+            ok = warp_wait(bar(Lay::kDKVFull), tile_it & 1u, w, lane);
+            if (!ok) break;
+            ++tile_it;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tcol = (which ? Lay::kTDK : Lay::kTDV) + wg * (cw / 2);
+                const float mul = which ? g.scale : 1.f;
+                __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
+                for (int c = 0; c < cw / 64; ++c) {
+                    tmem_ld32(tmem + lane_off + tcol + c * 32, rr);
+                    if (key_ok) {
+                        uint32_t o2[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o2[i] = pack_bf16x2(u2f(rr[2 * i]) * mul, u2f(rr[2 * i + 1]) * mul);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            d4[v4] = make_uint4(o2[4 * v4], o2[4 * v4 + 1], o2[4 * v4 + 2], o2[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+        }
+    } else {
+        // ------------------------------------------------------------ dQ read-out warpgroup
+        // As in bwd.cu, for one column chunk: TMA reduce-adds of 128-row x
+        // 32-column boxes staged through the dS tile, or (deterministic mode)
+        // ordered per-thread vector atomics under the chunk's semaphore.
+        const int quarter = warp & 3;
+        const int rq = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        setmaxnreg_inc<kRegsDq>();
+        const bool leader = warp == 12 && lane == 0;
+        uint8_t* stage = smem + Lay::kDSOff;
+        const uint32_t stage_s = base + Lay::kDSOff;
+        uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
+        bool ok = true;
+        uint32_t rr[32];
+        for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
+            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const int cw = chunk_width<HD>(f.c);
+            const int rounds = cw / 64;
+            for (int m = f.m_begin; m < f.m_end; ++m) {
+                ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
+                if (!ok) break;
+                ++dqc;
+                tc_fence_after_sync();
+                if (!p.deterministic) {
+                    uint32_t row[128];
+                    if (rounds == 2) {
+                        tmem_ld128(tmem + lane_off + Lay::kTDP, row);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
+                        }
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(Lay::kDQFree));
+#pragma unroll
+                    for (int rnd = 0; rnd < 2; ++rnd) {
+                        if (rnd >= rounds) break;
+                        if (rnd > 0) {
+                            ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
+                            ++sfree;
+                            if (!ok) break;
+                        }
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+                            const int c0 = rnd * 64 + c2 * 32;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
+                                    make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
+                                               row[c0 + 4 * j + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(Lay::kStageReady));
+                        if (leader) {
+                            if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
+                                for (int c2 = 0; c2 < 2; ++c2)
+                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
+                                                      f.h, f.q_row0 + m * kBM);
+                                bulk_commit_group();
+                                bulk_wait_group_read0();
+                            }
+                            mbar_arrive(bar(rnd == rounds - 1 ? Lay::kDSEmpty : Lay::kStageFree));
+                        }
+                        ++srdy;
+                    }
+                    if (!ok) break;
+                    continue;
+                }
+                if (leader) mbar_arrive(bar(Lay::kDSEmpty));
+                const int q = m * kBM + rq;
+                const bool q_ok = q < f.lq;
+                float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD + 128 * f.c;
+                // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in
+                // ascending block order under its own semaphore
+                const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                         : ((long)f.b * g.H + f.h) * p.nq + m;
+                int* sem = p.semaphores + 2 * tile + f.c;
+                if (leader) {
+                    sem_wait(sem, f.n, w);
+                    mbar_arrive(bar(Lay::kSemGo));
+                }
+                ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                ++sgo;
+                ok = ok && !*abort_flag;
+                for (int c = 0; c < cw / 32; ++c) {
+                    tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
+                    if (q_ok && ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            red_add_v4(dst + c * 32 + i, u2f(rr[i]), u2f(rr[i + 1]), u2f(rr[i + 2]), u2f(rr[i + 3]));
+                    }
+                }
+                tc_fence_before_sync();
+                mbar_arrive(bar(Lay::kDQFree));
+                __threadfence();
+                mbar_arrive(bar(Lay::kSemDone));
+                if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                ++sdone;
+                if (!ok) break;
+            }
+        }
+        if (leader) bulk_wait_group0();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int HD>
+cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
+                           int num_sms, cudaStream_t stream) {
+    using Lay = WideBwdLayout<HD>;
+    auto kern = bwd_wide_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    const int grid = p.g.cu_seqlens ? num_sms : min(2 * p.n_tiles, num_sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                            const void* varlen_map, int num_sms, cudaStream_t stream) {
+    const VarlenMap* vm = static_cast<const VarlenMap*>(varlen_map);
+    switch (p.g.d) {
+        case 192: return launch_wide_hd<192>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+        case 256: return launch_wide_hd<256>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

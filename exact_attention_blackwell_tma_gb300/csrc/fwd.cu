@@ -32,7 +32,6 @@ constexpr int kBN = 128;            // keys per K/V block
 constexpr int kRowsPerTile = 2 * kBM;
 constexpr int kThreads = 384;       // 12 warps
 constexpr float kTau = 8.0f;        // rescale threshold, log2 units (a factor of 256)
-constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;         // one 128-row x 64-column bf16 TMA box
 // Register split: the kernel is compiled for 168 registers per thread
@@ -132,25 +131,6 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
     f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
     return f;
 }
-
-// Lane 0 polls the barrier; the verdict is broadcast so the warp stays uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
-    return __shfl_sync(kFullMask, ok, 0) != 0;
-}
-
-// Bounded wait that ignores the abort flag: used only on the way out, to let
-// copies and MMAs already issued finish before the CTA releases its memory.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
-    uint64_t start = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - start > budget_ns) return;
-    }
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)

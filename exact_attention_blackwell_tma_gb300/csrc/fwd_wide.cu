@@ -27,7 +27,6 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kThreads = 256;       // 8 warps: load, MMA, 2 idle, 4 softmax
 constexpr float kTau = 8.0f;
-constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;
 
@@ -88,22 +87,6 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
     f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
     return f;
 }
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
-    return __shfl_sync(kFullMask, ok, 0) != 0;
-}
-
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
-    const uint64_t start = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - start > budget_ns) return;
-    }
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -43,7 +43,7 @@ struct BwdParams {
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
-    int* semaphores;          // deterministic mode: one counter per dQ tile, zeroed by preprocess
+    int* semaphores;          // deterministic mode: two counters per dQ tile (one per column chunk)
     int deterministic;
     int n_tiles;
     int nm;                   // dense: 128-row K/V blocks per (b, h)
@@ -52,6 +52,15 @@ struct BwdParams {
     int* status;
     uint64_t wait_budget_ns;
 };
+
+// Semaphores of the deterministic backward: two per dQ tile (one per dQ column
+// chunk of the wide kernel). A varlen sequence b starting at packed row s has
+// its query block m at index s/128 + b + m < T/128 + B + 1 within a head.
+// The host layer sizes the workspace and the launcher places the varlen map
+// after the semaphores with this one count.
+inline long bwd_semaphore_count(int B, int H, int Lq, bool varlen) {
+    return 2L * (varlen ? (long)H * (Lq / 128 + B + 1) : (long)B * H * ((Lq + 127) / 128));
+}
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -62,6 +71,13 @@ cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p, int num_sms,
                        cudaStream_t stream);
+
+// Main kernel of the backward for head dims 192 and 256 (preprocess and dQ
+// conversion are shared with the d <= 128 path). varlen_map: the VarlenMap the
+// preprocess kernel builds in the workspace (read only for varlen problems).
+cudaError_t launch_bwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p,
+                            const void* varlen_map, int num_sms, cudaStream_t stream);
 
 int* device_status_word();   // address of the module's device status word
 

@@ -90,6 +90,56 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+constexpr uint32_t kFullMask = 0xffffffffu;
+
+// Lane 0 polls the barrier; the verdict is broadcast so the warp stays uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+    return __shfl_sync(kFullMask, ok, 0) != 0;
+}
+
+// Bounded wait that ignores the abort flag: used only on the way out, to let
+// copies and MMAs already issued finish before the CTA releases its memory.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    const uint64_t start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - start > budget_ns) return;
+    }
+}
+
+// Bounded spin until *sem == target (deterministic dQ order). Acquire on success.
+__device__ __forceinline__ bool sem_wait(const int* sem, int target, const WaitCtx& w) {
+    uint64_t start = 0;
+    for (uint32_t it = 0;; ++it) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+        if (v == target) return true;
+        if ((it & 63u) == 63u) {
+            if (*w.abort_flag) return false;
+            if (*(volatile int*)w.status != kStatusOk) {
+                *w.abort_flag = 1;
+                return false;
+            }
+            uint64_t now = global_timer_ns();
+            if (start == 0) start = now;
+            else if (now - start > w.budget_ns) {
+                *w.abort_flag = 1;
+                atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

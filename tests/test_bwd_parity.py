@@ -41,7 +41,7 @@ def test_tiny_workload_full(causal, deterministic):
     check_all(inputs.make(w), causal, w.scale, list(range(w.H)), f"tiny causal={causal}", deterministic)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 192, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("L", [1, 77, 129, 300])
 def test_ragged_lengths_full(L, causal, d):
@@ -49,18 +49,20 @@ def test_ragged_lengths_full(L, causal, d):
     check_all(t, causal, float(np.float32(1 / np.sqrt(d))), [0, 1], f"L={L} causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("d", [64, 192])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Lq,Lk", [(200, 77), (77, 300), (384, 129)])
-def test_rectangular(Lq, Lk, causal):
-    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=64, seed=22)
-    check_all(t, causal, 0.125, [0, 1], f"Lq={Lq} Lk={Lk} causal={causal}")
+def test_rectangular(Lq, Lk, causal, d):
+    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=d, seed=22)
+    check_all(t, causal, 0.125, [0, 1], f"Lq={Lq} Lk={Lk} causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("d", [128, 192, 256])
 @pytest.mark.parametrize("deterministic", [False, True])
-def test_varlen_small_full(deterministic):
+def test_varlen_small_full(deterministic, d):
     lens = [1, 128, 200, 513, 77, 256]
     cu = inputs.cu_seqlens(lens)
-    T, H, d = int(cu[-1]), 2, 128
+    T, H = int(cu[-1]), 2
     g = torch.Generator("cpu").manual_seed(23)
     t = {n: torch.randn(T, H, d, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
     q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
@@ -70,14 +72,15 @@ def test_varlen_small_full(deterministic):
                                   deterministic=deterministic)
     binding.check_status()
     rq, rk, rv = oracle_bwd_subset(t, 0.1, True, heads=[0, 1], cu=cu.numpy())
-    assert_grad_close(to64(dq), rq, "varlen dQ")
-    assert_grad_close(to64(dk), rk, "varlen dK")
-    assert_grad_close(to64(dv), rv, "varlen dV")
+    assert_grad_close(to64(dq), rq, f"varlen d={d} dQ")
+    assert_grad_close(to64(dk), rk, f"varlen d={d} dK")
+    assert_grad_close(to64(dv), rv, f"varlen d={d} dV")
 
 
+@pytest.mark.parametrize("d", [128, 192])
 @pytest.mark.parametrize("causal", [False, True])
-def test_deterministic_is_bit_identical(causal):
-    t = inputs.small(B=2, H=4, L=1024, d=128, seed=24)
+def test_deterministic_is_bit_identical(causal, d):
+    t = inputs.small(B=2, H=4, L=1024, d=d, seed=24)
     ref = run_dense(t, causal, 0.088, deterministic=True)
     for _ in range(4):
         again = run_dense(t, causal, 0.088, deterministic=True)
@@ -129,7 +132,7 @@ def test_workload_b4h16l4096(causal, deterministic):
     _workload_check(inputs.MHA4K, causal, heads=[0, 15], deterministic=deterministic)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 192, 256])
 def test_workload_hdsweep(d):
     _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
 
