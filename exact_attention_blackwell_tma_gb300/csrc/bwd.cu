@@ -50,7 +50,7 @@ struct BwdLayout {
     static constexpr int kVOff = kTileBytes;
     static constexpr int kQOff = 2 * kTileBytes;                   // stage s: Q at +2s*tile, dO at +(2s+1)*tile
     static constexpr int kDSOff = kQOff + kStages * 2 * kTileBytes;  // dS^T, 128 x 128 bf16
-    static constexpr int kStatOff = kDSOff + 2 * kBox;             // stage s: lse2[128], D[128]
+    static constexpr int kStatOff = kDSOff + 2 * kBox;             // stage s: -lse2[128], -D[128]
     static constexpr int kBarOff = kStatOff + kStages * 1024;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kQFull = 2, kQEmpty = 2 + kStages,
                          kSFull = 2 + 2 * kStages, kDPFull = kSFull + 1,
@@ -277,21 +277,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t st = qc % NST;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NST) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
-                // row statistics for this query block: lse in log2 units and D
-                float* lse2 = stats + st * 256;
-                float* dd = lse2 + 128;
+                // row statistics for this query block, negated: -lse in log2 units and -D
+                float* nlse2 = stats + st * 256;
+                float* ndd = nlse2 + 128;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = m * kBM + lane * 4 + e;
-                    float lv = INFINITY, dv = 0.f;   // rows past the end: P = 0
+                    float lv = -INFINITY, dv = 0.f;   // negated; rows past the end: P = 0
                     if (r < f.lq) {
                         long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
                                          : ((long)f.b * g.H + f.h) * g.Lq + r;
-                        lv = p.lse[si] * kLog2e;
-                        dv = p.delta[si];
+                        lv = -p.lse[si] * kLog2e;
+                        dv = -p.delta[si];
                     }
-                    lse2[lane * 4 + e] = lv;
-                    dd[lane * 4 + e] = dv;
+                    nlse2[lane * 4 + e] = lv;
+                    ndd[lane * 4 + e] = dv;
                 }
                 __threadfence_block();
                 __syncwarp();
@@ -386,7 +386,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                do_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
                 }
                 __syncwarp();
-                // S^T for the next query block overlaps the dS computation
                 const bool more = m + 1 < f.m_end;
                 uint32_t st_next = st;
                 if (more) {
@@ -394,14 +393,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NST) & 1u, w, lane);
                     if (!ok) break;
                     tc_fence_after_sync();
-                }
-                // the compute warps must have read S^T before it is overwritten
-                if (more) {
-                    if (lane == 0) {
-                        mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next, 0));
-                        tc_commit(bar(Lay::kSFull));
-                    }
-                    __syncwarp();
                 }
                 // dK += dS^T Q (dS^T from tensor memory) and dQ = dS K (dS from shared memory)
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
@@ -425,6 +416,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     }
                 }
                 __syncwarp();
+                // S^T of the next query block only now; it overwrites P^T, which the
+                // dV MMA issued before it has consumed. Issued ahead of dK/dQ it
+                // delayed the dQ read-out and the next dP^T behind it (3-4% slower).
+                if (more) {
+                    if (lane == 0) {
+                        mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next, 0));
+                        tc_commit(bar(Lay::kSFull));
+                    }
+                    __syncwarp();
+                }
                 ++qc;
                 st = st_next;
             }
@@ -483,18 +484,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int i = 0; i < 32; ++i) pv[c * 32 + i] = u2f(rr[i]);
                 }
-                const float* lse2 = stats + st * 256 + wg * 64;
-                const float* dd = stats + st * 256 + 128 + wg * 64;
+                // the producer stages -lse (log2 units) and -D, so both steps are packed fp32 pairs
+                const float* nlse2 = stats + st * 256 + wg * 64;
+                const float* ndd = stats + st * 256 + 128 + wg * 64;
                 const int q0 = m * kBM + wg * 64;
                 const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+                const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float e = ex2_mufu(fmaf(pv[c], sl2, -lse2[c]));
+                for (int c = 0; c < 64; c += 2) {
+                    const float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+                    float x0, x1;
+                    f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sc2, f32x2(nl.x, nl.y)), x0, x1);
+                    float e0 = ex2_mufu(x0), e1 = ex2_mufu(x1);
                     if (!full) {
                         const int q = q0 + c;
-                        e = (key_ok && q >= q_lo && q < f.lq) ? e : 0.f;
+                        e0 = (key_ok && q >= q_lo && q < f.lq) ? e0 : 0.f;
+                        e1 = (key_ok && q + 1 >= q_lo && q + 1 < f.lq) ? e1 : 0.f;
                     }
-                    pv[c] = e;
+                    pv[c] = e0;
+                    pv[c + 1] = e1;
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
@@ -519,8 +527,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int cc = c * 32 + i + 2 * e;
-                            const float d0 = pv[cc] * (u2f(rr[i + 2 * e]) - dd[cc]);
-                            const float d1 = pv[cc + 1] * (u2f(rr[i + 2 * e + 1]) - dd[cc + 1]);
+                            const float2 nd = *reinterpret_cast<const float2*>(ndd + cc);
+                            float d0, d1;
+                            f32x2_split(fmul2(f32x2(pv[cc], pv[cc + 1]),
+                                              fadd2(f32x2(u2f(rr[i + 2 * e]), u2f(rr[i + 2 * e + 1])), f32x2(nd.x, nd.y))),
+                                        d0, d1);
                             ds2[cc >> 1] = pack_bf16x2(d0, d1);
                         }
                         // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)

@@ -43,7 +43,7 @@ struct WideBwdLayout {
     static constexpr int kVOff = kHalves * kBox;
     static constexpr int kRingOff = 2 * kHalves * kBox;
     static constexpr int kDSOff = kRingOff + kSlots * kPieceBytes;  // dS, 128 x 128 bf16 (also dQ staging)
-    static constexpr int kStatOff = kDSOff + 2 * kBox;              // 2 stages: lse2[128], D[128]
+    static constexpr int kStatOff = kDSOff + 2 * kBox;              // 2 stages: -lse2[128], -D[128]
     static constexpr int kBarOff = kStatOff + 2 * 1024;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kRFull = 2, kREmpty = 2 + kSlots, kStatFull = 2 + 2 * kSlots,
                          kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
@@ -197,23 +197,23 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     ok = warp_wait(bar(Lay::kREmpty + slot), ((ic / NS) & 1u) ^ 1u, w, lane);
                     if (!ok) break;
                     if (item == 0) {
-                        // row statistics of this query block (lse in log2 units, D); the
+                        // row statistics of this query block, negated (-lse in log2 units, -D); the
                         // stage is free: its previous block's dS was consumed before the
                         // ring slot just acquired could be released
-                        float* lse2 = stats + (qb & 1u) * 256;
-                        float* dd = lse2 + 128;
+                        float* nlse2 = stats + (qb & 1u) * 256;
+                        float* ndd = nlse2 + 128;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int r = m * kBM + lane * 4 + e;
-                            float lv = INFINITY, dv = 0.f;   // rows past the end: P = 0
+                            float lv = -INFINITY, dv = 0.f;   // negated; rows past the end: P = 0
                             if (r < f.lq) {
                                 const long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
                                                        : ((long)f.b * g.H + f.h) * g.Lq + r;
-                                lv = p.lse[si] * kLog2e;
-                                dv = p.delta[si];
+                                lv = -p.lse[si] * kLog2e;
+                                dv = -p.delta[si];
                             }
-                            lse2[lane * 4 + e] = lv;
-                            dd[lane * 4 + e] = dv;
+                            nlse2[lane * 4 + e] = lv;
+                            ndd[lane * 4 + e] = dv;
                         }
                         __threadfence_block();
                         __syncwarp();
@@ -347,11 +347,6 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tc_commit(bar(Lay::kREmpty + s3));
                 }
                 __syncwarp();
-                // with three ring slots the next S^T can overlap the dS computation
-                if (NS >= 3 && more) {
-                    ok = issue_s(qb + 1, pc, po);
-                    if (!ok) break;
-                }
                 // dK[:, chunk] += dS^T Q[:, chunk]; dQ[:, chunk] = dS K[:, chunk]
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
                 if (!ok) break;
@@ -378,7 +373,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 __syncwarp();
                 ++qb;
-                if (NS < 3 && more) {
+                // the next S^T only now: issued before dK/dQ it delayed the dQ read-out
+                // and the next dP^T behind it (measured 22% slower at d = 192)
+                if (more) {
                     ok = issue_s(qb, pc, po);
                     if (!ok) break;
                 }
@@ -438,18 +435,25 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < 32; ++i) pv[c * 32 + i] = u2f(rr[i]);
                 }
-                const float* lse2 = stats + stage * 256 + wg * 64;
-                const float* dd = stats + stage * 256 + 128 + wg * 64;
+                // the producer stages -lse (log2 units) and -D, so both steps are packed fp32 pairs
+                const float* nlse2 = stats + stage * 256 + wg * 64;
+                const float* ndd = stats + stage * 256 + 128 + wg * 64;
                 const int q0 = m * kBM + wg * 64;
                 const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+                const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float e = ex2_mufu(fmaf(pv[c], sl2, -lse2[c]));
+                for (int c = 0; c < 64; c += 2) {
+                    const float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+                    float x0, x1;
+                    f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sc2, f32x2(nl.x, nl.y)), x0, x1);
+                    float e0 = ex2_mufu(x0), e1 = ex2_mufu(x1);
                     if (!full) {
                         const int q = q0 + c;
-                        e = (key_ok && q >= q_lo && q < f.lq) ? e : 0.f;
+                        e0 = (key_ok && q >= q_lo && q < f.lq) ? e0 : 0.f;
+                        e1 = (key_ok && q + 1 >= q_lo && q + 1 < f.lq) ? e1 : 0.f;
                     }
-                    pv[c] = e;
+                    pv[c] = e0;
+                    pv[c + 1] = e1;
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
@@ -474,8 +478,11 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int cc = c * 32 + i + 2 * e;
-                            const float d0 = pv[cc] * (u2f(rr[i + 2 * e]) - dd[cc]);
-                            const float d1 = pv[cc + 1] * (u2f(rr[i + 2 * e + 1]) - dd[cc + 1]);
+                            const float2 nd = *reinterpret_cast<const float2*>(ndd + cc);
+                            float d0, d1;
+                            f32x2_split(fmul2(f32x2(pv[cc], pv[cc + 1]),
+                                              fadd2(f32x2(u2f(rr[i + 2 * e]), u2f(rr[i + 2 * e + 1])), f32x2(nd.x, nd.y))),
+                                        d0, d1);
                             ds2[cc >> 1] = pack_bf16x2(d0, d1);
                         }
                         // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r % 8)

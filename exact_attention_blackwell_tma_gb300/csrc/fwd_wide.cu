@@ -356,19 +356,24 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     m_run = m_new;
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float l0 = 0.f, l1 = 0.f;
+                // x = s * sl2 - m and the row sum on packed fp32 pairs
+                const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(neg_m, neg_m);
+                uint64_t acc_a = f32x2(0.f, 0.f), acc_b = acc_a;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2_mufu(fmaf(s[64 * hf + 2 * i], sl2, neg_m));
-                        const float p1 = ex2_mufu(fmaf(s[64 * hf + 2 * i + 1], sl2, neg_m));
-                        l0 += p0;
-                        l1 += p1;
+                        float x0, x1;
+                        f32x2_split(ffma2(f32x2(s[64 * hf + 2 * i], s[64 * hf + 2 * i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
+                        if (i & 1) acc_b = fadd2(acc_b, f32x2(p0, p1));
+                        else acc_a = fadd2(acc_a, f32x2(p0, p1));
                         rr[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(t_s + 32 * hf, rr);
                 }
+                float l0, l1;
+                f32x2_split(fadd2(acc_a, acc_b), l0, l1);
                 l_run += l0 + l1;
                 tmem_st_wait();
                 tc_fence_before_sync();

@@ -28,7 +28,7 @@
  *          only within itself. 1 <= B <= 1024.
  *
  * Arguments common to all calls:
- *   d       head dimension: forward 64 or 128; backward 64 or 128.
+ *   d       head dimension: 64, 128, 192 or 256 (forward and backward).
  *   scale   softmax scale, finite and > 0 (typically 1/sqrt(d)).
  *   causal  0 or 1.
  *   stream  CUDA stream the work is enqueued on; calls are asynchronous and
@@ -60,9 +60,10 @@ extern "C" {
 
 /*
  * Forward pass: writes o and lse (see the definitions above).
- * Tiles of 2x128 query rows run on a persistent grid (one CTA per SM) in a
- * longest-first order (FlashAttention-4 paper, Section 3.3 "Scheduling");
- * varlen batches are sorted longest-first on the device.
+ * Tiles of 2x128 query rows (d <= 128; one 128-row tile for d = 192, 256)
+ * run on a persistent grid (one CTA per SM) in a longest-first order
+ * (FlashAttention-4 paper, Section 3.3 "Scheduling"); varlen batches are
+ * sorted longest-first on the device.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int Lq, int Lk, int d, float scale, int causal,
@@ -81,9 +82,11 @@ size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, 
  * dk, dv (bf16, layouts of q, k, v). FlashAttention-4 paper, Section 3.2:
  * the kernel iterates over K/V blocks, recomputes S^T, keeps P^T and the
  * dK/dV accumulators in tensor memory, and accumulates dQ with fp32 global
- * atomics (Section 3.2.2). deterministic != 0 serialises each dQ tile's
- * accumulation in a fixed order with semaphores so repeated calls are
- * bit-identical (Section 3.2.4). workspace/ws_bytes: caller-owned device
+ * atomics (Section 3.2.2); for d = 192 and 256 each K/V block is worked on
+ * in two 128-column chunks of dK/dV/dQ, each recomputing S^T and dP^T, so
+ * that the accumulators fit in tensor memory. deterministic != 0 serialises
+ * each dQ tile's accumulation in a fixed order with semaphores so repeated
+ * calls are bit-identical (Section 3.2.4). workspace/ws_bytes: caller-owned device
  * memory of at least attn_bwd_workspace_size(...) bytes, 256-byte aligned,
  * not used concurrently by another call.
  */
