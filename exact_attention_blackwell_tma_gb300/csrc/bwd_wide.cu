@@ -104,7 +104,9 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     return f;
 }
 
-template <int HD>
+// kDet: deterministic dQ accumulation (a separate instantiation keeps the
+// other path's code out of each kernel)
+template <int HD, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -446,14 +448,13 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
                     float x0, x1;
                     f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sc2, f32x2(nl.x, nl.y)), x0, x1);
-                    float e0 = ex2_mufu(x0), e1 = ex2_mufu(x1);
-                    if (!full) {
-                        const int q = q0 + c;
-                        e0 = (key_ok && q >= q_lo && q < f.lq) ? e0 : 0.f;
-                        e1 = (key_ok && q + 1 >= q_lo && q + 1 < f.lq) ? e1 : 0.f;
-                    }
-                    pv[c] = e0;
-                    pv[c + 1] = e1;
+                    pv[c] = ex2_mufu(x0);
+                    pv[c + 1] = ex2_mufu(x1);
+                }
+                if (!full) {   // diagonal or ragged block: keep query columns [lo, hi) only
+                    const int lo = key_ok ? q_lo - q0 : 64, hi = f.lq - q0;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
@@ -548,7 +549,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!ok) break;
                 ++dqc;
                 tc_fence_after_sync();
-                if (!p.deterministic) {
+                if constexpr (!kDet) {
                     uint32_t row[128];
                     if (rounds == 2) {
                         tmem_ld128(tmem + lane_off + Lay::kTDP, row);
@@ -646,7 +647,7 @@ cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
                            int num_sms, cudaStream_t stream) {
     using Lay = WideBwdLayout<HD>;
-    auto kern = bwd_wide_kernel<HD>;
+    auto kern = p.deterministic ? bwd_wide_kernel<HD, true> : bwd_wide_kernel<HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

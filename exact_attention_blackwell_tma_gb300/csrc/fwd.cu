@@ -425,8 +425,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float l0 = 0.f, l1 = 0.f;
-                if (j + 1 < f.n_kv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
-                else exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
+                if constexpr (kPolyEvery > 0) {
+                    if (j + 1 < f.n_kv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
+                    else exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
+                } else {
+                    exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // one copy of the loop in the code
+                }
                 l_run += l0 + l1;
                 tmem_st_wait();
                 tc_fence_before_sync();

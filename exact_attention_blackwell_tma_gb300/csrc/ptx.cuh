@@ -66,28 +66,20 @@ struct WaitCtx {
 };
 
 // Wait for the phase with the given parity to complete. Gives up (returning
-// false) when the budget runs out, when another warp of this CTA has given up,
-// or when another CTA has reported a failure; the first to give up records it.
+// false) when the budget runs out or when another warp of this CTA has given
+// up; the first to give up records it in the device status word. The loop is
+// kept small: it is inlined at every wait site, and the kernels' size decides
+// how often warps resuming from a wait miss the instruction cache.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
     if (mbar_try_wait(bar, parity)) return true;
-    uint64_t start = 0;
+    const uint64_t deadline = global_timer_ns() + w.budget_ns;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*w.abort_flag) return false;
-            if (*(volatile int*)w.status != kStatusOk) {
-                *w.abort_flag = 1;
-                return false;
-            }
-            uint64_t now = global_timer_ns();
-            if (start == 0) start = now;
-            else if (now - start > w.budget_ns) {
-                *w.abort_flag = 1;
-                atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
-                return false;
-            }
-        }
+        if ((it & 255u) == 0 && (*w.abort_flag || global_timer_ns() > deadline)) break;
     }
+    *w.abort_flag = 1;
+    atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);   // no-op if another waiter recorded it first
+    return false;
 }
 
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -110,26 +102,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 
 // Bounded spin until *sem == target (deterministic dQ order). Acquire on success.
 __device__ __forceinline__ bool sem_wait(const int* sem, int target, const WaitCtx& w) {
-    uint64_t start = 0;
+    uint64_t deadline = 0;
     for (uint32_t it = 0;; ++it) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
         if (v == target) return true;
         if ((it & 63u) == 63u) {
-            if (*w.abort_flag) return false;
-            if (*(volatile int*)w.status != kStatusOk) {
-                *w.abort_flag = 1;
-                return false;
-            }
-            uint64_t now = global_timer_ns();
-            if (start == 0) start = now;
-            else if (now - start > w.budget_ns) {
-                *w.abort_flag = 1;
-                atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
-                return false;
-            }
+            const uint64_t now = global_timer_ns();
+            if (deadline == 0) deadline = now + w.budget_ns;
+            else if (*w.abort_flag || now > deadline) break;
         }
     }
+    *w.abort_flag = 1;
+    atomicCAS(w.status, kStatusOk, kStatusWaitTimeout);
+    return false;
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
