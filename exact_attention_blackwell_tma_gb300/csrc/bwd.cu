@@ -45,17 +45,25 @@ template <int HD>
 struct BwdLayout {
     static constexpr int kHalves = HD / 64;
     static constexpr int kTileBytes = kBM * HD * 2;
-    static constexpr int kStages = HD == 64 ? 3 : 2;               // Q/dO ring
+    // Q and dO have rings of their own: dO is consumed by dP^T and dV early in a
+    // query block, Q only by dK at its end, so one dO buffer suffices at d = 128.
+    // The space saved holds a second dS tile, so the next dS can be written while
+    // the previous dQ tile is still being staged through the other one.
+    static constexpr int kQStages = HD == 64 ? 3 : 2;
+    static constexpr int kDOStages = HD == 64 ? 2 : 1;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kTileBytes;
-    static constexpr int kQOff = 2 * kTileBytes;                   // stage s: Q at +2s*tile, dO at +(2s+1)*tile
-    static constexpr int kDSOff = kQOff + kStages * 2 * kTileBytes;  // dS^T, 128 x 128 bf16
-    static constexpr int kStatOff = kDSOff + 2 * kBox;             // stage s: -lse2[128], -D[128]
-    static constexpr int kBarOff = kStatOff + kStages * 1024;
-    static constexpr int kKVFull = 0, kKVEmpty = 1, kQFull = 2, kQEmpty = 2 + kStages,
-                         kSFull = 2 + 2 * kStages, kDPFull = kSFull + 1,
-                         kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,
-                         kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
+    static constexpr int kQOff = 2 * kTileBytes;                     // Q ring
+    static constexpr int kDOOff = kQOff + kQStages * kTileBytes;     // dO ring
+    static constexpr int kDSOff = kDOOff + kDOStages * kTileBytes;   // two dS^T tiles, 128 x 128 bf16 each
+    static constexpr int kDSBytes = 2 * kBox;
+    static constexpr int kStatOff = kDSOff + 2 * kDSBytes;           // per Q stage: -lse2[128], -D[128]
+    static constexpr int kBarOff = kStatOff + kQStages * 1024;
+    static constexpr int kKVFull = 0, kKVEmpty = 1, kQFull = 2, kQEmpty = kQFull + kQStages,
+                         kDOFull = kQEmpty + kQStages, kDOEmpty = kDOFull + kDOStages,
+                         kSFull = kDOEmpty + kDOStages, kDPFull = kSFull + 1,
+                         kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,   // two
+                         kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
                          kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kStageReady = kSemDone + 1,
                          kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -197,7 +205,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
            const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, const VarlenMap* vm) {
     using Lay = BwdLayout<HD>;
-    constexpr int NST = Lay::kStages;
+    constexpr int NQS = Lay::kQStages, NDS = Lay::kDOStages;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -213,15 +221,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (tid == 0) {
         mbar_init(bar(Lay::kKVFull), 1);
         mbar_init(bar(Lay::kKVEmpty), 1);
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NQS; ++s) {
             mbar_init(bar(Lay::kQFull + s), 1);
             mbar_init(bar(Lay::kQEmpty + s), 1);
+        }
+        for (int s = 0; s < NDS; ++s) {
+            mbar_init(bar(Lay::kDOFull + s), 1);
+            mbar_init(bar(Lay::kDOEmpty + s), 1);
         }
         mbar_init(bar(Lay::kSFull), 1);
         mbar_init(bar(Lay::kDPFull), 1);
         mbar_init(bar(Lay::kPFull), 256);
         mbar_init(bar(Lay::kDSFull), 256);
-        mbar_init(bar(Lay::kDSEmpty), 1);
+        mbar_init(bar(Lay::kDSEmpty + 0), 1);
+        mbar_init(bar(Lay::kDSEmpty + 1), 1);
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
@@ -276,8 +289,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             __syncwarp();
             ++tile_it;
             for (int m = f.m_begin; m < f.m_end && ok; ++m) {
-                const uint32_t st = qc % NST;
-                ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NST) & 1u) ^ 1u, w, lane);
+                const uint32_t st = qc % NQS;
+                ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NQS) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 // row statistics for this query block, negated: -lse in log2 units and -D
                 float* nlse2 = stats + st * 256;
@@ -298,13 +311,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_expect_tx(bar(Lay::kQFull + st), 2 * Lay::kTileBytes);
-                    const uint32_t qa = base + Lay::kQOff + st * 2 * Lay::kTileBytes;
-                    for (int hf = 0; hf < Lay::kHalves; ++hf) {
-                        tma_load_3d(qa + hf * kBox, &tmQ, bar(Lay::kQFull + st), hf * 64, f.h, f.q_row0 + m * kBM);
-                        tma_load_3d(qa + Lay::kTileBytes + hf * kBox, &tmDO, bar(Lay::kQFull + st), hf * 64, f.h,
-                                    f.q_row0 + m * kBM);
-                    }
+                    mbar_expect_tx(bar(Lay::kQFull + st), Lay::kTileBytes);
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
+                        tma_load_3d(base + Lay::kQOff + st * Lay::kTileBytes + hf * kBox, &tmQ, bar(Lay::kQFull + st),
+                                    hf * 64, f.h, f.q_row0 + m * kBM);
+                }
+                __syncwarp();
+                const uint32_t sd = qc % NDS;
+                ok = warp_wait(bar(Lay::kDOEmpty + sd), ((qc / NDS) & 1u) ^ 1u, w, lane);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_expect_tx(bar(Lay::kDOFull + sd), Lay::kTileBytes);
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
+                        tma_load_3d(base + Lay::kDOOff + sd * Lay::kTileBytes + hf * kBox, &tmDO,
+                                    bar(Lay::kDOFull + sd), hf * 64, f.h, f.q_row0 + m * kBM);
                 }
                 __syncwarp();
                 ++qc;
@@ -312,9 +332,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         if (lane == 0) {
             if (tile_it) drain_wait(bar(Lay::kKVFull), (tile_it - 1) & 1u, p.wait_budget_ns);
-            for (uint32_t i = 0; i < (uint32_t)NST && i < qc; ++i) {
+            for (uint32_t i = 0; i < (uint32_t)NQS && i < qc; ++i) {
                 const uint32_t n = qc - 1 - i;
-                drain_wait(bar(Lay::kQFull + n % NST), (n / NST) & 1u, p.wait_budget_ns);
+                drain_wait(bar(Lay::kQFull + n % NQS), (n / NQS) & 1u, p.wait_budget_ns);
+            }
+            for (uint32_t i = 0; i < (uint32_t)NDS && i < qc; ++i) {
+                const uint32_t n = qc - 1 - i;
+                drain_wait(bar(Lay::kDOFull + n % NDS), (n / NDS) & 1u, p.wait_budget_ns);
             }
         }
         __syncwarp();
@@ -329,13 +353,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const SmemDesc k_km = sdesc_sw128_split(base + Lay::kKOff, 16, 1024);
         const SmemDesc v_km = sdesc_sw128_split(base + Lay::kVOff, 16, 1024);
         const SmemDesc k_mn = sdesc_sw128_split(base + Lay::kKOff, kBox, 1024);
-        const SmemDesc ds_mn = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
+        const SmemDesc ds_mn0 = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
         const SmemDesc q_km0 = sdesc_sw128_split(base + Lay::kQOff, 16, 1024);
         const SmemDesc q_mn0 = sdesc_sw128_split(base + Lay::kQOff, kBox, 1024);
-        constexpr uint32_t kStageStep = desc_step(2 * Lay::kTileBytes);   // next Q/dO stage
-        constexpr uint32_t kDoStep = desc_step(Lay::kTileBytes);           // dO follows Q in a stage
-        auto at_stage = [&](SmemDesc d, uint32_t stage, uint32_t extra) {
-            d.lo += stage * kStageStep + extra;
+        const SmemDesc do_km0 = sdesc_sw128_split(base + Lay::kDOOff, 16, 1024);
+        const SmemDesc do_mn0 = sdesc_sw128_split(base + Lay::kDOOff, kBox, 1024);
+        auto at_stage = [&](SmemDesc d, uint32_t stage) {   // the stage-th tile of a ring
+            d.lo += stage * desc_step(Lay::kTileBytes);
             return d;
         };
         // D[128 x 128] = A[128 x d] * B[128 x d]^T, both K-major (d contiguous)
@@ -354,22 +378,27 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
             if (!ok) break;
             ++tile_it;
-            uint32_t st = qc % NST;
-            ok = warp_wait(bar(Lay::kQFull + st), (qc / NST) & 1u, w, lane);
+            uint32_t st = qc % NQS;
+            ok = warp_wait(bar(Lay::kQFull + st), (qc / NQS) & 1u, w, lane);
             if (!ok) break;
             tc_fence_after_sync();
             if (lane == 0) {   // S^T for the first query block
-                mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st, 0));
+                mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st));
                 tc_commit(bar(Lay::kSFull));
             }
             __syncwarp();
             for (int m = f.m_begin; m < f.m_end; ++m) {
-                const SmemDesc do_km = at_stage(q_km0, st, kDoStep), do_mn = at_stage(q_mn0, st, kDoStep);
-                const SmemDesc q_mn = at_stage(q_mn0, st, 0);
+                const uint32_t sd = qc % NDS, dsb = qc & 1u;   // dO stage, dS tile of this block
+                const SmemDesc do_km = at_stage(do_km0, sd), do_mn = at_stage(do_mn0, sd);
+                const SmemDesc q_mn = at_stage(q_mn0, st);
+                SmemDesc ds_mn = ds_mn0;
+                ds_mn.lo += dsb * desc_step(Lay::kDSBytes);
                 // dP^T = V dO^T into the dP/dQ block once the previous dQ tile is read out
                 ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dqf;
+                ok = warp_wait(bar(Lay::kDOFull + sd), (qc / NDS) & 1u, w, lane);
+                if (!ok) break;
                 tc_fence_after_sync();
                 if (lane == 0) {
                     mma_nt(tmem + Lay::kTDP, v_km, do_km);
@@ -386,13 +415,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     for (int k = 0; k < kBM / 16; ++k)
                         mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
                                do_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                    tc_commit(bar(Lay::kDOEmpty + sd));   // dO is no longer read
                 }
                 __syncwarp();
                 const bool more = m + 1 < f.m_end;
                 uint32_t st_next = st;
                 if (more) {
-                    st_next = (qc + 1) % NST;
-                    ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NST) & 1u, w, lane);
+                    st_next = (qc + 1) % NQS;
+                    ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NQS) & 1u, w, lane);
                     if (!ok) break;
                     tc_fence_after_sync();
                 }
@@ -423,7 +453,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 // delayed the dQ read-out and the next dP^T behind it (3-4% slower).
                 if (more) {
                     if (lane == 0) {
-                        mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next, 0));
+                        mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next));
                         tc_commit(bar(Lay::kSFull));
                     }
                     __syncwarp();
@@ -446,7 +476,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const int r = quarter * 32 + lane;         // key row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = g.scale_log2;
-        uint8_t* ds_tile = smem + Lay::kDSOff + wg * kBox;   // this warpgroup's 64 query columns
+        uint8_t* const ds_tiles = smem + Lay::kDSOff + wg * kBox;   // this warpgroup's 64 query columns
         const float* stats = reinterpret_cast<const float*>(smem + Lay::kStatOff);
         uint32_t sc = 0, qc = 0, dpc = 0, dsw = 0, tile_it = 0;
         bool ok = true;
@@ -471,11 +501,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             // query q (inside the sequence) is allowed for this key iff q_lo <= q < lq
             const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
             for (int m = f.m_begin; m < f.m_end; ++m) {
-                const uint32_t st = qc % NST;
+                const uint32_t st = qc % NQS;
+                uint8_t* ds_tile = ds_tiles + (qc & 1u) * Lay::kDSBytes;   // alternate dS tiles per block
                 ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
                 if (!ok) break;
                 ++sc;
-                ok = warp_wait(bar(Lay::kQFull + st), (qc / NST) & 1u, w, lane);   // stats visibility
+                ok = warp_wait(bar(Lay::kQFull + st), (qc / NQS) & 1u, w, lane);   // stats visibility
                 if (!ok) break;
                 ++qc;
                 tc_fence_after_sync();
@@ -516,7 +547,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (!ok) break;
                 ++dpc;
                 tc_fence_after_sync();
-                ok = warp_wait(bar(Lay::kDSEmpty), (dsw & 1u) ^ 1u, w, lane);
+                ok = warp_wait(bar(Lay::kDSEmpty + (dsw & 1u)), ((dsw >> 1) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dsw;
                 uint32_t ds2[32];   // dS^T, two bf16 per word
@@ -589,8 +620,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint8_t* stage = smem + Lay::kDSOff;
-        const uint32_t stage_s = base + Lay::kDSOff;
+
         uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
@@ -599,6 +629,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int m = f.m_begin; m < f.m_end; ++m) {
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
+                // the dS tile this block's dQ MMA read is free now: stage dQ through it
+                const uint32_t dsb = dqc & 1u;
+                uint8_t* stage = smem + Lay::kDSOff + dsb * Lay::kDSBytes;
+                const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
                 if constexpr (!kDet) {
@@ -644,7 +678,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                 bulk_commit_group();
                                 bulk_wait_group_read0();
                             }
-                            mbar_arrive(bar(rnd == HD / 64 - 1 ? Lay::kDSEmpty : Lay::kStageFree));
+                            mbar_arrive(bar(rnd == HD / 64 - 1 ? Lay::kDSEmpty + dsb : Lay::kStageFree));
                         }
                         ++srdy;
                     }
@@ -652,7 +686,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     continue;
                 }
                 // deterministic: ordered per-thread atomics; the dS^T tile is not used here
-                if (leader) mbar_arrive(bar(Lay::kDSEmpty));
+                if (leader) mbar_arrive(bar(Lay::kDSEmpty + dsb));
                 const int q = m * kBM + rq;
                 const bool q_ok = q < f.lq;
                 float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD;
