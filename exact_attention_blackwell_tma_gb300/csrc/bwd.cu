@@ -64,7 +64,7 @@ struct BwdLayout {
                          kSFull = kDOEmpty + kDOStages, kDPFull = kSFull + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,   // two
                          kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
-                         kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1, kStageReady = kSemDone + 1,
+                         kSemGo = kDKVFull + 1, kStageReady = kSemGo + 1,
                          kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -239,7 +239,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
-        mbar_init(bar(Lay::kSemDone), 128);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -610,18 +609,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     } else {
         // ------------------------------------------------------------ dQ read-out warpgroup
         // Each dQ tile (128 query rows x d, fp32) goes from tensor memory to the
-        // global accumulator. Default: staged through shared memory (the dS^T
-        // tile, idle at this point) in 128-row x 32-column swizzled boxes and
-        // added by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic
-        // mode: per-thread vector atomics under the tile's semaphore, in key-
-        // block order. Either way the dS^T tile is handed back afterwards.
+        // global accumulator: staged through shared memory (the dS^T tile this
+        // block's dQ MMA has read) in 128-row x 32-column swizzled boxes and added
+        // by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic mode:
+        // the same reduce-adds under the tile's semaphore, in key-block order,
+        // each block's completing before the next block's start.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-
-        uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -635,90 +633,78 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
-                if constexpr (!kDet) {
-                    // the whole dQ row leaves tensor memory at once, so the next dP^T can start
-                    uint32_t row[HD];
-                    if constexpr (HD == 128) {
-                        tmem_ld128(tmem + lane_off + Lay::kTDP, row);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < HD / 32; ++c) {
-                            tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
-                        }
+                int* sem = nullptr;
+                if constexpr (kDet) {
+                    // dQ tile (b, h, m) takes its key blocks' contributions in ascending
+                    // block order: block n waits until n blocks have added theirs. Every
+                    // block below n also sees query block m (causal or not).
+                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    sem = p.semaphores + tile;
+                    if (leader) {
+                        if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
                     }
-                    tc_fence_before_sync();
-                    mbar_arrive(bar(Lay::kDQFree));
-#pragma unroll
-                    for (int rnd = 0; rnd < HD / 64; ++rnd) {
-                        if (rnd > 0) {
-                            ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
-                            ++sfree;
-                            if (!ok) break;
-                        }
-#pragma unroll
-                        for (int c2 = 0; c2 < 2; ++c2) {
-                            uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
-                            const int c0 = rnd * 64 + c2 * 32;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)   // 128-byte swizzle: chunk j at j ^ (row % 8)
-                                *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
-                                    make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
-                                               row[c0 + 4 * j + 3]);
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(bar(Lay::kStageReady));
-                        if (leader) {
-                            if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                                // rows past the query block's sequence carry exact zeros (P = 0 there)
-                                for (int c2 = 0; c2 < 2; ++c2)
-                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, f.h,
-                                                      f.q_row0 + m * kBM);
-                                bulk_commit_group();
-                                bulk_wait_group_read0();
-                            }
-                            mbar_arrive(bar(rnd == HD / 64 - 1 ? Lay::kDSEmpty + dsb : Lay::kStageFree));
-                        }
-                        ++srdy;
-                    }
+                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                    ++sgo;
+                    ok = ok && !*abort_flag;
                     if (!ok) break;
-                    continue;
                 }
-                // deterministic: ordered per-thread atomics; the dS^T tile is not used here
-                if (leader) mbar_arrive(bar(Lay::kDSEmpty + dsb));
-                const int q = m * kBM + rq;
-                const bool q_ok = q < f.lq;
-                float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD;
-                // dQ tile (b, h, m) takes its key blocks' contributions in ascending
-                // block order: block n waits until n blocks have added theirs. Every
-                // block below n also sees query block m (causal or not).
-                const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                         : ((long)f.b * g.H + f.h) * p.nq + m;
-                int* sem = p.semaphores + tile;
-                if (leader) {
-                    sem_wait(sem, f.n, w);
-                    mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
-                }
-                ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
-                ++sgo;
-                ok = ok && !*abort_flag;
+                // the whole dQ row leaves tensor memory at once, so the next dP^T can start
+                // (deterministic mode: once the semaphore has let this block in)
+                uint32_t row[HD];
+                if constexpr (HD == 128) {
+                    tmem_ld128(tmem + lane_off + Lay::kTDP, row);
+                } else {
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
-                    if (q_ok && ok) {
+                    for (int c = 0; c < HD / 32; ++c) {
+                        tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            red_add_v4(dst + c * 32 + i, u2f(rr[i]), u2f(rr[i + 1]), u2f(rr[i + 2]), u2f(rr[i + 3]));
+                        for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
                     }
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-                __threadfence();
-                mbar_arrive(bar(Lay::kSemDone));
-                if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
-                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                ++sdone;
+#pragma unroll
+                for (int rnd = 0; rnd < HD / 64; ++rnd) {
+                    const bool last = rnd == HD / 64 - 1;
+                    if (rnd > 0) {
+                        ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
+                        ++sfree;
+                        if (!ok) break;
+                    }
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+                        const int c0 = rnd * 64 + c2 * 32;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)   // 128-byte swizzle: chunk j at j ^ (row % 8)
+                            *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
+                                make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
+                                           row[c0 + 4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(Lay::kStageReady));
+                    if (leader) {
+                        if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
+                            // rows past the query block's sequence carry exact zeros (P = 0 there)
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, f.h,
+                                                  f.q_row0 + m * kBM);
+                            bulk_commit_group();
+                            if (kDet && last) {
+                                // every reduce-add of this block is complete before the next block's start
+                                bulk_wait_group0();
+                                fence_proxy_async_global();
+                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                            } else {
+                                bulk_wait_group_read0();
+                            }
+                        }
+                        mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
+                    }
+                    ++srdy;
+                }
                 if (!ok) break;
             }
         }

@@ -166,6 +166,12 @@ __device__ __forceinline__ void bulk_wait_group0() {
 
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads).
+// Order this thread's generic-proxy global accesses with its async-proxy (TMA)
+// ones, e.g. a semaphore acquire before a TMA reduce-add, or a completed
+// reduce-add before a semaphore release.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
