@@ -222,7 +222,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kKVFull), 1);
         mbar_init(bar(Lay::kKVEmpty), 1);
         for (int s = 0; s < NQS; ++s) {
-            mbar_init(bar(Lay::kQFull + s), 1);
+            mbar_init(bar(Lay::kQFull + s), 2);   // the Q tile's bytes + the row statistics
             mbar_init(bar(Lay::kQEmpty + s), 1);
         }
         for (int s = 0; s < NDS; ++s) {
@@ -291,6 +291,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t st = qc % NQS;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NQS) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
+                // Q first (arrival 1 of 2 with its byte count), so the copy overlaps the
+                // global loads of the row statistics below (arrival 2 of 2)
+                if (lane == 0) {
+                    mbar_expect_tx(bar(Lay::kQFull + st), Lay::kTileBytes);
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
+                        tma_load_3d(base + Lay::kQOff + st * Lay::kTileBytes + hf * kBox, &tmQ, bar(Lay::kQFull + st),
+                                    hf * 64, f.h, f.q_row0 + m * kBM);
+                }
                 // row statistics for this query block, negated: -lse in log2 units and -D
                 float* nlse2 = stats + st * 256;
                 float* ndd = nlse2 + 128;
@@ -309,12 +317,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 __threadfence_block();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_expect_tx(bar(Lay::kQFull + st), Lay::kTileBytes);
-                    for (int hf = 0; hf < Lay::kHalves; ++hf)
-                        tma_load_3d(base + Lay::kQOff + st * Lay::kTileBytes + hf * kBox, &tmQ, bar(Lay::kQFull + st),
-                                    hf * 64, f.h, f.q_row0 + m * kBM);
-                }
+                if (lane == 0) mbar_arrive(bar(Lay::kQFull + st));
                 __syncwarp();
                 const uint32_t sd = qc % NDS;
                 ok = warp_wait(bar(Lay::kDOEmpty + sd), ((qc / NDS) & 1u) ^ 1u, w, lane);
@@ -418,13 +421,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 __syncwarp();
                 const bool more = m + 1 < f.m_end;
-                uint32_t st_next = st;
-                if (more) {
-                    st_next = (qc + 1) % NQS;
-                    ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NQS) & 1u, w, lane);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                }
+                const uint32_t st_next = more ? (qc + 1) % NQS : st;
                 // dK += dS^T Q (dS^T from tensor memory) and dQ = dS K (dS from shared memory)
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
                 if (!ok) break;
@@ -449,8 +446,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 __syncwarp();
                 // S^T of the next query block only now; it overwrites P^T, which the
                 // dV MMA issued before it has consumed. Issued ahead of dK/dQ it
-                // delayed the dQ read-out and the next dP^T behind it (3-4% slower).
+                // delayed the dQ read-out and the next dP^T behind it (3-4% slower);
+                // waiting for its Q ahead of dK/dQ delayed those too.
                 if (more) {
+                    ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NQS) & 1u, w, lane);
+                    if (!ok) break;
+                    tc_fence_after_sync();
                     if (lane == 0) {
                         mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next));
                         tc_commit(bar(Lay::kSFull));

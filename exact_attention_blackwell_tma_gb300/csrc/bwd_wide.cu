@@ -38,18 +38,24 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k >> 
 template <int HD>
 struct WideBwdLayout {
     static constexpr int kHalves = HD / 64;                       // 64-column boxes per row
-    static constexpr int kSlots = HD == 192 ? 3 : 2;              // Q/dO piece ring
+    static constexpr int kSlots = HD == 192 ? 3 : 2;                // Q/dO piece ring
+    // dS tiles. The d <= 128 kernel double-buffers dS so the next dS can be
+    // written while the previous dQ is staged through the other tile; here
+    // shared memory has room for that only by giving up a ring slot at d = 192,
+    // which measured 11% slower, so one tile.
+    static constexpr int kDSTiles = 1;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kHalves * kBox;
     static constexpr int kRingOff = 2 * kHalves * kBox;
-    static constexpr int kDSOff = kRingOff + kSlots * kPieceBytes;  // dS, 128 x 128 bf16 (also dQ staging)
-    static constexpr int kStatOff = kDSOff + 2 * kBox;              // 2 stages: -lse2[128], -D[128]
+    static constexpr int kDSOff = kRingOff + kSlots * kPieceBytes;  // dS tiles, 128 x 128 bf16 (also dQ staging)
+    static constexpr int kDSBytes = 2 * kBox;
+    static constexpr int kStatOff = kDSOff + kDSTiles * kDSBytes;   // 2 stages: -lse2[128], -D[128]
     static constexpr int kBarOff = kStatOff + 2 * 1024;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kRFull = 2, kREmpty = 2 + kSlots, kStatFull = 2 + 2 * kSlots,
                          kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
-                         kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 1, kDQFree = kDQFull + 1,
-                         kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1, kSemDone = kSemGo + 1,
-                         kStageReady = kSemDone + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
+                         kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1,
+                         kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1,
+                         kStageReady = kSemGo + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
                          kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -138,12 +144,12 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(Lay::kDPFull), 1);
         mbar_init(bar(Lay::kPFull), 256);
         mbar_init(bar(Lay::kDSFull), 256);
-        mbar_init(bar(Lay::kDSEmpty), 1);
+        mbar_init(bar(Lay::kDSEmpty + 0), 1);
+        mbar_init(bar(Lay::kDSEmpty + 1), 1);
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
-        mbar_init(bar(Lay::kSemDone), 128);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -255,7 +261,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const SmemDesc k_km = sdesc_sw128_split(base + Lay::kKOff, 16, 1024);
         const SmemDesc v_km = sdesc_sw128_split(base + Lay::kVOff, 16, 1024);
         const SmemDesc k_mn = sdesc_sw128_split(base + Lay::kKOff, kBox, 1024);
-        const SmemDesc ds_mn = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
+        const SmemDesc ds_mn0 = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
         const SmemDesc r_km0 = sdesc_sw128_split(base + Lay::kRingOff, 16, 1024);
         const SmemDesc r_mn0 = sdesc_sw128_split(base + Lay::kRingOff, kBox, 1024);
         auto at_slot = [&](SmemDesc d, uint32_t slot) {
@@ -358,6 +364,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after_sync();
                 if (lane == 0) {
                     const SmemDesc q_mn = at_slot(r_mn0, s4);
+                    SmemDesc ds_mn = ds_mn0;   // this block's dS tile
+                    ds_mn.lo += (qb % Lay::kDSTiles) * desc_step(Lay::kDSBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBM / 16; ++kk)
                         mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(kk), q_mn, desc_step(kk * 2048), id_kv,
@@ -397,7 +405,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int r = quarter * 32 + lane;         // key row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = g.scale_log2;
-        uint8_t* ds_tile = smem + Lay::kDSOff + wg * kBox;
+        uint8_t* const ds_tiles = smem + Lay::kDSOff + wg * kBox;
         const float* stats = reinterpret_cast<const float*>(smem + Lay::kStatOff);
         uint32_t sc = 0, qb = 0, dpc = 0, dsw = 0, tile_it = 0;
         bool ok = true;
@@ -467,7 +475,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!ok) break;
                 ++dpc;
                 tc_fence_after_sync();
-                ok = warp_wait(bar(Lay::kDSEmpty), (dsw & 1u) ^ 1u, w, lane);
+                const uint32_t dsb = dsw % Lay::kDSTiles;   // alternate dS tiles per block (d = 192)
+                uint8_t* ds_tile = ds_tiles + dsb * Lay::kDSBytes;
+                ok = warp_wait(bar(Lay::kDSEmpty + dsb), ((dsw / Lay::kDSTiles) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dsw;
                 uint32_t ds2[32];
@@ -528,16 +538,15 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
         // ------------------------------------------------------------ dQ read-out warpgroup
         // As in bwd.cu, for one column chunk: TMA reduce-adds of 128-row x
-        // 32-column boxes staged through the dS tile, or (deterministic mode)
-        // ordered per-thread vector atomics under the chunk's semaphore.
+        // 32-column boxes staged through this block's dS tile; deterministic
+        // mode: the same reduce-adds under the chunk's semaphore, each key block's
+        // completing before the next one's start.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint8_t* stage = smem + Lay::kDSOff;
-        const uint32_t stage_s = base + Lay::kDSOff;
-        uint32_t dqc = 0, sgo = 0, sdone = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -547,88 +556,79 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int m = f.m_begin; m < f.m_end; ++m) {
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
+                const uint32_t dsb = dqc % Lay::kDSTiles;   // the dS tile this block's dQ MMA read
+                uint8_t* stage = smem + Lay::kDSOff + dsb * Lay::kDSBytes;
+                const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
-                if constexpr (!kDet) {
-                    uint32_t row[128];
-                    if (rounds == 2) {
-                        tmem_ld128(tmem + lane_off + Lay::kTDP, row);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
-                        }
+                int* sem = nullptr;
+                if constexpr (kDet) {
+                    // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in
+                    // ascending block order under its own semaphore
+                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    sem = p.semaphores + 2 * tile + f.c;
+                    if (leader) {
+                        if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kSemGo));
                     }
-                    tc_fence_before_sync();
-                    mbar_arrive(bar(Lay::kDQFree));
-#pragma unroll
-                    for (int rnd = 0; rnd < 2; ++rnd) {
-                        if (rnd >= rounds) break;
-                        if (rnd > 0) {
-                            ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
-                            ++sfree;
-                            if (!ok) break;
-                        }
-#pragma unroll
-                        for (int c2 = 0; c2 < 2; ++c2) {
-                            uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
-                            const int c0 = rnd * 64 + c2 * 32;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
-                                    make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
-                                               row[c0 + 4 * j + 3]);
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(bar(Lay::kStageReady));
-                        if (leader) {
-                            if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                                for (int c2 = 0; c2 < 2; ++c2)
-                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
-                                                      f.h, f.q_row0 + m * kBM);
-                                bulk_commit_group();
-                                bulk_wait_group_read0();
-                            }
-                            mbar_arrive(bar(rnd == rounds - 1 ? Lay::kDSEmpty : Lay::kStageFree));
-                        }
-                        ++srdy;
-                    }
+                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                    ++sgo;
+                    ok = ok && !*abort_flag;
                     if (!ok) break;
-                    continue;
                 }
-                if (leader) mbar_arrive(bar(Lay::kDSEmpty));
-                const int q = m * kBM + rq;
-                const bool q_ok = q < f.lq;
-                float* dst = p.dq_acc + (((long)f.q_row0 + q) * g.H + f.h) * HD + 128 * f.c;
-                // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in
-                // ascending block order under its own semaphore
-                const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                         : ((long)f.b * g.H + f.h) * p.nq + m;
-                int* sem = p.semaphores + 2 * tile + f.c;
-                if (leader) {
-                    sem_wait(sem, f.n, w);
-                    mbar_arrive(bar(Lay::kSemGo));
-                }
-                ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
-                ++sgo;
-                ok = ok && !*abort_flag;
-                for (int c = 0; c < cw / 32; ++c) {
-                    tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
-                    if (q_ok && ok) {
+                uint32_t row[128];
+                if (rounds == 2) {
+                    tmem_ld128(tmem + lane_off + Lay::kTDP, row);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            red_add_v4(dst + c * 32 + i, u2f(rr[i]), u2f(rr[i + 1]), u2f(rr[i + 2]), u2f(rr[i + 3]));
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
                     }
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-                __threadfence();
-                mbar_arrive(bar(Lay::kSemDone));
-                if (leader && mbar_wait(bar(Lay::kSemDone), sdone & 1u, w) && ok)
-                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                ++sdone;
+#pragma unroll
+                for (int rnd = 0; rnd < 2; ++rnd) {
+                    if (rnd >= rounds) break;
+                    const bool last = rnd == rounds - 1;
+                    if (rnd > 0) {
+                        ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
+                        ++sfree;
+                        if (!ok) break;
+                    }
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
+                        const int c0 = rnd * 64 + c2 * 32;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
+                                make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
+                                           row[c0 + 4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(Lay::kStageReady));
+                    if (leader) {
+                        if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
+                                                  f.h, f.q_row0 + m * kBM);
+                            bulk_commit_group();
+                            if (kDet && last) {
+                                bulk_wait_group0();
+                                fence_proxy_async_global();
+                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                            } else {
+                                bulk_wait_group_read0();
+                            }
+                        }
+                        mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
+                    }
+                    ++srdy;
+                }
                 if (!ok) break;
             }
         }
