@@ -20,6 +20,9 @@
 
 namespace attn {
 
+// The index functions below are also compiled for the host, where
+// tests/test_sched.py checks their coverage and balance.
+
 constexpr int kMaxVarlenBatch = 1024;   // sequences per varlen call (shared-memory map)
 
 struct Tile {
@@ -28,11 +31,11 @@ struct Tile {
 
 // Walk position `rem` inside one batch entry with `nm` row blocks and H heads,
 // heads grouped `hs` at a time; `reverse` walks row blocks from the last.
-__device__ __forceinline__ void sched_within_batch(int rem, int nm, int H, int hs, bool reverse,
+__host__ __device__ __forceinline__ void sched_within_batch(int rem, int nm, int H, int hs, bool reverse,
                                                    int& h, int& m) {
     int s = rem / (hs * nm);
     int h0 = s * hs;
-    int sec_h = min(hs, H - h0);
+    const int sec_h = hs < H - h0 ? hs : H - h0;
     int idx = rem - s * hs * nm;
     int mi = idx / sec_h;
     h = h0 + (idx - mi * sec_h);
@@ -46,7 +49,7 @@ __device__ __forceinline__ void sched_within_batch(int rem, int nm, int H, int h
 // the busiest CTA with 17-23% more work than the mean, this order with under
 // 2% (host simulation of the 4096- and 8192-row workloads). Increasing in k,
 // so each CTA walks its tiles in increasing index order.
-__device__ __forceinline__ int snake_tile(int cta, int k, int grid) {
+__host__ __device__ __forceinline__ int snake_tile(int cta, int k, int grid) {
     return k * grid + ((k & 1) ? grid - 1 - cta : cta);
 }
 
@@ -55,7 +58,7 @@ __device__ __forceinline__ int snake_tile(int cta, int k, int grid) {
 // head. m_desc: a larger row-block index is the longer tile (forward). For
 // non-causal problems all tiles are equally long and the L2-section order
 // below is kept (it measured ~2% faster there).
-__device__ __forceinline__ Tile sched_dense_lpt(int t, int B, int H, int nm, bool m_desc) {
+__host__ __device__ __forceinline__ Tile sched_dense_lpt(int t, int B, int H, int nm, bool m_desc) {
     Tile ti;
     const int level = t / (B * H);
     const int rem = t - level * (B * H);
@@ -65,7 +68,7 @@ __device__ __forceinline__ Tile sched_dense_lpt(int t, int B, int H, int nm, boo
     return ti;
 }
 
-__device__ __forceinline__ Tile sched_dense(int t, int H, int nm, int hs, bool reverse) {
+__host__ __device__ __forceinline__ Tile sched_dense(int t, int H, int nm, int hs, bool reverse) {
     Tile ti;
     int per_b = H * nm;
     ti.b = t / per_b;
@@ -110,7 +113,7 @@ __device__ __forceinline__ void sched_varlen_build(VarlenMap& vm, const int* cu,
     __syncthreads();
 }
 
-__device__ __forceinline__ Tile sched_varlen(const VarlenMap& vm, int t, int B, int H, int rows_per_block,
+__host__ __device__ __forceinline__ Tile sched_varlen(const VarlenMap& vm, int t, int B, int H, int rows_per_block,
                                              int hs, bool reverse) {
     int lo = 0, hi = B - 1;   // largest k with pre[k] <= t
     while (lo < hi) {

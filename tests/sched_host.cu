@@ -1,0 +1,139 @@
+// Host-side checks of the persistent tile scheduler (csrc/sched.cuh), compiled
+// by tests/test_sched.py with nvcc and run without a GPU. The index functions
+// under test are the ones the kernels call. Prints "OK" and exits 0 when every
+// check passes; otherwise prints the first failure and exits 1.
+#include <cstdio>
+#include <cstdlib>
+#include <set>
+#include <tuple>
+#include <vector>
+#include <algorithm>
+
+#include "sched.cuh"
+
+using namespace attn;
+
+static int fail(const char* what, int a, int b, int c) {
+    std::printf("FAIL %s (%d %d %d)\n", what, a, b, c);
+    std::exit(1);
+}
+
+// every tile index in [0, n) is handed to exactly one CTA, each CTA's
+// sequence increases (the kernels' loop condition relies on it)
+static void check_snake(int n, int grid) {
+    std::vector<int> seen(n, 0);
+    for (int c = 0; c < grid; ++c) {
+        int prev = -1;
+        for (int k = 0;; ++k) {
+            const int t = snake_tile(c, k, grid);
+            if (t >= n) break;
+            if (t <= prev) fail("snake not increasing", c, k, t);
+            prev = t;
+            ++seen[t];
+        }
+    }
+    for (int t = 0; t < n; ++t)
+        if (seen[t] != 1) fail("snake coverage", n, grid, t);
+}
+
+// the dense walks enumerate every (b, h, m) exactly once
+static void check_dense(int B, int H, int nm, int hs) {
+    for (int mode = 0; mode < 4; ++mode) {
+        std::set<std::tuple<int, int, int>> got;
+        int prev_m = -1;
+        for (int t = 0; t < B * H * nm; ++t) {
+            Tile ti = mode < 2 ? sched_dense(t, H, nm, hs, mode == 1) : sched_dense_lpt(t, B, H, nm, mode == 3);
+            if (ti.b < 0 || ti.b >= B || ti.h < 0 || ti.h >= H || ti.m < 0 || ti.m >= nm)
+                fail("dense tile out of range", B, H, t);
+            got.insert({ti.b, ti.h, ti.m});
+            if (mode >= 2) {   // longest first: the row-block level moves monotonically
+                const int level = mode == 3 ? nm - 1 - ti.m : ti.m;
+                if (level < prev_m) fail("lpt order", B, H, t);
+                prev_m = level;
+            }
+        }
+        if ((int)got.size() != B * H * nm) fail("dense coverage", B, H, nm);
+    }
+}
+
+// a varlen map as the device builds it: sequences sorted longest first (ties by
+// index), prefix counts of H * ceil(L / rows) tiles
+static void build_map(VarlenMap& vm, const std::vector<int>& lens, int H, int rows) {
+    const int B = (int)lens.size();
+    vm.start[0] = 0;
+    for (int i = 0; i < B; ++i) vm.start[i + 1] = vm.start[i] + lens[i];
+    std::vector<int> idx(B);
+    for (int i = 0; i < B; ++i) idx[i] = i;
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return lens[a] > lens[b]; });
+    int acc = 0;
+    for (int k = 0; k < B; ++k) {
+        vm.order[k] = idx[k];
+        vm.pre[k] = acc;
+        acc += H * ((lens[idx[k]] + rows - 1) / rows);
+    }
+    vm.pre[B] = acc;
+}
+
+static void check_varlen(const std::vector<int>& lens, int H, int rows, int hs) {
+    static VarlenMap vm;
+    build_map(vm, lens, H, rows);
+    const int B = (int)lens.size(), n = vm.pre[B];
+    std::set<std::tuple<int, int, int>> got;
+    int prev_len = 1 << 30;
+    for (int t = 0; t < n; ++t) {
+        Tile ti = sched_varlen(vm, t, B, H, rows, hs, true);
+        const int L = lens[ti.b], nm = (L + rows - 1) / rows;
+        if (ti.h < 0 || ti.h >= H || ti.m < 0 || ti.m >= nm) fail("varlen tile out of range", ti.b, ti.h, ti.m);
+        if (L > prev_len) fail("varlen not longest first", t, L, prev_len);
+        prev_len = L;
+        got.insert({ti.b, ti.h, ti.m});
+    }
+    int expect = 0;
+    for (int L : lens) expect += H * ((L + rows - 1) / rows);
+    if ((int)got.size() != expect || n != expect) fail("varlen coverage", n, expect, (int)got.size());
+}
+
+// causal balance: per-CTA sums of tile lengths under the longest-first order
+// and the boustrophedon hand-out stay within `tol` of the mean
+static void check_causal_balance(int B, int H, int L, int rows, bool fwd, int grid, double tol) {
+    const int nm = (L + rows - 1) / rows, n = B * H * nm;
+    std::vector<double> work(grid, 0.0);
+    for (int c = 0; c < grid; ++c)
+        for (int k = 0;; ++k) {
+            const int t = snake_tile(c, k, grid);
+            if (t >= n) break;
+            Tile ti = sched_dense_lpt(t, B, H, nm, fwd);
+            // forward: row block m sees (m+1)*rows keys; backward: key block m is
+            // seen by the query rows from m*rows to L
+            work[c] += fwd ? (double)(ti.m + 1) : (double)(nm - ti.m);
+        }
+    double mx = 0, sum = 0;
+    for (double w : work) {
+        mx = std::max(mx, w);
+        sum += w;
+    }
+    const double mean = sum / grid;
+    if (mx > mean * (1.0 + tol)) fail("causal imbalance (max/mean in percent)", (int)(100 * mx / mean), L, fwd);
+}
+
+int main() {
+    for (int n : {1, 7, 152, 153, 1000, 1024, 4096})
+        for (int grid : {1, 2, 148, 152})
+            check_snake(n, grid);
+    check_dense(1, 1, 1, 1);
+    check_dense(2, 3, 5, 2);
+    check_dense(4, 16, 16, 16);
+    check_dense(2, 16, 64, 5);
+    check_dense(1, 32, 128, 7);
+    check_varlen({1, 128, 200, 513, 77, 256}, 3, 128, 2);
+    check_varlen({1, 128, 200, 513, 77, 256}, 3, 256, 3);
+    check_varlen({16384, 256, 300, 300, 4096, 1}, 16, 128, 16);
+    // the causal workloads of the benchmark, forward (256-row tiles) and backward (128-key blocks)
+    check_causal_balance(4, 16, 4096, 256, true, 152, 0.03);
+    check_causal_balance(4, 16, 4096, 128, false, 152, 0.03);
+    check_causal_balance(2, 16, 8192, 256, true, 152, 0.03);
+    check_causal_balance(2, 16, 8192, 128, false, 152, 0.03);
+    check_causal_balance(1, 32, 32768, 256, true, 152, 0.03);
+    std::printf("OK\n");
+    return 0;
+}
