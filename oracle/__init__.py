@@ -56,12 +56,12 @@ def bind(path: str):
     lib.oracle_fwd.restype = ctypes.c_int
     lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                               ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                _ip, _ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_bwd.restype = ctypes.c_int
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                               ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
     return lib
 
@@ -121,22 +121,29 @@ def _dims(q, k, cu):
     return B, H, L, L, d
 
 
+def _dv(v, k):
+    """Head dim of v (may differ from that of q and k); v must match k otherwise."""
+    if v.shape[:-1] != k.shape[:-1]:
+        raise ValueError("v must have the rows and heads of k")
+    return v.shape[-1]
+
+
 def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None):
     """O and LSE (natural log) by the definition. Returns (o, lse) as float64.
 
+    q and k share a head dim; v (and O) may have another one.
     ``rows``: optional query-row indices (per sequence) to evaluate; the other
     rows of the returned arrays are NaN.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     cu = _i32(cu_seqlens)
     B, H, Lq, Lk, d = _dims(q, k, cu)
-    o = np.full(q.shape[:-1] + (v.shape[-1],), np.nan)
-    if v.shape[-1] != d:
-        raise ValueError("the oracle takes the same head dim for q/k and v")
+    dv = _dv(v, k)
+    o = np.full(q.shape[:-1] + (dv,), np.nan)
     lse = np.full((B, H, Lq) if cu is None else (H, q.shape[0]), np.nan)
     r = _i32(rows)
     rc = _load().oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
-                            B, H, Lq, Lk, d, float(scale), int(bool(causal)),
+                            B, H, Lq, Lk, d, dv, float(scale), int(bool(causal)),
                             _ptr(cu, _ip), _ptr(r, _ip), 0 if r is None else len(r),
                             nthreads or default_threads())
     if rc != 0:
@@ -154,13 +161,16 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     cu = _i32(cu_seqlens)
     B, H, Lq, Lk, d = _dims(q, k, cu)
+    dvd = _dv(v, k)
+    if dout.shape != q.shape[:-1] + (dvd,):
+        raise ValueError("dout must have the rows and heads of q and the head dim of v")
     dq = np.full(q.shape, np.nan)
     dk = np.full(k.shape, np.nan)
     dv = np.full(v.shape, np.nan)
     qr, kr = _i32(qrows), _i32(krows)
     rc = _load().oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp),
                             _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
-                            B, H, Lq, Lk, d, float(scale), int(bool(causal)), _ptr(cu, _ip),
+                            B, H, Lq, Lk, d, dvd, float(scale), int(bool(causal)), _ptr(cu, _ip),
                             _ptr(qr, _ip), 0 if qr is None else len(qr),
                             _ptr(kr, _ip), 0 if kr is None else len(kr),
                             nthreads or default_threads())

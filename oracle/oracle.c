@@ -17,6 +17,10 @@
  *     P_ij  = exp(s_ij - LSE_i)
  *     O_i   = sum_j P_ij v_j
  *
+ * q and k have head dim d; v, o, dout and dv have their own head dim dv
+ * (equal to d for the textbook case; the FlashAttention-4 paper's Section 5.1
+ * also measures d = 192 for q/k with 128 for v, Fig. 5).
+ *
  * Backward, for the scalar loss L = sum(O * dO) (FlashAttention-4 paper,
  * Section 3.2.2: five products -- S recomputed, dP = dO V^T, dV = P^T dO,
  * dQ = dS K, dK = dS^T Q):
@@ -57,7 +61,7 @@
 typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv;
-    int B, H, Lq, Lk, d, causal;
+    int B, H, Lq, Lk, d, dvh, causal;   /* dvh: head dim of v, o, dout, dv */
     double scale;
     const int *cu;          /* NULL for dense */
     /* per (b, h, row) statistics used by the backward pass */
@@ -79,6 +83,12 @@ static int seq_lk(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b
 static long row_off(const job_t *J, int b, int i, int h, int L) {
     if (J->cu) return ((long)(J->cu[b] + i) * J->H + h) * J->d;
     return (((long)b * L + i) * J->H + h) * J->d;
+}
+
+/* the same for a [.., L, H, dv] tensor (v, o, dout, dv) */
+static long row_off_v(const job_t *J, int b, int i, int h, int L) {
+    if (J->cu) return ((long)(J->cu[b] + i) * J->H + h) * J->dvh;
+    return (((long)b * L + i) * J->H + h) * J->dvh;
 }
 
 /* index of (b, h, i) into an lse-shaped array */
@@ -122,16 +132,16 @@ static double row_lse(const job_t *J, int b, int h, int i) {
     return m + log(sum);
 }
 
-/* O_i = sum_j exp(s_ij - LSE_i) v_j  (written into out[0..d)) */
+/* O_i = sum_j exp(s_ij - LSE_i) v_j  (written into out[0..dv)) */
 static void row_out(const job_t *J, int b, int h, int i, double lse, double *out) {
-    int d = J->d, lk = seq_lk(J, b);
-    for (int c = 0; c < d; c++) out[c] = 0.0;
+    int dv = J->dvh, lk = seq_lk(J, b);
+    for (int c = 0; c < dv; c++) out[c] = 0.0;
     if (lse == -INFINITY) return;
     for (int j = 0; j < lk; j++) {
         if (!allowed(J, b, i, j)) continue;
         double p = exp(score(J, b, h, i, j) - lse);
-        const double *vj = J->v + row_off(J, b, j, h, J->Lk);
-        for (int c = 0; c < d; c++) out[c] += p * vj[c];
+        const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);
+        for (int c = 0; c < dv; c++) out[c] += p * vj[c];
     }
 }
 
@@ -139,9 +149,9 @@ static void row_out(const job_t *J, int b, int h, int i, double lse, double *out
 static double dscore(const job_t *J, int b, int h, int i, int j) {
     long st = stat_off(J, b, h, i);
     double p = exp(score(J, b, h, i, j) - J->lse_all[st]);
-    const double *doi = J->dout + row_off(J, b, i, h, J->Lq);
-    const double *vj = J->v + row_off(J, b, j, h, J->Lk);
-    return p * (dot(doi, vj, J->d) - J->D_all[st]);
+    const double *doi = J->dout + row_off_v(J, b, i, h, J->Lq);
+    const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);
+    return p * (dot(doi, vj, J->dvh) - J->D_all[st]);
 }
 
 /* ---- work items -------------------------------------------------------- */
@@ -150,18 +160,18 @@ static double dscore(const job_t *J, int b, int h, int i, int j) {
 enum { PH_FWD = 0, PH_STATS = 1, PH_DQ = 2, PH_DKV = 3 };
 
 static void do_item(job_t *J, int b, int h, int i) {
-    int d = J->d;
+    int d = J->d, dv = J->dvh;
     if (J->phase == PH_FWD) {
         double lse = row_lse(J, b, h, i);
         J->lse[stat_off(J, b, h, i)] = lse;
-        row_out(J, b, h, i, lse, J->o + row_off(J, b, i, h, J->Lq));
+        row_out(J, b, h, i, lse, J->o + row_off_v(J, b, i, h, J->Lq));
     } else if (J->phase == PH_STATS) {
         long st = stat_off(J, b, h, i);
-        double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)dv);
         double lse = row_lse(J, b, h, i);
         row_out(J, b, h, i, lse, tmp);
         J->lse_all[st] = lse;
-        J->D_all[st] = dot(J->dout + row_off(J, b, i, h, J->Lq), tmp, d);
+        J->D_all[st] = dot(J->dout + row_off_v(J, b, i, h, J->Lq), tmp, dv);
         free(tmp);
     } else if (J->phase == PH_DQ) {
         double *dqi = J->dq + row_off(J, b, i, h, J->Lq);
@@ -178,19 +188,18 @@ static void do_item(job_t *J, int b, int h, int i) {
     } else { /* PH_DKV: item row index is a key row j */
         int j = i, lq = seq_lq(J, b);
         double *dkj = J->dk + row_off(J, b, j, h, J->Lk);
-        double *dvj = J->dv + row_off(J, b, j, h, J->Lk);
-        for (int c = 0; c < d; c++) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        double *dvj = J->dv + row_off_v(J, b, j, h, J->Lk);
+        for (int c = 0; c < d; c++) dkj[c] = 0.0;
+        for (int c = 0; c < dv; c++) dvj[c] = 0.0;
         for (int r = 0; r < lq; r++) {
             if (!allowed(J, b, r, j)) continue;
             long st = stat_off(J, b, h, r);
             double p = exp(score(J, b, h, r, j) - J->lse_all[st]);
-            const double *dor = J->dout + row_off(J, b, r, h, J->Lq);
+            const double *dor = J->dout + row_off_v(J, b, r, h, J->Lq);
             const double *qr = J->q + row_off(J, b, r, h, J->Lq);
-            double ds = p * (dot(dor, J->v + row_off(J, b, j, h, J->Lk), d) - J->D_all[st]);
-            for (int c = 0; c < d; c++) {
-                dkj[c] += ds * qr[c];
-                dvj[c] += p * dor[c];
-            }
+            double ds = p * (dot(dor, J->v + row_off_v(J, b, j, h, J->Lk), dv) - J->D_all[st]);
+            for (int c = 0; c < d; c++) dkj[c] += ds * qr[c];
+            for (int c = 0; c < dv; c++) dvj[c] += p * dor[c];
         }
         for (int c = 0; c < d; c++) dkj[c] *= J->scale;
     }
@@ -249,8 +258,8 @@ static int *make_items(const job_t *J, const int *rows, int nrows, int kind, lon
     return items;
 }
 
-static int check_args(int B, int H, int Lq, int Lk, int d, const int *cu) {
-    if (B < 0 || H < 1 || d < 1) return -1;
+static int check_args(int B, int H, int Lq, int Lk, int d, int dv, const int *cu) {
+    if (B < 0 || H < 1 || d < 1 || dv < 1) return -1;
     if (!cu && (Lq < 0 || Lk < 0)) return -1;
     if (cu) {
         if (cu[0] != 0) return -1;
@@ -260,20 +269,20 @@ static int check_args(int B, int H, int Lq, int Lk, int d, const int *cu) {
 }
 
 static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
-                     int B, int H, int Lq, int Lk, int d, double scale, int causal, const int *cu) {
+                     int B, int H, int Lq, int Lk, int d, int dv, double scale, int causal, const int *cu) {
     memset(J, 0, sizeof(*J));
     J->q = q; J->k = k; J->v = v; J->dout = dout;
-    J->B = B; J->H = H; J->Lq = Lq; J->Lk = Lk; J->d = d;
+    J->B = B; J->H = H; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
     J->scale = scale; J->causal = causal != 0; J->cu = cu;
 }
 
 int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
-               int B, int H, int Lq, int Lk, int d, double scale, int causal,
+               int B, int H, int Lq, int Lk, int d, int dv, double scale, int causal,
                const int *cu_seqlens, const int *rows, int nrows, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (check_args(B, H, Lq, Lk, d, cu_seqlens)) return -1;
+    if (check_args(B, H, Lq, Lk, d, dv, cu_seqlens)) return -1;
     job_t J;
-    init_job(&J, q, k, v, NULL, B, H, Lq, Lk, d, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, NULL, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlens);
     J.o = o; J.lse = lse;
     long n;
     int *items = make_items(&J, rows, nrows, 0, &n);
@@ -285,14 +294,14 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
 
 int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
                double *dq, double *dk, double *dv,
-               int B, int H, int Lq, int Lk, int d, double scale, int causal,
+               int B, int H, int Lq, int Lk, int d, int dvd, double scale, int causal,
                const int *cu_seqlens, const int *qrows, int nqrows,
                const int *krows, int nkrows, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    if (check_args(B, H, Lq, Lk, d, cu_seqlens)) return -1;
+    if (check_args(B, H, Lq, Lk, d, dvd, cu_seqlens)) return -1;
     if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
     job_t J;
-    init_job(&J, q, k, v, dout, B, H, Lq, Lk, d, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, dout, B, H, Lq, Lk, d, dvd, scale, causal, cu_seqlens);
     J.dq = dq; J.dk = dk; J.dv = dv;
 
     /* longest sequence, the range of relative row indices */

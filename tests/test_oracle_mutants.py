@@ -23,13 +23,15 @@ MUTANTS = [
     ("top-left causal alignment", "return j <= i + (lk - lq);", "return j <= i;"),
     ("LSE without the max", "return m + log(sum);", "return log(sum);"),
     ("base-2 exponential", "sum += exp(score(J, b, h, i, j) - m);", "sum += exp2(score(J, b, h, i, j) - m);"),
-    ("O sums keys instead of values", "const double *vj = J->v + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < d; c++) out[c]",
-     "const double *vj = J->k + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < d; c++) out[c]"),
+    ("O sums keys instead of values", "const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);\n        for (int c = 0; c < dv; c++) out[c]",
+     "const double *vj = J->k + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < dv; c++) out[c]"),
     ("score uses key row i", "const double *kj = J->k + row_off(J, b, j, h, J->Lk);\n    return",
      "const double *kj = J->k + row_off(J, b, i < J->Lk ? i : 0, h, J->Lk);\n    return"),
-    ("dS sign flip", "return p * (dot(doi, vj, J->d) - J->D_all[st]);", "return p * (dot(doi, vj, J->d) + J->D_all[st]);"),
+    ("dS sign flip", "return p * (dot(doi, vj, J->dvh) - J->D_all[st]);", "return p * (dot(doi, vj, J->dvh) + J->D_all[st]);"),
     ("D dropped", "J->D_all[st] = dot(", "J->D_all[st] = 0.0 * dot("),
     ("dQ without scale", "for (int c = 0; c < d; c++) dqi[c] *= J->scale;", ""),
+    ("O written with the q/k head dim", "row_out(J, b, h, i, lse, J->o + row_off_v(J, b, i, h, J->Lq));",
+     "row_out(J, b, h, i, lse, J->o + row_off(J, b, i, h, J->Lq));"),
     ("dK without scale", "for (int c = 0; c < d; c++) dkj[c] *= J->scale;", ""),
     ("dV weighted by dS", "dvj[c] += p * dor[c];", "dvj[c] += ds * dor[c];"),
     ("dK from dO instead of Q", "dkj[c] += ds * qr[c];", "dkj[c] += ds * dor[c];"),
@@ -51,6 +53,8 @@ BATTERY = [
     (pins.test_bwd_finite_differences, (7, 8, True)),
     (pins.test_bwd_finite_differences_rectangular_and_varlen, ()),
     (pins.test_bwd_column_sums, ()),
+    (pins.test_fwd_matches_textbook_softmax_value_dim, (2, 3, 5, 5, 4, 3, False)),
+    (pins.test_bwd_finite_differences_value_dim, (True,)),
 ]
 
 

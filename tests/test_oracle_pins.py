@@ -98,6 +98,26 @@ def test_fwd_matches_textbook_softmax(B, H, Lq, Lk, d, causal):
     np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Lq,Lk,d,dv", [(2, 3, 5, 5, 4, 3), (1, 2, 7, 11, 6, 9), (1, 1, 9, 4, 5, 2)])
+def test_fwd_matches_textbook_softmax_value_dim(B, H, Lq, Lk, d, dv, causal):
+    """v (and O) with a head dim of their own, as the FlashAttention-4 paper's
+    Section 5.1 measures at d = 192 for q/k and 128 for v."""
+    q, k, v = rnd((B, Lq, H, d), 7), rnd((B, Lk, H, d), 8), rnd((B, Lk, H, dv), 9)
+    o, lse = oracle.fwd(q, k, v, 0.45, causal)
+    o_ref, lse_ref = textbook(q, k, v, 0.45, causal)
+    assert o.shape == (B, Lq, H, dv)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_single_key_returns_v_row_of_its_own_width():
+    q, k, v = rnd((1, 4, 2, 6), 10), rnd((1, 1, 2, 6), 11), rnd((1, 1, 2, 3), 12)
+    o, _ = oracle.fwd(q, k, v, 0.5, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), rtol=0, atol=1e-13)
+
+
 def test_single_key_returns_v():
     q, k, v = rnd((2, 6, 3, 8), 4), rnd((2, 1, 3, 8), 5), rnd((2, 1, 3, 8), 6)
     s = 0.3 * np.einsum("bihc,bhc->bhi", q, k[:, 0])
@@ -286,6 +306,17 @@ def test_bwd_finite_differences_rectangular_and_varlen():
         for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
             assert np.abs(got - ref).max() < 1e-7
     assert sum(lens) == 5
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_finite_differences_value_dim(causal):
+    q, k = rnd((1, 5, 2, 4), 60), rnd((1, 6, 2, 4), 61)
+    v, do = rnd((1, 6, 2, 3), 62), rnd((1, 5, 2, 3), 63)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.7, causal)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    fq, fk, fv = finite_diff(q, k, v, do, 0.7, causal)
+    for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.abs(got - ref).max() < 1e-7
 
 
 def test_bwd_column_sums():
