@@ -6,6 +6,7 @@ varlen offset. The copy is compiled and bound in place of the real oracle, and
 the pin battery from test_oracle_pins.py is run against it; at least one pin
 must fail. The real oracle must pass the same battery.
 """
+import multiprocessing
 import os
 import shutil
 import subprocess
@@ -78,8 +79,17 @@ def test_real_oracle_passes_battery():
     assert run_battery() == []
 
 
+def _battery_in_child(so_path, conn):
+    """Run the battery against the mutant library in a separate process: a
+    mutant may write out of bounds (a wrong row stride), which must not corrupt
+    the test process. Sends back the list of failed pins."""
+    oracle._lib = oracle.bind(so_path)
+    conn.send(run_battery())
+    conn.close()
+
+
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutant_is_caught(name, old, new, src_text, tmp_path, monkeypatch):
+def test_mutant_is_caught(name, old, new, src_text, tmp_path):
     assert src_text.count(old) == 1, f"mutation site for '{name}' not unique"
     mutated = src_text.replace(old, new)
     c_path = tmp_path / "mutant.c"
@@ -87,7 +97,17 @@ def test_mutant_is_caught(name, old, new, src_text, tmp_path, monkeypatch):
     so_path = tmp_path / "libmutant.so"
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so_path),
                            str(c_path), "-lm", "-lpthread"])
-    monkeypatch.setattr(oracle, "_lib", oracle.bind(str(so_path)))
-    failed = run_battery()
+    ctx = multiprocessing.get_context("spawn")
+    parent, child = ctx.Pipe(duplex=False)
+    proc = ctx.Process(target=_battery_in_child, args=(str(so_path), child))
+    proc.start()
+    child.close()
+    try:
+        failed = parent.recv() if parent.poll(300) else ["no result"]
+    except EOFError:   # the child died before reporting: the mutant crashed a pin
+        failed = ["child crashed"]
+    proc.join(60)
+    if proc.exitcode != 0:   # a crash of the mutant counts as a failed pin
+        failed = failed + [f"child exit code {proc.exitcode}"]
     assert failed, f"mutant '{name}' passed every pin"
     shutil.rmtree(tmp_path, ignore_errors=True)
