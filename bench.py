@@ -43,11 +43,18 @@ WORKLOADS = {
     "b2h16l8192d64": (inputs.HDSWEEP.with_(d=64), (True,)),
     "b2h16l8192d192": (inputs.HDSWEEP.with_(d=192), (True,)),
     "b2h16l8192d256": (inputs.HDSWEEP.with_(d=256), (True,)),
+    # q/k head dim 192 with v head dim 128 (attn_fwd_hdim): forward only
+    "b2h16l8192dqk192dv128": (inputs.HDSWEEP.with_(d=192, dv=128), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
     "b1h32l32768d128": (inputs.LONG, (True, False)),
 }
 DEFAULT_WORKLOAD = "b4h16l4096d128"
 L2_BYTES = 129 * 1024 * 1024
+
+
+def kinds_of(w):
+    """The calls a step makes: the backward exists for v head dim = q/k head dim."""
+    return ("fwd", "bwd") if w.d_v == w.d else ("fwd",)
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
 # workload's dominant kernel, from the ncu capture summarised in the named
@@ -107,7 +114,7 @@ class Problem:
         self.host = t
         self.q, self.k, self.v, self.do = (t[n].to(device) for n in ("q", "k", "v", "do"))
         self.cu = t["cu_seqlens"].to(device) if w.varlen else None
-        self.o = torch.empty_like(self.q)
+        self.o = torch.empty(self.q.shape[:-1] + (w.d_v,), dtype=self.q.dtype, device=device)
         self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
         if w.varlen:
             self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.total, w.total, w.d
@@ -119,8 +126,8 @@ class Problem:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def fwd(self, causal):
-        rc = binding.attn_fwd(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Lq, self.Lk, self.d,
-                              self.w.scale, causal, self.cu)
+        rc = binding.attn_fwd_hdim(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Lq, self.Lk,
+                                   self.d, self.w.d_v, self.w.scale, causal, self.cu)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -241,21 +248,24 @@ def oracle_sample(w, variants, nthreads=None):
 
     def sample_flops(Lp):
         sw = w.with_(lengths=None, B=1, H=1, L=Lp)
-        return sum(flops(sw, c, "fwd") + flops(sw, c, "bwd") for c in variants)
+        return sum(flops(sw, c, kind) for c in variants for kind in kinds_of(w))
 
     Lp = L
     while Lp > 128 and sample_flops(Lp) > ORACLE_SAMPLE_FLOPS:
         Lp = max(128, (Lp // 2) // 128 * 128)
     f64 = {n: x[:, :Lp].float().numpy().astype(np.float64) for n, x in src.items()}
     total_flops, secs = 0, 0.0
+    kinds = kinds_of(w)
     for causal in variants:
         t0 = time.perf_counter()
         oracle.fwd(f64["q"], f64["k"], f64["v"], w.scale, causal, nthreads=nthreads)
-        oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads)
+        if "bwd" in kinds:
+            oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads)
         secs += time.perf_counter() - t0
     total_flops = sample_flops(Lp)
     what = f"{where}" + (f", leading {Lp}x{Lp} block" if Lp < L else "") + \
-        f" of {w.name}, forward+backward, {'/'.join('causal' if c else 'non-causal' for c in variants)}"
+        f" of {w.name}, {'+'.join({'fwd': 'forward', 'bwd': 'backward'}[k] for k in kinds_of(w))}, " + \
+        f"{'/'.join('causal' if c else 'non-causal' for c in variants)}"
     return total_flops, secs, nthreads, what
 
 
@@ -289,20 +299,19 @@ def run_ours(args, world, rank, local, dist):
     dev = torch.device("cuda", local)
     pk = load_peaks()
     prob = Problem(w, dev)
-    step_flops = sum(flops(w, c, "fwd") + flops(w, c, "bwd") for c in variants)
-    input_bytes = sum(x.numel() * x.element_size() for x in (prob.q, prob.k, prob.v, prob.do))
+    kinds = kinds_of(w)
+    step_flops = sum(flops(w, c, kind) for c in variants for kind in kinds)
+    used = (prob.q, prob.k, prob.v, prob.do) if "bwd" in kinds else (prob.q, prob.k, prob.v)
+    input_bytes = sum(x.numel() * x.element_size() for x in used)
 
     def step(ev=None):
         for c in variants:
-            if ev is not None:
-                ev[("fwd", c)][0].record()
-            prob.fwd(c)
-            if ev is not None:
-                ev[("fwd", c)][1].record()
-                ev[("bwd", c)][0].record()
-            prob.bwd(c)
-            if ev is not None:
-                ev[("bwd", c)][1].record()
+            for kind in kinds:
+                if ev is not None:
+                    ev[(kind, c)][0].record()
+                prob.fwd(c) if kind == "fwd" else prob.bwd(c)
+                if ev is not None:
+                    ev[(kind, c)][1].record()
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -310,7 +319,7 @@ def run_ours(args, world, rank, local, dist):
 
     # ---- timed region: K steps, per-call events on the launching stream
     evs = [{(k, c): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for k in ("fwd", "bwd") for c in variants} for _ in range(args.steps)]
+            for k in kinds for c in variants} for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(dist)
@@ -346,21 +355,20 @@ def run_ours(args, world, rank, local, dist):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        host = {n: prob.host[n].pin_memory() for n in ("q", "k", "v", "do")}
-        outs = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-                for n, x in (("o", prob.o), ("lse", prob.lse), ("dq", prob.dq), ("dk", prob.dk),
-                             ("dv", prob.dv))}
+        ins = ("q", "k", "v", "do") if "bwd" in kinds else ("q", "k", "v")
+        host = {n: prob.host[n].pin_memory() for n in ins}
+        out_names = ("o", "lse", "dq", "dk", "dv") if "bwd" in kinds else ("o", "lse")
+        outs = {n: torch.empty(getattr(prob, n).shape, dtype=getattr(prob, n).dtype, pin_memory=True)
+                for n in out_names}
         h2d = sum(x.numel() * x.element_size() for x in host.values())
         d2h = len(variants) * sum(x.numel() * x.element_size() for x in outs.values())
 
         def e2e_step():
-            prob.q.copy_(host["q"], non_blocking=True)
-            prob.k.copy_(host["k"], non_blocking=True)
-            prob.v.copy_(host["v"], non_blocking=True)
-            prob.do.copy_(host["do"], non_blocking=True)
+            for n, src in host.items():
+                getattr(prob, n).copy_(src, non_blocking=True)
             for c in variants:
-                prob.fwd(c)
-                prob.bwd(c)
+                for kind in kinds:
+                    prob.fwd(c) if kind == "fwd" else prob.bwd(c)
                 for n, dst in outs.items():
                     dst.copy_(getattr(prob, n), non_blocking=True)
 
@@ -388,7 +396,8 @@ def run_ours(args, world, rank, local, dist):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": args.workload, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                "config": {"workload": args.workload, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.d_v,
+                           "calls": list(kinds),
                            "variants": ["causal" if c else "non-causal" for c in variants],
                            "flops_per_step": step_flops,
                            "l2": f"inputs {input_bytes / 2**20:.0f} MiB > 129 MiB L2; no flush between steps",
@@ -396,7 +405,7 @@ def run_ours(args, world, rank, local, dist):
                 "frac_of_peak": value / world / pk["bf16"],
                 "roofline": roofline, "roofline_calls": rooflines,
                 "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * len(variants) * 4,
+                "gpu_launches": args.steps * len(variants) * (4 if "bwd" in kinds else 1),
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     return 0

@@ -33,6 +33,8 @@ class AttnError(RuntimeError):
 def _declare(lib):
     lib.attn_fwd.restype = c_int
     lib.attn_fwd.argtypes = [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_void_p, c_void_p]
+    lib.attn_fwd_hdim.restype = c_int
+    lib.attn_fwd_hdim.argtypes = [c_void_p] * 5 + [c_int] * 6 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
     lib.attn_bwd_workspace_size.argtypes = [c_int] * 7
     lib.attn_bwd.restype = c_int
@@ -115,6 +117,11 @@ def attn_fwd(q, k, v, o, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens=None, s
     return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, scale, int(causal),
                            _ptr(cu_seqlens), _stream(stream))
 
+def attn_fwd_hdim(q, k, v, o, lse, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlens=None, stream=None) -> int:
+    return load().attn_fwd_hdim(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, dv, scale,
+                                int(causal), _ptr(cu_seqlens), _stream(stream))
+
+
 
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
     return load().attn_bwd_workspace_size(B, H, Lq, Lk, d, int(causal), int(deterministic))
@@ -164,15 +171,20 @@ def _check_tensors(*ts):
 
 def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
             stream=None):
-    """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens)."""
+    """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens).
+    v (and O) may have a head dim of their own (d = 192 with 128)."""
     _check_tensors(q, k, v, cu_seqlens)
     B, H, Lq, Lk, d = _dims(q, k, cu_seqlens)
+    dv = v.shape[-1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
-    _check(attn_fwd(q, k, v, out, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens, stream))
+    if dv == d:
+        _check(attn_fwd(q, k, v, out, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens, stream))
+    else:
+        _check(attn_fwd_hdim(q, k, v, out, lse, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlens, stream))
     return out, lse
 
 

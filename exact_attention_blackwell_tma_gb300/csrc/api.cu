@@ -157,10 +157,13 @@ int* device_status_word() {
 
 using namespace attn;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
-                        int Lk, int d, float scale, int causal, const int* cu_seqlens, cudaStream_t stream) {
+extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int Lq, int Lk, int d, int dv, float scale, int causal, const int* cu_seqlens,
+                             cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, false);
     if (rc) return rc;
+    if (dv != d && !(d == 192 && dv == 128))
+        return fail(ATTN_ERR_ARG, "head dims d=%d, dv=%d not supported (dv = d, or d = 192 with dv = 128)", d, dv);
     const long rows_q = cu_seqlens ? (long)Lq : (long)B * Lq;
     const long rows_k = cu_seqlens ? (long)Lk : (long)B * Lk;
     if (rows_q == 0) return ok();   // nothing to compute; pointers may be null
@@ -180,6 +183,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
+    p.dv = dv;
     p.lse = lse;
     // d <= 128: a work tile is two 128-row Q tiles; wider heads: one
     const bool wide = d > 128;
@@ -194,11 +198,18 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     const long krows = rows_k > 0 ? rows_k : rows_q;
     const void* kp = rows_k > 0 ? k : q;
     const void* vp = rows_k > 0 ? v : q;
-    if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, H, d) || !make_map(&tv, vp, krows, H, d))
+    // (a problem with no keys maps v like q, so its width must be d there)
+    if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, H, d) ||
+        !make_map(&tv, vp, krows, H, rows_k > 0 ? dv : d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream) : launch_fwd(tq, tk, tv, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
+                        int Lk, int d, float scale, int causal, const int* cu_seqlens, cudaStream_t stream) {
+    return attn_fwd_hdim(q, k, v, o, lse, B, H, Lq, Lk, d, d, scale, causal, cu_seqlens, stream);
 }
 
 namespace {

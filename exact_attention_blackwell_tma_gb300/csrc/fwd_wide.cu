@@ -1,4 +1,5 @@
-// Forward kernel for head dims above 128 (192, 256).
+// Forward kernel for head dims above 128: d = 192, 256, and d_qk = 192 with
+// d_v = 128 (the FlashAttention-4 paper's Section 5.1, Fig. 5 shape).
 //
 // Same operation and warp roles as fwd.cu, but tensor memory cannot hold two
 // Q tiles' S and O at these head dims (2 x (128 + d) > 512 columns), so a work
@@ -30,10 +31,14 @@ constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;
 
-template <int HD>
+// HD: head dim of q and k; DV: head dim of v and O (equal except for the
+// d_qk = 192, d_v = 128 shape).
+template <int HD, int DV>
 struct WideLayout {
-    static constexpr int kHalves = HD / 64;
-    static constexpr int kTileBytes = kBM * HD * 2;
+    static constexpr int kHalves = HD / 64;               // 64-column boxes of a Q/K row
+    static constexpr int kHalvesV = DV / 64;              // ... of a V row
+    static constexpr int kTileBytes = kBM * HD * 2;       // Q/K tile; ring slots have this size
+    static constexpr int kVTileBytes = kBM * DV * 2;
     static constexpr int kStages = HD == 192 ? 3 : 2;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTileBytes;
@@ -48,7 +53,8 @@ struct WideLayout {
     static constexpr int kSmemBytes = kMapOff + (int)sizeof(VarlenMap) + 1024;
     static constexpr uint32_t kTmemO = 256;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(256 + HD <= (int)kTmemCols, "tensor memory budget");
+    static_assert(256 + DV <= (int)kTmemCols, "tensor memory budget");
+    static_assert(DV <= HD, "a V tile must fit a ring slot");
 };
 
 struct WideTile {
@@ -88,11 +94,11 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
     return f;
 }
 
-template <int HD>
+template <int HD, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using Lay = WideLayout<HD>;
+    using Lay = WideLayout<HD, DV>;
     constexpr int S = Lay::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -152,8 +158,9 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t slot = kv_cnt % S, ph = (kv_cnt / S) & 1u;
             if (!warp_wait(bar(Lay::kKVEmpty + slot), ph ^ 1u, w, lane)) return false;
             if (lane == 0) {
-                mbar_expect_tx(bar(Lay::kKVFull + slot), Lay::kTileBytes);
-                for (int hf = 0; hf < Lay::kHalves; ++hf)
+                const int boxes = kv ? Lay::kHalvesV : Lay::kHalves;
+                mbar_expect_tx(bar(Lay::kKVFull + slot), boxes * kBox);
+                for (int hf = 0; hf < boxes; ++hf)
                     tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox, kv ? &tmV : &tmK,
                                 bar(Lay::kKVFull + slot), hf * 64, f.h, f.k_row0 + j * kBN);
             }
@@ -192,7 +199,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
-        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, HD, false, true);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, DV, false, true);
         const SmemDesc q_desc = sdesc_sw128_split(base + Lay::kQOff, 16, 1024);
         const SmemDesc k_desc0 = sdesc_sw128_split(base + Lay::kKVOff, 16, 1024);
         const SmemDesc v_desc0 = sdesc_sw128_split(base + Lay::kKVOff, kBox, 1024);
@@ -294,13 +301,13 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int r = f.m * kBM + row_in_tile;
             const bool valid = r < f.lq;
             const long prow = (long)f.q_row0 + row_in_tile;
-            __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * HD;
+            __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * DV;
             float* lptr = varlen ? p.lse + (long)f.h * g.Lq + prow : p.lse + ((long)f.b * g.H + f.h) * g.Lq + r;
             if (f.n_kv == 0) {
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(optr);
 #pragma unroll
-                    for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
                     *lptr = -INFINITY;
                 }
                 continue;
@@ -345,7 +352,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (!ok) break;
                         tc_fence_after_sync();
 #pragma unroll
-                        for (int c = 0; c < HD / 32; ++c) {
+                        for (int c = 0; c < DV / 32; ++c) {
                             tmem_ld32(t_o + c * 32, rr);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) rr[i] = f2u(u2f(rr[i]) * alpha);
@@ -387,7 +394,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after_sync();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) {
                 tmem_ld32(t_o + c * 32, rr);
                 if (valid) {
                     uint32_t o2[16];
@@ -412,11 +419,11 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-template <int HD>
+template <int HD, int DV>
 cudaError_t launch_fwd_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const FwdParams& p, int num_sms, cudaStream_t stream) {
-    using Lay = WideLayout<HD>;
-    auto kern = fwd_wide_kernel<HD>;
+    using Lay = WideLayout<HD, DV>;
+    auto kern = fwd_wide_kernel<HD, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.g.cu_seqlens ? num_sms : min(p.n_tiles, num_sms);
@@ -429,11 +436,10 @@ cudaError_t launch_fwd_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_sms, cudaStream_t stream) {
-    switch (p.g.d) {
-        case 192: return launch_fwd_wide_hd<192>(tq, tk, tv, p, num_sms, stream);
-        case 256: return launch_fwd_wide_hd<256>(tq, tk, tv, p, num_sms, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    if (p.g.d == 192 && p.dv == 192) return launch_fwd_wide_hd<192, 192>(tq, tk, tv, p, num_sms, stream);
+    if (p.g.d == 256 && p.dv == 256) return launch_fwd_wide_hd<256, 256>(tq, tk, tv, p, num_sms, stream);
+    if (p.g.d == 192 && p.dv == 128) return launch_fwd_wide_hd<192, 128>(tq, tk, tv, p, num_sms, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -24,7 +24,8 @@ struct Geometry {
 
 struct FwdParams {
     Geometry g;
-    __nv_bfloat16* o;         // same layout as q
+    __nv_bfloat16* o;         // rows and heads of q, head dim dv
+    int dv;                   // head dim of v and o (g.d for q and k)
     float* lse;               // dense [B, H, Lq]; varlen [H, T]
     int n_tiles;              // dense: exact count; varlen: computed on device
     int nm;                   // dense: query blocks per (b, h): 256 rows (d <= 128) or 128 rows
@@ -65,7 +66,8 @@ inline long bwd_semaphore_count(int B, int H, int Lq, bool varlen) {
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int num_sms, cudaStream_t stream);
-// Head dims 192 and 256: one 128-row Q tile per work tile (nm counts 128-row blocks).
+// Head dims 192 and 256 (and d_qk = 192 with d_v = 128): one 128-row Q tile per
+// work tile (nm counts 128-row blocks).
 cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

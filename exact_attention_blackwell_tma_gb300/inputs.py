@@ -37,11 +37,16 @@ class Workload:
     kspike_frac: float = 0.0          # fraction of positions whose K rows are scaled
     kspike: float = 4.0
     lengths: Optional[tuple] = None   # varlen: per-sequence lengths
+    dv: Optional[int] = None          # head dim of v (and dO); None: the same as q and k
 
     @property
     def scale(self) -> float:
         """1/sqrt(d), rounded to fp32 (the C ABI takes a 32-bit float)."""
         return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def d_v(self) -> int:
+        return self.d if self.dv is None else self.dv
 
     @property
     def varlen(self) -> bool:
@@ -60,8 +65,8 @@ class Workload:
         return self.B * self.H * per_seq(self.L)
 
     def fwd_flops(self) -> int:
-        """Algorithmic forward FLOPs: two GEMMs of 2*d FLOPs per unmasked pair."""
-        return 4 * self.d * self.pairs()
+        """Algorithmic forward FLOPs: 2*d (S = Q K^T) + 2*d_v (O = P V) per unmasked pair."""
+        return 2 * (self.d + self.d_v) * self.pairs()
 
     def bwd_flops(self) -> int:
         """Algorithmic backward FLOPs: five GEMMs, i.e. 2.5x the forward."""
@@ -103,9 +108,10 @@ def make(w: Workload, with_grad: bool = True) -> dict:
     Dense layout ``[B, L, H, d]``; varlen ``[T, H, d]`` plus ``cu_seqlens``.
     """
     shape = (w.total, w.H, w.d) if w.varlen else (w.B, w.L, w.H, w.d)
+    vshape = shape[:-1] + (w.d_v,)
     q = _randn(shape, 10 * w.seed + 0)
     k = _randn(shape, 10 * w.seed + 1)
-    v = _randn(shape, 10 * w.seed + 2)
+    v = _randn(vshape, 10 * w.seed + 2)
     if w.kspike_frac > 0:
         g = torch.Generator("cpu").manual_seed(10 * w.seed + 4)
         n = max(1, int(round(w.kspike_frac * w.L)))
@@ -116,18 +122,20 @@ def make(w: Workload, with_grad: bool = True) -> dict:
             k[b, pos] *= w.kspike
     out = {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
     if with_grad:
-        out["do"] = _randn(shape, 10 * w.seed + 3).to(torch.bfloat16)
+        out["do"] = _randn(vshape, 10 * w.seed + 3).to(torch.bfloat16)
     if w.varlen:
         out["cu_seqlens"] = cu_seqlens(w.lengths)
     return out
 
 
-def small(B=1, H=2, L=128, d=64, causal=False, seed=1, Lk=None) -> dict:
-    """Small dense problem with possibly different query and key lengths."""
+def small(B=1, H=2, L=128, d=64, causal=False, seed=1, Lk=None, dv=None) -> dict:
+    """Small dense problem with possibly different query and key lengths (and
+    a head dim of its own for v and dO)."""
     Lk = L if Lk is None else Lk
+    dv = d if dv is None else dv
     return {
         "q": _randn((B, L, H, d), 10 * seed + 0).to(torch.bfloat16),
         "k": _randn((B, Lk, H, d), 10 * seed + 1).to(torch.bfloat16),
-        "v": _randn((B, Lk, H, d), 10 * seed + 2).to(torch.bfloat16),
-        "do": _randn((B, L, H, d), 10 * seed + 3).to(torch.bfloat16),
+        "v": _randn((B, Lk, H, dv), 10 * seed + 2).to(torch.bfloat16),
+        "do": _randn((B, L, H, dv), 10 * seed + 3).to(torch.bfloat16),
     }

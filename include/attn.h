@@ -70,6 +70,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              const int* cu_seqlens, cudaStream_t stream);
 
 /*
+ * Forward pass with a head dim of its own for v and o: q and k are
+ * [.., H, d], v and o are [.., H, dv] (o has the rows of q). Supported:
+ * dv = d (the same as attn_fwd), and d = 192 with dv = 128 (the shape of the
+ * FlashAttention-4 paper's Section 5.1, Fig. 5). LSE as in attn_fwd. Other
+ * pairs return ATTN_ERR_ARG. No backward for dv != d.
+ */
+int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int Lq, int Lk, int d, int dv, float scale, int causal,
+                  const int* cu_seqlens, cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (same size
  * arguments as attn_bwd; for varlen pass Lq = Lk = T). The workspace holds the
  * fp32 dQ accumulator, the row terms D_i = <dO_i, O_i>, and the semaphores of

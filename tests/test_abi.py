@@ -61,6 +61,11 @@ def test_argument_errors_need_no_gpu(built):
     assert lib.attn_fwd(dummy + 2, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 64, 0.1, 0, None, None) == -2
     # varlen requires Lq == Lk (both the packed row count)
     assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 2, 1, 128, 64, 64, 0.1, 0, dummy, None) == -1
+    # separate value head dim: only (192, 128) besides dv = d
+    assert lib.attn_fwd_hdim(dummy, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 128, 64, 0.1, 0, None, None) == -1
+    assert "dv=64" in binding.last_error()
+    assert lib.attn_fwd_hdim(dummy + 2, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 192, 128, 0.1, 0, None,
+                             None) == -2
     # backward: workspace too small
     ws = lib.attn_bwd_workspace_size(1, 1, 128, 128, 64, 0, 0)
     assert ws > 0

@@ -81,6 +81,38 @@ def test_varlen_small_full(causal, d):
     assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"varlen causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [1, 77, 128, 129, 300, 513])
+def test_value_head_dim_192_128(L, causal):
+    """q/k head dim 192 with v (and O) head dim 128 (attn_fwd_hdim)."""
+    t = inputs.small(B=2, H=3, L=L, d=192, dv=128, seed=31)
+    scale = float(np.float32(1.0 / np.sqrt(192)))
+    o, lse = run_dense(t, causal, scale)
+    assert o.shape == (2, L, 3, 128)
+    o_ref, lse_ref = oracle_fwd_subset(t, scale, causal, heads=[0, 1, 2])
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"d192/dv128 L={L} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_value_head_dim_rectangular_and_varlen(causal):
+    t = inputs.small(B=2, H=2, L=200, Lk=77, d=192, dv=128, seed=32)
+    o, lse = run_dense(t, causal, 0.07)
+    o_ref, lse_ref = oracle_fwd_subset(t, 0.07, causal, heads=[0, 1])
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"d192/dv128 Lq=200 Lk=77 causal={causal}")
+    lens = [1, 128, 200, 513, 77, 256]
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    g = torch.Generator("cpu").manual_seed(33)
+    tv = {"q": torch.randn(T, 2, 192, generator=g).to(torch.bfloat16),
+          "k": torch.randn(T, 2, 192, generator=g).to(torch.bfloat16),
+          "v": torch.randn(T, 2, 128, generator=g).to(torch.bfloat16)}
+    q, k, v = (tv[n].cuda() for n in ("q", "k", "v"))
+    o, lse = binding.forward(q, k, v, causal=causal, scale=0.07, cu_seqlens=cu.cuda())
+    binding.check_status()
+    o_ref, lse_ref = oracle_fwd_subset(tv, 0.07, causal, heads=[0, 1], cu=cu.numpy())
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, f"d192/dv128 varlen causal={causal}")
+
+
 def test_empty_batch_is_a_no_op():
     q = torch.empty(0, 128, 2, 64, dtype=torch.bfloat16, device="cuda")
     o, lse = binding.forward(q, q, q, causal=True)
@@ -125,6 +157,11 @@ def test_workload_b4h16l4096(causal):
 @pytest.mark.parametrize("d", [64, 128, 192, 256])
 def test_workload_hdsweep(d):
     _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
+
+
+def test_workload_hdsweep_value_head_dim():
+    """B2 H16 L8192, q/k head dim 192, v head dim 128, causal, spiky K."""
+    _workload_check(inputs.HDSWEEP.with_(d=192, dv=128), True, heads=[3])
 
 
 @pytest.mark.parametrize("causal", [False, True])
