@@ -55,12 +55,12 @@ def bind(path: str):
     lib = ctypes.CDLL(path)
     lib.oracle_fwd.restype = ctypes.c_int
     lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp,
-                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                _ip, _ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_bwd.restype = ctypes.c_int
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp,
-                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
     return lib
@@ -103,23 +103,26 @@ def _ptr(a, typ):
 
 
 def _dims(q, k, cu):
+    """B, H (query heads), Hkv (key/value heads), Lq, Lk, d."""
     if cu is None:
         if q.ndim != 4 or k.ndim != 4:
             raise ValueError("dense tensors must be [B, L, H, d]")
         B, Lq, H, d = q.shape
-        Lk = k.shape[1]
-        if k.shape[0] != B or k.shape[2] != H or k.shape[3] != d:
+        Lk, Hkv = k.shape[1], k.shape[2]
+        if k.shape[0] != B or k.shape[3] != d:
             raise ValueError("q/k shape mismatch")
-        return B, H, Lq, Lk, d
-    if q.ndim != 3:
-        raise ValueError("varlen tensors must be [T, H, d]")
-    T, H, d = q.shape
-    B = len(cu) - 1
-    if cu[-1] != T or k.shape[0] != T:
-        raise ValueError("cu_seqlens[-1] must equal the packed length")
-    L = int(np.max(np.diff(cu))) if B > 0 else 0
-    return B, H, L, L, d
-
+    else:
+        if q.ndim != 3:
+            raise ValueError("varlen tensors must be [T, H, d]")
+        T, H, d = q.shape
+        Hkv = k.shape[1]
+        B = len(cu) - 1
+        if cu[-1] != T or k.shape[0] != T or k.shape[2] != d:
+            raise ValueError("cu_seqlens[-1] must equal the packed length")
+        Lq = Lk = int(np.max(np.diff(cu))) if B > 0 else 0
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    return B, H, Hkv, Lq, Lk, d
 
 def _dv(v, k):
     """Head dim of v (may differ from that of q and k); v must match k otherwise."""
@@ -137,13 +140,13 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     cu = _i32(cu_seqlens)
-    B, H, Lq, Lk, d = _dims(q, k, cu)
+    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu)
     dv = _dv(v, k)
     o = np.full(q.shape[:-1] + (dv,), np.nan)
     lse = np.full((B, H, Lq) if cu is None else (H, q.shape[0]), np.nan)
     r = _i32(rows)
     rc = _load().oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
-                            B, H, Lq, Lk, d, dv, float(scale), int(bool(causal)),
+                            B, H, Hkv, Lq, Lk, d, dv, float(scale), int(bool(causal)),
                             _ptr(cu, _ip), _ptr(r, _ip), 0 if r is None else len(r),
                             nthreads or default_threads())
     if rc != 0:
@@ -160,7 +163,7 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     cu = _i32(cu_seqlens)
-    B, H, Lq, Lk, d = _dims(q, k, cu)
+    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu)
     dvd = _dv(v, k)
     if dout.shape != q.shape[:-1] + (dvd,):
         raise ValueError("dout must have the rows and heads of q and the head dim of v")
@@ -170,7 +173,7 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     qr, kr = _i32(qrows), _i32(krows)
     rc = _load().oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp),
                             _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
-                            B, H, Lq, Lk, d, dvd, float(scale), int(bool(causal)), _ptr(cu, _ip),
+                            B, H, Hkv, Lq, Lk, d, dvd, float(scale), int(bool(causal)), _ptr(cu, _ip),
                             _ptr(qr, _ip), 0 if qr is None else len(qr),
                             _ptr(kr, _ip), 0 if kr is None else len(kr),
                             nthreads or default_threads())

@@ -21,6 +21,13 @@
  * (equal to d for the textbook case; the FlashAttention-4 paper's Section 5.1
  * also measures d = 192 for q/k with 128 for v, Fig. 5).
  *
+ * Grouped heads (multi-query and grouped-query attention, which the paper's
+ * Section 3.3 schedules by key/value head): q, o, dout, dq have H heads; k, v,
+ * dk, dv have Hkv heads (H a multiple of Hkv), and query head h reads
+ * key/value head h / (H / Hkv), so consecutive query heads share one key/value
+ * head. dk and dv of a key/value head sum over the query heads of its group.
+ * Hkv = H is the plain multi-head case.
+ *
  * Backward, for the scalar loss L = sum(O * dO) (FlashAttention-4 paper,
  * Section 3.2.2: five products -- S recomputed, dP = dO V^T, dV = P^T dO,
  * dQ = dS K, dK = dS^T Q):
@@ -39,9 +46,10 @@
  * outputs (rows of O / dQ, rows of dK / dV) between them.
  *
  * Layouts (row-major, element counts):
- *   dense  : q, o, dq  [B, Lq, H, d];  k, v, dk, dv [B, Lk, H, d];  lse [B, H, Lq]
+ *   dense  : q, o, dq  [B, Lq, H, d];  k, v, dk, dv [B, Lk, Hkv, d];  lse [B, H, Lq]
  *   varlen : cu_seqlens[B+1] (host, int32) packs B sequences; sequence b has
- *            Lq_b = Lk_b = cu[b+1]-cu[b] rows; q,k,v,o,...  [T, H, d]; lse [H, T]
+ *            Lq_b = Lk_b = cu[b+1]-cu[b] rows; q, o, dq [T, H, d];
+ *            k, v, dk, dv [T, Hkv, d]; lse [H, T]
  *            (T = cu[B]); Lq and Lk are then ignored.
  *
  * Row subsets: `rows` (nrows entries) lists query-row indices, relative to
@@ -61,7 +69,7 @@
 typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv;
-    int B, H, Lq, Lk, d, dvh, causal;   /* dvh: head dim of v, o, dout, dv */
+    int B, H, Hkv, Lq, Lk, d, dvh, causal;   /* Hkv: heads of k, v; dvh: head dim of v, o, dout, dv */
     double scale;
     const int *cu;          /* NULL for dense */
     /* per (b, h, row) statistics used by the backward pass */
@@ -91,6 +99,21 @@ static long row_off_v(const job_t *J, int b, int i, int h, int L) {
     return (((long)b * L + i) * J->H + h) * J->dvh;
 }
 
+/* key/value head read by query head h */
+static int kvh(const job_t *J, int h) { return h / (J->H / J->Hkv); }
+
+/* element offset of row j of key/value head hk in a [.., L, Hkv, d] tensor (k, dk) */
+static long row_off_k(const job_t *J, int b, int j, int hk, int L) {
+    if (J->cu) return ((long)(J->cu[b] + j) * J->Hkv + hk) * J->d;
+    return (((long)b * L + j) * J->Hkv + hk) * J->d;
+}
+
+/* the same with head dim dvh (v, dv) */
+static long row_off_kv(const job_t *J, int b, int j, int hk, int L) {
+    if (J->cu) return ((long)(J->cu[b] + j) * J->Hkv + hk) * J->dvh;
+    return (((long)b * L + j) * J->Hkv + hk) * J->dvh;
+}
+
 /* index of (b, h, i) into an lse-shaped array */
 static long stat_off(const job_t *J, int b, int h, int i) {
     if (J->cu) return (long)h * J->cu[J->B] + J->cu[b] + i;
@@ -112,7 +135,7 @@ static double dot(const double *a, const double *b, int n) {
 
 static double score(const job_t *J, int b, int h, int i, int j) {
     const double *qi = J->q + row_off(J, b, i, h, J->Lq);
-    const double *kj = J->k + row_off(J, b, j, h, J->Lk);
+    const double *kj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);
     return J->scale * dot(qi, kj, J->d);
 }
 
@@ -140,7 +163,7 @@ static void row_out(const job_t *J, int b, int h, int i, double lse, double *out
     for (int j = 0; j < lk; j++) {
         if (!allowed(J, b, i, j)) continue;
         double p = exp(score(J, b, h, i, j) - lse);
-        const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);
+        const double *vj = J->v + row_off_kv(J, b, j, kvh(J, h), J->Lk);
         for (int c = 0; c < dv; c++) out[c] += p * vj[c];
     }
 }
@@ -150,7 +173,7 @@ static double dscore(const job_t *J, int b, int h, int i, int j) {
     long st = stat_off(J, b, h, i);
     double p = exp(score(J, b, h, i, j) - J->lse_all[st]);
     const double *doi = J->dout + row_off_v(J, b, i, h, J->Lq);
-    const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);
+    const double *vj = J->v + row_off_kv(J, b, j, kvh(J, h), J->Lk);
     return p * (dot(doi, vj, J->dvh) - J->D_all[st]);
 }
 
@@ -181,26 +204,29 @@ static void do_item(job_t *J, int b, int h, int i) {
         for (int j = 0; j < lk; j++) {
             if (!allowed(J, b, i, j)) continue;
             double ds = dscore(J, b, h, i, j);
-            const double *kj = J->k + row_off(J, b, j, h, J->Lk);
+            const double *kj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);
             for (int c = 0; c < d; c++) dqi[c] += ds * kj[c];
         }
         for (int c = 0; c < d; c++) dqi[c] *= J->scale;
-    } else { /* PH_DKV: item row index is a key row j */
-        int j = i, lq = seq_lq(J, b);
-        double *dkj = J->dk + row_off(J, b, j, h, J->Lk);
-        double *dvj = J->dv + row_off_v(J, b, j, h, J->Lk);
+    } else { /* PH_DKV: item (b, hk, j): key row j of key/value head hk, summed
+                over the query heads of its group */
+        int j = i, hk = h, lq = seq_lq(J, b), g = J->H / J->Hkv;
+        double *dkj = J->dk + row_off_k(J, b, j, hk, J->Lk);
+        double *dvj = J->dv + row_off_kv(J, b, j, hk, J->Lk);
+        const double *vj = J->v + row_off_kv(J, b, j, hk, J->Lk);
         for (int c = 0; c < d; c++) dkj[c] = 0.0;
         for (int c = 0; c < dv; c++) dvj[c] = 0.0;
-        for (int r = 0; r < lq; r++) {
-            if (!allowed(J, b, r, j)) continue;
-            long st = stat_off(J, b, h, r);
-            double p = exp(score(J, b, h, r, j) - J->lse_all[st]);
-            const double *dor = J->dout + row_off_v(J, b, r, h, J->Lq);
-            const double *qr = J->q + row_off(J, b, r, h, J->Lq);
-            double ds = p * (dot(dor, J->v + row_off_v(J, b, j, h, J->Lk), dv) - J->D_all[st]);
-            for (int c = 0; c < d; c++) dkj[c] += ds * qr[c];
-            for (int c = 0; c < dv; c++) dvj[c] += p * dor[c];
-        }
+        for (int hq = hk * g; hq < hk * g + g; hq++)
+            for (int r = 0; r < lq; r++) {
+                if (!allowed(J, b, r, j)) continue;
+                long st = stat_off(J, b, hq, r);
+                double p = exp(score(J, b, hq, r, j) - J->lse_all[st]);
+                const double *dor = J->dout + row_off_v(J, b, r, hq, J->Lq);
+                const double *qr = J->q + row_off(J, b, r, hq, J->Lq);
+                double ds = p * (dot(dor, vj, dv) - J->D_all[st]);
+                for (int c = 0; c < d; c++) dkj[c] += ds * qr[c];
+                for (int c = 0; c < dv; c++) dvj[c] += p * dor[c];
+            }
         for (int c = 0; c < d; c++) dkj[c] *= J->scale;
     }
 }
@@ -238,7 +264,7 @@ static int *make_items(const job_t *J, const int *rows, int nrows, int kind, lon
     long cap = 0;
     for (int b = 0; b < J->B; b++) {
         int L = kind ? seq_lk(J, b) : seq_lq(J, b);
-        cap += (long)J->H * (rows ? nrows : L);
+        cap += (long)(kind ? J->Hkv : J->H) * (rows ? nrows : L);
     }
     int *items = (int *)malloc(sizeof(int) * 3 * (size_t)(cap > 0 ? cap : 1));
     if (!items) return NULL;
@@ -246,7 +272,7 @@ static int *make_items(const job_t *J, const int *rows, int nrows, int kind, lon
     for (int b = 0; b < J->B; b++) {
         int L = kind ? seq_lk(J, b) : seq_lq(J, b);
         int cnt = rows ? nrows : L;
-        for (int h = 0; h < J->H; h++)
+        for (int h = 0; h < (kind ? J->Hkv : J->H); h++)   /* key rows: key/value heads */
             for (int t = 0; t < cnt; t++) {
                 int i = rows ? rows[t] : t;
                 if (i < 0 || i >= L) continue;
@@ -258,8 +284,8 @@ static int *make_items(const job_t *J, const int *rows, int nrows, int kind, lon
     return items;
 }
 
-static int check_args(int B, int H, int Lq, int Lk, int d, int dv, const int *cu) {
-    if (B < 0 || H < 1 || d < 1 || dv < 1) return -1;
+static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu) {
+    if (B < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || dv < 1) return -1;
     if (!cu && (Lq < 0 || Lk < 0)) return -1;
     if (cu) {
         if (cu[0] != 0) return -1;
@@ -269,20 +295,21 @@ static int check_args(int B, int H, int Lq, int Lk, int d, int dv, const int *cu
 }
 
 static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
-                     int B, int H, int Lq, int Lk, int d, int dv, double scale, int causal, const int *cu) {
+                     int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
+                     const int *cu) {
     memset(J, 0, sizeof(*J));
     J->q = q; J->k = k; J->v = v; J->dout = dout;
-    J->B = B; J->H = H; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
+    J->B = B; J->H = H; J->Hkv = Hkv; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
     J->scale = scale; J->causal = causal != 0; J->cu = cu;
 }
 
 int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
-               int B, int H, int Lq, int Lk, int d, int dv, double scale, int causal,
+               int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
                const int *cu_seqlens, const int *rows, int nrows, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (check_args(B, H, Lq, Lk, d, dv, cu_seqlens)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens)) return -1;
     job_t J;
-    init_job(&J, q, k, v, NULL, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens);
     J.o = o; J.lse = lse;
     long n;
     int *items = make_items(&J, rows, nrows, 0, &n);
@@ -294,14 +321,14 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
 
 int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
                double *dq, double *dk, double *dv,
-               int B, int H, int Lq, int Lk, int d, int dvd, double scale, int causal,
+               int B, int H, int Hkv, int Lq, int Lk, int d, int dvd, double scale, int causal,
                const int *cu_seqlens, const int *qrows, int nqrows,
                const int *krows, int nkrows, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    if (check_args(B, H, Lq, Lk, d, dvd, cu_seqlens)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens)) return -1;
     if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
     job_t J;
-    init_job(&J, q, k, v, dout, B, H, Lq, Lk, d, dvd, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, cu_seqlens);
     J.dq = dq; J.dk = dk; J.dv = dv;
 
     /* longest sequence, the range of relative row indices */

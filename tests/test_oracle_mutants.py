@@ -24,10 +24,14 @@ MUTANTS = [
     ("top-left causal alignment", "return j <= i + (lk - lq);", "return j <= i;"),
     ("LSE without the max", "return m + log(sum);", "return log(sum);"),
     ("base-2 exponential", "sum += exp(score(J, b, h, i, j) - m);", "sum += exp2(score(J, b, h, i, j) - m);"),
-    ("O sums keys instead of values", "const double *vj = J->v + row_off_v(J, b, j, h, J->Lk);\n        for (int c = 0; c < dv; c++) out[c]",
-     "const double *vj = J->k + row_off(J, b, j, h, J->Lk);\n        for (int c = 0; c < dv; c++) out[c]"),
-    ("score uses key row i", "const double *kj = J->k + row_off(J, b, j, h, J->Lk);\n    return",
-     "const double *kj = J->k + row_off(J, b, i < J->Lk ? i : 0, h, J->Lk);\n    return"),
+    ("O sums keys instead of values", "const double *vj = J->v + row_off_kv(J, b, j, kvh(J, h), J->Lk);\n        for (int c = 0; c < dv; c++) out[c]",
+     "const double *vj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);\n        for (int c = 0; c < dv; c++) out[c]"),
+    ("score uses key row i", "const double *kj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);\n    return",
+     "const double *kj = J->k + row_off_k(J, b, i < J->Lk ? i : 0, kvh(J, h), J->Lk);\n    return"),
+    ("interleaved head groups", "static int kvh(const job_t *J, int h) { return h / (J->H / J->Hkv); }",
+     "static int kvh(const job_t *J, int h) { return h % J->Hkv; }"),
+    ("dK/dV from the group's first query head only", "for (int hq = hk * g; hq < hk * g + g; hq++)",
+     "for (int hq = hk * g; hq < hk * g + 1; hq++)"),
     ("dS sign flip", "return p * (dot(doi, vj, J->dvh) - J->D_all[st]);", "return p * (dot(doi, vj, J->dvh) + J->D_all[st]);"),
     ("D dropped", "J->D_all[st] = dot(", "J->D_all[st] = 0.0 * dot("),
     ("dQ without scale", "for (int c = 0; c < d; c++) dqi[c] *= J->scale;", ""),
@@ -56,6 +60,8 @@ BATTERY = [
     (pins.test_bwd_column_sums, ()),
     (pins.test_fwd_matches_textbook_softmax_value_dim, (2, 3, 5, 5, 4, 3, False)),
     (pins.test_bwd_finite_differences_value_dim, (True,)),
+    (pins.test_fwd_grouped_heads_match_textbook, (1, 6, 3, 7, 9, 3, True)),
+    (pins.test_bwd_finite_differences_grouped_heads, (False,)),
 ]
 
 

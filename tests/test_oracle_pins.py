@@ -118,6 +118,21 @@ def test_single_key_returns_v_row_of_its_own_width():
     np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Hkv,Lq,Lk,d", [(2, 4, 2, 5, 5, 4), (1, 6, 3, 7, 9, 3), (1, 4, 1, 6, 6, 5)])
+def test_fwd_grouped_heads_match_textbook(B, H, Hkv, Lq, Lk, d, causal):
+    """Grouped key/value heads: query head h reads key/value head h // (H / Hkv).
+    The textbook softmax on K and V with each key/value head repeated for the
+    query heads of its group gives the same result (Hkv = 1 is multi-query)."""
+    q, k, v = rnd((B, Lq, H, d), 13), rnd((B, Lk, Hkv, d), 14), rnd((B, Lk, Hkv, d), 15)
+    o, lse = oracle.fwd(q, k, v, 0.55, causal)
+    g = H // Hkv
+    o_ref, lse_ref = textbook(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2), 0.55, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-12, atol=1e-12)
+
+
 def test_single_key_returns_v():
     q, k, v = rnd((2, 6, 3, 8), 4), rnd((2, 1, 3, 8), 5), rnd((2, 1, 3, 8), 6)
     s = 0.3 * np.einsum("bihc,bhc->bhi", q, k[:, 0])
@@ -315,6 +330,18 @@ def test_bwd_finite_differences_value_dim(causal):
     dq, dk, dv = oracle.bwd(q, k, v, do, 0.7, causal)
     assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
     fq, fk, fv = finite_diff(q, k, v, do, 0.7, causal)
+    for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.abs(got - ref).max() < 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_finite_differences_grouped_heads(causal):
+    """dK and dV of a key/value head sum over the query heads of its group."""
+    q, k = rnd((1, 5, 4, 3), 64), rnd((1, 6, 2, 3), 65)
+    v, do = rnd((1, 6, 2, 3), 66), rnd((1, 5, 4, 3), 67)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.8, causal)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    fq, fk, fv = finite_diff(q, k, v, do, 0.8, causal)
     for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
         assert np.abs(got - ref).max() < 1e-7
 
