@@ -3,7 +3,9 @@
 
 A step is one pass of the whole path over one batch of synthetic input: for
 each mask variant of the workload, the forward (attn_fwd) and the backward
-(attn_bwd: preprocess, main kernel, dQ conversion). The default workload is
+(attn_bwd: preprocess, main kernel, dQ conversion), called through their
+grouped-head forms (attn_fwd_gqa, attn_bwd_gqa; key/value heads = H except
+in the grouped workload). The default workload is
 B=4, H=16, L=4096, d=128 (bf16), causal and non-causal. Throughput is
 algorithmic FLOPs / time: forward 4*d per unmasked (query, key) pair,
 backward 2.5x that.
@@ -45,6 +47,8 @@ WORKLOADS = {
     "b2h16l8192d256": (inputs.HDSWEEP.with_(d=256), (True,)),
     # q/k head dim 192 with v head dim 128 (attn_fwd_hdim): forward only
     "b2h16l8192dqk192dv128": (inputs.HDSWEEP.with_(d=192, dv=128), (True,)),
+    # grouped heads (attn_fwd_gqa / attn_bwd_gqa): 16 query heads over 2 key/value heads
+    "b2h16kv2l8192d128": (inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
     "b1h32l32768d128": (inputs.LONG, (True, False)),
 }
@@ -116,6 +120,7 @@ class Problem:
         self.cu = t["cu_seqlens"].to(device) if w.varlen else None
         self.o = torch.empty(self.q.shape[:-1] + (w.d_v,), dtype=self.q.dtype, device=device)
         self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
+        self.Hkv = w.H_kv
         if w.varlen:
             self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.total, w.total, w.d
             self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=device)
@@ -126,15 +131,15 @@ class Problem:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def fwd(self, causal):
-        rc = binding.attn_fwd_hdim(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Lq, self.Lk,
-                                   self.d, self.w.d_v, self.w.scale, causal, self.cu)
+        rc = binding.attn_fwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
+                                  self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
     def bwd(self, causal):
-        rc = binding.attn_bwd(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
-                              self.B, self.H, self.Lq, self.Lk, self.d, self.w.scale, causal, self.cu, 0,
-                              self.ws, self.ws.numel())
+        rc = binding.attn_bwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
+                                  self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.scale, causal, self.cu,
+                                  0, self.ws, self.ws.numel())
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -396,7 +401,8 @@ def run_ours(args, world, rank, local, dist):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": args.workload, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.d_v,
+                "config": {"workload": args.workload, "B": w.B, "H": w.H, "H_kv": w.H_kv, "L": w.L, "d": w.d,
+                           "d_v": w.d_v,
                            "calls": list(kinds),
                            "variants": ["causal" if c else "non-causal" for c in variants],
                            "flops_per_step": step_flops,

@@ -35,11 +35,16 @@ def _declare(lib):
     lib.attn_fwd.argtypes = [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_fwd_hdim.restype = c_int
     lib.attn_fwd_hdim.argtypes = [c_void_p] * 5 + [c_int] * 6 + [c_float, c_int, c_void_p, c_void_p]
+    lib.attn_fwd_gqa.restype = c_int
+    lib.attn_fwd_gqa.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
     lib.attn_bwd_workspace_size.argtypes = [c_int] * 7
     lib.attn_bwd.restype = c_int
     lib.attn_bwd.argtypes = ([c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p, c_size_t,
                                                                c_void_p])
+    lib.attn_bwd_gqa.restype = c_int
+    lib.attn_bwd_gqa.argtypes = ([c_void_p] * 9 + [c_int] * 6 + [c_float, c_int, c_void_p, c_int, c_void_p,
+                                                                   c_size_t, c_void_p])
     lib.attn_bwd_noalloc.restype = c_int
     lib.attn_bwd_noalloc.argtypes = [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p]
     lib.attn_last_error.restype = ctypes.c_char_p
@@ -122,6 +127,10 @@ def attn_fwd_hdim(q, k, v, o, lse, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlen
                                 int(causal), _ptr(cu_seqlens), _stream(stream))
 
 
+def attn_fwd_gqa(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens=None, stream=None) -> int:
+    return load().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Lq, Lk, d, dv, scale,
+                               int(causal), _ptr(cu_seqlens), _stream(stream))
+
 
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
     return load().attn_bwd_workspace_size(B, H, Lq, Lk, d, int(causal), int(deterministic))
@@ -132,6 +141,13 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, 
     return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                            _ptr(dv), B, H, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens), int(deterministic),
                            _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens, deterministic,
+                 workspace, ws_bytes, stream=None) -> int:
+    return load().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, Hkv, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens),
+                               int(deterministic), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
@@ -154,11 +170,12 @@ def attn_check_status(stream=None) -> int:
 # ---------------------------------------------------------------- tensor-level helpers
 
 def _dims(q, k, cu_seqlens):
+    """B, H, Lq, Lk, d and the key/value heads Hkv."""
     if cu_seqlens is None:
         B, Lq, H, d = q.shape
-        return B, H, Lq, k.shape[1], d
+        return B, H, Lq, k.shape[1], d, k.shape[2]
     T, H, d = q.shape
-    return cu_seqlens.numel() - 1, H, T, k.shape[0], d
+    return cu_seqlens.numel() - 1, H, T, k.shape[0], d, k.shape[1]
 
 
 def _check_tensors(*ts):
@@ -172,16 +189,19 @@ def _check_tensors(*ts):
 def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
             stream=None):
     """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens).
-    v (and O) may have a head dim of their own (d = 192 with 128)."""
+    v (and O) may have a head dim of their own (d = 192 with 128); k and v may
+    have fewer heads than q (grouped heads: query head h reads h // (H // Hkv))."""
     _check_tensors(q, k, v, cu_seqlens)
-    B, H, Lq, Lk, d = _dims(q, k, cu_seqlens)
+    B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     dv = v.shape[-1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     if out is None:
         out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
-    if dv == d:
+    if Hkv != H:
+        _check(attn_fwd_gqa(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, stream))
+    elif dv == d:
         _check(attn_fwd(q, k, v, out, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens, stream))
     else:
         _check(attn_fwd_hdim(q, k, v, out, lse, B, H, Lq, Lk, d, dv, scale, causal, cu_seqlens, stream))
@@ -190,9 +210,10 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
 
 def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu_seqlens=None,
              deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None):
-    """dQ, dK, dV (bf16) for the loss sum(O * dO)."""
+    """dQ, dK, dV (bf16) for the loss sum(O * dO); k and v may have fewer heads
+    than q (grouped heads), dK and dV then have theirs."""
     _check_tensors(q, k, v, o, lse, dout, cu_seqlens)
-    B, H, Lq, Lk, d = _dims(q, k, cu_seqlens)
+    B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
@@ -200,8 +221,13 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check(attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
-                    deterministic, workspace, workspace.numel() * workspace.element_size(), stream))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if Hkv != H:
+        _check(attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
+                            deterministic, workspace, ws_bytes, stream))
+    else:
+        _check(attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
+                        deterministic, workspace, ws_bytes, stream))
     return dq, dk, dv
 
 

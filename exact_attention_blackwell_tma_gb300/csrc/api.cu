@@ -120,11 +120,13 @@ uint64_t wait_budget_ns() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Heads per L2 section for the LPT walk: K and V of a section should fit in
-// about half of the 129 MB L2 (FlashAttention-4 paper, Section 3.3).
-int head_section(int H, long keys, int d) {
+// Heads per L2 section for the LPT walk: the two bf16 tensors every tile of a
+// head streams (K and V in the forward, Q and dO in the backward) should fit
+// in about half of the 129 MB L2 (FlashAttention-4 paper, Section 3.3).
+// `rows` is the rows of those tensors per walked head.
+int head_section(int H, long rows, int d) {
     const double budget = 64.0 * 1024 * 1024;
-    double per_head = 2.0 * 2.0 * (double)keys * d;   // K and V, bf16
+    double per_head = 2.0 * 2.0 * (double)rows * d;   // two tensors, bf16
     int hs = per_head > 0 ? (int)(budget / per_head) : H;
     if (hs < 1) hs = 1;
     if (hs > H) hs = H;
@@ -146,6 +148,12 @@ int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu
     return ATTN_OK;
 }
 
+int check_heads(int H, int Hkv) {
+    if (Hkv < 1 || Hkv > H || H % Hkv != 0)
+        return fail(ATTN_ERR_ARG, "key/value heads %d must divide the query heads %d", Hkv, H);
+    return ATTN_OK;
+}
+
 }  // namespace
 
 int* device_status_word() {
@@ -157,10 +165,12 @@ int* device_status_word() {
 
 using namespace attn;
 
-extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                             int Lq, int Lk, int d, int dv, float scale, int causal, const int* cu_seqlens,
-                             cudaStream_t stream) {
+extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
+                            const int* cu_seqlens, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, false);
+    if (rc) return rc;
+    rc = check_heads(H, Hkv);
     if (rc) return rc;
     if (dv != d && !(d == 192 && dv == 128))
         return fail(ATTN_ERR_ARG, "head dims d=%d, dv=%d not supported (dv = d, or d = 192 with dv = 128)", d, dv);
@@ -178,6 +188,8 @@ extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* 
     p.g.Lq = Lq;
     p.g.Lk = Lk;
     p.g.d = d;
+    p.g.Hkv = Hkv;
+    p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
     p.g.causal = causal ? 1 : 0;
     p.g.scale = scale;
@@ -190,7 +202,8 @@ extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* 
     const int rows_per_tile = wide ? 128 : 256;
     p.nm = (Lq + rows_per_tile - 1) / rows_per_tile;
     p.n_tiles = cu_seqlens ? 0 : B * H * p.nm;
-    p.head_section = head_section(H, cu_seqlens ? (rows_k / B) : Lk, d);
+    // the query heads of a group share their K and V in L2
+    p.head_section = head_section(H, (cu_seqlens ? (rows_k / B) : Lk) / p.g.group, d);
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();
     CUtensorMap tq, tk, tv;
@@ -199,17 +212,24 @@ extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* 
     const void* kp = rows_k > 0 ? k : q;
     const void* vp = rows_k > 0 ? v : q;
     // (a problem with no keys maps v like q, so its width must be d there)
-    if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, H, d) ||
-        !make_map(&tv, vp, krows, H, rows_k > 0 ? dv : d))
+    // (q has at least as many heads as k and v, so a view of it with Hkv heads is in bounds)
+    if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, Hkv, d) ||
+        !make_map(&tv, vp, krows, Hkv, rows_k > 0 ? dv : d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream) : launch_fwd(tq, tk, tv, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
 
+extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int Lq, int Lk, int d, int dv, float scale, int causal, const int* cu_seqlens,
+                             cudaStream_t stream) {
+    return attn_fwd_gqa(q, k, v, o, lse, B, H, H, Lq, Lk, d, dv, scale, causal, cu_seqlens, stream);
+}
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
                         int Lk, int d, float scale, int causal, const int* cu_seqlens, cudaStream_t stream) {
-    return attn_fwd_hdim(q, k, v, o, lse, B, H, Lq, Lk, d, d, scale, causal, cu_seqlens, stream);
+    return attn_fwd_gqa(q, k, v, o, lse, B, H, H, Lq, Lk, d, d, scale, causal, cu_seqlens, stream);
 }
 
 namespace {
@@ -244,11 +264,13 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, i
     return a.total > b.total ? a.total : b.total;
 }
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
-                        float scale, int causal, const int* cu_seqlens, int deterministic, void* workspace,
-                        size_t ws_bytes, cudaStream_t stream) {
+extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
+                            int d, float scale, int causal, const int* cu_seqlens, int deterministic,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, true);
+    if (rc) return rc;
+    rc = check_heads(H, Hkv);
     if (rc) return rc;
     const bool varlen = cu_seqlens != nullptr;
     const long rows_q = varlen ? (long)Lq : (long)B * Lq;
@@ -274,6 +296,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.g.Lq = Lq;
     p.g.Lk = Lk;
     p.g.d = d;
+    p.g.Hkv = Hkv;
+    p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
     p.g.causal = causal ? 1 : 0;
     p.g.scale = scale;
@@ -290,20 +314,33 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.deterministic = deterministic ? 1 : 0;
     p.nm = (Lk + 127) / 128;
     p.nq = (Lq + 127) / 128;
-    p.n_tiles = varlen ? 0 : B * H * p.nm;
-    p.head_section = head_section(H, varlen ? (rows_q / B) : Lq, d);
+    // a work tile is one key block of one key/value head; it streams Q and dO
+    // of every query head of the group
+    p.n_tiles = varlen ? 0 : B * Hkv * p.nm;
+    p.head_section = head_section(Hkv, (varlen ? (rows_q / B) : Lq) * (long)p.g.group, d);
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();
     CUtensorMap tq, tk, tv, tdo, tdq;
     const long qrows = rows_q > 0 ? rows_q : rows_k;
     const long krows = rows_k > 0 ? rows_k : rows_q;
-    if (!make_map(&tq, rows_q > 0 ? q : k, qrows, H, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, H, d) ||
-        !make_map(&tv, rows_k > 0 ? v : q, krows, H, d) || !make_map(&tdo, rows_q > 0 ? dout : k, qrows, H, d) ||
-        !make_map_f32(&tdq, p.dq_acc, qrows, H, d))
+    // Without query rows (or keys) the matching descriptors are never used; they
+    // view the other tensor, with the heads of the smaller one so they stay in bounds.
+    const int hq_map = rows_q > 0 ? H : Hkv;
+    if (!make_map(&tq, rows_q > 0 ? q : k, qrows, hq_map, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, Hkv, d) ||
+        !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d) ||
+        !make_map(&tdo, rows_q > 0 ? dout : k, qrows, hq_map, d) || !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                        float scale, int causal, const int* cu_seqlens, int deterministic, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+    return attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, H, Lq, Lk, d, scale, causal, cu_seqlens,
+                        deterministic, workspace, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- backward without allocation

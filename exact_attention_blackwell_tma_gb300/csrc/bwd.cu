@@ -78,19 +78,36 @@ struct BwdLayout {
 };
 
 struct BwdTile {
-    int b, h, n;       // batch, head, 128-key block
+    int b, h, n;       // batch, key/value head, 128-key block
     int lq, lk;
     int q_row0;        // packed row of query 0 of the sequence
     int k_row0;        // packed row of key 0 of the sequence
     int m_begin, m_end;  // 128-row query blocks that see this key block
+    int hq0;           // first query head of the key/value head's group
+    int nblk;          // query blocks the tile visits: group x (m_end - m_begin)
 };
+
+// The tile's query blocks in visiting order: every query head of the group
+// (all of them before the next key block, so dK and dV of the block collect
+// the whole group in tensor memory), each over [m_begin, m_end).
+struct QWalk {
+    int h, m;   // query head, 128-row query block
+    __device__ __forceinline__ void next(const BwdTile& f) {
+        if (++m == f.m_end) {
+            m = f.m_begin;
+            ++h;
+        }
+    }
+};
+__device__ __forceinline__ QWalk qwalk(const BwdTile& f) { return QWalk{f.hq0, f.m_begin}; }
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
-    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.H, kBN, p.head_section, false)
-                 : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, false) : sched_dense(t, g.H, p.nm, p.head_section, false));
+    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false)
+                 : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, false)
+                             : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
     BwdTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -113,6 +130,8 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
     }
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
+    f.hq0 = f.h * g.group;
+    f.nblk = g.group * (f.m_end - f.m_begin);
     return f;
 }
 
@@ -174,7 +193,7 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
                 vm_out->pre[k] = acc;
                 const int b = vm_out->order[k];
                 const int L = vm_out->start[b + 1] - vm_out->start[b];
-                acc += g.H * ((L + kBN - 1) / kBN);
+                acc += g.Hkv * ((L + kBN - 1) / kBN);   // work tiles are per key/value head
             }
             vm_out->pre[B] = acc;
         }
@@ -287,7 +306,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             __syncwarp();
             ++tile_it;
-            for (int m = f.m_begin; m < f.m_end && ok; ++m) {
+            QWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk && ok; ++u, qw.next(f)) {
+                const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NQS) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
@@ -297,7 +318,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     mbar_expect_tx(bar(Lay::kQFull + st), Lay::kTileBytes);
                     for (int hf = 0; hf < Lay::kHalves; ++hf)
                         tma_load_3d(base + Lay::kQOff + st * Lay::kTileBytes + hf * kBox, &tmQ, bar(Lay::kQFull + st),
-                                    hf * 64, f.h, f.q_row0 + m * kBM);
+                                    hf * 64, qw.h, f.q_row0 + m * kBM);
                 }
                 // row statistics for this query block, negated: -lse in log2 units and -D
                 float* nlse2 = stats + st * 256;
@@ -307,8 +328,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     const int r = m * kBM + lane * 4 + e;
                     float lv = -INFINITY, dv = 0.f;   // negated; rows past the end: P = 0
                     if (r < f.lq) {
-                        long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
-                                         : ((long)f.b * g.H + f.h) * g.Lq + r;
+                        long si = varlen ? (long)qw.h * g.Lq + f.q_row0 + r
+                                         : ((long)f.b * g.H + qw.h) * g.Lq + r;
                         lv = -p.lse[si] * kLog2e;
                         dv = -p.delta[si];
                     }
@@ -326,7 +347,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     mbar_expect_tx(bar(Lay::kDOFull + sd), Lay::kTileBytes);
                     for (int hf = 0; hf < Lay::kHalves; ++hf)
                         tma_load_3d(base + Lay::kDOOff + sd * Lay::kTileBytes + hf * kBox, &tmDO,
-                                    bar(Lay::kDOFull + sd), hf * 64, f.h, f.q_row0 + m * kBM);
+                                    bar(Lay::kDOFull + sd), hf * 64, qw.h, f.q_row0 + m * kBM);
                 }
                 __syncwarp();
                 ++qc;
@@ -389,7 +410,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 tc_commit(bar(Lay::kSFull));
             }
             __syncwarp();
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            for (int u = 0; u < f.nblk; ++u) {
                 const uint32_t sd = qc % NDS, dsb = qc & 1u;   // dO stage, dS tile of this block
                 const SmemDesc do_km = at_stage(do_km0, sd), do_mn = at_stage(do_mn0, sd);
                 const SmemDesc q_mn = at_stage(q_mn0, st);
@@ -416,11 +437,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
                         mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
-                               do_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                               do_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
                     tc_commit(bar(Lay::kDOEmpty + sd));   // dO is no longer read
                 }
                 __syncwarp();
-                const bool more = m + 1 < f.m_end;
+                const bool more = u + 1 < f.nblk;
                 const uint32_t st_next = more ? (qc + 1) % NQS : st;
                 // dK += dS^T Q (dS^T from tensor memory) and dQ = dS K (dS from shared memory)
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
@@ -431,7 +452,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
                         mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(k),
-                               q_mn, desc_step(k * 2048), kIdKV, (m > f.m_begin || k > 0) ? 1u : 0u);
+                               q_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k)
                         mma_ss(tmem + Lay::kTDP, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
@@ -486,8 +507,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
-            __nv_bfloat16* dv_ptr = p.dv + (krow * g.H + f.h) * HD + wg * (HD / 2);
-            __nv_bfloat16* dk_ptr = p.dk + (krow * g.H + f.h) * HD + wg * (HD / 2);
+            __nv_bfloat16* dv_ptr = p.dv + (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
+            __nv_bfloat16* dk_ptr = p.dk + (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
             if (f.m_begin >= f.m_end) {   // no query sees this key block
                 if (key_ok) {
 #pragma unroll
@@ -500,7 +521,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             // query q (inside the sequence) is allowed for this key iff q_lo <= q < lq
             const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            QWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+                const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 uint8_t* ds_tile = ds_tiles + (qc & 1u) * Lay::kDSBytes;   // alternate dS tiles per block
                 ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
@@ -625,7 +648,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const BwdTile f = bwd_tile(t, p, vmp);
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            QWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+                const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
                 // the dS tile this block's dQ MMA read is free now: stage dQ through it
@@ -639,8 +664,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     // dQ tile (b, h, m) takes its key blocks' contributions in ascending
                     // block order: block n waits until n blocks have added theirs. Every
                     // block below n also sees query block m (causal or not).
-                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + tile;
                     if (leader) {
                         if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
@@ -690,7 +715,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
                             // rows past the query block's sequence carry exact zeros (P = 0 there)
                             for (int c2 = 0; c2 < 2; ++c2)
-                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, f.h,
+                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
                                                   f.q_row0 + m * kBM);
                             bulk_commit_group();
                             if (kDet && last) {

@@ -72,11 +72,26 @@ template <int HD>
 __device__ __forceinline__ int chunk_width(int c) { return min(128, HD - 128 * c); }
 
 struct WideBwdTile {
-    int b, h, n, c;      // batch, head, 128-key block, column chunk
+    int b, h, n, c;      // batch, key/value head, 128-key block, column chunk
     int lq, lk;
     int q_row0, k_row0;  // packed rows of query 0 / key 0 of the sequence
     int m_begin, m_end;  // query blocks that see this key block
+    int hq0;             // first query head of the key/value head's group
+    int nblk;            // query blocks the tile visits: group x (m_end - m_begin)
 };
+
+// The tile's query blocks in visiting order: every query head of the group,
+// each over [m_begin, m_end).
+struct WideQWalk {
+    int h, m;   // query head, 128-row query block
+    __device__ __forceinline__ void next(const WideBwdTile& f) {
+        if (++m == f.m_end) {
+            m = f.m_begin;
+            ++h;
+        }
+    }
+};
+__device__ __forceinline__ WideQWalk qwalk(const WideBwdTile& f) { return WideQWalk{f.hq0, f.m_begin}; }
 
 __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
@@ -85,9 +100,9 @@ __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b
 __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
     const int u = t >> 1;
-    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.H, kBN, p.head_section, false)
-                 : (g.causal ? sched_dense_lpt(u, g.B, g.H, p.nm, false)
-                             : sched_dense(u, g.H, p.nm, p.head_section, false));
+    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false)
+                 : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, false)
+                             : sched_dense(u, g.Hkv, p.nm, p.head_section, false));
     WideBwdTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -107,6 +122,8 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     f.m_begin = 0;
     if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
+    f.hq0 = f.h * g.group;
+    f.nblk = g.group * (f.m_end - f.m_begin);
     return f;
 }
 
@@ -199,7 +216,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             ++tile_it;
             const int pc = f.c, po = 1 - f.c;
-            for (int m = f.m_begin; m < f.m_end && ok; ++m) {
+            WideQWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk && ok; ++u, qw.next(f)) {
+                const int m = qw.m;
                 for (int item = 0; item < kItemsPerBlock; ++item) {
                     const uint32_t slot = ic % NS;
                     ok = warp_wait(bar(Lay::kREmpty + slot), ((ic / NS) & 1u) ^ 1u, w, lane);
@@ -215,8 +234,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                             const int r = m * kBM + lane * 4 + e;
                             float lv = -INFINITY, dv = 0.f;   // negated; rows past the end: P = 0
                             if (r < f.lq) {
-                                const long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r
-                                                       : ((long)f.b * g.H + f.h) * g.Lq + r;
+                                const long si = varlen ? (long)qw.h * g.Lq + f.q_row0 + r
+                                                       : ((long)f.b * g.H + qw.h) * g.Lq + r;
                                 lv = -p.lse[si] * kLog2e;
                                 dv = -p.delta[si];
                             }
@@ -234,7 +253,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         mbar_expect_tx(bar(Lay::kRFull + slot), nb * kBox);
                         for (int bb = 0; bb < nb; ++bb)
                             tma_load_3d(base + Lay::kRingOff + slot * kPieceBytes + bb * kBox, src,
-                                        bar(Lay::kRFull + slot), (2 * piece + bb) * 64, f.h, f.q_row0 + m * kBM);
+                                        bar(Lay::kRFull + slot), (2 * piece + bb) * 64, qw.h, f.q_row0 + m * kBM);
                     }
                     __syncwarp();
                     ++ic;
@@ -323,9 +342,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after_sync();
             ok = issue_s(qb, pc, po);
             if (!ok) break;
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            for (int u = 0; u < f.nblk; ++u) {
                 const uint32_t i0 = qb * kItemsPerBlock;
-                const bool more = m + 1 < f.m_end;
+                const bool more = u + 1 < f.nblk;
                 // dP^T = V dO^T once the previous dQ chunk has left tensor memory
                 ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
                 if (!ok) break;
@@ -351,7 +370,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < kBM / 16; ++kk)
                         mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(kk), do_mn, desc_step(kk * 2048), id_kv,
-                               (m > f.m_begin || kk > 0) ? 1u : 0u);
+                               (u > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(Lay::kREmpty + s3));
                 }
                 __syncwarp();
@@ -369,7 +388,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < kBM / 16; ++kk)
                         mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(kk), q_mn, desc_step(kk * 2048), id_kv,
-                               (m > f.m_begin || kk > 0) ? 1u : 0u);
+                               (u > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         mma_ss(tmem + Lay::kTDP, ds_mn, desc_step(kk * 2048), kc_mn, desc_step(kk * 2048), id_dq,
@@ -417,8 +436,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
             const int col0 = 128 * f.c + wg * (cw / 2);   // this warpgroup's dK/dV columns
-            __nv_bfloat16* dv_ptr = p.dv + (krow * g.H + f.h) * HD + col0;
-            __nv_bfloat16* dk_ptr = p.dk + (krow * g.H + f.h) * HD + col0;
+            __nv_bfloat16* dv_ptr = p.dv + (krow * g.Hkv + f.h) * HD + col0;
+            __nv_bfloat16* dk_ptr = p.dk + (krow * g.Hkv + f.h) * HD + col0;
             if (f.m_begin >= f.m_end) {   // no query sees this key block
                 if (key_ok) {
                     for (int c = 0; c < cw / 16; ++c) {
@@ -429,7 +448,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 continue;
             }
             const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            WideQWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+                const int m = qw.m;
                 ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
                 if (!ok) break;
                 ++sc;
@@ -553,7 +574,9 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const WideBwdTile f = wide_bwd_tile(t, p, vmp);
             const int cw = chunk_width<HD>(f.c);
             const int rounds = cw / 64;
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            WideQWalk qw = qwalk(f);
+            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+                const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
                 const uint32_t dsb = dqc % Lay::kDSTiles;   // the dS tile this block's dQ MMA read
@@ -565,8 +588,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if constexpr (kDet) {
                     // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in
                     // ascending block order under its own semaphore
-                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + 2 * tile + f.c;
                     if (leader) {
                         if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
@@ -615,7 +638,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
                             for (int c2 = 0; c2 < 2; ++c2)
                                 tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
-                                                  f.h, f.q_row0 + m * kBM);
+                                                  qw.h, f.q_row0 + m * kBM);
                             bulk_commit_group();
                             if (kDet && last) {
                                 bulk_wait_group0();

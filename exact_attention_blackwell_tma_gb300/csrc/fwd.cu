@@ -106,7 +106,8 @@ __device__ __forceinline__ void exp_row_to_tmem(const float (&s)[128], float sl2
 }
 
 struct FwdTile {
-    int b, h, mp;      // batch, head, 256-row query block
+    int b, h, mp;      // batch, query head, 256-row query block
+    int hk;            // key/value head read by query head h
     int lq, lk;        // sequence lengths
     int q_row0;        // packed row of the first query row of the tile
     int k_row0;        // packed row of the first key of the sequence
@@ -120,6 +121,7 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
     FwdTile f;
     f.b = ti.b;
     f.h = ti.h;
+    f.hk = ti.h / g.group;
     f.mp = ti.m;
     if (varlen) {
         int s0 = vm.start[ti.b];
@@ -224,7 +226,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         mbar_expect_tx(bar(Lay::kKVFull + slot), Lay::kTileBytes);
                         for (int hf = 0; hf < Lay::kHalves; ++hf)
                             tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox,
-                                        kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.h,
+                                        kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.hk,
                                         f.k_row0 + j * kBN);
                     }
                     __syncwarp();

@@ -58,7 +58,8 @@ struct WideLayout {
 };
 
 struct WideTile {
-    int b, h, m;
+    int b, h, m;     // batch, query head, 128-row query block
+    int hk;          // key/value head read by query head h
     int lq, lk;
     int q_row0;      // packed row of the tile's first query row
     int k_row0;
@@ -73,6 +74,7 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
     WideTile f;
     f.b = ti.b;
     f.h = ti.h;
+    f.hk = ti.h / g.group;
     f.m = ti.m;
     if (varlen) {
         const int s0 = vm.start[ti.b];
@@ -162,7 +164,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_expect_tx(bar(Lay::kKVFull + slot), boxes * kBox);
                 for (int hf = 0; hf < boxes; ++hf)
                     tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox, kv ? &tmV : &tmK,
-                                bar(Lay::kKVFull + slot), hf * 64, f.h, f.k_row0 + j * kBN);
+                                bar(Lay::kKVFull + slot), hf * 64, f.hk, f.k_row0 + j * kBN);
             }
             __syncwarp();
             ++kv_cnt;

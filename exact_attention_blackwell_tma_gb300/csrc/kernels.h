@@ -14,8 +14,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Problem geometry as the kernels see it. Rows are "packed": a dense tensor
 // [B, L, H, d] is viewed as [B*L, H, d], batch b starting at packed row b*L;
 // a varlen tensor [T, H, d] has sequence b starting at cu_seqlens[b].
+// Grouped heads: q, o, dO, dq have H heads, k, v, dk, dv have Hkv; query head
+// h reads key/value head h / group (group = H / Hkv; 1 for multi-head).
 struct Geometry {
     int B, H, Lq, Lk, d;      // dense: sizes; varlen: Lq = Lk = T (packed rows)
+    int Hkv, group;           // key/value heads, query heads per key/value head
     const int* cu_seqlens;    // device, B+1 entries, or null (dense)
     int causal;
     float scale;              // softmax scale (> 0)

@@ -13,7 +13,8 @@ Section 5, Figs. 4-8 sweep sequence length and head dim):
     (seed ``10*s + 4``; the same positions for every head of a batch entry) so
     that the running row maximum jumps and conditional rescaling is exercised;
   * the variable-length batch draws its sequence lengths uniformly from
-    ``[lo, hi]`` (seed ``10*s + 5``) and packs the sequences back to back.
+    ``[lo, hi]`` (seed ``10*s + 5``) and packs the sequences back to back;
+  * grouped heads: K and V (and the spikes) are drawn with ``hkv`` heads.
 """
 from __future__ import annotations
 
@@ -38,6 +39,7 @@ class Workload:
     kspike: float = 4.0
     lengths: Optional[tuple] = None   # varlen: per-sequence lengths
     dv: Optional[int] = None          # head dim of v (and dO); None: the same as q and k
+    hkv: Optional[int] = None         # key/value heads (grouped heads); None: H
 
     @property
     def scale(self) -> float:
@@ -47,6 +49,10 @@ class Workload:
     @property
     def d_v(self) -> int:
         return self.d if self.dv is None else self.dv
+
+    @property
+    def H_kv(self) -> int:
+        return self.H if self.hkv is None else self.hkv
 
     @property
     def varlen(self) -> bool:
@@ -108,10 +114,10 @@ def make(w: Workload, with_grad: bool = True) -> dict:
     Dense layout ``[B, L, H, d]``; varlen ``[T, H, d]`` plus ``cu_seqlens``.
     """
     shape = (w.total, w.H, w.d) if w.varlen else (w.B, w.L, w.H, w.d)
-    vshape = shape[:-1] + (w.d_v,)
+    kshape = shape[:-2] + (w.H_kv, w.d)
     q = _randn(shape, 10 * w.seed + 0)
-    k = _randn(shape, 10 * w.seed + 1)
-    v = _randn(vshape, 10 * w.seed + 2)
+    k = _randn(kshape, 10 * w.seed + 1)
+    v = _randn(kshape[:-1] + (w.d_v,), 10 * w.seed + 2)
     if w.kspike_frac > 0:
         g = torch.Generator("cpu").manual_seed(10 * w.seed + 4)
         n = max(1, int(round(w.kspike_frac * w.L)))
@@ -122,20 +128,21 @@ def make(w: Workload, with_grad: bool = True) -> dict:
             k[b, pos] *= w.kspike
     out = {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
     if with_grad:
-        out["do"] = _randn(vshape, 10 * w.seed + 3).to(torch.bfloat16)
+        out["do"] = _randn(shape[:-1] + (w.d_v,), 10 * w.seed + 3).to(torch.bfloat16)
     if w.varlen:
         out["cu_seqlens"] = cu_seqlens(w.lengths)
     return out
 
 
-def small(B=1, H=2, L=128, d=64, causal=False, seed=1, Lk=None, dv=None) -> dict:
-    """Small dense problem with possibly different query and key lengths (and
-    a head dim of its own for v and dO)."""
+def small(B=1, H=2, L=128, d=64, causal=False, seed=1, Lk=None, dv=None, Hkv=None) -> dict:
+    """Small dense problem with possibly different query and key lengths (a
+    head dim of its own for v and dO, and fewer key/value heads)."""
     Lk = L if Lk is None else Lk
     dv = d if dv is None else dv
+    Hkv = H if Hkv is None else Hkv
     return {
         "q": _randn((B, L, H, d), 10 * seed + 0).to(torch.bfloat16),
-        "k": _randn((B, Lk, H, d), 10 * seed + 1).to(torch.bfloat16),
-        "v": _randn((B, Lk, H, dv), 10 * seed + 2).to(torch.bfloat16),
+        "k": _randn((B, Lk, Hkv, d), 10 * seed + 1).to(torch.bfloat16),
+        "v": _randn((B, Lk, Hkv, dv), 10 * seed + 2).to(torch.bfloat16),
         "do": _randn((B, L, H, dv), 10 * seed + 3).to(torch.bfloat16),
     }

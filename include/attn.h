@@ -26,6 +26,12 @@
  *          cu_seqlens[B] = T; tensors are [T, H, d], lse is fp32 [H, T].
  *          Sequence b covers rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends
  *          only within itself. 1 <= B <= 1024.
+ *   grouped heads (attn_fwd_gqa, attn_bwd_gqa): k, v, dk, dv have Hkv heads
+ *          instead of H ([B, Lk, Hkv, d] or [T, Hkv, d]); H must be a
+ *          multiple of Hkv, and query head h reads key/value head
+ *          h / (H / Hkv), so consecutive query heads share one (multi-query
+ *          attention: Hkv = 1). dk and dv of a key/value head sum over the
+ *          query heads that read it. The other entry points are Hkv = H.
  *
  * Arguments common to all calls:
  *   d       head dimension: 64, 128, 192 or 256 (forward and backward).
@@ -81,6 +87,18 @@ int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* l
                   const int* cu_seqlens, cudaStream_t stream);
 
 /*
+ * Forward pass with grouped key/value heads (see "grouped heads" above) and a
+ * head dim of its own for v and o (the pairs attn_fwd_hdim accepts). The
+ * query heads of a group are walked next to one another, so the group's K and
+ * V are read from L2 after their first load (FlashAttention-4 paper,
+ * Section 3.3, MQA/GQA order). Hkv < 1 or H not a multiple of Hkv returns
+ * ATTN_ERR_ARG.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
+                 const int* cu_seqlens, cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (same size
  * arguments as attn_bwd; for varlen pass Lq = Lk = T). The workspace holds the
  * fp32 dQ accumulator, the row terms D_i = <dO_i, O_i>, and the semaphores of
@@ -106,6 +124,21 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              int B, int H, int Lq, int Lk, int d, float scale, int causal,
              const int* cu_seqlens, int deterministic, void* workspace, size_t ws_bytes,
              cudaStream_t stream);
+
+/*
+ * Backward pass with grouped key/value heads (see "grouped heads" above; dv
+ * = d). A work tile is one 128-key block of one key/value head: it visits the
+ * query blocks of every query head of the group in turn and keeps dK and dV
+ * of the whole group in tensor memory, so they need no reduction across CTAs
+ * and are bit-identical across runs even with deterministic = 0 (the
+ * FlashAttention-4 paper, Section 3.2.4, reduces them across CTAs instead).
+ * The workspace is attn_bwd_workspace_size(B, H, ...) with the query heads H.
+ */
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv,
+                 int B, int H, int Hkv, int Lq, int Lk, int d, float scale, int causal,
+                 const int* cu_seqlens, int deterministic, void* workspace, size_t ws_bytes,
+                 cudaStream_t stream);
 
 /*
  * Backward pass that allocates nothing: the same operation, arguments and

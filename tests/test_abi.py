@@ -66,6 +66,15 @@ def test_argument_errors_need_no_gpu(built):
     assert "dv=64" in binding.last_error()
     assert lib.attn_fwd_hdim(dummy + 2, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 192, 128, 0.1, 0, None,
                              None) == -2
+    # grouped heads: the key/value heads must divide the query heads
+    assert lib.attn_fwd_gqa(dummy, dummy, dummy, dummy, dummy, 1, 6, 4, 128, 128, 128, 128, 0.1, 0, None,
+                            None) == -1
+    assert "key/value heads 4" in binding.last_error()
+    assert lib.attn_fwd_gqa(dummy, dummy, dummy, dummy, dummy, 1, 4, 0, 128, 128, 128, 128, 0.1, 0, None,
+                            None) == -1
+    assert lib.attn_fwd_gqa(dummy, dummy, dummy, dummy, dummy, 1, 2, 4, 128, 128, 128, 128, 0.1, 0, None,
+                            None) == -1
+    assert lib.attn_bwd_gqa(*([dummy] * 9), 1, 8, 3, 128, 128, 64, 0.1, 0, None, 0, dummy, 1 << 30, None) == -1
     # backward: workspace too small
     ws = lib.attn_bwd_workspace_size(1, 1, 128, 128, 64, 0, 0)
     assert ws > 0
