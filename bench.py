@@ -127,7 +127,7 @@ class Problem:
         else:
             self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.L, w.L, w.d
             self.lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=device)
-        ws = max(binding.attn_bwd_workspace_size(self.B, self.H, self.Lq, self.Lk, self.d, 1, 0), 1)
+        ws = max(binding.attn_bwd_gqa_workspace_size(self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, 1, 0), 1)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def fwd(self, causal):

@@ -42,6 +42,8 @@ def _declare(lib):
     lib.attn_bwd.restype = c_int
     lib.attn_bwd.argtypes = ([c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p, c_size_t,
                                                                c_void_p])
+    lib.attn_bwd_gqa_workspace_size.restype = c_size_t
+    lib.attn_bwd_gqa_workspace_size.argtypes = [c_int] * 8
     lib.attn_bwd_gqa.restype = c_int
     lib.attn_bwd_gqa.argtypes = ([c_void_p] * 9 + [c_int] * 6 + [c_float, c_int, c_void_p, c_int, c_void_p,
                                                                    c_size_t, c_void_p])
@@ -143,6 +145,10 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, 
                            _ptr(workspace), ws_bytes, _stream(stream))
 
 
+def attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic) -> int:
+    return load().attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, int(causal), int(deterministic))
+
+
 def attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens, deterministic,
                  workspace, ws_bytes, stream=None) -> int:
     return load().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
@@ -215,7 +221,7 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
     _check_tensors(q, k, v, o, lse, dout, cu_seqlens)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic)
+    need = attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq

@@ -235,33 +235,42 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
 namespace {
 
 struct BwdWorkspace {
-    size_t dq_off, delta_off, sem_off, total;
+    size_t dq_off, delta_off, part_off, sem_off, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-BwdWorkspace bwd_layout(int B, int H, int Lq, int d, bool varlen) {
+// dQ accumulator | D terms | partial dK/dV slots (split grouped heads) |
+// semaphores | varlen map (placed by the launcher right after the semaphores)
+BwdWorkspace bwd_layout(int B, int H, int Hkv, int Lq, int Lk, int d, bool varlen) {
     BwdWorkspace w{};
     const size_t rows_q = varlen ? (size_t)Lq : (size_t)B * Lq;
+    const long rows_k = varlen ? (long)Lk : (long)B * Lk;
     const size_t n_sem = (size_t)bwd_semaphore_count(B, H, Lq, varlen);
+    const int split = bwd_head_split(B, Hkv, H / Hkv, Lk, varlen);
     w.dq_off = 0;
     w.delta_off = align256(rows_q * H * d * sizeof(float));
-    w.sem_off = w.delta_off + align256(rows_q * H * sizeof(float));
+    w.part_off = w.delta_off + align256(rows_q * H * sizeof(float));
+    w.sem_off = w.part_off + align256(bwd_partial_bytes(split, rows_k, Hkv, d));
     w.total = w.sem_off + align256(n_sem * sizeof(int)) + align256(sizeof(VarlenMap));
     return w;
 }
 
 }  // namespace
 
-extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, int deterministic) {
-    (void)Lk;
+extern "C" size_t attn_bwd_gqa_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int causal,
+                                              int deterministic) {
     (void)causal;
     (void)deterministic;
-    if (B < 0 || H <= 0 || Lq < 0 || d <= 0) return 0;
-    // varlen and dense share the formula when Lq is the packed count; the
-    // varlen semaphore bound is the larger one, so take the maximum.
-    BwdWorkspace a = bwd_layout(B, H, Lq, d, false), b = bwd_layout(B, H, Lq, d, true);
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Lq < 0 || Lk < 0 || d <= 0) return 0;
+    // varlen and dense share the formula when Lq and Lk are the packed count;
+    // the varlen semaphore bound is the larger one, so take the maximum.
+    BwdWorkspace a = bwd_layout(B, H, Hkv, Lq, Lk, d, false), b = bwd_layout(B, H, Hkv, Lq, Lk, d, true);
     return a.total > b.total ? a.total : b.total;
+}
+
+extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, int deterministic) {
+    return attn_bwd_gqa_workspace_size(B, H, H, Lq, Lk, d, causal, deterministic);
 }
 
 extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -281,14 +290,14 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
-    const size_t need = attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic);
+    const size_t need = attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic);
     if (!workspace || ws_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
     DevInfo di;
     if (!device_info(&di)) return fail(ATTN_ERR_LAUNCH, "cannot query the current device");
-    BwdWorkspace wl = bwd_layout(B, H, Lq, d, varlen);
+    BwdWorkspace wl = bwd_layout(B, H, Hkv, Lq, Lk, d, varlen);
     char* ws = static_cast<char*>(workspace);
     BwdParams p{};
     p.g.B = B;
@@ -315,8 +324,10 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     p.nm = (Lk + 127) / 128;
     p.nq = (Lq + 127) / 128;
     // a work tile is one key block of one key/value head; it streams Q and dO
-    // of every query head of the group
-    p.n_tiles = varlen ? 0 : B * Hkv * p.nm;
+    // of the query heads of the group (of its share of them when split)
+    p.split = bwd_head_split(B, Hkv, p.g.group, Lk, varlen);
+    p.dkv_part = p.split > 1 ? reinterpret_cast<float*>(ws + wl.part_off) : nullptr;
+    p.n_tiles = varlen ? 0 : B * Hkv * p.nm * p.split;
     p.head_section = head_section(Hkv, (varlen ? (rows_q / B) : Lq) * (long)p.g.group, d);
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();

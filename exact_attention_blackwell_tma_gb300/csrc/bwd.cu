@@ -83,13 +83,14 @@ struct BwdTile {
     int q_row0;        // packed row of query 0 of the sequence
     int k_row0;        // packed row of key 0 of the sequence
     int m_begin, m_end;  // 128-row query blocks that see this key block
-    int hq0;           // first query head of the key/value head's group
-    int nblk;          // query blocks the tile visits: group x (m_end - m_begin)
+    int hq0;           // first query head the tile visits
+    int nblk;          // query blocks the tile visits: (group / split) x (m_end - m_begin)
+    int s;             // which of the key block's split tiles (0 when split == 1)
 };
 
-// The tile's query blocks in visiting order: every query head of the group
-// (all of them before the next key block, so dK and dV of the block collect
-// the whole group in tensor memory), each over [m_begin, m_end).
+// The tile's query blocks in visiting order: every query head of its share of
+// the group (the whole group unless split, so dK and dV of the block collect
+// it in tensor memory), each over [m_begin, m_end).
 struct QWalk {
     int h, m;   // query head, 128-row query block
     __device__ __forceinline__ void next(const BwdTile& f) {
@@ -105,6 +106,10 @@ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b :
 
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
+    // the split tiles of one key block are neighbours in the walk, so they run
+    // at the same time and share the block's K and V in L2
+    const int sp = t % p.split;
+    t /= p.split;
     Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false)
                  : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, false)
                              : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
@@ -130,8 +135,10 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
     }
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
-    f.hq0 = f.h * g.group;
-    f.nblk = g.group * (f.m_end - f.m_begin);
+    const int per = g.group / p.split;
+    f.s = sp;
+    f.hq0 = f.h * g.group + sp * per;
+    f.nblk = per * (f.m_end - f.m_begin);
     return f;
 }
 
@@ -197,6 +204,32 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
             }
             vm_out->pre[B] = acc;
         }
+    }
+}
+
+// Split grouped heads: dK = scale * (sum of the dK slots), dV = sum of the dV
+// slots, in slot order, fp32 -> bf16, 4 elements per step. n4: float4 per slot.
+__global__ void bwd_dkv_sum(const float* __restrict__ part, __nv_bfloat16* __restrict__ dk,
+                            __nv_bfloat16* __restrict__ dv, long n4, int split, float scale) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    const float4* p4 = reinterpret_cast<const float4*>(part);
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n4; i += stride) {
+        const bool is_v = i >= n4;
+        const long j = is_v ? i - n4 : i;
+        const float4* src = p4 + (is_v ? (long)split * n4 : 0) + j;
+        float4 a = src[0];
+        for (int sl = 1; sl < split; ++sl) {
+            const float4 b = src[(long)sl * n4];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        const float mul = is_v ? 1.f : scale;
+        uint2 o;
+        o.x = pack_bf16x2(a.x * mul, a.y * mul);
+        o.y = pack_bf16x2(a.z * mul, a.w * mul);
+        reinterpret_cast<uint2*>(is_v ? dv : dk)[j] = o;
     }
 }
 
@@ -282,7 +315,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
     const bool varlen = g.cu_seqlens != nullptr;
     const VarlenMap* vmp = varlen ? vm : nullptr;
-    const int n_tiles = varlen ? vm->pre[g.B] : p.n_tiles;
+    const int n_tiles = varlen ? vm->pre[g.B] * p.split : p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -507,14 +540,27 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
-            __nv_bfloat16* dv_ptr = p.dv + (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
-            __nv_bfloat16* dk_ptr = p.dk + (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
+            const long kv_off = (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
+            __nv_bfloat16* dv_ptr = p.dv + kv_off;
+            __nv_bfloat16* dk_ptr = p.dk + kv_off;
+            // split tiles: fp32 partial slots (dK slot f.s, dV slot split + f.s)
+            const bool partial = p.split > 1;
+            const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
+            float* pk_ptr = partial ? p.dkv_part + f.s * slot + kv_off : nullptr;
+            float* pv_ptr = partial ? p.dkv_part + (p.split + f.s) * slot + kv_off : nullptr;
             if (f.m_begin >= f.m_end) {   // no query sees this key block
                 if (key_ok) {
+                    if (partial) {
+                        for (int c = 0; c < HD / 8; ++c) {
+                            reinterpret_cast<float4*>(pv_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            reinterpret_cast<float4*>(pk_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < HD / 16; ++c) {
-                        reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
-                        reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                        for (int c = 0; c < HD / 16; ++c) {
+                            reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
+                            reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
                 continue;
@@ -614,10 +660,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t col0 = (which ? Lay::kTDK : Lay::kTDV) + wg * (HD / 2);
                 const float mul = which ? g.scale : 1.f;
                 __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
+                float* pdst = which ? pk_ptr : pv_ptr;
 #pragma unroll
                 for (int c = 0; c < HD / 64; ++c) {
                     tmem_ld32(tmem + lane_off + col0 + c * 32, rr);
-                    if (key_ok) {
+                    if (key_ok && partial) {   // unscaled: the sum kernel scales dK
+                        float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            d4[v4] = make_float4(u2f(rr[4 * v4]), u2f(rr[4 * v4 + 1]), u2f(rr[4 * v4 + 2]),
+                                                 u2f(rr[4 * v4 + 3]));
+                    } else if (key_ok) {
                         uint32_t o2[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o2[i] = pack_bf16x2(u2f(rr[2 * i]) * mul, u2f(rr[2 * i + 1]) * mul);
@@ -786,6 +839,16 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
+    }
+    if (p.split > 1) {
+        const long rows_k = varlen ? (long)g.Lk : (long)g.B * g.Lk;
+        const long n4 = rows_k * g.Hkv * HD / 4;
+        int blocks = (int)((2 * n4 + 255) / 256);
+        if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+        if (blocks < 1) blocks = 1;
+        bwd_dkv_sum<<<blocks, 256, 0, stream>>>(p.dkv_part, p.dk, p.dv, n4, p.split, g.scale);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     {
         const long n8 = rows_q * g.H * HD / 8;

@@ -76,12 +76,13 @@ struct WideBwdTile {
     int lq, lk;
     int q_row0, k_row0;  // packed rows of query 0 / key 0 of the sequence
     int m_begin, m_end;  // query blocks that see this key block
-    int hq0;             // first query head of the key/value head's group
-    int nblk;            // query blocks the tile visits: group x (m_end - m_begin)
+    int hq0;             // first query head the tile visits
+    int nblk;            // query blocks the tile visits: (group / split) x (m_end - m_begin)
+    int s;               // which of the key block's split tiles (0 when split == 1)
 };
 
-// The tile's query blocks in visiting order: every query head of the group,
-// each over [m_begin, m_end).
+// The tile's query blocks in visiting order: every query head of the tile's
+// share of the group, each over [m_begin, m_end).
 struct WideQWalk {
     int h, m;   // query head, 128-row query block
     __device__ __forceinline__ void next(const WideBwdTile& f) {
@@ -95,11 +96,13 @@ __device__ __forceinline__ WideQWalk qwalk(const WideBwdTile& f) { return WideQW
 
 __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
-// Tile t: key-block tile t/2 of the d <= 128 walk, chunk t%2 (the two chunks of
-// a key block run at the same time on neighbouring CTAs and share its loads in L2).
+// Tile t: key-block tile t/2 of the d <= 128 walk (split tiles included), chunk
+// t%2 (the two chunks of a key block run at the same time on neighbouring CTAs
+// and share its loads in L2).
 __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
-    const int u = t >> 1;
+    const int sp = (t >> 1) % p.split;
+    const int u = (t >> 1) / p.split;
     Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false)
                  : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, false)
                              : sched_dense(u, g.Hkv, p.nm, p.head_section, false));
@@ -122,8 +125,10 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     f.m_begin = 0;
     if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
-    f.hq0 = f.h * g.group;
-    f.nblk = g.group * (f.m_end - f.m_begin);
+    const int per = g.group / p.split;
+    f.s = sp;
+    f.hq0 = f.h * g.group + sp * per;
+    f.nblk = per * (f.m_end - f.m_begin);
     return f;
 }
 
@@ -191,7 +196,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
     const bool varlen = g.cu_seqlens != nullptr;
     const VarlenMap* vmp = varlen ? vm : nullptr;
-    const int n_tiles = 2 * (varlen ? vm->pre[g.B] : p.n_tiles);
+    const int n_tiles = 2 * (varlen ? vm->pre[g.B] * p.split : p.n_tiles);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -436,13 +441,26 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
             const int col0 = 128 * f.c + wg * (cw / 2);   // this warpgroup's dK/dV columns
-            __nv_bfloat16* dv_ptr = p.dv + (krow * g.Hkv + f.h) * HD + col0;
-            __nv_bfloat16* dk_ptr = p.dk + (krow * g.Hkv + f.h) * HD + col0;
+            const long kv_off = (krow * g.Hkv + f.h) * HD + col0;
+            __nv_bfloat16* dv_ptr = p.dv + kv_off;
+            __nv_bfloat16* dk_ptr = p.dk + kv_off;
+            // split tiles: fp32 partial slots (dK slot f.s, dV slot split + f.s)
+            const bool partial = p.split > 1;
+            const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
+            float* pk_ptr = partial ? p.dkv_part + f.s * slot + kv_off : nullptr;
+            float* pv_ptr = partial ? p.dkv_part + (p.split + f.s) * slot + kv_off : nullptr;
             if (f.m_begin >= f.m_end) {   // no query sees this key block
                 if (key_ok) {
-                    for (int c = 0; c < cw / 16; ++c) {
-                        reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
-                        reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                    if (partial) {
+                        for (int c = 0; c < cw / 8; ++c) {
+                            reinterpret_cast<float4*>(pv_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            reinterpret_cast<float4*>(pk_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    } else {
+                        for (int c = 0; c < cw / 16; ++c) {
+                            reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
+                            reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
                 continue;
@@ -541,9 +559,16 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint32_t tcol = (which ? Lay::kTDK : Lay::kTDV) + wg * (cw / 2);
                 const float mul = which ? g.scale : 1.f;
                 __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
+                float* pdst = which ? pk_ptr : pv_ptr;
                 for (int c = 0; c < cw / 64; ++c) {
                     tmem_ld32(tmem + lane_off + tcol + c * 32, rr);
-                    if (key_ok) {
+                    if (key_ok && partial) {   // unscaled: the sum kernel scales dK
+                        float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            d4[v4] = make_float4(u2f(rr[4 * v4]), u2f(rr[4 * v4 + 1]), u2f(rr[4 * v4 + 2]),
+                                                 u2f(rr[4 * v4 + 3]));
+                    } else if (key_ok) {
                         uint32_t o2[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o2[i] = pack_bf16x2(u2f(rr[2 * i]) * mul, u2f(rr[2 * i + 1]) * mul);

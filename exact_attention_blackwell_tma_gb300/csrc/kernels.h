@@ -48,8 +48,11 @@ struct BwdParams {
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     int* semaphores;          // deterministic mode: two counters per dQ tile (one per column chunk)
+    float* dkv_part;          // split > 1: fp32 partial dK (slots 0..split-1), then partial dV, each
+                              // slot laid out like k; null otherwise
+    int split;                // tiles per key block of a key/value head (divides g.group)
     int deterministic;
-    int n_tiles;
+    int n_tiles;              // dense: exact count, split included
     int nm;                   // dense: 128-row K/V blocks per (b, h)
     int nq;                   // dense: 128-row Q blocks per (b, h)
     int head_section;
@@ -64,6 +67,28 @@ struct BwdParams {
 // after the semaphores with this one count.
 inline long bwd_semaphore_count(int B, int H, int Lq, bool varlen) {
     return 2L * (varlen ? (long)H * (Lq / 128 + B + 1) : (long)B * H * ((Lq + 127) / 128));
+}
+
+// Grouped heads in the backward: a work tile is one 128-key block of one
+// key/value head and the query heads of its group that it visits. With one
+// tile per key block a problem with few key/value heads has too few tiles to
+// balance the SMs (the longest tile carries the whole group's longest rows),
+// so the group's query heads are split over `split` tiles, split the smallest
+// divisor of the group that gives at least kSplitTargetTiles tiles (a fixed
+// target, about four per SM, so the workspace depends on the sizes alone).
+// Split tiles write fp32 partial dK and dV to slots of their own, which a last
+// kernel sums in slot order: the result is the same on every run.
+constexpr long kSplitTargetTiles = 640;
+inline int bwd_head_split(int B, int Hkv, int group, int Lk, bool varlen) {
+    const long kblocks = varlen ? (Lk + 127) / 128 : (long)B * ((Lk + 127) / 128);
+    const long tiles = kblocks * Hkv;
+    for (int s = 1; s < group; ++s)
+        if (group % s == 0 && tiles * s >= kSplitTargetTiles) return s;
+    return group > 0 ? group : 1;
+}
+// Bytes of the partial dK/dV slots for a split (0 when split == 1).
+inline size_t bwd_partial_bytes(int split, long rows_k, int Hkv, int d) {
+    return split > 1 ? (size_t)2 * split * rows_k * Hkv * d * sizeof(float) : 0;
 }
 
 // Launchers (return cudaSuccess or the launch error).

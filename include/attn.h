@@ -126,13 +126,26 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              cudaStream_t stream);
 
 /*
+ * Workspace for attn_bwd_gqa: as attn_bwd_workspace_size, plus fp32 slots
+ * for partial dK and dV when the backward splits a group's query heads over
+ * several work tiles (see attn_bwd_gqa). Hkv = H gives attn_bwd_workspace_size.
+ * Returns 0 for invalid sizes (including H not a multiple of Hkv).
+ */
+size_t attn_bwd_gqa_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int causal,
+                                   int deterministic);
+
+/*
  * Backward pass with grouped key/value heads (see "grouped heads" above; dv
  * = d). A work tile is one 128-key block of one key/value head: it visits the
- * query blocks of every query head of the group in turn and keeps dK and dV
- * of the whole group in tensor memory, so they need no reduction across CTAs
- * and are bit-identical across runs even with deterministic = 0 (the
- * FlashAttention-4 paper, Section 3.2.4, reduces them across CTAs instead).
- * The workspace is attn_bwd_workspace_size(B, H, ...) with the query heads H.
+ * query blocks of the group's query heads in turn and keeps their dK and dV
+ * in tensor memory. When that gives fewer than 640 work tiles (about four per
+ * SM, too few to balance causal work), the group's query heads are split
+ * over the smallest number of tiles per key block (a divisor of H / Hkv) that
+ * reaches 640; each writes partial dK and dV to fp32 workspace slots that a
+ * last kernel sums in slot order. Either way dK and dV need no atomics and
+ * are bit-identical across runs even with deterministic = 0 (the
+ * FlashAttention-4 paper, Section 3.2.4, reduces them across CTAs with
+ * atomics instead). workspace: attn_bwd_gqa_workspace_size(...) bytes.
  */
 int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv,

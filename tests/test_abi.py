@@ -88,3 +88,25 @@ def test_workspace_size_grows_with_problem(built):
     b = lib.attn_bwd_workspace_size(4, 16, 4096, 4096, 128, 1, 0)
     assert b > a > 4 * 16 * 4096 * 128 // 4   # at least the fp32 dQ accumulator
     assert lib.attn_bwd_workspace_size(-1, 1, 1, 1, 64, 0, 0) == 0
+    # grouped heads: Hkv = H is the plain size; few key/value heads add partial dK/dV slots
+    mha = lib.attn_bwd_workspace_size(2, 16, 8192, 8192, 128, 1, 0)
+    assert lib.attn_bwd_gqa_workspace_size(2, 16, 16, 8192, 8192, 128, 1, 0) == mha
+    assert lib.attn_bwd_gqa_workspace_size(2, 16, 2, 8192, 8192, 128, 1, 0) > mha
+    assert lib.attn_bwd_gqa_workspace_size(2, 16, 3, 8192, 8192, 128, 1, 0) == 0
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,split", [
+    (2, 16, 2, 8192, 128, 4),    # 256 key-block tiles: 4 tiles per key block reach 640
+    (2, 16, 1, 8192, 128, 8),    # multi-query: 128 tiles, split 8
+    (5, 32, 16, 1024, 64, 1),    # 640 tiles already
+    (2, 4, 2, 300, 64, 2),       # small: the whole group is split
+    (1, 6, 2, 256, 128, 3),      # the group size when no divisor reaches the target
+])
+def test_grouped_split_policy(built, B, H, Hkv, L, d, split):
+    """The partial dK/dV slots in the workspace follow the split rule of the
+    header: the smallest divisor of H / Hkv giving at least 640 work tiles."""
+    lib = binding.load()
+    base = lib.attn_bwd_gqa_workspace_size(B, H, H, L, L, d, 1, 0)
+    got = lib.attn_bwd_gqa_workspace_size(B, H, Hkv, L, L, d, 1, 0)
+    part = 2 * split * B * L * Hkv * d * 4 if split > 1 else 0
+    assert got - base == (part + 255) // 256 * 256

@@ -53,6 +53,17 @@ def test_grouped_full(L, H, Hkv, causal, d):
     _full_check(t, causal, float(np.float32(1 / np.sqrt(d))), f"H={H} Hkv={Hkv} L={L} causal={causal} d={d}")
 
 
+@pytest.mark.parametrize("d", [64, 192])
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_grouped_unsplit(deterministic, d):
+    """5 x 8 key blocks x 16 key/value heads = 640 work tiles: one tile per key
+    block carries the whole group (the small problems above split the group
+    over tiles with partial dK/dV slots; the B2 L8192 workload below splits it
+    in part, 4 tiles of 2 heads)."""
+    t = inputs.small(B=5, H=32, L=1024, d=d, seed=48, Hkv=16)
+    _full_check(t, True, 0.1, f"unsplit det={deterministic} d={d}", deterministic=deterministic)
+
+
 @pytest.mark.parametrize("d", [128, 192])
 @pytest.mark.parametrize("causal", [False, True])
 def test_grouped_deterministic(causal, d):
@@ -92,8 +103,9 @@ def test_grouped_value_head_dim_forward(causal):
 
 
 def test_dk_dv_repeatable_without_deterministic_mode():
-    """dK and dV of a key/value head are summed inside one CTA in a fixed order,
-    so they repeat bit for bit even when dQ's accumulation order varies."""
+    """dK and dV take no atomics (one tile accumulates a key block's group, or
+    split tiles write slots summed in slot order), so they repeat bit for bit
+    even when dQ's accumulation order varies."""
     t = inputs.small(B=2, H=8, L=1024, d=128, seed=46, Hkv=1)
     first = _run(t, True, 0.088)
     for _ in range(3):
