@@ -10,9 +10,10 @@ their sources in the FlashAttention-4 paper). The shared object is compiled
 with gcc on first use (or by ``build()``) next to the source.
 
 Arrays are numpy, any real dtype (converted to float64; bf16 values widen
-exactly). Layouts: dense q/o/dq ``[B, Lq, H, d]``, k/v/dk/dv ``[B, Lk, H, d]``,
-lse ``[B, H, Lq]``; varlen (``cu_seqlens`` given, one array for Q and K)
-``[T, H, d]`` and lse ``[H, T]``.
+exactly). Layouts: dense q/o/dq ``[B, Lq, H, d]``, k/v/dk/dv ``[B, Lk, Hkv, d]``,
+lse ``[B, H, Lq]``; varlen (``cu_seqlens`` given for the queries, and
+``cu_seqlens_k`` for the keys when their lengths differ) q ``[Tq, H, d]``,
+k ``[Tk, Hkv, d]`` and lse ``[H, Tq]``.
 
 Every function here has pins in ``tests/test_oracle_pins.py`` (closed forms,
 a textbook softmax restatement, finite differences, invariants); none is
@@ -57,12 +58,12 @@ def bind(path: str):
     lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                               _ip, _ip, ctypes.c_int, ctypes.c_int]
+                               _ip, _ip, _ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_bwd.restype = ctypes.c_int
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                               _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
+                               _ip, _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
     return lib
 
 
@@ -102,7 +103,7 @@ def _ptr(a, typ):
     return a.ctypes.data_as(typ)
 
 
-def _dims(q, k, cu):
+def _dims(q, k, cu, cuk=None):
     """B, H (query heads), Hkv (key/value heads), Lq, Lk, d."""
     if cu is None:
         if q.ndim != 4 or k.ndim != 4:
@@ -117,9 +118,13 @@ def _dims(q, k, cu):
         T, H, d = q.shape
         Hkv = k.shape[1]
         B = len(cu) - 1
-        if cu[-1] != T or k.shape[0] != T or k.shape[2] != d:
-            raise ValueError("cu_seqlens[-1] must equal the packed length")
-        Lq = Lk = int(np.max(np.diff(cu))) if B > 0 else 0
+        ck = cu if cuk is None else cuk
+        if len(ck) != len(cu):
+            raise ValueError("cu_seqlens_k must have the length of cu_seqlens")
+        if cu[-1] != T or k.shape[0] != ck[-1] or k.shape[2] != d:
+            raise ValueError("cu_seqlens[-1] (cu_seqlens_k[-1]) must equal the packed query (key) length")
+        Lq = int(np.max(np.diff(cu))) if B > 0 else 0
+        Lk = int(np.max(np.diff(ck))) if B > 0 else 0
     if Hkv < 1 or H % Hkv != 0:
         raise ValueError("query heads must be a multiple of key/value heads")
     return B, H, Hkv, Lq, Lk, d
@@ -131,23 +136,27 @@ def _dv(v, k):
     return v.shape[-1]
 
 
-def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None):
+def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None, cu_seqlens_k=None):
     """O and LSE (natural log) by the definition. Returns (o, lse) as float64.
 
-    q and k share a head dim; v (and O) may have another one.
+    q and k share a head dim; v (and O) may have another one; k and v may have
+    fewer heads (grouped heads). ``cu_seqlens_k``: key offsets of a varlen
+    batch whose key lengths differ from its query lengths.
     ``rows``: optional query-row indices (per sequence) to evaluate; the other
     rows of the returned arrays are NaN.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    cu = _i32(cu_seqlens)
-    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu)
+    cu, cuk = _i32(cu_seqlens), _i32(cu_seqlens_k)
+    if cuk is not None and cu is None:
+        raise ValueError("cu_seqlens_k needs cu_seqlens")
+    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu, cuk)
     dv = _dv(v, k)
     o = np.full(q.shape[:-1] + (dv,), np.nan)
     lse = np.full((B, H, Lq) if cu is None else (H, q.shape[0]), np.nan)
     r = _i32(rows)
     rc = _load().oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
                             B, H, Hkv, Lq, Lk, d, dv, float(scale), int(bool(causal)),
-                            _ptr(cu, _ip), _ptr(r, _ip), 0 if r is None else len(r),
+                            _ptr(cu, _ip), _ptr(cuk, _ip), _ptr(r, _ip), 0 if r is None else len(r),
                             nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_fwd failed with code {rc}")
@@ -155,15 +164,17 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
 
 
 def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, krows=None,
-        nthreads=None):
+        nthreads=None, cu_seqlens_k=None):
     """dQ, dK, dV of L = sum(O * dO) by the definition. Returns float64 arrays.
 
     ``qrows`` / ``krows``: optional row subsets for dQ / (dK, dV); other rows NaN.
     Pass an empty list to skip a group entirely.
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-    cu = _i32(cu_seqlens)
-    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu)
+    cu, cuk = _i32(cu_seqlens), _i32(cu_seqlens_k)
+    if cuk is not None and cu is None:
+        raise ValueError("cu_seqlens_k needs cu_seqlens")
+    B, H, Hkv, Lq, Lk, d = _dims(q, k, cu, cuk)
     dvd = _dv(v, k)
     if dout.shape != q.shape[:-1] + (dvd,):
         raise ValueError("dout must have the rows and heads of q and the head dim of v")
@@ -174,7 +185,7 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     rc = _load().oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp),
                             _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
                             B, H, Hkv, Lq, Lk, d, dvd, float(scale), int(bool(causal)), _ptr(cu, _ip),
-                            _ptr(qr, _ip), 0 if qr is None else len(qr),
+                            _ptr(cuk, _ip), _ptr(qr, _ip), 0 if qr is None else len(qr),
                             _ptr(kr, _ip), 0 if kr is None else len(kr),
                             nthreads or default_threads())
     if rc != 0:

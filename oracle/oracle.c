@@ -47,10 +47,14 @@
  *
  * Layouts (row-major, element counts):
  *   dense  : q, o, dq  [B, Lq, H, d];  k, v, dk, dv [B, Lk, Hkv, d];  lse [B, H, Lq]
- *   varlen : cu_seqlens[B+1] (host, int32) packs B sequences; sequence b has
- *            Lq_b = Lk_b = cu[b+1]-cu[b] rows; q, o, dq [T, H, d];
- *            k, v, dk, dv [T, Hkv, d]; lse [H, T]
- *            (T = cu[B]); Lq and Lk are then ignored.
+ *   varlen : cu_seqlens[B+1] (host, int32) packs B sequences of queries;
+ *            cu_seqlens_k[B+1] packs their keys (NULL: the same offsets, so
+ *            Lk_b = Lq_b). Sequence b has Lq_b = cu[b+1]-cu[b] query rows
+ *            and Lk_b = cu_k[b+1]-cu_k[b] keys, each its own problem (causal
+ *            bottom-right aligned within it, as the FlashAttention-4 paper's
+ *            Section 3.3 mixes sequences of different query and key lengths);
+ *            q, o, dq [Tq, H, d]; k, v, dk, dv [Tk, Hkv, d]; lse [H, Tq]
+ *            (Tq = cu[B], Tk = cu_k[B]); Lq and Lk are then ignored.
  *
  * Row subsets: `rows` (nrows entries) lists query-row indices, relative to
  * each sequence, whose O / LSE / dQ are wanted; `krows` lists key-row indices
@@ -72,6 +76,7 @@ typedef struct {
     int B, H, Hkv, Lq, Lk, d, dvh, causal;   /* Hkv: heads of k, v; dvh: head dim of v, o, dout, dv */
     double scale;
     const int *cu;          /* NULL for dense */
+    const int *cuk;         /* key offsets (varlen): cu_seqlens_k, or cu */
     /* per (b, h, row) statistics used by the backward pass */
     double *lse_all;        /* [B*H*Lq_max] or varlen [H*T] */
     double *D_all;
@@ -85,7 +90,7 @@ typedef struct {
 /* ---- sequence geometry ------------------------------------------------- */
 
 static int seq_lq(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lq; }
-static int seq_lk(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lk; }
+static int seq_lk(const job_t *J, int b) { return J->cu ? J->cuk[b + 1] - J->cuk[b] : J->Lk; }
 
 /* element offset of row i of sequence b, head h, in a [.., L, H, d] tensor */
 static long row_off(const job_t *J, int b, int i, int h, int L) {
@@ -104,13 +109,13 @@ static int kvh(const job_t *J, int h) { return h / (J->H / J->Hkv); }
 
 /* element offset of row j of key/value head hk in a [.., L, Hkv, d] tensor (k, dk) */
 static long row_off_k(const job_t *J, int b, int j, int hk, int L) {
-    if (J->cu) return ((long)(J->cu[b] + j) * J->Hkv + hk) * J->d;
+    if (J->cu) return ((long)(J->cuk[b] + j) * J->Hkv + hk) * J->d;
     return (((long)b * L + j) * J->Hkv + hk) * J->d;
 }
 
 /* the same with head dim dvh (v, dv) */
 static long row_off_kv(const job_t *J, int b, int j, int hk, int L) {
-    if (J->cu) return ((long)(J->cu[b] + j) * J->Hkv + hk) * J->dvh;
+    if (J->cu) return ((long)(J->cuk[b] + j) * J->Hkv + hk) * J->dvh;
     return (((long)b * L + j) * J->Hkv + hk) * J->dvh;
 }
 
@@ -284,32 +289,37 @@ static int *make_items(const job_t *J, const int *rows, int nrows, int kind, lon
     return items;
 }
 
-static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu) {
+static int check_offsets(int B, const int *cu) {
+    if (cu[0] != 0) return -1;
+    for (int b = 0; b < B; b++) if (cu[b + 1] < cu[b]) return -1;
+    return 0;
+}
+
+static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu, const int *cuk) {
     if (B < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || dv < 1) return -1;
     if (!cu && (Lq < 0 || Lk < 0)) return -1;
-    if (cu) {
-        if (cu[0] != 0) return -1;
-        for (int b = 0; b < B; b++) if (cu[b + 1] < cu[b]) return -1;
-    }
+    if (cuk && !cu) return -1;
+    if (cu && check_offsets(B, cu)) return -1;
+    if (cuk && check_offsets(B, cuk)) return -1;
     return 0;
 }
 
 static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
                      int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
-                     const int *cu) {
+                     const int *cu, const int *cuk) {
     memset(J, 0, sizeof(*J));
     J->q = q; J->k = k; J->v = v; J->dout = dout;
     J->B = B; J->H = H; J->Hkv = Hkv; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
-    J->scale = scale; J->causal = causal != 0; J->cu = cu;
+    J->scale = scale; J->causal = causal != 0; J->cu = cu; J->cuk = cuk ? cuk : cu;
 }
 
 int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
-               const int *cu_seqlens, const int *rows, int nrows, int nthreads) {
+               const int *cu_seqlens, const int *cu_seqlens_k, const int *rows, int nrows, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens, cu_seqlens_k)) return -1;
     job_t J;
-    init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, cu_seqlens_k);
     J.o = o; J.lse = lse;
     long n;
     int *items = make_items(&J, rows, nrows, 0, &n);
@@ -322,13 +332,13 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
 int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
                double *dq, double *dk, double *dv,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dvd, double scale, int causal,
-               const int *cu_seqlens, const int *qrows, int nqrows,
+               const int *cu_seqlens, const int *cu_seqlens_k, const int *qrows, int nqrows,
                const int *krows, int nkrows, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens, cu_seqlens_k)) return -1;
     if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
     job_t J;
-    init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, cu_seqlens);
+    init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, cu_seqlens, cu_seqlens_k);
     J.dq = dq; J.dk = dk; J.dv = dv;
 
     /* longest sequence, the range of relative row indices */

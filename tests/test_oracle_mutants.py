@@ -28,6 +28,11 @@ MUTANTS = [
      "const double *vj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);\n        for (int c = 0; c < dv; c++) out[c]"),
     ("score uses key row i", "const double *kj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);\n    return",
      "const double *kj = J->k + row_off_k(J, b, i < J->Lk ? i : 0, kvh(J, h), J->Lk);\n    return"),
+    ("keys of sequence b at its query offset", "if (J->cu) return ((long)(J->cuk[b] + j) * J->Hkv + hk) * J->d;",
+     "if (J->cu) return ((long)(J->cu[b] + j) * J->Hkv + hk) * J->d;"),
+    ("key length of sequence b from the query offsets",
+     "static int seq_lk(const job_t *J, int b) { return J->cu ? J->cuk[b + 1] - J->cuk[b] : J->Lk; }",
+     "static int seq_lk(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lk; }"),
     ("interleaved head groups", "static int kvh(const job_t *J, int h) { return h / (J->H / J->Hkv); }",
      "static int kvh(const job_t *J, int h) { return h % J->Hkv; }"),
     ("dK/dV from the group's first query head only", "for (int hq = hk * g; hq < hk * g + g; hq++)",
@@ -62,6 +67,8 @@ BATTERY = [
     (pins.test_bwd_finite_differences_value_dim, (True,)),
     (pins.test_fwd_grouped_heads_match_textbook, (1, 6, 3, 7, 9, 3, True)),
     (pins.test_bwd_finite_differences_grouped_heads, (False,)),
+    (pins.test_varlen_separate_key_lengths_is_per_sequence_attention, ()),
+    (pins.test_bwd_finite_differences_varlen_separate_keys, (True,)),
 ]
 
 

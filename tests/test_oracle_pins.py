@@ -251,6 +251,36 @@ def test_varlen_is_per_sequence_attention():
             np.testing.assert_allclose(lse[:, a:a + L], lb[0], atol=1e-12)
 
 
+LENS_Q, LENS_K = [3, 1, 6, 0, 4, 2], [5, 2, 2, 3, 4, 0]   # longer, shorter, equal and empty sides
+
+
+def _offsets(lens):
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+
+def test_varlen_separate_key_lengths_is_per_sequence_attention():
+    """With key offsets of their own, sequence b is the rectangular problem of
+    its Lq_b queries and Lk_b keys (causal bottom-right aligned within it)."""
+    cu, cuk = _offsets(LENS_Q), _offsets(LENS_K)
+    H, Hkv, d = 4, 2, 3
+    q, k, v = rnd((cu[-1], H, d), 90), rnd((cuk[-1], Hkv, d), 91), rnd((cuk[-1], Hkv, d), 92)
+    for causal in (False, True):
+        o, lse = oracle.fwd(q, k, v, 0.6, causal, cu_seqlens=cu, cu_seqlens_k=cuk)
+        for b in range(len(LENS_Q)):
+            a, L, c, M = cu[b], LENS_Q[b], cuk[b], LENS_K[b]
+            if L == 0 or M == 0:
+                assert (o[a:a + L] == 0).all() and np.isneginf(lse[:, a:a + L]).all()
+                continue
+            ob, lb = textbook(q[None, a:a + L], np.repeat(k[None, c:c + M], 2, axis=2),
+                              np.repeat(v[None, c:c + M], 2, axis=2), 0.6, causal)
+            np.testing.assert_allclose(o[a:a + L], ob[0], atol=1e-12)
+            ref = lb[0]
+            fin = np.isfinite(ref)
+            if fin.any():
+                np.testing.assert_allclose(lse[:, a:a + L][fin], ref[fin], atol=1e-12)
+            assert np.isneginf(lse[:, a:a + L][~fin]).all()
+
+
 def test_row_subset_matches_full():
     q, k, v = rnd((2, 10, 2, 4), 36), rnd((2, 10, 2, 4), 37), rnd((2, 10, 2, 4), 38)
     full_o, full_l = oracle.fwd(q, k, v, 0.5, True)
@@ -321,6 +351,31 @@ def test_bwd_finite_differences_rectangular_and_varlen():
         for got, ref in ((dq, fq), (dk, fk), (dv, fv)):
             assert np.abs(got - ref).max() < 1e-7
     assert sum(lens) == 5
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_finite_differences_varlen_separate_keys(causal):
+    """Packed sequences whose key lengths differ from their query lengths."""
+    cu, cuk = _offsets([2, 3, 1]), _offsets([3, 1, 2])
+    q, do = rnd((cu[-1], 2, 3), 93), rnd((cu[-1], 2, 3), 94)
+    k, v = rnd((cuk[-1], 1, 3), 95), rnd((cuk[-1], 1, 3), 96)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.8, causal, cu_seqlens=cu, cu_seqlens_k=cuk)
+    assert dk.shape == k.shape
+
+    def loss2(q_, k_, v_):
+        o, _ = oracle.fwd(q_, k_, v_, 0.8, causal, cu_seqlens=cu, cu_seqlens_k=cuk)
+        return float(np.sum(o * do))
+
+    for got, which in ((dq, 0), (dk, 1), (dv, 2)):
+        arrs = [q, k, v]
+        g = np.zeros_like(arrs[which])
+        for idx in np.ndindex(g.shape):
+            plus = [a.copy() for a in arrs]
+            minus = [a.copy() for a in arrs]
+            plus[which][idx] += 1e-6
+            minus[which][idx] -= 1e-6
+            g[idx] = (loss2(*plus) - loss2(*minus)) / 2e-6
+        assert np.abs(got - g).max() < 1e-7
 
 
 @pytest.mark.parametrize("causal", [False, True])
