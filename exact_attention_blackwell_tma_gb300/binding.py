@@ -37,6 +37,8 @@ def _declare(lib):
     lib.attn_fwd_hdim.argtypes = [c_void_p] * 5 + [c_int] * 6 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_fwd_gqa.restype = c_int
     lib.attn_fwd_gqa.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p]
+    lib.attn_fwd_varlen.restype = c_int
+    lib.attn_fwd_varlen.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
     lib.attn_bwd_workspace_size.argtypes = [c_int] * 7
     lib.attn_bwd.restype = c_int
@@ -47,6 +49,9 @@ def _declare(lib):
     lib.attn_bwd_gqa.restype = c_int
     lib.attn_bwd_gqa.argtypes = ([c_void_p] * 9 + [c_int] * 6 + [c_float, c_int, c_void_p, c_int, c_void_p,
                                                                    c_size_t, c_void_p])
+    lib.attn_bwd_varlen.restype = c_int
+    lib.attn_bwd_varlen.argtypes = ([c_void_p] * 9 + [c_int] * 6 + [c_float, c_int, c_void_p, c_void_p, c_int,
+                                                                      c_void_p, c_size_t, c_void_p])
     lib.attn_bwd_noalloc.restype = c_int
     lib.attn_bwd_noalloc.argtypes = [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p]
     lib.attn_last_error.restype = ctypes.c_char_p
@@ -134,6 +139,12 @@ def attn_fwd_gqa(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_se
                                int(causal), _ptr(cu_seqlens), _stream(stream))
 
 
+def attn_fwd_varlen(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu_seqlens_q, cu_seqlens_k,
+                    stream=None) -> int:
+    return load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Tq, Tk, d, dv, scale,
+                                  int(causal), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
+
+
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
     return load().attn_bwd_workspace_size(B, H, Lq, Lk, d, int(causal), int(deterministic))
 
@@ -154,6 +165,14 @@ def attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale,
     return load().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                _ptr(dv), B, H, Hkv, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens),
                                int(deterministic), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, scale, causal, cu_seqlens_q,
+                    cu_seqlens_k, deterministic, workspace, ws_bytes, stream=None) -> int:
+    return load().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, H, Hkv, Tq, Tk, d, scale, int(causal), _ptr(cu_seqlens_q),
+                                  _ptr(cu_seqlens_k), int(deterministic), _ptr(workspace), ws_bytes,
+                                  _stream(stream))
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens,
@@ -193,11 +212,12 @@ def _check_tensors(*ts):
 
 
 def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
-            stream=None):
+            stream=None, cu_seqlens_k=None):
     """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens).
     v (and O) may have a head dim of their own (d = 192 with 128); k and v may
-    have fewer heads than q (grouped heads: query head h reads h // (H // Hkv))."""
-    _check_tensors(q, k, v, cu_seqlens)
+    have fewer heads than q (grouped heads: query head h reads h // (H // Hkv)).
+    cu_seqlens_k: key offsets of a varlen batch whose key lengths differ."""
+    _check_tensors(q, k, v, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     dv = v.shape[-1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -205,7 +225,10 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
         out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
-    if Hkv != H:
+    if cu_seqlens_k is not None:
+        _check(attn_fwd_varlen(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens,
+                               cu_seqlens_k, stream))
+    elif Hkv != H:
         _check(attn_fwd_gqa(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, stream))
     elif dv == d:
         _check(attn_fwd(q, k, v, out, lse, B, H, Lq, Lk, d, scale, causal, cu_seqlens, stream))
@@ -215,10 +238,11 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
 
 
 def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu_seqlens=None,
-             deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None):
+             deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None,
+             cu_seqlens_k=None):
     """dQ, dK, dV (bf16) for the loss sum(O * dO); k and v may have fewer heads
-    than q (grouped heads), dK and dV then have theirs."""
-    _check_tensors(q, k, v, o, lse, dout, cu_seqlens)
+    than q (grouped heads), dK and dV then have theirs. cu_seqlens_k as in forward()."""
+    _check_tensors(q, k, v, o, lse, dout, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     need = attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic)
@@ -228,7 +252,10 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = workspace.numel() * workspace.element_size()
-    if Hkv != H:
+    if cu_seqlens_k is not None:
+        _check(attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
+                               cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
+    elif Hkv != H:
         _check(attn_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
                             deterministic, workspace, ws_bytes, stream))
     else:

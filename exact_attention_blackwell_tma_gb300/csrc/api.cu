@@ -133,14 +133,17 @@ int head_section(int H, long rows, int d) {
     return hs;
 }
 
-int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu, bool bwd) {
+// cu_k: the key offsets of a varlen problem (== cu when one array serves both,
+// which needs Lq == Lk == T).
+int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu, const int* cu_k) {
     if (B < 0 || H <= 0 || Lq < 0 || Lk < 0) return fail(ATTN_ERR_ARG, "bad sizes B=%d H=%d Lq=%d Lk=%d", B, H, Lq, Lk);
-    (void)bwd;
     if (d != 64 && d != 128 && d != 192 && d != 256)
         return fail(ATTN_ERR_ARG, "head dim %d not supported (64, 128, 192, 256)", d);
     if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_ARG, "scale must be finite and > 0");
     if (cu) {
-        if (Lq != Lk) return fail(ATTN_ERR_ARG, "varlen: Lq and Lk must both be the packed row count T");
+        if (!cu_k) return fail(ATTN_ERR_ARG, "varlen: null key offsets");
+        if (cu_k == cu && Lq != Lk)
+            return fail(ATTN_ERR_ARG, "varlen: Lq and Lk must both be the packed row count T");
         if (B < 1 || B > kMaxVarlenBatch) return fail(ATTN_ERR_ARG, "varlen: B must be in [1, %d]", kMaxVarlenBatch);
     }
     long rows_q = cu ? (long)Lq : (long)B * Lq, rows_k = cu ? (long)Lk : (long)B * Lk;
@@ -165,10 +168,14 @@ int* device_status_word() {
 
 using namespace attn;
 
-extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                            int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
-                            const int* cu_seqlens, cudaStream_t stream) {
-    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, false);
+namespace {
+
+// The forward behind every entry point: dense (cu_seqlens null), varlen with
+// one offset array (cu_seqlens_k == cu_seqlens) or with key offsets of their own.
+int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Lq,
+              int Lk, int d, int dv, float scale, int causal, const int* cu_seqlens, const int* cu_seqlens_k,
+              cudaStream_t stream) {
+    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
     if (rc) return rc;
     rc = check_heads(H, Hkv);
     if (rc) return rc;
@@ -191,6 +198,7 @@ extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
     p.g.Hkv = Hkv;
     p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
+    p.g.cu_seqlens_k = cu_seqlens ? cu_seqlens_k : nullptr;
     p.g.causal = causal ? 1 : 0;
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
@@ -219,6 +227,22 @@ extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
     cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream) : launch_fwd(tq, tk, tv, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
+                            const int* cu_seqlens, cudaStream_t stream) {
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, cu_seqlens, stream);
+}
+
+extern "C" int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_fwd_varlen: null offsets");
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu_seqlens_q, cu_seqlens_k,
+                     stream);
 }
 
 extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -273,11 +297,14 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, i
     return attn_bwd_gqa_workspace_size(B, H, H, Lq, Lk, d, causal, deterministic);
 }
 
-extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
-                            int d, float scale, int causal, const int* cu_seqlens, int deterministic,
-                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, true);
+namespace {
+
+// The backward behind every entry point (cu_seqlens_k as in fwd_entry).
+int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk, int d, float scale, int causal,
+              const int* cu_seqlens, const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
+              cudaStream_t stream) {
+    int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
     if (rc) return rc;
     rc = check_heads(H, Hkv);
     if (rc) return rc;
@@ -308,6 +335,7 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     p.g.Hkv = Hkv;
     p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
+    p.g.cu_seqlens_k = cu_seqlens ? cu_seqlens_k : nullptr;
     p.g.causal = causal ? 1 : 0;
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
@@ -344,6 +372,26 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+}  // namespace
+
+extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
+                            int d, float scale, int causal, const int* cu_seqlens, int deterministic,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
+                     cu_seqlens, deterministic, workspace, ws_bytes, stream);
+}
+
+extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Tq,
+                               int Tk, int d, float scale, int causal, const int* cu_seqlens_q,
+                               const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_bwd_varlen: null offsets");
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, scale, causal, cu_seqlens_q,
+                     cu_seqlens_k, deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

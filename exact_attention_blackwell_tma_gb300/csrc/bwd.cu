@@ -110,7 +110,7 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
     // at the same time and share the block's K and V in L2
     const int sp = t % p.split;
     t /= p.split;
-    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false)
+    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false, true)
                  : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, false)
                              : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
     BwdTile f;
@@ -118,9 +118,10 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
     f.h = ti.h;
     f.n = ti.m;   // ascending: for causal the smallest key blocks carry the most work
     if (vm) {
-        const int s0 = vm->start[ti.b];
-        f.lq = f.lk = vm->start[ti.b + 1] - s0;
-        f.q_row0 = f.k_row0 = s0;
+        f.lq = vm_lq(*vm, ti.b);
+        f.lk = vm_lk(*vm, ti.b);
+        f.q_row0 = vm->start[ti.b];
+        f.k_row0 = vm->start_k[ti.b];
     } else {
         f.lq = g.Lq;
         f.lk = g.Lk;
@@ -180,30 +181,9 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
     for (long i = tid; i < n_acc4; i += stride) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (long i = tid; i < n_sem; i += stride) p.semaphores[i] = 0;
     if (g.cu_seqlens && blockIdx.x == 0) {
-        // longest-first map of the sequences (FlashAttention-4 paper, Section 3.3, varlen LPT)
-        const int B = g.B;
-        for (int i = threadIdx.x; i <= B; i += blockDim.x) vm_out->start[i] = g.cu_seqlens[i];
-        __syncthreads();
-        for (int i = threadIdx.x; i < B; i += blockDim.x) {
-            const int li = vm_out->start[i + 1] - vm_out->start[i];
-            int rank = 0;
-            for (int j = 0; j < B; ++j) {
-                const int lj = vm_out->start[j + 1] - vm_out->start[j];
-                rank += (lj > li) || (lj == li && j < i);
-            }
-            vm_out->order[rank] = i;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int acc = 0;
-            for (int k = 0; k < B; ++k) {
-                vm_out->pre[k] = acc;
-                const int b = vm_out->order[k];
-                const int L = vm_out->start[b + 1] - vm_out->start[b];
-                acc += g.Hkv * ((L + kBN - 1) / kBN);   // work tiles are per key/value head
-            }
-            vm_out->pre[B] = acc;
-        }
+        // longest-first map of the sequences (FlashAttention-4 paper, Section 3.3,
+        // varlen LPT); work tiles are key blocks of key/value heads
+        sched_varlen_build(*vm_out, g.cu_seqlens, g.cu_seqlens_k, g.B, g.Hkv, kBN, true, threadIdx.x, blockDim.x);
     }
 }
 
@@ -540,15 +520,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
-            const long kv_off = (krow * g.Hkv + f.h) * HD + wg * (HD / 2);
-            __nv_bfloat16* dv_ptr = p.dv + kv_off;
-            __nv_bfloat16* dk_ptr = p.dk + kv_off;
-            // split tiles: fp32 partial slots (dK slot f.s, dV slot split + f.s)
+            // this thread's dK/dV row: bf16 outputs, or (split tiles) fp32 partial
+            // slots, dK slot f.s and dV slot split + f.s; computed where used, so
+            // that no pointer stays live through the query-block loop
             const bool partial = p.split > 1;
-            const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
-            float* pk_ptr = partial ? p.dkv_part + f.s * slot + kv_off : nullptr;
-            float* pv_ptr = partial ? p.dkv_part + (p.split + f.s) * slot + kv_off : nullptr;
+            auto kv_off = [&]() { return (krow * g.Hkv + f.h) * HD + wg * (HD / 2); };
+            auto part_slot = [&](int which) {   // 0: dV, 1: dK
+                const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
+                return p.dkv_part + (which ? f.s : p.split + f.s) * slot + kv_off();
+            };
             if (f.m_begin >= f.m_end) {   // no query sees this key block
+                __nv_bfloat16* dv_ptr = p.dv + kv_off();
+                __nv_bfloat16* dk_ptr = p.dk + kv_off();
+                float* pk_ptr = partial ? part_slot(1) : nullptr;
+                float* pv_ptr = partial ? part_slot(0) : nullptr;
                 if (key_ok) {
                     if (partial) {
                         for (int c = 0; c < HD / 8; ++c) {
@@ -659,8 +644,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col0 = (which ? Lay::kTDK : Lay::kTDV) + wg * (HD / 2);
                 const float mul = which ? g.scale : 1.f;
-                __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
-                float* pdst = which ? pk_ptr : pv_ptr;
+                __nv_bfloat16* dst = (which ? p.dk : p.dv) + kv_off();
+                float* pdst = partial ? part_slot(which) : nullptr;
 #pragma unroll
                 for (int c = 0; c < HD / 64; ++c) {
                     tmem_ld32(tmem + lane_off + col0 + c * 32, rr);

@@ -103,7 +103,7 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     const Geometry& g = p.g;
     const int sp = (t >> 1) % p.split;
     const int u = (t >> 1) / p.split;
-    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false)
+    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false, true)
                  : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, false)
                              : sched_dense(u, g.Hkv, p.nm, p.head_section, false));
     WideBwdTile f;
@@ -112,9 +112,10 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     f.n = ti.m;
     f.c = t & 1;
     if (vm) {
-        const int s0 = vm->start[ti.b];
-        f.lq = f.lk = vm->start[ti.b + 1] - s0;
-        f.q_row0 = f.k_row0 = s0;
+        f.lq = vm_lq(*vm, ti.b);
+        f.lk = vm_lk(*vm, ti.b);
+        f.q_row0 = vm->start[ti.b];
+        f.k_row0 = vm->start_k[ti.b];
     } else {
         f.lq = g.Lq;
         f.lk = g.Lk;
@@ -440,16 +441,20 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
-            const int col0 = 128 * f.c + wg * (cw / 2);   // this warpgroup's dK/dV columns
-            const long kv_off = (krow * g.Hkv + f.h) * HD + col0;
-            __nv_bfloat16* dv_ptr = p.dv + kv_off;
-            __nv_bfloat16* dk_ptr = p.dk + kv_off;
-            // split tiles: fp32 partial slots (dK slot f.s, dV slot split + f.s)
+            // this thread's dK/dV chunk row: bf16 outputs, or (split tiles) fp32
+            // partial slots, dK slot f.s and dV slot split + f.s; computed where
+            // used, so that no pointer stays live through the query-block loop
             const bool partial = p.split > 1;
-            const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
-            float* pk_ptr = partial ? p.dkv_part + f.s * slot + kv_off : nullptr;
-            float* pv_ptr = partial ? p.dkv_part + (p.split + f.s) * slot + kv_off : nullptr;
+            auto kv_off = [&]() { return (krow * g.Hkv + f.h) * HD + 128 * f.c + wg * (cw / 2); };
+            auto part_slot = [&](int which) {   // 0: dV, 1: dK
+                const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
+                return p.dkv_part + (which ? f.s : p.split + f.s) * slot + kv_off();
+            };
             if (f.m_begin >= f.m_end) {   // no query sees this key block
+                __nv_bfloat16* dv_ptr = p.dv + kv_off();
+                __nv_bfloat16* dk_ptr = p.dk + kv_off();
+                float* pk_ptr = partial ? part_slot(1) : nullptr;
+                float* pv_ptr = partial ? part_slot(0) : nullptr;
                 if (key_ok) {
                     if (partial) {
                         for (int c = 0; c < cw / 8; ++c) {
@@ -558,8 +563,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tcol = (which ? Lay::kTDK : Lay::kTDV) + wg * (cw / 2);
                 const float mul = which ? g.scale : 1.f;
-                __nv_bfloat16* dst = which ? dk_ptr : dv_ptr;
-                float* pdst = which ? pk_ptr : pv_ptr;
+                __nv_bfloat16* dst = (which ? p.dk : p.dv) + kv_off();
+                float* pdst = partial ? part_slot(which) : nullptr;
                 for (int c = 0; c < cw / 64; ++c) {
                     tmem_ld32(tmem + lane_off + tcol + c * 32, rr);
                     if (key_ok && partial) {   // unscaled: the sum kernel scales dK

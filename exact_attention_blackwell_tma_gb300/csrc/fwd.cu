@@ -116,7 +116,7 @@ struct FwdTile {
 
 __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
     const Geometry& g = p.g;
-    Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0)
+    Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0, false)
                      : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, true) : sched_dense(t, g.H, p.nm, p.head_section, false));
     FwdTile f;
     f.b = ti.b;
@@ -124,10 +124,10 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
     f.hk = ti.h / g.group;
     f.mp = ti.m;
     if (varlen) {
-        int s0 = vm.start[ti.b];
-        f.lq = f.lk = vm.start[ti.b + 1] - s0;
-        f.q_row0 = s0 + ti.m * kRowsPerTile;
-        f.k_row0 = s0;
+        f.lq = vm_lq(vm, ti.b);
+        f.lk = vm_lk(vm, ti.b);
+        f.q_row0 = vm.start[ti.b] + ti.m * kRowsPerTile;
+        f.k_row0 = vm.start_k[ti.b];
     } else {
         f.lq = g.Lq;
         f.lk = g.Lk;
@@ -189,7 +189,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
     int n_tiles = p.n_tiles;
     if (varlen) {
-        sched_varlen_build(vm, g.cu_seqlens, g.B, g.H, kRowsPerTile, tid, kThreads);
+        sched_varlen_build(vm, g.cu_seqlens, g.cu_seqlens_k, g.B, g.H, kRowsPerTile, false, tid, kThreads);
         n_tiles = vm.pre[g.B];
     }
     tc_fence_before_sync();

@@ -68,7 +68,7 @@ struct WideTile {
 
 __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
     const Geometry& g = p.g;
-    Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kBM, p.head_section, g.causal != 0)
+    Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kBM, p.head_section, g.causal != 0, false)
                      : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, true)
                                  : sched_dense(t, g.H, p.nm, p.head_section, false));
     WideTile f;
@@ -77,10 +77,10 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
     f.hk = ti.h / g.group;
     f.m = ti.m;
     if (varlen) {
-        const int s0 = vm.start[ti.b];
-        f.lq = f.lk = vm.start[ti.b + 1] - s0;
-        f.q_row0 = s0 + ti.m * kBM;
-        f.k_row0 = s0;
+        f.lq = vm_lq(vm, ti.b);
+        f.lk = vm_lk(vm, ti.b);
+        f.q_row0 = vm.start[ti.b] + ti.m * kBM;
+        f.k_row0 = vm.start_k[ti.b];
     } else {
         f.lq = g.Lq;
         f.lk = g.Lk;
@@ -142,7 +142,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     int n_tiles = p.n_tiles;
     if (varlen) {
-        sched_varlen_build(vm, g.cu_seqlens, g.B, g.H, kBM, tid, kThreads);
+        sched_varlen_build(vm, g.cu_seqlens, g.cu_seqlens_k, g.B, g.H, kBM, false, tid, kThreads);
         n_tiles = vm.pre[g.B];
     }
     tc_fence_before_sync();

@@ -17,9 +17,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Grouped heads: q, o, dO, dq have H heads, k, v, dk, dv have Hkv; query head
 // h reads key/value head h / group (group = H / Hkv; 1 for multi-head).
 struct Geometry {
-    int B, H, Lq, Lk, d;      // dense: sizes; varlen: Lq = Lk = T (packed rows)
+    int B, H, Lq, Lk, d;      // dense: sizes; varlen: Lq, Lk = packed query and key rows
     int Hkv, group;           // key/value heads, query heads per key/value head
-    const int* cu_seqlens;    // device, B+1 entries, or null (dense)
+    const int* cu_seqlens;    // device, B+1 query offsets, or null (dense)
+    const int* cu_seqlens_k;  // device, B+1 key offsets (varlen; cu_seqlens when they are shared)
     int causal;
     float scale;              // softmax scale (> 0)
     float scale_log2;         // scale * log2(e)

@@ -6,7 +6,10 @@
 //    m-blocks in reverse (longest causal rows first), and within an m-block
 //    the heads of the section;
 //  * varlen LPT: sequences are sorted by the cost of their longest work tile
-//    (descending) into a virtual-to-real batch map that the kernel walks.
+//    (descending) into a virtual-to-real batch map that the kernel walks. The
+//    forward's tiles cover query rows and the longest visits every key, so it
+//    sorts by key count; the backward's cover keys and sorts by query count
+//    (the same order when queries and keys share their offsets).
 // Blog post on FA4 (qian.cx), "StaticPersistentTileScheduler": at most one
 // CTA per SM; CTA c takes tiles c, c + grid, c + 2*grid, ...
 //
@@ -76,26 +79,38 @@ __host__ __device__ __forceinline__ Tile sched_dense(int t, int H, int nm, int h
     return ti;
 }
 
-// Shared-memory tables for a varlen problem.
+// Tables for a varlen problem (shared memory in the forward, the workspace in
+// the backward).
 struct VarlenMap {
-    int start[kMaxVarlenBatch + 1];   // cu_seqlens copy
-    int order[kMaxVarlenBatch];       // virtual -> real sequence (longest first)
-    int pre[kMaxVarlenBatch + 1];     // prefix count of tiles in virtual order
+    int start[kMaxVarlenBatch + 1];     // query offsets (cu_seqlens copy)
+    int start_k[kMaxVarlenBatch + 1];   // key offsets (cu_seqlens_k, or cu_seqlens again)
+    int order[kMaxVarlenBatch];         // virtual -> real sequence (longest first)
+    int pre[kMaxVarlenBatch + 1];       // prefix count of tiles in virtual order
 };
 
-// Build the map with all `nthreads` threads of the CTA; ends with __syncthreads.
-// rows_per_block: query rows per work tile; the tile count of a sequence of
-// length L is H * ceil(L / rows_per_block).
-__device__ __forceinline__ void sched_varlen_build(VarlenMap& vm, const int* cu, int B, int H,
-                                                   int rows_per_block, int tid, int nthreads) {
-    for (int i = tid; i <= B; i += nthreads) vm.start[i] = cu[i];
+__host__ __device__ __forceinline__ int vm_lq(const VarlenMap& vm, int b) { return vm.start[b + 1] - vm.start[b]; }
+__host__ __device__ __forceinline__ int vm_lk(const VarlenMap& vm, int b) { return vm.start_k[b + 1] - vm.start_k[b]; }
+
+// Build the map with all `nthreads` threads of the calling CTA (every thread
+// of it must call); ends with __syncthreads. over_keys = false: work tiles
+// cover query rows (forward), a sequence has heads * ceil(Lq / rows_per_block)
+// of them and sorts by Lk; over_keys = true: tiles cover keys (backward),
+// heads * ceil(Lk / rows_per_block), sorted by Lq. Ties: the other length,
+// then the sequence index.
+__device__ __forceinline__ void sched_varlen_build(VarlenMap& vm, const int* cu, const int* cu_k, int B,
+                                                   int heads, int rows_per_block, bool over_keys, int tid,
+                                                   int nthreads) {
+    for (int i = tid; i <= B; i += nthreads) {
+        vm.start[i] = cu[i];
+        vm.start_k[i] = cu_k[i];
+    }
     __syncthreads();
     for (int i = tid; i < B; i += nthreads) {
-        int li = vm.start[i + 1] - vm.start[i];
+        const int ki = over_keys ? vm_lq(vm, i) : vm_lk(vm, i), oi = over_keys ? vm_lk(vm, i) : vm_lq(vm, i);
         int rank = 0;
         for (int j = 0; j < B; ++j) {
-            int lj = vm.start[j + 1] - vm.start[j];
-            rank += (lj > li) || (lj == li && j < i);
+            const int kj = over_keys ? vm_lq(vm, j) : vm_lk(vm, j), oj = over_keys ? vm_lk(vm, j) : vm_lq(vm, j);
+            rank += (kj > ki) || (kj == ki && (oj > oi || (oj == oi && j < i)));
         }
         vm.order[rank] = i;
     }
@@ -104,17 +119,18 @@ __device__ __forceinline__ void sched_varlen_build(VarlenMap& vm, const int* cu,
         int acc = 0;
         for (int k = 0; k < B; ++k) {
             vm.pre[k] = acc;
-            int b = vm.order[k];
-            int L = vm.start[b + 1] - vm.start[b];
-            acc += H * ((L + rows_per_block - 1) / rows_per_block);
+            const int b = vm.order[k];
+            const int L = over_keys ? vm_lk(vm, b) : vm_lq(vm, b);
+            acc += heads * ((L + rows_per_block - 1) / rows_per_block);
         }
         vm.pre[B] = acc;
     }
     __syncthreads();
 }
 
+// over_keys as in sched_varlen_build: the tile's row blocks split Lk, else Lq.
 __host__ __device__ __forceinline__ Tile sched_varlen(const VarlenMap& vm, int t, int B, int H, int rows_per_block,
-                                             int hs, bool reverse) {
+                                             int hs, bool reverse, bool over_keys) {
     int lo = 0, hi = B - 1;   // largest k with pre[k] <= t
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -123,8 +139,8 @@ __host__ __device__ __forceinline__ Tile sched_varlen(const VarlenMap& vm, int t
     }
     Tile ti;
     ti.b = vm.order[lo];
-    int L = vm.start[ti.b + 1] - vm.start[ti.b];
-    int nm = (L + rows_per_block - 1) / rows_per_block;
+    const int L = over_keys ? vm_lk(vm, ti.b) : vm_lq(vm, ti.b);
+    const int nm = (L + rows_per_block - 1) / rows_per_block;
     sched_within_batch(t - vm.pre[lo], nm, H, hs, reverse, ti.h, ti.m);
     return ti;
 }

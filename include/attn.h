@@ -26,6 +26,15 @@
  *          cu_seqlens[B] = T; tensors are [T, H, d], lse is fp32 [H, T].
  *          Sequence b covers rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends
  *          only within itself. 1 <= B <= 1024.
+ *   varlen with key offsets of their own (attn_fwd_varlen, attn_bwd_varlen):
+ *          cu_seqlens_q packs the queries (Tq rows) and cu_seqlens_k the keys
+ *          (Tk rows) of the same B sequences; sequence b has Lq_b =
+ *          cu_seqlens_q[b+1]-cu_seqlens_q[b] queries and Lk_b keys and is
+ *          its own rectangular problem, causal bottom-right aligned within it
+ *          (j <= i + Lk_b - Lq_b); q, o, dq, dO are [Tq, H, d], k, v, dk, dv
+ *          [Tk, Hkv, d], lse fp32 [H, Tq]. Either length may be 0 for a
+ *          sequence (no keys: O = 0, LSE = -inf). Both arrays on the device,
+ *          same rules as cu_seqlens.
  *   grouped heads (attn_fwd_gqa, attn_bwd_gqa): k, v, dk, dv have Hkv heads
  *          instead of H ([B, Lk, Hkv, d] or [T, Hkv, d]); H must be a
  *          multiple of Hkv, and query head h reads key/value head
@@ -126,6 +135,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              cudaStream_t stream);
 
 /*
+ * Forward pass of a packed batch whose sequences have key lengths of their
+ * own (see "varlen with key offsets" above), e.g. prefill and decode steps
+ * in one call (FlashAttention-4 paper, Section 3.3, varlen scheduling).
+ * Grouped heads and the head-dim pairs as in attn_fwd_gqa. Sequences are
+ * walked longest first by key count (the longest work tile of a sequence
+ * visits all its keys). Null offsets return ATTN_ERR_ARG.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream);
+
+/*
  * Workspace for attn_bwd_gqa: as attn_bwd_workspace_size, plus fp32 slots
  * for partial dK and dV when the backward splits a group's query heads over
  * several work tiles (see attn_bwd_gqa). Hkv = H gives attn_bwd_workspace_size.
@@ -152,6 +173,19 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
                  int B, int H, int Hkv, int Lq, int Lk, int d, float scale, int causal,
                  const int* cu_seqlens, int deterministic, void* workspace, size_t ws_bytes,
                  cudaStream_t stream);
+
+/*
+ * Backward pass of a packed batch with key offsets of their own (dv = d);
+ * otherwise as attn_bwd_gqa. Sequences are walked longest first by query
+ * count (the backward's work tiles are key blocks, and the longest visits
+ * every query block). workspace: attn_bwd_gqa_workspace_size(B, H, Hkv, Tq,
+ * Tk, d, causal, deterministic) bytes.
+ */
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv,
+                    int B, int H, int Hkv, int Tq, int Tk, int d, float scale, int causal,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic,
+                    void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Backward pass that allocates nothing: the same operation, arguments and

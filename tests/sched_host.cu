@@ -56,41 +56,59 @@ static void check_dense(int B, int H, int nm, int hs) {
     }
 }
 
-// a varlen map as the device builds it: sequences sorted longest first (ties by
-// index), prefix counts of H * ceil(L / rows) tiles
-static void build_map(VarlenMap& vm, const std::vector<int>& lens, int H, int rows) {
-    const int B = (int)lens.size();
-    vm.start[0] = 0;
-    for (int i = 0; i < B; ++i) vm.start[i + 1] = vm.start[i] + lens[i];
+// a varlen map as the device builds it: tiles split the query rows (forward)
+// or the keys (over_keys, backward); sequences sorted by the other length,
+// longest first (ties: the tiled length, then the index); prefix counts of
+// H * ceil(tiled length / rows) tiles
+static void build_map(VarlenMap& vm, const std::vector<int>& lq, const std::vector<int>& lk, int H, int rows,
+                      bool over_keys) {
+    const int B = (int)lq.size();
+    vm.start[0] = vm.start_k[0] = 0;
+    for (int i = 0; i < B; ++i) {
+        vm.start[i + 1] = vm.start[i] + lq[i];
+        vm.start_k[i + 1] = vm.start_k[i] + lk[i];
+    }
+    const std::vector<int>& key = over_keys ? lq : lk;
+    const std::vector<int>& tiled = over_keys ? lk : lq;
     std::vector<int> idx(B);
     for (int i = 0; i < B; ++i) idx[i] = i;
-    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return lens[a] > lens[b]; });
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
+        return key[a] != key[b] ? key[a] > key[b] : tiled[a] > tiled[b];
+    });
     int acc = 0;
     for (int k = 0; k < B; ++k) {
         vm.order[k] = idx[k];
         vm.pre[k] = acc;
-        acc += H * ((lens[idx[k]] + rows - 1) / rows);
+        acc += H * ((tiled[idx[k]] + rows - 1) / rows);
     }
     vm.pre[B] = acc;
 }
 
-static void check_varlen(const std::vector<int>& lens, int H, int rows, int hs) {
+static void check_varlen(const std::vector<int>& lq, const std::vector<int>& lk, int H, int rows, int hs,
+                         bool over_keys) {
     static VarlenMap vm;
-    build_map(vm, lens, H, rows);
-    const int B = (int)lens.size(), n = vm.pre[B];
+    build_map(vm, lq, lk, H, rows, over_keys);
+    const int B = (int)lq.size(), n = vm.pre[B];
+    const std::vector<int>& key = over_keys ? lq : lk;
+    const std::vector<int>& tiled = over_keys ? lk : lq;
     std::set<std::tuple<int, int, int>> got;
     int prev_len = 1 << 30;
     for (int t = 0; t < n; ++t) {
-        Tile ti = sched_varlen(vm, t, B, H, rows, hs, true);
-        const int L = lens[ti.b], nm = (L + rows - 1) / rows;
+        Tile ti = sched_varlen(vm, t, B, H, rows, hs, true, over_keys);
+        const int L = tiled[ti.b], nm = (L + rows - 1) / rows;
         if (ti.h < 0 || ti.h >= H || ti.m < 0 || ti.m >= nm) fail("varlen tile out of range", ti.b, ti.h, ti.m);
-        if (L > prev_len) fail("varlen not longest first", t, L, prev_len);
-        prev_len = L;
+        if (key[ti.b] > prev_len) fail("varlen not longest first", t, key[ti.b], prev_len);
+        prev_len = key[ti.b];
         got.insert({ti.b, ti.h, ti.m});
     }
     int expect = 0;
-    for (int L : lens) expect += H * ((L + rows - 1) / rows);
+    for (int L : tiled) expect += H * ((L + rows - 1) / rows);
     if ((int)got.size() != expect || n != expect) fail("varlen coverage", n, expect, (int)got.size());
+}
+
+static void check_varlen(const std::vector<int>& lens, int H, int rows, int hs) {
+    check_varlen(lens, lens, H, rows, hs, false);
+    check_varlen(lens, lens, H, rows, hs, true);
 }
 
 // causal balance: per-CTA sums of tile lengths under the longest-first order
@@ -128,6 +146,11 @@ int main() {
     check_varlen({1, 128, 200, 513, 77, 256}, 3, 128, 2);
     check_varlen({1, 128, 200, 513, 77, 256}, 3, 256, 3);
     check_varlen({16384, 256, 300, 300, 4096, 1}, 16, 128, 16);
+    // key lengths of their own (prefill and decode mixed; empty sides)
+    for (bool over_keys : {false, true}) {
+        check_varlen({1, 1, 4096, 0, 77, 513}, {8192, 300, 4096, 5, 0, 128}, 4, 128, 2, over_keys);
+        check_varlen({1, 1, 4096, 0, 77, 513}, {8192, 300, 4096, 5, 0, 128}, 3, 256, 3, over_keys);
+    }
     // the causal workloads of the benchmark, forward (256-row tiles) and backward (128-key blocks)
     check_causal_balance(4, 16, 4096, 256, true, 152, 0.03);
     check_causal_balance(4, 16, 4096, 128, false, 152, 0.03);
