@@ -50,6 +50,9 @@ WORKLOADS = {
     # grouped heads (attn_fwd_gqa / attn_bwd_gqa): 16 query heads over 2 key/value heads
     "b2h16kv2l8192d128": (inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
+    # 16 prefill sequences (queries = keys) and 16 decode steps (1-16 queries
+    # against a long key cache), 4 key/value heads (attn_fwd_varlen / attn_bwd_varlen)
+    "mix32_prefill_decode_h16kv4d128": (inputs.PREFILL_DECODE, (True,)),
     "b1h32l32768d128": (inputs.LONG, (True, False)),
 }
 DEFAULT_WORKLOAD = "b4h16l4096d128"
@@ -118,11 +121,12 @@ class Problem:
         self.host = t
         self.q, self.k, self.v, self.do = (t[n].to(device) for n in ("q", "k", "v", "do"))
         self.cu = t["cu_seqlens"].to(device) if w.varlen else None
+        self.cuk = t["cu_seqlens_k"].to(device) if "cu_seqlens_k" in t else None
         self.o = torch.empty(self.q.shape[:-1] + (w.d_v,), dtype=self.q.dtype, device=device)
         self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
         self.Hkv = w.H_kv
         if w.varlen:
-            self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.total, w.total, w.d
+            self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.total, w.total_k, w.d
             self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=device)
         else:
             self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.L, w.L, w.d
@@ -131,12 +135,25 @@ class Problem:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def fwd(self, causal):
+        if self.cuk is not None:
+            rc = binding.attn_fwd_varlen(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
+                                         self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu, self.cuk)
+            if rc:
+                raise binding.AttnError(rc, binding.last_error())
+            return
         rc = binding.attn_fwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
                                   self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
     def bwd(self, causal):
+        if self.cuk is not None:
+            rc = binding.attn_bwd_varlen(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk,
+                                         self.dv, self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.scale,
+                                         causal, self.cu, self.cuk, 0, self.ws, self.ws.numel())
+            if rc:
+                raise binding.AttnError(rc, binding.last_error())
+            return
         rc = binding.attn_bwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
                                   self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.scale, causal, self.cu,
                                   0, self.ws, self.ws.numel())
@@ -242,17 +259,23 @@ def oracle_sample(w, variants, nthreads=None):
     t = inputs.make(w)
     nthreads = nthreads or oracle.default_threads()
     if w.varlen:
+        # the longest prefill sequence (queries = keys), head 0
         cu = t["cu_seqlens"]
-        a, L = int(cu[0]), int(cu[1] - cu[0])
-        src = {n: t[n][a:a + L, :1].unsqueeze(0) for n in ("q", "k", "v", "do")}
-        where = "sequence 0, head 0"
+        cuk = t.get("cu_seqlens_k", cu)
+        lq, lk = cu[1:] - cu[:-1], cuk[1:] - cuk[:-1]
+        same = [b for b in range(w.B) if int(lq[b]) == int(lk[b])]
+        s = max(same, key=lambda b: int(lq[b])) if w.lengths_k is not None else 0
+        a, c, L = int(cu[s]), int(cuk[s]), int(lq[s])
+        src = {n: t[n][a:a + L, :1].unsqueeze(0) for n in ("q", "do")}
+        src.update({n: t[n][c:c + L, :1].unsqueeze(0) for n in ("k", "v")})
+        where = f"sequence {s}, head 0"
     else:
         L = w.L
         src = {n: t[n][:1, :, :1] for n in ("q", "k", "v", "do")}
         where = "batch 0, head 0"
 
     def sample_flops(Lp):
-        sw = w.with_(lengths=None, B=1, H=1, L=Lp)
+        sw = w.with_(lengths=None, lengths_k=None, hkv=None, B=1, H=1, L=Lp)
         return sum(flops(sw, c, kind) for c in variants for kind in kinds_of(w))
 
     Lp = L

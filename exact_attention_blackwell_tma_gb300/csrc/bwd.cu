@@ -90,11 +90,14 @@ struct BwdTile {
 
 // The tile's query blocks in visiting order: every query head of its share of
 // the group (the whole group unless split, so dK and dV of the block collect
-// it in tensor memory), each over [m_begin, m_end).
+// it in tensor memory), each over [m_begin, m_end). kGQA = false (one query
+// head per key/value head): the head never changes.
 struct QWalk {
     int h, m;   // query head, 128-row query block
+    template <bool kGQA>
     __device__ __forceinline__ void next(const BwdTile& f) {
-        if (++m == f.m_end) {
+        ++m;
+        if (kGQA && m == f.m_end) {
             m = f.m_begin;
             ++h;
         }
@@ -104,12 +107,19 @@ __device__ __forceinline__ QWalk qwalk(const BwdTile& f) { return QWalk{f.hq0, f
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
+// kGQA: grouped heads (the kernels for one query head per key/value head are
+// instantiated without the group walk and the split, which keeps their code
+// and registers as small as before grouped heads existed)
+template <bool kGQA>
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
     // the split tiles of one key block are neighbours in the walk, so they run
     // at the same time and share the block's K and V in L2
-    const int sp = t % p.split;
-    t /= p.split;
+    int sp = 0;
+    if constexpr (kGQA) {
+        sp = t % p.split;
+        t /= p.split;
+    }
     Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false, true)
                  : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, false)
                              : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
@@ -136,10 +146,16 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
     }
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
-    const int per = g.group / p.split;
-    f.s = sp;
-    f.hq0 = f.h * g.group + sp * per;
-    f.nblk = per * (f.m_end - f.m_begin);
+    if constexpr (kGQA) {
+        const int per = g.group / p.split;
+        f.s = sp;
+        f.hq0 = f.h * g.group + sp * per;
+        f.nblk = per * (f.m_end - f.m_begin);
+    } else {
+        f.s = 0;
+        f.hq0 = f.h;
+        f.nblk = f.m_end - f.m_begin;
+    }
     return f;
 }
 
@@ -230,8 +246,8 @@ __global__ void bwd_convert(const float* __restrict__ acc, __nv_bfloat16* __rest
 
 // ----------------------------------------------------------------------------
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
-// other path's code out of each kernel)
-template <int HD, bool kDet>
+// other path's code out of each kernel); kGQA: grouped heads (bwd_tile)
+template <int HD, bool kDet, bool kGQA>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -295,7 +311,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
     const bool varlen = g.cu_seqlens != nullptr;
     const VarlenMap* vmp = varlen ? vm : nullptr;
-    const int n_tiles = varlen ? vm->pre[g.B] * p.split : p.n_tiles;
+    const int n_tiles = varlen ? vm->pre[g.B] * (kGQA ? p.split : 1) : p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -304,7 +320,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -320,7 +336,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             __syncwarp();
             ++tile_it;
             QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk && ok; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk && ok; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NQS) & 1u) ^ 1u, w, lane);
@@ -409,7 +425,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
             if (!ok) break;
@@ -516,14 +532,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
             // this thread's dK/dV row: bf16 outputs, or (split tiles) fp32 partial
             // slots, dK slot f.s and dV slot split + f.s; computed where used, so
             // that no pointer stays live through the query-block loop
-            const bool partial = p.split > 1;
+            const bool partial = kGQA && p.split > 1;
             auto kv_off = [&]() { return (krow * g.Hkv + f.h) * HD + wg * (HD / 2); };
             auto part_slot = [&](int which) {   // 0: dV, 1: dK
                 const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
@@ -553,7 +569,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             // query q (inside the sequence) is allowed for this key iff q_lo <= q < lq
             const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
             QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 uint8_t* ds_tile = ds_tiles + (qc & 1u) * Lay::kDSBytes;   // alternate dS tiles per block
@@ -685,9 +701,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
             QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
@@ -810,7 +826,9 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
     } else {
         using Lay = BwdLayout<HD>;
-        auto kern = p.deterministic ? bwd_kernel<HD, true> : bwd_kernel<HD, false>;
+        const bool gqa = g.group > 1;
+        auto kern = p.deterministic ? (gqa ? bwd_kernel<HD, true, true> : bwd_kernel<HD, true, false>)
+                                    : (gqa ? bwd_kernel<HD, false, true> : bwd_kernel<HD, false, false>);
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;

@@ -85,8 +85,10 @@ struct WideBwdTile {
 // share of the group, each over [m_begin, m_end).
 struct WideQWalk {
     int h, m;   // query head, 128-row query block
+    template <bool kGQA>
     __device__ __forceinline__ void next(const WideBwdTile& f) {
-        if (++m == f.m_end) {
+        ++m;
+        if (kGQA && m == f.m_end) {
             m = f.m_begin;
             ++h;
         }
@@ -99,10 +101,12 @@ __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b
 // Tile t: key-block tile t/2 of the d <= 128 walk (split tiles included), chunk
 // t%2 (the two chunks of a key block run at the same time on neighbouring CTAs
 // and share its loads in L2).
+// kGQA: grouped heads, as in bwd.cu's bwd_tile
+template <bool kGQA>
 __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
-    const int sp = (t >> 1) % p.split;
-    const int u = (t >> 1) / p.split;
+    const int sp = kGQA ? (t >> 1) % p.split : 0;
+    const int u = kGQA ? (t >> 1) / p.split : t >> 1;
     Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false, true)
                  : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, false)
                              : sched_dense(u, g.Hkv, p.nm, p.head_section, false));
@@ -126,16 +130,22 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
     f.m_begin = 0;
     if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
     if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
-    const int per = g.group / p.split;
-    f.s = sp;
-    f.hq0 = f.h * g.group + sp * per;
-    f.nblk = per * (f.m_end - f.m_begin);
+    if constexpr (kGQA) {
+        const int per = g.group / p.split;
+        f.s = sp;
+        f.hq0 = f.h * g.group + sp * per;
+        f.nblk = per * (f.m_end - f.m_begin);
+    } else {
+        f.s = 0;
+        f.hq0 = f.h;
+        f.nblk = f.m_end - f.m_begin;
+    }
     return f;
 }
 
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
-// other path's code out of each kernel)
-template <int HD, bool kDet>
+// other path's code out of each kernel); kGQA: grouped heads
+template <int HD, bool kDet, bool kGQA>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -197,7 +207,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const WaitCtx w{abort_flag, p.status, p.wait_budget_ns};
     const bool varlen = g.cu_seqlens != nullptr;
     const VarlenMap* vmp = varlen ? vm : nullptr;
-    const int n_tiles = 2 * (varlen ? vm->pre[g.B] * p.split : p.n_tiles);
+    const int n_tiles = 2 * (varlen ? vm->pre[g.B] * (kGQA ? p.split : 1) : p.n_tiles);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -206,7 +216,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -223,7 +233,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ++tile_it;
             const int pc = f.c, po = 1 - f.c;
             WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk && ok; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk && ok; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 for (int item = 0; item < kItemsPerBlock; ++item) {
                     const uint32_t slot = ic % NS;
@@ -331,7 +341,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             const int pc = f.c, po = 1 - f.c;
             const bool narrow = chunk_width<HD>(f.c) == 64;
@@ -436,7 +446,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
             const int cw = chunk_width<HD>(f.c);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
@@ -444,7 +454,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // this thread's dK/dV chunk row: bf16 outputs, or (split tiles) fp32
             // partial slots, dK slot f.s and dV slot split + f.s; computed where
             // used, so that no pointer stays live through the query-block loop
-            const bool partial = p.split > 1;
+            const bool partial = kGQA && p.split > 1;
             auto kv_off = [&]() { return (krow * g.Hkv + f.h) * HD + 128 * f.c + wg * (cw / 2); };
             auto part_slot = [&](int which) {   // 0: dV, 1: dK
                 const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
@@ -472,7 +482,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
             WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
                 if (!ok) break;
@@ -601,11 +611,11 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
             const int cw = chunk_width<HD>(f.c);
             const int rounds = cw / 64;
             WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next(f)) {
+            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
@@ -700,7 +710,9 @@ cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
                            int num_sms, cudaStream_t stream) {
     using Lay = WideBwdLayout<HD>;
-    auto kern = p.deterministic ? bwd_wide_kernel<HD, true> : bwd_wide_kernel<HD, false>;
+    const bool gqa = p.g.group > 1;
+    auto kern = p.deterministic ? (gqa ? bwd_wide_kernel<HD, true, true> : bwd_wide_kernel<HD, true, false>)
+                                : (gqa ? bwd_wide_kernel<HD, false, true> : bwd_wide_kernel<HD, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

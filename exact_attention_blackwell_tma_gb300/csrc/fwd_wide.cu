@@ -38,7 +38,6 @@ struct WideLayout {
     static constexpr int kHalves = HD / 64;               // 64-column boxes of a Q/K row
     static constexpr int kHalvesV = DV / 64;              // ... of a V row
     static constexpr int kTileBytes = kBM * HD * 2;       // Q/K tile; ring slots have this size
-    static constexpr int kVTileBytes = kBM * DV * 2;
     static constexpr int kStages = HD == 192 ? 3 : 2;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTileBytes;

@@ -14,7 +14,12 @@ Section 5, Figs. 4-8 sweep sequence length and head dim):
     that the running row maximum jumps and conditional rescaling is exercised;
   * the variable-length batch draws its sequence lengths uniformly from
     ``[lo, hi]`` (seed ``10*s + 5``) and packs the sequences back to back;
-  * grouped heads: K and V (and the spikes) are drawn with ``hkv`` heads.
+  * grouped heads: K and V (and the spikes) are drawn with ``hkv`` heads;
+  * a batch with key lengths of their own (``lengths_k``) packs K and V by
+    those lengths; the prefill/decode mix draws (seed ``10*s + 6``) half its
+    sequences as prefill (queries = keys, uniform in ``[lo, hi]``) and half
+    as decode steps (1 to 16 queries against a key cache uniform in
+    ``[lo_k, hi_k]``), in a shuffled order.
 """
 from __future__ import annotations
 
@@ -40,6 +45,7 @@ class Workload:
     lengths: Optional[tuple] = None   # varlen: per-sequence lengths
     dv: Optional[int] = None          # head dim of v (and dO); None: the same as q and k
     hkv: Optional[int] = None         # key/value heads (grouped heads); None: H
+    lengths_k: Optional[tuple] = None # varlen: per-sequence key lengths; None: the query lengths
 
     @property
     def scale(self) -> float:
@@ -62,13 +68,29 @@ class Workload:
     def total(self) -> int:
         return sum(self.lengths) if self.varlen else self.B * self.L
 
+    @property
+    def keys(self) -> tuple:
+        """Per-sequence key lengths of a varlen batch."""
+        return self.lengths if self.lengths_k is None else self.lengths_k
+
+    @property
+    def total_k(self) -> int:
+        return sum(self.keys) if self.varlen else self.B * self.L
+
     def pairs(self) -> int:
-        """Number of unmasked (query, key) pairs summed over batch and heads."""
-        def per_seq(L):
-            return L * (L + 1) // 2 if self.causal else L * L
+        """Number of unmasked (query, key) pairs summed over batch and heads
+        (causal: bottom-right aligned, j <= i + Lk - Lq)."""
+        def per_seq(lq, lk):
+            if not self.causal:
+                return lq * lk
+            # row i sees min(lk, max(0, i + 1 + lk - lq)) keys
+            full = max(0, min(lq, lq - lk))          # rows before the first visible key
+            n = lq - full                             # rows that see 1 + (i - full) ... keys
+            first = lk - lq + full + 1 if n else 0
+            return n * first + n * (n - 1) // 2 if n else 0
         if self.varlen:
-            return self.H * sum(per_seq(L) for L in self.lengths)
-        return self.B * self.H * per_seq(self.L)
+            return self.H * sum(per_seq(a, b) for a, b in zip(self.lengths, self.keys))
+        return self.B * self.H * per_seq(self.L, self.L)
 
     def fwd_flops(self) -> int:
         """Algorithmic forward FLOPs: 2*d (S = Q K^T) + 2*d_v (O = P V) per unmasked pair."""
@@ -87,6 +109,22 @@ def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
     return tuple(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g))
 
 
+def prefill_decode_lengths(n: int, lo: int, hi: int, lo_k: int, hi_k: int, seed: int):
+    """(query lengths, key lengths) of n sequences, half prefill, half decode."""
+    g = torch.Generator("cpu").manual_seed(10 * seed + 6)
+    lq, lk = [], []
+    for i in range(n):
+        if i < n // 2:
+            L = int(torch.randint(lo, hi + 1, (1,), generator=g))
+            lq.append(L)
+            lk.append(L)
+        else:
+            lq.append(int(torch.randint(1, 17, (1,), generator=g)))
+            lk.append(int(torch.randint(lo_k, hi_k + 1, (1,), generator=g)))
+    perm = torch.randperm(n, generator=g).tolist()
+    return tuple(lq[i] for i in perm), tuple(lk[i] for i in perm)
+
+
 def cu_seqlens(lengths) -> torch.Tensor:
     cu = [0]
     for L in lengths:
@@ -101,6 +139,9 @@ HDSWEEP = Workload("b2h16l8192", B=2, H=16, L=8192, d=128, causal=True, seed=3, 
 VARLEN = Workload("varlen32_h16d128", B=32, H=16, L=16384, d=128, causal=True, seed=4,
                   lengths=varlen_lengths(32, 256, 16384, 4))
 LONG = Workload("b1h32l32768d128", B=1, H=32, L=32768, d=128, causal=True, seed=5)
+_PD_Q, _PD_K = prefill_decode_lengths(32, 256, 8192, 1024, 16384, 6)
+PREFILL_DECODE = Workload("mix32_prefill_decode_h16kv4d128", B=32, H=16, L=16384, d=128, causal=True, seed=6,
+                          lengths=_PD_Q, lengths_k=_PD_K, hkv=4)
 
 
 def _randn(shape, seed: int) -> torch.Tensor:
@@ -114,7 +155,7 @@ def make(w: Workload, with_grad: bool = True) -> dict:
     Dense layout ``[B, L, H, d]``; varlen ``[T, H, d]`` plus ``cu_seqlens``.
     """
     shape = (w.total, w.H, w.d) if w.varlen else (w.B, w.L, w.H, w.d)
-    kshape = shape[:-2] + (w.H_kv, w.d)
+    kshape = (w.total_k, w.H_kv, w.d) if w.varlen else (w.B, w.L, w.H_kv, w.d)
     q = _randn(shape, 10 * w.seed + 0)
     k = _randn(kshape, 10 * w.seed + 1)
     v = _randn(kshape[:-1] + (w.d_v,), 10 * w.seed + 2)
@@ -131,6 +172,8 @@ def make(w: Workload, with_grad: bool = True) -> dict:
         out["do"] = _randn(shape[:-1] + (w.d_v,), 10 * w.seed + 3).to(torch.bfloat16)
     if w.varlen:
         out["cu_seqlens"] = cu_seqlens(w.lengths)
+        if w.lengths_k is not None:
+            out["cu_seqlens_k"] = cu_seqlens(w.lengths_k)
     return out
 
 

@@ -99,3 +99,36 @@ def test_argument_errors():
     rc = binding.attn_fwd_varlen(q, k, v, o, lse, 2, 2, 2, q.shape[0], k.shape[0], 64, 64, 0.1, True, cu.cuda(),
                                  None)
     assert rc == binding.ATTN_ERR_ARG
+
+
+def test_workload_prefill_decode_mix():
+    """The benchmark's mix: 16 prefill sequences (256-8192 rows) and 16 decode
+    steps (1-16 queries against 1024-16384 keys), H16 over 4 key/value heads,
+    d128, causal; sampled query and key rows of four sequences against the
+    oracle, dK/dV on the whole group of key/value head 1."""
+    w = inputs.PREFILL_DECODE
+    t = inputs.make(w)
+    cu, cuk = t["cu_seqlens"], t["cu_seqlens_k"]
+    o, lse, dq, dk, dv = _run(t, cu, cuk, True, w.scale)
+    lq, lk = np.diff(cu.numpy()), np.diff(cuk.numpy())
+    G = w.H // w.H_kv
+    prefill = [b for b in range(w.B) if lq[b] == lk[b]]
+    decode = [b for b in range(w.B) if lq[b] != lk[b]]
+    picks = [max(prefill, key=lambda b: lq[b]), min(prefill, key=lambda b: lq[b]),
+             max(decode, key=lambda b: lk[b]), max(decode, key=lambda b: lq[b])]
+    rng = np.random.default_rng(7)
+    for b in picks:
+        a, c, L, M = int(cu[b]), int(cuk[b]), int(lq[b]), int(lk[b])
+        qrows = sorted(set(rng.choice(L, size=min(L, 12), replace=False).tolist()) | {0, L - 1})
+        krows = sorted(set(rng.choice(M, size=min(M, 8), replace=False).tolist()) | {0, M - 1})
+        kh = 1
+        grp = list(range(kh * G, kh * G + G))
+        sub = {n: to64(t[n][a:a + L][:, grp])[None] for n in ("q", "do")}
+        sub.update({n: to64(t[n][c:c + M][:, [kh]])[None] for n in ("k", "v")})
+        o_ref, lse_ref = oracle.fwd(sub["q"], sub["k"], sub["v"], w.scale, True, rows=qrows)
+        assert_fwd_close(to64(o[a:a + L][qrows][:, grp])[None], to64(lse[grp][:, a:a + L][:, qrows])[None],
+                         o_ref[:, qrows], lse_ref[:, :, qrows], f"mix seq {b} (Lq={L}, Lk={M})")
+        rq, rk, rv = oracle.bwd(sub["q"], sub["k"], sub["v"], sub["do"], w.scale, True, qrows=qrows, krows=krows)
+        assert_grad_close(to64(dq[a:a + L][qrows][:, grp])[None], rq[:, qrows], f"mix seq {b} dQ")
+        assert_grad_close(to64(dk[c:c + M][krows][:, [kh]])[None], rk[:, krows], f"mix seq {b} dK")
+        assert_grad_close(to64(dv[c:c + M][krows][:, [kh]])[None], rv[:, krows], f"mix seq {b} dV")
