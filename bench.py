@@ -2,13 +2,13 @@
 """Throughput benchmark of the attention hot path on GB300.
 
 A step is one pass of the whole path over one batch of synthetic input: for
-each mask variant of the workload, the forward (attn_fwd) and the backward
-(attn_bwd: preprocess, main kernel, dQ conversion), called through their
-grouped-head forms (attn_fwd_gqa, attn_bwd_gqa; key/value heads = H except
-in the grouped workload). The default workload is
-B=4, H=16, L=4096, d=128 (bf16), causal and non-causal. Throughput is
-algorithmic FLOPs / time: forward 4*d per unmasked (query, key) pair,
-backward 2.5x that.
+each mask variant of the workload, the forward and the backward (preprocess,
+main kernel, dQ conversion), called through the general entry points
+attn_fwd_ex / attn_bwd_ex (attn_fwd_varlen / attn_bwd_varlen for the
+prefill/decode mix). The default workload is B=4, H=16, L=4096, d=128
+(bf16), causal and non-causal. Throughput is algorithmic FLOPs / time:
+forward 2*(d + d_v) per unmasked (query, key) pair, backward 2*(3d + 2d_v)
+(2.5x the forward when d_v = d).
 
   python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -45,9 +45,9 @@ WORKLOADS = {
     "b2h16l8192d64": (inputs.HDSWEEP.with_(d=64), (True,)),
     "b2h16l8192d192": (inputs.HDSWEEP.with_(d=192), (True,)),
     "b2h16l8192d256": (inputs.HDSWEEP.with_(d=256), (True,)),
-    # q/k head dim 192 with v head dim 128 (attn_fwd_hdim): forward only
+    # q/k head dim 192 with v head dim 128 (attn_fwd_ex / attn_bwd_ex)
     "b2h16l8192dqk192dv128": (inputs.HDSWEEP.with_(d=192, dv=128), (True,)),
-    # grouped heads (attn_fwd_gqa / attn_bwd_gqa): 16 query heads over 2 key/value heads
+    # grouped heads: 16 query heads over 2 key/value heads
     "b2h16kv2l8192d128": (inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
     # 16 prefill sequences (queries = keys) and 16 decode steps (1-16 queries
@@ -60,8 +60,8 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 def kinds_of(w):
-    """The calls a step makes: the backward exists for v head dim = q/k head dim."""
-    return ("fwd", "bwd") if w.d_v == w.d else ("fwd",)
+    """The calls a step makes: the forward and the backward."""
+    return ("fwd", "bwd")
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
 # workload's dominant kernel, from the ncu capture summarised in the named
@@ -131,7 +131,8 @@ class Problem:
         else:
             self.B, self.H, self.Lq, self.Lk, self.d = w.B, w.H, w.L, w.L, w.d
             self.lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=device)
-        ws = max(binding.attn_bwd_gqa_workspace_size(self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, 1, 0), 1)
+        ws = max(binding.attn_bwd_ex_workspace_size(self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.d_v,
+                                                    1, 0), 1)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def fwd(self, causal):
@@ -141,8 +142,8 @@ class Problem:
             if rc:
                 raise binding.AttnError(rc, binding.last_error())
             return
-        rc = binding.attn_fwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
-                                  self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu)
+        rc = binding.attn_fwd_ex(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
+                                 self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu, None)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -154,9 +155,9 @@ class Problem:
             if rc:
                 raise binding.AttnError(rc, binding.last_error())
             return
-        rc = binding.attn_bwd_gqa(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
-                                  self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.scale, causal, self.cu,
-                                  0, self.ws, self.ws.numel())
+        rc = binding.attn_bwd_ex(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
+                                 self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.d_v, self.w.scale, causal,
+                                 self.cu, None, 0, self.ws, self.ws.numel())
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 

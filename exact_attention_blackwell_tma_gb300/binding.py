@@ -37,6 +37,13 @@ def _declare(lib):
     lib.attn_fwd_hdim.argtypes = [c_void_p] * 5 + [c_int] * 6 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_fwd_gqa.restype = c_int
     lib.attn_fwd_gqa.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p]
+    lib.attn_fwd_ex.restype = c_int
+    lib.attn_fwd_ex.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
+    lib.attn_bwd_ex_workspace_size.restype = c_size_t
+    lib.attn_bwd_ex_workspace_size.argtypes = [c_int] * 9
+    lib.attn_bwd_ex.restype = c_int
+    lib.attn_bwd_ex.argtypes = ([c_void_p] * 9 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_int, c_void_p,
+                                                                  c_size_t, c_void_p])
     lib.attn_fwd_varlen.restype = c_int
     lib.attn_fwd_varlen.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
@@ -145,6 +152,23 @@ def attn_fwd_varlen(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu
                                   int(causal), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
 
 
+def attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q=None, cu_seqlens_k=None,
+                stream=None) -> int:
+    return load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Lq, Lk, d, d_v, scale,
+                              int(causal), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
+
+
+def attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic) -> int:
+    return load().attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, int(causal), int(deterministic))
+
+
+def attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
+                cu_seqlens_k, deterministic, workspace, ws_bytes, stream=None) -> int:
+    return load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                              _ptr(dv), B, H, Hkv, Lq, Lk, d, d_v, scale, int(causal), _ptr(cu_seqlens_q),
+                              _ptr(cu_seqlens_k), int(deterministic), _ptr(workspace), ws_bytes, _stream(stream))
+
+
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
     return load().attn_bwd_workspace_size(B, H, Lq, Lk, d, int(causal), int(deterministic))
 
@@ -241,18 +265,23 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
              deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None,
              cu_seqlens_k=None):
     """dQ, dK, dV (bf16) for the loss sum(O * dO); k and v may have fewer heads
-    than q (grouped heads), dK and dV then have theirs. cu_seqlens_k as in forward()."""
+    than q (grouped heads), dK and dV then have theirs; v (dO, dV) may have a head
+    dim of its own (d = 192 with 128). cu_seqlens_k as in forward()."""
     _check_tensors(q, k, v, o, lse, dout, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    need = attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic)
+    d_v = v.shape[-1]
+    need = attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = workspace.numel() * workspace.element_size()
-    if cu_seqlens_k is not None:
+    if d_v != d:
+        _check(attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens,
+                           cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
+    elif cu_seqlens_k is not None:
         _check(attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
                                cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
     elif Hkv != H:

@@ -237,6 +237,14 @@ extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
     return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, cu_seqlens, stream);
 }
 
+extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                           int Lq, int Lk, int d, int d_v, float scale, int causal, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, cudaStream_t stream) {
+    if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_fwd_ex: key offsets without query offsets");
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
+                     cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, stream);
+}
+
 extern "C" int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
                                const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream) {
@@ -266,7 +274,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // dQ accumulator | D terms | partial dK/dV slots (split grouped heads) |
 // semaphores | varlen map (placed by the launcher right after the semaphores)
-BwdWorkspace bwd_layout(int B, int H, int Hkv, int Lq, int Lk, int d, bool varlen) {
+BwdWorkspace bwd_layout(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, bool varlen) {
     BwdWorkspace w{};
     const size_t rows_q = varlen ? (size_t)Lq : (size_t)B * Lq;
     const long rows_k = varlen ? (long)Lk : (long)B * Lk;
@@ -275,22 +283,27 @@ BwdWorkspace bwd_layout(int B, int H, int Hkv, int Lq, int Lk, int d, bool varle
     w.dq_off = 0;
     w.delta_off = align256(rows_q * H * d * sizeof(float));
     w.part_off = w.delta_off + align256(rows_q * H * sizeof(float));
-    w.sem_off = w.part_off + align256(bwd_partial_bytes(split, rows_k, Hkv, d));
+    w.sem_off = w.part_off + align256(bwd_partial_bytes(split, rows_k, Hkv, d, dv));
     w.total = w.sem_off + align256(n_sem * sizeof(int)) + align256(sizeof(VarlenMap));
     return w;
 }
 
 }  // namespace
 
-extern "C" size_t attn_bwd_gqa_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int causal,
-                                              int deterministic) {
+extern "C" size_t attn_bwd_ex_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, int causal,
+                                             int deterministic) {
     (void)causal;
     (void)deterministic;
-    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Lq < 0 || Lk < 0 || d <= 0) return 0;
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Lq < 0 || Lk < 0 || d <= 0 || d_v <= 0) return 0;
     // varlen and dense share the formula when Lq and Lk are the packed count;
     // the varlen semaphore bound is the larger one, so take the maximum.
-    BwdWorkspace a = bwd_layout(B, H, Hkv, Lq, Lk, d, false), b = bwd_layout(B, H, Hkv, Lq, Lk, d, true);
+    BwdWorkspace a = bwd_layout(B, H, Hkv, Lq, Lk, d, d_v, false), b = bwd_layout(B, H, Hkv, Lq, Lk, d, d_v, true);
     return a.total > b.total ? a.total : b.total;
+}
+
+extern "C" size_t attn_bwd_gqa_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int causal,
+                                              int deterministic) {
+    return attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d, causal, deterministic);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d, int causal, int deterministic) {
@@ -301,13 +314,16 @@ namespace {
 
 // The backward behind every entry point (cu_seqlens_k as in fwd_entry).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk, int d, float scale, int causal,
-              const int* cu_seqlens, const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
-              cudaStream_t stream) {
+              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale,
+              int causal, const int* cu_seqlens, const int* cu_seqlens_k, int deterministic, void* workspace,
+              size_t ws_bytes, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
     if (rc) return rc;
     rc = check_heads(H, Hkv);
     if (rc) return rc;
+    if (d_v != d && !(d == 192 && d_v == 128))
+        return fail(ATTN_ERR_ARG, "head dims d=%d, d_v=%d not supported (d_v = d, or d = 192 with d_v = 128)", d,
+                    d_v);
     const bool varlen = cu_seqlens != nullptr;
     const long rows_q = varlen ? (long)Lq : (long)B * Lq;
     const long rows_k = varlen ? (long)Lk : (long)B * Lk;
@@ -317,14 +333,14 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(ATTN_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
-    const size_t need = attn_bwd_gqa_workspace_size(B, H, Hkv, Lq, Lk, d, causal, deterministic);
+    const size_t need = attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic);
     if (!workspace || ws_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
     DevInfo di;
     if (!device_info(&di)) return fail(ATTN_ERR_LAUNCH, "cannot query the current device");
-    BwdWorkspace wl = bwd_layout(B, H, Hkv, Lq, Lk, d, varlen);
+    BwdWorkspace wl = bwd_layout(B, H, Hkv, Lq, Lk, d, d_v, varlen);
     char* ws = static_cast<char*>(workspace);
     BwdParams p{};
     p.g.B = B;
@@ -354,6 +370,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     // a work tile is one key block of one key/value head; it streams Q and dO
     // of the query heads of the group (of its share of them when split)
     p.split = bwd_head_split(B, Hkv, p.g.group, Lk, varlen);
+    p.d_v = d_v;
     p.dkv_part = p.split > 1 ? reinterpret_cast<float*>(ws + wl.part_off) : nullptr;
     p.n_tiles = varlen ? 0 : B * Hkv * p.nm * p.split;
     p.head_section = head_section(Hkv, (varlen ? (rows_q / B) : Lq) * (long)p.g.group, d);
@@ -365,9 +382,10 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     // Without query rows (or keys) the matching descriptors are never used; they
     // view the other tensor, with the heads of the smaller one so they stay in bounds.
     const int hq_map = rows_q > 0 ? H : Hkv;
+    // (v and dO are d_v <= d wide, so a fallback view of q or k with that width stays in bounds too)
     if (!make_map(&tq, rows_q > 0 ? q : k, qrows, hq_map, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, Hkv, d) ||
-        !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d) ||
-        !make_map(&tdo, rows_q > 0 ? dout : k, qrows, hq_map, d) || !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d))
+        !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d_v) ||
+        !make_map(&tdo, rows_q > 0 ? dout : k, qrows, hq_map, d_v) || !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
@@ -380,8 +398,18 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
                             const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
                             int d, float scale, int causal, const int* cu_seqlens, int deterministic,
                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, scale, causal, cu_seqlens,
                      cu_seqlens, deterministic, workspace, ws_bytes, stream);
+}
+
+extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
+                           int d, int d_v, float scale, int causal, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
+    if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_bwd_ex: key offsets without query offsets");
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
+                     cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -390,7 +418,7 @@ extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, cons
                                const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
                                cudaStream_t stream) {
     if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_bwd_varlen: null offsets");
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, scale, causal, cu_seqlens_q,
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, d, scale, causal, cu_seqlens_q,
                      cu_seqlens_k, deterministic, workspace, ws_bytes, stream);
 }
 

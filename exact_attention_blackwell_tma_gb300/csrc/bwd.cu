@@ -166,14 +166,14 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
     const Geometry& g = p.g;
     const long stride = (long)gridDim.x * blockDim.x;
     const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int d = g.d;
+    const int dv = p.d_v;   // O and dO have the head dim of v
     for (long i = tid; i < rows_q * g.H; i += stride) {
         const long row = i / g.H;
         const int h = (int)(i - row * g.H);
-        const uint4* o4 = reinterpret_cast<const uint4*>(p.o + i * d);
-        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + i * d);
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.o + i * dv);
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + i * dv);
         float acc = 0.f;
-        for (int c = 0; c < d / 8; ++c) {
+        for (int c = 0; c < dv / 8; ++c) {
             uint4 a = o4[c], b = d4[c];
             const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
@@ -204,15 +204,17 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
 }
 
 // Split grouped heads: dK = scale * (sum of the dK slots), dV = sum of the dV
-// slots, in slot order, fp32 -> bf16, 4 elements per step. n4: float4 per slot.
+// slots, in slot order, fp32 -> bf16, 4 elements per step. n4k, n4v: float4
+// per dK slot and per dV slot (the dV slots follow the split dK slots).
 __global__ void bwd_dkv_sum(const float* __restrict__ part, __nv_bfloat16* __restrict__ dk,
-                            __nv_bfloat16* __restrict__ dv, long n4, int split, float scale) {
+                            __nv_bfloat16* __restrict__ dv, long n4k, long n4v, int split, float scale) {
     const long stride = (long)gridDim.x * blockDim.x;
     const float4* p4 = reinterpret_cast<const float4*>(part);
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n4; i += stride) {
-        const bool is_v = i >= n4;
-        const long j = is_v ? i - n4 : i;
-        const float4* src = p4 + (is_v ? (long)split * n4 : 0) + j;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4k + n4v; i += stride) {
+        const bool is_v = i >= n4k;
+        const long j = is_v ? i - n4k : i;
+        const long n4 = is_v ? n4v : n4k;
+        const float4* src = p4 + (is_v ? (long)split * n4k : 0) + j;
         float4 a = src[0];
         for (int sl = 1; sl < split; ++sl) {
             const float4 b = src[(long)sl * n4];
@@ -845,11 +847,11 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     }
     if (p.split > 1) {
         const long rows_k = varlen ? (long)g.Lk : (long)g.B * g.Lk;
-        const long n4 = rows_k * g.Hkv * HD / 4;
-        int blocks = (int)((2 * n4 + 255) / 256);
+        const long n4k = rows_k * g.Hkv * HD / 4, n4v = rows_k * g.Hkv * p.d_v / 4;
+        int blocks = (int)((n4k + n4v + 255) / 256);
         if (blocks > 8 * num_sms) blocks = 8 * num_sms;
         if (blocks < 1) blocks = 1;
-        bwd_dkv_sum<<<blocks, 256, 0, stream>>>(p.dkv_part, p.dk, p.dv, n4, p.split, g.scale);
+        bwd_dkv_sum<<<blocks, 256, 0, stream>>>(p.dkv_part, p.dk, p.dv, n4k, n4v, p.split, g.scale);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

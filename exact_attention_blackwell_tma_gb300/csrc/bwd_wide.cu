@@ -15,6 +15,11 @@
 //    is kept for dV), then Q[c] again for dK (o = the other chunk).
 // Tensor memory: S^T at 0 (P^T over it), dP^T at 128 (dS^T over it, then the
 // dQ chunk), dV chunk at 256, dK chunk at 384. Every wait is bounded.
+//
+// A head dim of its own for v (d_qk = 192, d_v = 128, the FlashAttention-4
+// paper's Section 5.1 shape): dP^T contracts over the 128 columns of V and dO,
+// which are one ring piece, so a query block takes four ring items -- Q[o],
+// Q[c], dO, Q[c] -- and chunk 0 owns all of dV while chunk 1 has none.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -28,16 +33,19 @@ constexpr int kThreads = 512;         // 16 warps, roles as in bwd.cu
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 16384;           // 128 rows x 64 bf16 columns
 constexpr int kPieceBytes = 2 * kBox; // 128 rows x 128 columns
-constexpr int kItemsPerBlock = 5;     // ring items per query block
 constexpr int kLaunchRegs = 128;
 constexpr uint32_t kRegsLoadMma = 72, kRegsCompute = 128, kRegsDq = 184;
 static_assert((kRegsLoadMma + 2 * kRegsCompute + kRegsDq) * 128 <= kLaunchRegs * kThreads, "register split");
 
 __device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
 
-template <int HD>
+// HD: head dim of q and k; DV: of v and dO (HD, or 128 with HD = 192)
+template <int HD, int DV>
 struct WideBwdLayout {
     static constexpr int kHalves = HD / 64;                       // 64-column boxes per row
+    static constexpr int kHalvesV = DV / 64;                      // ... of a V / dO row
+    // ring items per query block: Q[o], Q[c], dO[o], dO[c], Q[c]; or Q[o], Q[c], dO, Q[c]
+    static constexpr int kItems = DV == HD ? 5 : 4;
     static constexpr int kSlots = HD == 192 ? 3 : 2;                // Q/dO piece ring
     // dS tiles. The d <= 128 kernel double-buffers dS so the next dS can be
     // written while the previous dQ is staged through the other tile; here
@@ -46,7 +54,7 @@ struct WideBwdLayout {
     static constexpr int kDSTiles = 1;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kHalves * kBox;
-    static constexpr int kRingOff = 2 * kHalves * kBox;
+    static constexpr int kRingOff = kVOff + kHalvesV * kBox;
     static constexpr int kDSOff = kRingOff + kSlots * kPieceBytes;  // dS tiles, 128 x 128 bf16 (also dQ staging)
     static constexpr int kDSBytes = 2 * kBox;
     static constexpr int kStatOff = kDSOff + kDSTiles * kDSBytes;   // 2 stages: -lse2[128], -D[128]
@@ -145,13 +153,14 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
 
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
 // other path's code out of each kernel); kGQA: grouped heads
-template <int HD, bool kDet, bool kGQA>
+template <int HD, int DV, bool kDet, bool kGQA>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, const VarlenMap* vm) {
-    using Lay = WideBwdLayout<HD>;
+    using Lay = WideBwdLayout<HD, DV>;
     constexpr int NS = Lay::kSlots;
+    constexpr int kItemsPerBlock = Lay::kItems;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -221,13 +230,13 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
             if (lane == 0) {
-                mbar_expect_tx(bar(Lay::kKVFull), 2 * Lay::kHalves * kBox);
-                for (int hf = 0; hf < Lay::kHalves; ++hf) {
+                mbar_expect_tx(bar(Lay::kKVFull), (Lay::kHalves + Lay::kHalvesV) * kBox);
+                for (int hf = 0; hf < Lay::kHalves; ++hf)
                     tma_load_3d(base + Lay::kKOff + hf * kBox, &tmK, bar(Lay::kKVFull), hf * 64, f.h,
                                 f.k_row0 + f.n * kBN);
+                for (int hf = 0; hf < Lay::kHalvesV; ++hf)
                     tma_load_3d(base + Lay::kVOff + hf * kBox, &tmV, bar(Lay::kKVFull), hf * 64, f.h,
                                 f.k_row0 + f.n * kBN);
-                }
             }
             __syncwarp();
             ++tile_it;
@@ -262,9 +271,17 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(Lay::kStatFull + (qb & 1u)));
                     }
-                    const int piece = (item == 0 || item == 2) ? po : pc;
-                    const int nb = piece_boxes<HD>(piece);
-                    const CUtensorMap* src = (item == 2 || item == 3) ? &tmDO : &tmQ;
+                    int piece, nb;
+                    const CUtensorMap* src;
+                    if constexpr (Lay::kItems == 5) {
+                        piece = (item == 0 || item == 2) ? po : pc;
+                        nb = piece_boxes<HD>(piece);
+                        src = (item == 2 || item == 3) ? &tmDO : &tmQ;
+                    } else {   // item 2: the whole of dO (one piece)
+                        piece = item == 0 ? po : (item == 2 ? 0 : pc);
+                        nb = item == 2 ? Lay::kHalvesV : piece_boxes<HD>(piece);
+                        src = item == 2 ? &tmDO : &tmQ;
+                    }
                     if (lane == 0) {
                         mbar_expect_tx(bar(Lay::kRFull + slot), nb * kBox);
                         for (int bb = 0; bb < nb; ++bb)
@@ -365,36 +382,51 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ok = warp_wait(bar(Lay::kDQFree), (dqf & 1u) ^ 1u, w, lane);
                 if (!ok) break;
                 ++dqf;
-                uint32_t s2, s3, s4;
-                ok = item_wait(i0 + 2, s2) && item_wait(i0 + 3, s3);
+                uint32_t s2, s3 = 0, s4;
+                ok = item_wait(i0 + 2, s2) && (Lay::kItems == 4 || item_wait(i0 + 3, s3));
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (lane == 0) {
-                    mma_piece(tmem + Lay::kTDP, v_km, po, s2, false);
-                    mma_piece(tmem + Lay::kTDP, v_km, pc, s3, true);
+                    if constexpr (Lay::kItems == 5) {
+                        mma_piece(tmem + Lay::kTDP, v_km, po, s2, false);
+                        mma_piece(tmem + Lay::kTDP, v_km, pc, s3, true);
+                        tc_commit(bar(Lay::kREmpty + s2));
+                    } else {   // over the DV columns of V and of the one dO piece
+                        const SmemDesc b = at_slot(r_km0, s2);
+#pragma unroll
+                        for (int bb = 0; bb < Lay::kHalvesV; ++bb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t off = desc_step(bb * kBox + kk * 32);
+                                mma_ss(tmem + Lay::kTDP, v_km, off, b, off, kIdSq, (bb > 0 || kk > 0) ? 1u : 0u);
+                            }
+                    }
                     tc_commit(bar(Lay::kDPFull));
-                    tc_commit(bar(Lay::kREmpty + s2));
                 }
                 __syncwarp();
-                // dV[:, chunk] += P^T dO[:, chunk] (P^T from tensor memory)
+                // dV[:, chunk] += P^T dO[:, chunk] (P^T from tensor memory); with DV < HD
+                // chunk 0 owns all of dV and chunk 1 none
                 ok = warp_wait(bar(Lay::kPFull), pcnt & 1u, w, lane);
                 if (!ok) break;
                 ++pcnt;
                 tc_fence_after_sync();
                 if (lane == 0) {
-                    const SmemDesc do_mn = at_slot(r_mn0, s3);
+                    const uint32_t s_do = Lay::kItems == 5 ? s3 : s2;
+                    if (Lay::kItems == 5 || f.c == 0) {
+                        const SmemDesc do_mn = at_slot(r_mn0, s_do);
 #pragma unroll
-                    for (int kk = 0; kk < kBM / 16; ++kk)
-                        mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(kk), do_mn, desc_step(kk * 2048), id_kv,
-                               (u > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(Lay::kREmpty + s3));
+                        for (int kk = 0; kk < kBM / 16; ++kk)
+                            mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(kk), do_mn, desc_step(kk * 2048),
+                                   id_kv, (u > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar(Lay::kREmpty + s_do));
                 }
                 __syncwarp();
                 // dK[:, chunk] += dS^T Q[:, chunk]; dQ[:, chunk] = dS K[:, chunk]
                 ok = warp_wait(bar(Lay::kDSFull), dsc & 1u, w, lane);
                 if (!ok) break;
                 ++dsc;
-                ok = item_wait(i0 + 4, s4);
+                ok = item_wait(i0 + kItemsPerBlock - 1, s4);
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (lane == 0) {
@@ -455,26 +487,27 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // partial slots, dK slot f.s and dV slot split + f.s; computed where
             // used, so that no pointer stays live through the query-block loop
             const bool partial = kGQA && p.split > 1;
-            auto kv_off = [&]() { return (krow * g.Hkv + f.h) * HD + 128 * f.c + wg * (cw / 2); };
-            auto part_slot = [&](int which) {   // 0: dV, 1: dK
-                const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
-                return p.dkv_part + (which ? f.s : p.split + f.s) * slot + kv_off();
+            // columns of the chunk: cw of dK; of dV cw too, or with DV < HD all DV
+            // columns in chunk 0 and none in chunk 1
+            const int cwv = DV == HD ? cw : (f.c == 0 ? DV : 0);
+            auto kv_off = [&](int which) {   // 0: dV (rows of DV), 1: dK (rows of HD)
+                return which ? (krow * g.Hkv + f.h) * HD + 128 * f.c + wg * (cw / 2)
+                             : (krow * g.Hkv + f.h) * DV + 128 * f.c + wg * (cwv / 2);
+            };
+            auto part_slot = [&](int which) {   // dK slots (HD wide) first, then the dV slots (DV wide)
+                const long rows = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv;
+                return p.dkv_part + (which ? f.s * rows * HD : (p.split * HD + f.s * DV) * rows) + kv_off(which);
             };
             if (f.m_begin >= f.m_end) {   // no query sees this key block
-                __nv_bfloat16* dv_ptr = p.dv + kv_off();
-                __nv_bfloat16* dk_ptr = p.dk + kv_off();
-                float* pk_ptr = partial ? part_slot(1) : nullptr;
-                float* pv_ptr = partial ? part_slot(0) : nullptr;
                 if (key_ok) {
-                    if (partial) {
-                        for (int c = 0; c < cw / 8; ++c) {
-                            reinterpret_cast<float4*>(pv_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            reinterpret_cast<float4*>(pk_ptr)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                    } else {
-                        for (int c = 0; c < cw / 16; ++c) {
-                            reinterpret_cast<uint4*>(dv_ptr)[c] = make_uint4(0, 0, 0, 0);
-                            reinterpret_cast<uint4*>(dk_ptr)[c] = make_uint4(0, 0, 0, 0);
+                    for (int which = 0; which < 2; ++which) {
+                        const int cols = (which ? cw : cwv) / 2;
+                        if (partial) {
+                            float4* z = reinterpret_cast<float4*>(part_slot(which));
+                            for (int c = 0; c < cols / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            uint4* z = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + kv_off(which));
+                            for (int c = 0; c < cols / 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
                         }
                     }
                 }
@@ -571,11 +604,12 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after_sync();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const uint32_t tcol = (which ? Lay::kTDK : Lay::kTDV) + wg * (cw / 2);
+                const int cols = which ? cw : cwv;
+                const uint32_t tcol = (which ? Lay::kTDK : Lay::kTDV) + wg * (cols / 2);
                 const float mul = which ? g.scale : 1.f;
-                __nv_bfloat16* dst = (which ? p.dk : p.dv) + kv_off();
+                __nv_bfloat16* dst = (which ? p.dk : p.dv) + kv_off(which);
                 float* pdst = partial ? part_slot(which) : nullptr;
-                for (int c = 0; c < cw / 64; ++c) {
+                for (int c = 0; c < cols / 64; ++c) {
                     tmem_ld32(tmem + lane_off + tcol + c * 32, rr);
                     if (key_ok && partial) {   // unscaled: the sum kernel scales dK
                         float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
@@ -705,14 +739,14 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-template <int HD>
+template <int HD, int DV>
 cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
                            int num_sms, cudaStream_t stream) {
-    using Lay = WideBwdLayout<HD>;
+    using Lay = WideBwdLayout<HD, DV>;
     const bool gqa = p.g.group > 1;
-    auto kern = p.deterministic ? (gqa ? bwd_wide_kernel<HD, true, true> : bwd_wide_kernel<HD, true, false>)
-                                : (gqa ? bwd_wide_kernel<HD, false, true> : bwd_wide_kernel<HD, false, false>);
+    auto kern = p.deterministic ? (gqa ? bwd_wide_kernel<HD, DV, true, true> : bwd_wide_kernel<HD, DV, true, false>)
+                                : (gqa ? bwd_wide_kernel<HD, DV, false, true> : bwd_wide_kernel<HD, DV, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
@@ -731,9 +765,11 @@ cudaError_t launch_bwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                             const void* varlen_map, int num_sms, cudaStream_t stream) {
     const VarlenMap* vm = static_cast<const VarlenMap*>(varlen_map);
+    if (p.g.d == 192 && p.d_v == 128) return launch_wide_hd<192, 128>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+    if (p.d_v != p.g.d) return cudaErrorInvalidValue;
     switch (p.g.d) {
-        case 192: return launch_wide_hd<192>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
-        case 256: return launch_wide_hd<256>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+        case 192: return launch_wide_hd<192, 192>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+        case 256: return launch_wide_hd<256, 256>(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -49,9 +49,10 @@ struct BwdParams {
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     int* semaphores;          // deterministic mode: two counters per dQ tile (one per column chunk)
-    float* dkv_part;          // split > 1: fp32 partial dK (slots 0..split-1), then partial dV, each
-                              // slot laid out like k; null otherwise
+    float* dkv_part;          // split > 1: fp32 partial dK (slots 0..split-1, each laid out like k),
+                              // then partial dV (slots laid out like v); null otherwise
     int split;                // tiles per key block of a key/value head (divides g.group)
+    int d_v;                  // head dim of v, o, dO, dv (g.d, or 128 with g.d = 192)
     int deterministic;
     int n_tiles;              // dense: exact count, split included
     int nm;                   // dense: 128-row K/V blocks per (b, h)
@@ -87,9 +88,9 @@ inline int bwd_head_split(int B, int Hkv, int group, int Lk, bool varlen) {
         if (group % s == 0 && tiles * s >= kSplitTargetTiles) return s;
     return group > 0 ? group : 1;
 }
-// Bytes of the partial dK/dV slots for a split (0 when split == 1).
-inline size_t bwd_partial_bytes(int split, long rows_k, int Hkv, int d) {
-    return split > 1 ? (size_t)2 * split * rows_k * Hkv * d * sizeof(float) : 0;
+// Bytes of the partial dK/dV slots for a split (0 when split == 1); dv: head dim of v.
+inline size_t bwd_partial_bytes(int split, long rows_k, int Hkv, int d, int dv) {
+    return split > 1 ? (size_t)split * rows_k * Hkv * (d + dv) * sizeof(float) : 0;
 }
 
 // Launchers (return cudaSuccess or the launch error).

@@ -97,8 +97,9 @@ class Workload:
         return 2 * (self.d + self.d_v) * self.pairs()
 
     def bwd_flops(self) -> int:
-        """Algorithmic backward FLOPs: five GEMMs, i.e. 2.5x the forward."""
-        return 10 * self.d * self.pairs()
+        """Algorithmic backward FLOPs: five GEMMs per unmasked pair -- S and dK, dQ
+        over d, dP and dV over d_v: 2 * (3 d + 2 d_v) (2.5x the forward when d_v = d)."""
+        return 2 * (3 * self.d + 2 * self.d_v) * self.pairs()
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -89,7 +89,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * [.., H, d], v and o are [.., H, dv] (o has the rows of q). Supported:
  * dv = d (the same as attn_fwd), and d = 192 with dv = 128 (the shape of the
  * FlashAttention-4 paper's Section 5.1, Fig. 5). LSE as in attn_fwd. Other
- * pairs return ATTN_ERR_ARG. No backward for dv != d.
+ * pairs return ATTN_ERR_ARG. The backward for dv != d is attn_bwd_ex.
  */
 int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse,
                   int B, int H, int Lq, int Lk, int d, int dv, float scale, int causal,
@@ -145,6 +145,38 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int H, int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
                     const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream);
+
+/*
+ * The general forward: every entry point above is this one with some
+ * arguments fixed. Hkv key/value heads (grouped heads), a head dim d_v of
+ * its own for v and o (d_v = d, or d = 192 with d_v = 128), and either
+ * dense tensors (cu_seqlens_q == NULL, cu_seqlens_k == NULL), packed
+ * sequences with one offset array (cu_seqlens_k == NULL: Lq = Lk = T), or
+ * packed sequences with key offsets of their own (Lq = Tq, Lk = Tk).
+ * cu_seqlens_k without cu_seqlens_q returns ATTN_ERR_ARG.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream);
+
+/*
+ * Workspace for attn_bwd_ex (any of the arguments attn_bwd_ex accepts).
+ */
+size_t attn_bwd_ex_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, int causal,
+                                  int deterministic);
+
+/*
+ * The general backward, arguments as in attn_fwd_ex (dv here is the dV
+ * output; d_v the head dim of v, o, dO and dV). With d = 192 and d_v = 128
+ * the d = 192 kernel's two column chunks split dK and dQ at column 128;
+ * chunk 0 also owns all of dV and chunk 1 skips the dV product, and the
+ * products with V and dO contract over their 128 columns.
+ */
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv,
+                int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic,
+                void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Workspace for attn_bwd_gqa: as attn_bwd_workspace_size, plus fp32 slots

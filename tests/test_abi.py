@@ -35,6 +35,27 @@ def test_library_exports_every_declared_symbol(built):
         assert hasattr(lib, name), f"{name} declared in attn.h but not exported"
 
 
+def declared_arg_counts():
+    """Number of parameters of every function attn.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, args in re.findall(r"\b(attn_\w+)\s*\(([^)]*)\)\s*;", text):
+        args = args.strip()
+        out[name] = 0 if args in ("", "void") else len(args.split(","))
+    return out
+
+
+def test_binding_declares_the_header_signatures(built):
+    """Every ctypes declaration in the binding has the header's argument count."""
+    lib = binding.load()
+    counts = declared_arg_counts()
+    assert len(counts) == len(declared_functions())
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        assert len(fn.argtypes) == n, f"{name}: binding has {len(fn.argtypes)} arguments, attn.h {n}"
+
+
 def test_error_codes_match_header(built):
     text = open(HEADER).read()
     codes = dict(re.findall(r"#define (ATTN_\w+) \(?(-?\d+)\)?", text))

@@ -88,6 +88,61 @@ def test_deterministic_is_bit_identical(causal, d):
             assert torch.equal(a, b)
 
 
+# ------------------------------------------------------------------ d_qk = 192, d_v = 128
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [1, 77, 129, 300])
+def test_value_head_dim_192_128(L, causal, deterministic):
+    """q/k head dim 192, v (dO, dV) head dim 128: every element of dQ, dK, dV."""
+    t = inputs.small(B=2, H=2, L=L, d=192, dv=128, seed=25)
+    check_all(t, causal, float(np.float32(1 / np.sqrt(192))), [0, 1], f"d192/dv128 L={L} causal={causal}",
+              deterministic)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lk", [(200, 77), (77, 300)])
+def test_value_head_dim_rectangular(Lq, Lk, causal):
+    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=192, dv=128, seed=26)
+    check_all(t, causal, 0.07, [0, 1], f"d192/dv128 Lq={Lq} Lk={Lk} causal={causal}")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_value_head_dim_grouped_varlen(deterministic):
+    """d192/dv128 with grouped heads (split over tiles: partial dK slots 192
+    wide, dV slots 128 wide) and packed sequences with key offsets of their own."""
+    lq, lk = [1, 128, 200, 513, 0, 300], [300, 1, 200, 129, 77, 256]
+    cu, cuk = inputs.cu_seqlens(lq), inputs.cu_seqlens(lk)
+    g = torch.Generator("cpu").manual_seed(27)
+    Tq, Tk, H, Hkv = int(cu[-1]), int(cuk[-1]), 4, 2
+    t = {"q": torch.randn(Tq, H, 192, generator=g).to(torch.bfloat16),
+         "k": torch.randn(Tk, Hkv, 192, generator=g).to(torch.bfloat16),
+         "v": torch.randn(Tk, Hkv, 128, generator=g).to(torch.bfloat16),
+         "do": torch.randn(Tq, H, 128, generator=g).to(torch.bfloat16)}
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
+    cq, ck = cu.cuda(), cuk.cuda()
+    o, lse = binding.forward(q, k, v, causal=True, scale=0.07, cu_seqlens=cq, cu_seqlens_k=ck)
+    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=True, scale=0.07, cu_seqlens=cq, cu_seqlens_k=ck,
+                                  deterministic=deterministic)
+    binding.check_status()
+    assert dv.shape == (Tk, Hkv, 128)
+    import oracle
+    rq, rk, rv = oracle.bwd(*(to64(t[n]) for n in ("q", "k", "v", "do")), 0.07, True, cu_seqlens=cu.numpy(),
+                            cu_seqlens_k=cuk.numpy())
+    assert_grad_close(to64(dq), rq, "d192/dv128 grouped varlen dQ")
+    assert_grad_close(to64(dk), rk, "d192/dv128 grouped varlen dK")
+    assert_grad_close(to64(dv), rv, "d192/dv128 grouped varlen dV")
+
+
+def test_value_head_dim_deterministic_is_bit_identical():
+    t = inputs.small(B=2, H=4, L=1024, d=192, dv=128, seed=28)
+    ref = run_dense(t, True, 0.07, deterministic=True)
+    for _ in range(3):
+        again = run_dense(t, True, 0.07, deterministic=True)
+        for a, b in zip(ref, again):
+            assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------------ workload shapes
 
 def _rows(L, n, seed, tail=None):
@@ -135,6 +190,11 @@ def test_workload_b4h16l4096(causal, deterministic):
 @pytest.mark.parametrize("d", [64, 128, 192, 256])
 def test_workload_hdsweep(d):
     _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
+
+
+def test_workload_hdsweep_value_head_dim():
+    """B2 H16 L8192, q/k head dim 192, v head dim 128, causal, spiky K."""
+    _workload_check(inputs.HDSWEEP.with_(d=192, dv=128), True, heads=[3])
 
 
 @pytest.mark.parametrize("causal", [False, True])
