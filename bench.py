@@ -69,17 +69,31 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 815.650e6 + 477.293e6,
+        "bytes": 816.805e6 + 476.954e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "5de711aa6492a307a4247d55ae963fb25c4a39ada109f25f41b880198e0dfc44",
+                "f6dbc802a34cccea3c05ee3fe34d6c5584a0d43f633a594767a1aa2f65473b73",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
-                "8a2b249b24ac9f0a63ec3001be461463eebd7488576a7205cc512304c606dfaf",
+                "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "df0d49be08e91a5af1915a88e846ff18290504aaaf7c403e83b57046f345fe3b",
+                "7461566b8f5b9bc1c0b78962afeccfd7da83249e471aeb494d8a93a994faf92f",
+        },
+    },
+    ("b4h16l4096d128", "bwd", True): {
+        "bytes": 1904.177e6 + 973.910e6,
+        "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
+        "sources": {
+            "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
+                "f6dbc802a34cccea3c05ee3fe34d6c5584a0d43f633a594767a1aa2f65473b73",
+            "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
+                "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
+            "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
+                "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
+            "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
+                "7461566b8f5b9bc1c0b78962afeccfd7da83249e471aeb494d8a93a994faf92f",
         },
     },
 }
@@ -249,12 +263,14 @@ def barrier(dist):
 ORACLE_SAMPLE_FLOPS = 3e11
 
 
-def oracle_sample(w, variants, nthreads=None):
-    """fp64 oracle (forward + backward) on one head of batch entry 0 (varlen:
-    of sequence 0) for each variant; when the whole head would exceed the
-    sample budget, on its leading L' x L' block (the first L' queries and keys;
-    for a causal mask exactly the attention of that prefix). Returns
-    (algorithmic flops of the sample, seconds, threads, description)."""
+def oracle_sample(w, variants, nthreads=None, budget=ORACLE_SAMPLE_FLOPS):
+    """fp64 oracle (forward + backward) for each variant on the first heads of
+    batch entry 0 (varlen: of the longest prefill sequence), as many as the
+    sample budget holds; when one whole head would exceed it, on the leading
+    L' x L' block of head 0 (the first L' queries and keys; for a causal mask
+    exactly the attention of that prefix). Each query head is paired with the
+    key/value head it reads. Returns (algorithmic flops of the sample,
+    seconds, threads, description)."""
     import numpy as np
     import oracle
     t = inputs.make(w)
@@ -267,21 +283,26 @@ def oracle_sample(w, variants, nthreads=None):
         same = [b for b in range(w.B) if int(lq[b]) == int(lk[b])]
         s = max(same, key=lambda b: int(lq[b])) if w.lengths_k is not None else 0
         a, c, L = int(cu[s]), int(cuk[s]), int(lq[s])
-        src = {n: t[n][a:a + L, :1].unsqueeze(0) for n in ("q", "do")}
-        src.update({n: t[n][c:c + L, :1].unsqueeze(0) for n in ("k", "v")})
-        where = f"sequence {s}, head 0"
+        full = {n: t[n][a:a + L].unsqueeze(0) for n in ("q", "do")}
+        full.update({n: t[n][c:c + L].unsqueeze(0) for n in ("k", "v")})
+        where = f"sequence {s}"
     else:
         L = w.L
-        src = {n: t[n][:1, :, :1] for n in ("q", "k", "v", "do")}
-        where = "batch 0, head 0"
+        full = {n: t[n][:1] for n in ("q", "k", "v", "do")}
+        where = "batch 0"
 
-    def sample_flops(Lp):
-        sw = w.with_(lengths=None, lengths_k=None, hkv=None, B=1, H=1, L=Lp)
+    def sample_flops(Lp, nh=1):
+        sw = w.with_(lengths=None, lengths_k=None, hkv=None, B=1, H=nh, L=Lp)
         return sum(flops(sw, c, kind) for c in variants for kind in kinds_of(w))
 
     Lp = L
-    while Lp > 128 and sample_flops(Lp) > ORACLE_SAMPLE_FLOPS:
+    while Lp > 128 and sample_flops(Lp) > budget:
         Lp = max(128, (Lp // 2) // 128 * 128)
+    nh = max(1, min(w.H, int(budget // sample_flops(Lp)))) if Lp == L else 1
+    group = w.H // w.H_kv
+    src = {n: full[n][:, :, :nh] for n in ("q", "do")}
+    src.update({n: full[n][:, :, [h // group for h in range(nh)]] for n in ("k", "v")})
+    where += f", heads 0-{nh - 1}" if nh > 1 else ", head 0"
     f64 = {n: x[:, :Lp].float().numpy().astype(np.float64) for n, x in src.items()}
     total_flops, secs = 0, 0.0
     kinds = kinds_of(w)
@@ -291,7 +312,7 @@ def oracle_sample(w, variants, nthreads=None):
         if "bwd" in kinds:
             oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads)
         secs += time.perf_counter() - t0
-    total_flops = sample_flops(Lp)
+    total_flops = sample_flops(Lp, nh)
     what = f"{where}" + (f", leading {Lp}x{Lp} block" if Lp < L else "") + \
         f" of {w.name}, {'+'.join({'fwd': 'forward', 'bwd': 'backward'}[k] for k in kinds_of(w))}, " + \
         f"{'/'.join('causal' if c else 'non-causal' for c in variants)}"
@@ -302,12 +323,14 @@ def run_reference(args, world, rank, dist):
     if rank != 0:
         return 0
     w, variants = WORKLOADS[args.workload]
+    # the whole run stays near a dozen budgets (about two minutes on 16 cores)
+    budget = ORACLE_SAMPLE_FLOPS * min(1.0, 12.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(w, variants)
+        oracle_sample(w, variants, budget=budget)
     fl, secs = 0, 0.0
     threads, sample = None, ""
     for _ in range(args.steps):
-        f, sec, threads, sample = oracle_sample(w, variants)
+        f, sec, threads, sample = oracle_sample(w, variants, budget=budget)
         fl += f
         secs += sec
     value = fl / secs / 1e12
