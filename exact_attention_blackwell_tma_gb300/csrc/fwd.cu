@@ -111,7 +111,9 @@ struct FwdTile {
     int lq, lk;        // sequence lengths
     int q_row0;        // packed row of the first query row of the tile
     int k_row0;        // packed row of the first key of the sequence
-    int n_kv;          // K/V blocks to visit (0: every row is fully masked)
+    int n_kv;          // K/V blocks to visit (0: every row is fully masked); Q tile 1 visits all
+    int n_kv0;         // K/V blocks Q tile 0 visits: n_kv, or one fewer (causal: the block past
+                       // its diagonal is fully masked for it), or 0 (none of its rows sees a key)
 };
 
 __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
@@ -134,12 +136,15 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
         f.q_row0 = ti.b * g.Lq + ti.m * kRowsPerTile;
         f.k_row0 = ti.b * g.Lk;
     }
-    int keys = f.lk;
-    if (g.causal) {
-        int row_last = min(ti.m * kRowsPerTile + kRowsPerTile - 1, f.lq - 1);
-        keys = min(f.lk, row_last + 1 + f.lk - f.lq);   // bottom-right aligned mask
+    int keys = f.lk, keys0 = f.lk;
+    if (g.causal) {   // bottom-right aligned mask: row r sees keys below r + 1 + lk - lq
+        const int row_last = min(ti.m * kRowsPerTile + kRowsPerTile - 1, f.lq - 1);
+        const int row_last0 = min(ti.m * kRowsPerTile + kBM - 1, f.lq - 1);
+        keys = min(f.lk, row_last + 1 + f.lk - f.lq);
+        keys0 = min(f.lk, row_last0 + 1 + f.lk - f.lq);
     }
     f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
+    f.n_kv0 = keys0 > 0 ? (keys0 + kBN - 1) / kBN : 0;
     return f;
 }
 
@@ -280,6 +285,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
             const FwdTile f = fwd_tile(t, p, vm, varlen);
             if (f.n_kv == 0) continue;
+            const int n0 = f.n_kv0;   // Q tile 0 stops after its own last visible block
             ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
             if (!ok) break;
             uint32_t slot_k = kv_cnt % S;
@@ -288,8 +294,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             ++kv_cnt;
             tc_fence_after_sync();
             if (lane == 0) {
-                issue_s(0, slot_k);
-                tc_commit(bar(Lay::kSFull + 0));
+                if (n0 > 0) {
+                    issue_s(0, slot_k);
+                    tc_commit(bar(Lay::kSFull + 0));
+                }
                 issue_s(1, slot_k);
                 tc_commit(bar(Lay::kSFull + 1));
                 tc_commit(bar(Lay::kKVEmpty + slot_k));
@@ -302,25 +310,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (!ok) break;
                 ++kv_cnt;
                 const bool more = j + 1 < f.n_kv;
-                // tile 0: PV for block j, then S for block j+1
-                ok = warp_wait(bar(Lay::kPFull + 0), pc0 & 1u, w, lane);
-                if (!ok) break;
-                ++pc0;
-                tc_fence_after_sync();
-                if (lane == 0) issue_pv(0, slot_v, j > 0);
-                __syncwarp();
-                if (more) {
+                // tile 0: PV for block j, then S for block j+1 (while it sees them)
+                if (j < n0) {
+                    ok = warp_wait(bar(Lay::kPFull + 0), pc0 & 1u, w, lane);
+                    if (!ok) break;
+                    ++pc0;
+                    tc_fence_after_sync();
+                    if (lane == 0) issue_pv(0, slot_v, j > 0);
+                    __syncwarp();
+                }
+                if (more) {   // K of block j+1, for tile 1 (and tile 0 if it sees it)
                     slot_k = kv_cnt % S;
                     ok = warp_wait(bar(Lay::kKVFull + slot_k), (kv_cnt / S) & 1u, w, lane);
                     if (!ok) break;
                     ++kv_cnt;
                     tc_fence_after_sync();
-                    if (lane == 0) {
+                }
+                if (lane == 0) {
+                    if (j + 1 < n0) {
                         issue_s(0, slot_k);
                         tc_commit(bar(Lay::kSFull + 0));
+                    } else if (j + 1 == n0) {
+                        tc_commit(bar(Lay::kOFull + 0));   // after PV(0, j): tile 0 is done
                     }
-                } else if (lane == 0) {
-                    tc_commit(bar(Lay::kOFull + 0));
                 }
                 __syncwarp();
                 // tile 1
@@ -372,7 +384,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * HD;
             float* lptr = varlen ? p.lse + (long)f.h * g.Lq + prow
                                  : p.lse + ((long)f.b * g.H + f.h) * g.Lq + r;
-            if (f.n_kv == 0) {
+            const int nkv = tq ? f.n_kv : f.n_kv0;   // blocks this Q tile visits
+            if (nkv == 0) {
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(optr);
 #pragma unroll
@@ -383,7 +396,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             const int col_limit = g.causal ? min(f.lk, r + 1 + f.lk - f.lq) : f.lk;
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < f.n_kv; ++j) {
+            for (int j = 0; j < nkv; ++j) {
                 ok = warp_wait(bar(Lay::kSFull + tq), sc & 1u, w, lane);
                 if (!ok) break;
                 ++sc;
@@ -428,7 +441,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float l0 = 0.f, l1 = 0.f;
                 if constexpr (kPolyEvery > 0) {
-                    if (j + 1 < f.n_kv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
+                    if (j + 1 < nkv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
                     else exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
                 } else {
                     exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // one copy of the loop in the code
