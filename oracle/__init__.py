@@ -58,11 +58,13 @@ def bind(path: str):
     lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int,
                                _ip, _ip, _ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_bwd.restype = ctypes.c_int
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int,
                                _ip, _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
     return lib
 
@@ -136,12 +138,16 @@ def _dv(v, k):
     return v.shape[-1]
 
 
-def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None, cu_seqlens_k=None):
+def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None, cu_seqlens_k=None,
+        window_left: int = -1, window_right: int = -1):
     """O and LSE (natural log) by the definition. Returns (o, lse) as float64.
 
     q and k share a head dim; v (and O) may have another one; k and v may have
     fewer heads (grouped heads). ``cu_seqlens_k``: key offsets of a varlen
-    batch whose key lengths differ from its query lengths.
+    batch whose key lengths differ from its query lengths. ``window_left`` /
+    ``window_right``: query i sees keys i + delta - window_left ..
+    i + delta + window_right (delta = Lk - Lq; -1: no bound; causal sets the
+    right bound to 0).
     ``rows``: optional query-row indices (per sequence) to evaluate; the other
     rows of the returned arrays are NaN.
     """
@@ -156,6 +162,7 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
     r = _i32(rows)
     rc = _load().oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
                             B, H, Hkv, Lq, Lk, d, dv, float(scale), int(bool(causal)),
+                            int(window_left), int(window_right),
                             _ptr(cu, _ip), _ptr(cuk, _ip), _ptr(r, _ip), 0 if r is None else len(r),
                             nthreads or default_threads())
     if rc != 0:
@@ -164,7 +171,7 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
 
 
 def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, krows=None,
-        nthreads=None, cu_seqlens_k=None):
+        nthreads=None, cu_seqlens_k=None, window_left: int = -1, window_right: int = -1):
     """dQ, dK, dV of L = sum(O * dO) by the definition. Returns float64 arrays.
 
     ``qrows`` / ``krows``: optional row subsets for dQ / (dK, dV); other rows NaN.
@@ -184,7 +191,8 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     qr, kr = _i32(qrows), _i32(krows)
     rc = _load().oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp),
                             _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
-                            B, H, Hkv, Lq, Lk, d, dvd, float(scale), int(bool(causal)), _ptr(cu, _ip),
+                            B, H, Hkv, Lq, Lk, d, dvd, float(scale), int(bool(causal)),
+                            int(window_left), int(window_right), _ptr(cu, _ip),
                             _ptr(cuk, _ip), _ptr(qr, _ip), 0 if qr is None else len(qr),
                             _ptr(kr, _ip), 0 if kr is None else len(kr),
                             nthreads or default_threads())

@@ -13,6 +13,13 @@
  *
  *     allowed(i, j) = j < Lk                       (non-causal)
  *                   = j <= i + (Lk - Lq)           (causal, bottom-right aligned)
+ *   and with a local window (window_left wl, window_right wr; -1: no bound;
+ *   causal means wr = 0), with delta = Lk - Lq:
+ *     allowed(i, j) = 0 <= j < Lk,  j >= i + delta - wl (wl >= 0),
+ *                     j <= i + delta + wr (wr >= 0)
+ *   (a band around the bottom-right diagonal: the FlashAttention-4 paper's
+ *   Section 4 lists masking strategies among the primitives its kernels
+ *   compose; the band is the plainest one beyond the causal mask).
  *     LSE_i = m_i + ln sum_j exp(s_ij - m_i),  m_i = max_j s_ij   (allowed j)
  *     P_ij  = exp(s_ij - LSE_i)
  *     O_i   = sum_j P_ij v_j
@@ -37,7 +44,8 @@
  *     dK_j  = scale * sum_i dS_ij q_i
  *     dV_j  = sum_i P_ij dO_i
  *
- * A row with no allowed key (only possible when causal and Lq > Lk) has
+ * A row with no allowed key (causal with Lq > Lk, or a window that holds no
+ * key of the row) has
  * O_i = 0, LSE_i = -inf, and contributes nothing to any gradient.
  *
  * Every output element is evaluated directly from its formula, with a single
@@ -73,7 +81,8 @@
 typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv;
-    int B, H, Hkv, Lq, Lk, d, dvh, causal;   /* Hkv: heads of k, v; dvh: head dim of v, o, dout, dv */
+    int B, H, Hkv, Lq, Lk, d, dvh;   /* Hkv: heads of k, v; dvh: head dim of v, o, dout, dv */
+    int wl, wr;                      /* window bounds (-1: none); causal is wr = 0 */
     double scale;
     const int *cu;          /* NULL for dense */
     const int *cuk;         /* key offsets (varlen): cu_seqlens_k, or cu */
@@ -127,8 +136,10 @@ static long stat_off(const job_t *J, int b, int h, int i) {
 
 static int allowed(const job_t *J, int b, int i, int j) {
     int lq = seq_lq(J, b), lk = seq_lk(J, b);
+    int delta = lk - lq;
     if (j < 0 || j >= lk) return 0;
-    if (J->causal) return j <= i + (lk - lq);
+    if (J->wr >= 0 && j > i + delta + J->wr) return 0;
+    if (J->wl >= 0 && j < i + delta - J->wl) return 0;
     return 1;
 }
 
@@ -295,8 +306,10 @@ static int check_offsets(int B, const int *cu) {
     return 0;
 }
 
-static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu, const int *cuk) {
+static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu, const int *cuk,
+                      int wl, int wr) {
     if (B < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || dv < 1) return -1;
+    if (wl < -1 || wr < -1) return -1;
     if (!cu && (Lq < 0 || Lk < 0)) return -1;
     if (cuk && !cu) return -1;
     if (cu && check_offsets(B, cu)) return -1;
@@ -306,20 +319,23 @@ static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, cons
 
 static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
                      int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
-                     const int *cu, const int *cuk) {
+                     int wl, int wr, const int *cu, const int *cuk) {
     memset(J, 0, sizeof(*J));
     J->q = q; J->k = k; J->v = v; J->dout = dout;
     J->B = B; J->H = H; J->Hkv = Hkv; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
-    J->scale = scale; J->causal = causal != 0; J->cu = cu; J->cuk = cuk ? cuk : cu;
+    J->scale = scale; J->wl = wl; J->wr = causal ? 0 : wr;
+    J->cu = cu; J->cuk = cuk ? cuk : cu;
 }
 
 int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
+               int window_left, int window_right,
                const int *cu_seqlens, const int *cu_seqlens_k, const int *rows, int nrows, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens, cu_seqlens_k)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens, cu_seqlens_k, window_left, window_right)) return -1;
     job_t J;
-    init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, cu_seqlens_k);
+    init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, window_left, window_right, cu_seqlens,
+             cu_seqlens_k);
     J.o = o; J.lse = lse;
     long n;
     int *items = make_items(&J, rows, nrows, 0, &n);
@@ -332,13 +348,15 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
 int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
                double *dq, double *dk, double *dv,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dvd, double scale, int causal,
+               int window_left, int window_right,
                const int *cu_seqlens, const int *cu_seqlens_k, const int *qrows, int nqrows,
                const int *krows, int nkrows, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens, cu_seqlens_k)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens, cu_seqlens_k, window_left, window_right)) return -1;
     if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
     job_t J;
-    init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, cu_seqlens, cu_seqlens_k);
+    init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, window_left, window_right, cu_seqlens,
+             cu_seqlens_k);
     J.dq = dq; J.dk = dk; J.dv = dv;
 
     /* longest sequence, the range of relative row indices */
@@ -356,8 +374,9 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
     }
 
     /* Query rows whose LSE_i and D_i are needed: the requested dQ rows, plus
-       every row that can see a requested key row (for a dense causal problem
-       key j is seen by rows i >= j - (Lk - Lq); otherwise by all rows). */
+       every row that can see a requested key row (for a dense problem with a
+       right bound wr, key j is seen by rows i >= j - (Lk - Lq) - wr only;
+       otherwise by all rows). */
     int want_dq = !(qrows && nqrows == 0);
     int want_dkv = !(krows && nkrows == 0);
     if (want_dq) {
@@ -366,10 +385,10 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
     }
     if (want_dkv) {
         int i0 = 0;
-        if (krows && causal && !cu_seqlens) {
+        if (krows && J.wr >= 0 && !cu_seqlens) {
             int jmin = Lk;
             for (int t = 0; t < nkrows; t++) if (krows[t] >= 0 && krows[t] < jmin) jmin = krows[t];
-            i0 = jmin - (Lk - Lq);
+            i0 = jmin - (Lk - Lq) - J.wr;
             if (i0 < 0) i0 = 0;
         }
         for (int i = i0; i < lmax; i++) need[i] = 1;

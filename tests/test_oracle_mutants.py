@@ -20,8 +20,14 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = [
     ("drop scale in scores", "return J->scale * dot(qi, kj, J->d);", "return dot(qi, kj, J->d);"),
-    ("strict causal boundary", "return j <= i + (lk - lq);", "return j < i + (lk - lq);"),
-    ("top-left causal alignment", "return j <= i + (lk - lq);", "return j <= i;"),
+    ("strict causal boundary", "if (J->wr >= 0 && j > i + delta + J->wr) return 0;",
+     "if (J->wr >= 0 && j >= i + delta + J->wr) return 0;"),
+    ("top-left causal alignment", "int delta = lk - lq;", "int delta = 0;"),
+    ("window left bound off by one", "if (J->wl >= 0 && j < i + delta - J->wl) return 0;",
+     "if (J->wl >= 0 && j <= i + delta - J->wl) return 0;"),
+    ("window left bound on the wrong side", "if (J->wl >= 0 && j < i + delta - J->wl) return 0;",
+     "if (J->wl >= 0 && j < i + delta + J->wl) return 0;"),
+    ("causal ignored when a right window is given", "J->wr = causal ? 0 : wr;", "J->wr = wr >= 0 ? wr : (causal ? 0 : wr);"),
     ("LSE without the max", "return m + log(sum);", "return log(sum);"),
     ("base-2 exponential", "sum += exp(score(J, b, h, i, j) - m);", "sum += exp2(score(J, b, h, i, j) - m);"),
     ("O sums keys instead of values", "const double *vj = J->v + row_off_kv(J, b, j, kvh(J, h), J->Lk);\n        for (int c = 0; c < dv; c++) out[c]",
@@ -68,6 +74,10 @@ BATTERY = [
     (pins.test_fwd_grouped_heads_match_textbook, (1, 6, 3, 7, 9, 3, True)),
     (pins.test_bwd_finite_differences_grouped_heads, (False,)),
     (pins.test_varlen_separate_key_lengths_is_per_sequence_attention, ()),
+    (pins.test_window_matches_textbook_band, (9, 4, 3, 1)),
+    (pins.test_window_matches_textbook_band, (7, 7, 2, 0)),
+    (pins.test_zero_window_returns_the_diagonal_value, ()),
+    (pins.test_bwd_finite_differences_window, (2, 1)),
     (pins.test_bwd_finite_differences_varlen_separate_keys, (True,)),
 ]
 

@@ -281,6 +281,69 @@ def test_varlen_separate_key_lengths_is_per_sequence_attention():
             assert np.isneginf(lse[:, a:a + L][~fin]).all()
 
 
+def textbook_window(q, k, v, scale, wl, wr):
+    """softmax over the band i + delta - wl <= j <= i + delta + wr (delta = Lk - Lq,
+    -1: no bound), written with scipy on a dense mask, tiny sizes."""
+    B, Lq, H, d = q.shape
+    Lk = k.shape[1]
+    s = np.einsum("bihc,bjhc->bhij", q, k) * scale
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    keep = np.ones((Lq, Lk), dtype=bool)
+    if wr >= 0:
+        keep &= j <= i + (Lk - Lq) + wr
+    if wl >= 0:
+        keep &= j >= i + (Lk - Lq) - wl
+    s = np.where(keep, s, -np.inf)
+    with np.errstate(invalid="ignore"):
+        lse = logsumexp(s, axis=-1)
+        p = softmax(s, axis=-1)
+    p = np.nan_to_num(p, nan=0.0)
+    return np.einsum("bhij,bjhc->bihc", p, v), lse
+
+
+@pytest.mark.parametrize("wl,wr", [(0, 0), (2, 0), (3, 1), (-1, 2), (4, -1), (1, 5)])
+@pytest.mark.parametrize("Lq,Lk", [(7, 7), (5, 9), (9, 4)])
+def test_window_matches_textbook_band(Lq, Lk, wl, wr):
+    """A local window is softmax over a band around the bottom-right diagonal;
+    rows whose band holds no key get O = 0 and LSE = -inf."""
+    q, k, v = rnd((2, Lq, 2, 3), 80), rnd((2, Lk, 2, 3), 81), rnd((2, Lk, 2, 3), 82)
+    o, lse = oracle.fwd(q, k, v, 0.7, False, window_left=wl, window_right=wr)
+    o_ref, lse_ref = textbook_window(q, k, v, 0.7, wl, wr)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], atol=1e-12)
+    assert np.isneginf(lse[~fin]).all()
+    # causal sets the right bound to 0 whatever window_right says
+    o_c, _ = oracle.fwd(q, k, v, 0.7, True, window_left=wl, window_right=wr)
+    o_c_ref, _ = textbook_window(q, k, v, 0.7, wl, 0)
+    np.testing.assert_allclose(o_c, o_c_ref, atol=1e-12)
+
+
+def test_zero_window_returns_the_diagonal_value():
+    """window_left = window_right = 0: row i sees only key i + Lk - Lq, so
+    O_i = v_{i + Lk - Lq} and LSE_i = its score; rows with no such key get 0."""
+    Lq, Lk = 6, 4
+    q, k, v = rnd((1, Lq, 1, 5), 83), rnd((1, Lk, 1, 5), 84), rnd((1, Lk, 1, 5), 85)
+    o, lse = oracle.fwd(q, k, v, 0.9, False, window_left=0, window_right=0)
+    for i in range(Lq):
+        j = i + Lk - Lq
+        if 0 <= j < Lk:
+            np.testing.assert_allclose(o[0, i, 0], v[0, j, 0], atol=1e-14)
+            np.testing.assert_allclose(lse[0, 0, i], 0.9 * q[0, i, 0] @ k[0, j, 0], atol=1e-13)
+        else:
+            assert (o[0, i, 0] == 0).all() and np.isneginf(lse[0, 0, i])
+
+
+def test_window_wider_than_the_sequence_is_no_window():
+    q, k, v = rnd((1, 8, 2, 4), 86), rnd((1, 8, 2, 4), 87), rnd((1, 8, 2, 4), 88)
+    for causal in (False, True):
+        a = oracle.fwd(q, k, v, 0.5, causal)
+        b = oracle.fwd(q, k, v, 0.5, causal, window_left=8, window_right=8)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
 def test_row_subset_matches_full():
     q, k, v = rnd((2, 10, 2, 4), 36), rnd((2, 10, 2, 4), 37), rnd((2, 10, 2, 4), 38)
     full_o, full_l = oracle.fwd(q, k, v, 0.5, True)
@@ -375,6 +438,27 @@ def test_bwd_finite_differences_varlen_separate_keys(causal):
             plus[which][idx] += 1e-6
             minus[which][idx] -= 1e-6
             g[idx] = (loss2(*plus) - loss2(*minus)) / 2e-6
+        assert np.abs(got - g).max() < 1e-7
+
+
+@pytest.mark.parametrize("wl,wr", [(1, 0), (2, 1), (0, -1)])
+def test_bwd_finite_differences_window(wl, wr):
+    q, k, v, do = rnd((1, 6, 2, 3), 97), rnd((1, 5, 2, 3), 98), rnd((1, 5, 2, 3), 99), rnd((1, 6, 2, 3), 100)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.8, False, window_left=wl, window_right=wr)
+
+    def loss_w(q_, k_, v_):
+        o, _ = oracle.fwd(q_, k_, v_, 0.8, False, window_left=wl, window_right=wr)
+        return float(np.sum(o * do))
+
+    for got, which in ((dq, 0), (dk, 1), (dv, 2)):
+        arrs = [q, k, v]
+        g = np.zeros_like(arrs[which])
+        for idx in np.ndindex(g.shape):
+            plus = [a.copy() for a in arrs]
+            minus = [a.copy() for a in arrs]
+            plus[which][idx] += 1e-6
+            minus[which][idx] -= 1e-6
+            g[idx] = (loss_w(*plus) - loss_w(*minus)) / 2e-6
         assert np.abs(got - g).max() < 1e-7
 
 
