@@ -47,6 +47,8 @@ WORKLOADS = {
     "b2h16l8192d256": (inputs.HDSWEEP.with_(d=256), (True,)),
     # q/k head dim 192 with v head dim 128 (attn_fwd_ex / attn_bwd_ex)
     "b2h16l8192dqk192dv128": (inputs.HDSWEEP.with_(d=192, dv=128), (True,)),
+    # causal with a local window of 4096 keys (attn_fwd_ex / attn_bwd_ex window bounds)
+    "b2h16l8192d128_window4096": (inputs.HDSWEEP.with_(name="b2h16l8192d128_window4096", window=(4096, 0)), (True,)),
     # grouped heads: 16 query heads over 2 key/value heads
     "b2h16kv2l8192d128": (inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
@@ -157,7 +159,8 @@ class Problem:
                 raise binding.AttnError(rc, binding.last_error())
             return
         rc = binding.attn_fwd_ex(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
-                                 self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.cu, None)
+                                 self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.w.window[0],
+                                 self.w.window[1], self.cu, None)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -171,7 +174,7 @@ class Problem:
             return
         rc = binding.attn_bwd_ex(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
                                  self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.d_v, self.w.scale, causal,
-                                 self.cu, None, 0, self.ws, self.ws.numel())
+                                 self.w.window[0], self.w.window[1], self.cu, None, 0, self.ws, self.ws.numel())
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -308,9 +311,11 @@ def oracle_sample(w, variants, nthreads=None, budget=ORACLE_SAMPLE_FLOPS):
     kinds = kinds_of(w)
     for causal in variants:
         t0 = time.perf_counter()
-        oracle.fwd(f64["q"], f64["k"], f64["v"], w.scale, causal, nthreads=nthreads)
+        oracle.fwd(f64["q"], f64["k"], f64["v"], w.scale, causal, nthreads=nthreads, window_left=w.window[0],
+                   window_right=w.window[1])
         if "bwd" in kinds:
-            oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads)
+            oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads,
+                       window_left=w.window[0], window_right=w.window[1])
         secs += time.perf_counter() - t0
     total_flops = sample_flops(Lp, nh)
     what = f"{where}" + (f", leading {Lp}x{Lp} block" if Lp < L else "") + \
@@ -449,7 +454,7 @@ def run_ours(args, world, rank, local, dist):
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": args.workload, "B": w.B, "H": w.H, "H_kv": w.H_kv, "L": w.L, "d": w.d,
-                           "d_v": w.d_v,
+                           "d_v": w.d_v, "window": list(w.window),
                            "calls": list(kinds),
                            "variants": ["causal" if c else "non-causal" for c in variants],
                            "flops_per_step": step_flops,

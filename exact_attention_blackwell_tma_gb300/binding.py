@@ -38,12 +38,13 @@ def _declare(lib):
     lib.attn_fwd_gqa.restype = c_int
     lib.attn_fwd_gqa.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_fwd_ex.restype = c_int
-    lib.attn_fwd_ex.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
+    lib.attn_fwd_ex.argtypes = ([c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_void_p,
+                                                                  c_void_p])
     lib.attn_bwd_ex_workspace_size.restype = c_size_t
     lib.attn_bwd_ex_workspace_size.argtypes = [c_int] * 9
     lib.attn_bwd_ex.restype = c_int
-    lib.attn_bwd_ex.argtypes = ([c_void_p] * 9 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_int, c_void_p,
-                                                                  c_size_t, c_void_p])
+    lib.attn_bwd_ex.argtypes = ([c_void_p] * 9 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_void_p,
+                                                                  c_int, c_void_p, c_size_t, c_void_p])
     lib.attn_fwd_varlen.restype = c_int
     lib.attn_fwd_varlen.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
@@ -152,21 +153,23 @@ def attn_fwd_varlen(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu
                                   int(causal), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
 
 
-def attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q=None, cu_seqlens_k=None,
-                stream=None) -> int:
+def attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left=-1, window_right=-1,
+                cu_seqlens_q=None, cu_seqlens_k=None, stream=None) -> int:
     return load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Lq, Lk, d, d_v, scale,
-                              int(causal), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
+                              int(causal), int(window_left), int(window_right), _ptr(cu_seqlens_q),
+                              _ptr(cu_seqlens_k), _stream(stream))
 
 
 def attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic) -> int:
     return load().attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, int(causal), int(deterministic))
 
 
-def attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
-                cu_seqlens_k, deterministic, workspace, ws_bytes, stream=None) -> int:
+def attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left,
+                window_right, cu_seqlens_q, cu_seqlens_k, deterministic, workspace, ws_bytes, stream=None) -> int:
     return load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                              _ptr(dv), B, H, Hkv, Lq, Lk, d, d_v, scale, int(causal), _ptr(cu_seqlens_q),
-                              _ptr(cu_seqlens_k), int(deterministic), _ptr(workspace), ws_bytes, _stream(stream))
+                              _ptr(dv), B, H, Hkv, Lq, Lk, d, d_v, scale, int(causal), int(window_left),
+                              int(window_right), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(deterministic),
+                              _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
@@ -236,11 +239,12 @@ def _check_tensors(*ts):
 
 
 def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
-            stream=None, cu_seqlens_k=None):
+            stream=None, cu_seqlens_k=None, window=(-1, -1)):
     """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens).
     v (and O) may have a head dim of their own (d = 192 with 128); k and v may
     have fewer heads than q (grouped heads: query head h reads h // (H // Hkv)).
-    cu_seqlens_k: key offsets of a varlen batch whose key lengths differ."""
+    cu_seqlens_k: key offsets of a varlen batch whose key lengths differ.
+    window: (left, right) bounds of a local window, -1 for an open side."""
     _check_tensors(q, k, v, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     dv = v.shape[-1]
@@ -249,7 +253,10 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
         out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
-    if cu_seqlens_k is not None:
+    if tuple(window) != (-1, -1):
+        _check(attn_fwd_ex(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, window[0], window[1],
+                           cu_seqlens, cu_seqlens_k, stream))
+    elif cu_seqlens_k is not None:
         _check(attn_fwd_varlen(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens,
                                cu_seqlens_k, stream))
     elif Hkv != H:
@@ -263,10 +270,10 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
 
 def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu_seqlens=None,
              deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None,
-             cu_seqlens_k=None):
+             cu_seqlens_k=None, window=(-1, -1)):
     """dQ, dK, dV (bf16) for the loss sum(O * dO); k and v may have fewer heads
     than q (grouped heads), dK and dV then have theirs; v (dO, dV) may have a head
-    dim of its own (d = 192 with 128). cu_seqlens_k as in forward()."""
+    dim of its own (d = 192 with 128). cu_seqlens_k and window as in forward()."""
     _check_tensors(q, k, v, o, lse, dout, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -278,9 +285,9 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = workspace.numel() * workspace.element_size()
-    if d_v != d:
-        _check(attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens,
-                           cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
+    if d_v != d or tuple(window) != (-1, -1):
+        _check(attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window[0],
+                           window[1], cu_seqlens, cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
     elif cu_seqlens_k is not None:
         _check(attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
                                cu_seqlens_k, deterministic, workspace, ws_bytes, stream))

@@ -151,6 +151,18 @@ int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu
     return ATTN_OK;
 }
 
+int check_window(int wl, int wr) {
+    if (wl < -1 || wr < -1) return fail(ATTN_ERR_ARG, "window bounds must be >= 0, or -1 for none (%d, %d)", wl, wr);
+    return ATTN_OK;
+}
+
+// causal != 0 sets the right bound to 0 (whatever window_right says)
+void set_mask(Geometry* g, int causal, int wl, int wr) {
+    g->win_left = wl;
+    g->win_right = causal ? 0 : wr;
+    g->causal = g->win_right >= 0 ? 1 : 0;
+}
+
 int check_heads(int H, int Hkv) {
     if (Hkv < 1 || Hkv > H || H % Hkv != 0)
         return fail(ATTN_ERR_ARG, "key/value heads %d must divide the query heads %d", Hkv, H);
@@ -173,9 +185,11 @@ namespace {
 // The forward behind every entry point: dense (cu_seqlens null), varlen with
 // one offset array (cu_seqlens_k == cu_seqlens) or with key offsets of their own.
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Lq,
-              int Lk, int d, int dv, float scale, int causal, const int* cu_seqlens, const int* cu_seqlens_k,
-              cudaStream_t stream) {
+              int Lk, int d, int dv, float scale, int causal, int window_left, int window_right,
+              const int* cu_seqlens, const int* cu_seqlens_k, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
+    if (rc) return rc;
+    rc = check_window(window_left, window_right);
     if (rc) return rc;
     rc = check_heads(H, Hkv);
     if (rc) return rc;
@@ -199,7 +213,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
     p.g.cu_seqlens_k = cu_seqlens ? cu_seqlens_k : nullptr;
-    p.g.causal = causal ? 1 : 0;
+    set_mask(&p.g, causal, window_left, window_right);
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
@@ -234,23 +248,25 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                             int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
                             const int* cu_seqlens, cudaStream_t stream) {
-    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens, cu_seqlens, stream);
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, -1, -1, cu_seqlens, cu_seqlens,
+                     stream);
 }
 
 extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
-                           int Lq, int Lk, int d, int d_v, float scale, int causal, const int* cu_seqlens_q,
-                           const int* cu_seqlens_k, cudaStream_t stream) {
+                           int Lq, int Lk, int d, int d_v, float scale, int causal, int window_left,
+                           int window_right, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                           cudaStream_t stream) {
     if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_fwd_ex: key offsets without query offsets");
-    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
-                     cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, stream);
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left, window_right,
+                     cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, stream);
 }
 
 extern "C" int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
                                const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream) {
     if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_fwd_varlen: null offsets");
-    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu_seqlens_q, cu_seqlens_k,
-                     stream);
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, -1, -1, cu_seqlens_q,
+                     cu_seqlens_k, stream);
 }
 
 extern "C" int attn_fwd_hdim(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -315,9 +331,11 @@ namespace {
 // The backward behind every entry point (cu_seqlens_k as in fwd_entry).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
               void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale,
-              int causal, const int* cu_seqlens, const int* cu_seqlens_k, int deterministic, void* workspace,
-              size_t ws_bytes, cudaStream_t stream) {
+              int causal, int window_left, int window_right, const int* cu_seqlens, const int* cu_seqlens_k,
+              int deterministic, void* workspace, size_t ws_bytes, cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
+    if (rc) return rc;
+    rc = check_window(window_left, window_right);
     if (rc) return rc;
     rc = check_heads(H, Hkv);
     if (rc) return rc;
@@ -352,7 +370,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.g.group = H / Hkv;
     p.g.cu_seqlens = cu_seqlens;
     p.g.cu_seqlens_k = cu_seqlens ? cu_seqlens_k : nullptr;
-    p.g.causal = causal ? 1 : 0;
+    set_mask(&p.g, causal, window_left, window_right);
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
     p.o = static_cast<const __nv_bfloat16*>(o);
@@ -398,18 +416,19 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
                             const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
                             int d, float scale, int causal, const int* cu_seqlens, int deterministic,
                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, scale, causal, cu_seqlens,
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, scale, causal, -1, -1, cu_seqlens,
                      cu_seqlens, deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
-                           int d, int d_v, float scale, int causal, const int* cu_seqlens_q,
-                           const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
-                           cudaStream_t stream) {
+                           int d, int d_v, float scale, int causal, int window_left, int window_right,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
     if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_bwd_ex: key offsets without query offsets");
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, cu_seqlens_q,
-                     cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, deterministic, workspace, ws_bytes, stream);
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left,
+                     window_right, cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, deterministic,
+                     workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -418,8 +437,8 @@ extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, cons
                                const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
                                cudaStream_t stream) {
     if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_bwd_varlen: null offsets");
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, d, scale, causal, cu_seqlens_q,
-                     cu_seqlens_k, deterministic, workspace, ws_bytes, stream);
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, d, scale, causal, -1, -1,
+                     cu_seqlens_q, cu_seqlens_k, deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

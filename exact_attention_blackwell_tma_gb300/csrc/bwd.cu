@@ -20,6 +20,7 @@
 //   bwd_convert  dQ = scale * accumulator -> bf16.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "mask.cuh"
 #include "sched.cuh"
 
 namespace attn {
@@ -105,12 +106,13 @@ struct QWalk {
 };
 __device__ __forceinline__ QWalk qwalk(const BwdTile& f) { return QWalk{f.hq0, f.m_begin}; }
 
+
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // kGQA: grouped heads (the kernels for one query head per key/value head are
 // instantiated without the group walk and the split, which keeps their code
 // and registers as small as before grouped heads existed)
-template <bool kGQA>
+template <bool kGQA, bool kBand>
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
     // the split tiles of one key block are neighbours in the walk, so they run
@@ -138,14 +140,18 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         f.q_row0 = ti.b * g.Lq;
         f.k_row0 = ti.b * g.Lk;
     }
-    f.m_end = (f.lq + kBM - 1) / kBM;
-    f.m_begin = 0;
-    if (g.causal) {
-        // query i sees key j iff j <= i + (lk - lq): the first query block that
-        // sees the block's first key holds row n*kBN - (lk - lq)
-        f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
+    // the query blocks whose rows see some key of this block (the mask band;
+    // none: the tile writes zero dK/dV rows). No mask or the causal one: all
+    // blocks, or those from the one holding row n*kBN - (lk - lq) on.
+    if constexpr (kBand) {
+        band_query_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), f.n * kBN, f.n * kBN + kBN - 1, kBM,
+                          &f.m_begin, &f.m_end);
+    } else {
+        f.m_end = (f.lq + kBM - 1) / kBM;
+        f.m_begin = 0;
+        if (g.causal) f.m_begin = max(0, floor_div(f.n * kBN - (f.lk - f.lq), kBM));
+        if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
     }
-    if (f.n * kBN >= f.lk) f.m_end = f.m_begin;   // (not produced by the walk; kept for safety)
     if constexpr (kGQA) {
         const int per = g.group / p.split;
         f.s = sp;
@@ -248,8 +254,12 @@ __global__ void bwd_convert(const float* __restrict__ acc, __nv_bfloat16* __rest
 
 // ----------------------------------------------------------------------------
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
-// other path's code out of each kernel); kGQA: grouped heads (bwd_tile)
-template <int HD, bool kDet, bool kGQA>
+// other path's code out of each kernel); kGQA: grouped heads (bwd_tile);
+// kBand: the mask is a local window other than the plain causal mask (a
+// left bound, or a right bound past the diagonal); the kernels for no mask
+// and the causal mask keep their closed forms (a key's query rows run from
+// its diagonal, or from 0, to the sequence's end)
+template <int HD, bool kDet, bool kGQA, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -322,7 +332,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -427,7 +437,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
             if (!ok) break;
@@ -534,7 +544,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
@@ -568,8 +578,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 continue;
             }
-            // query q (inside the sequence) is allowed for this key iff q_lo <= q < lq
-            const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+            // query q is allowed for this key iff q_lo <= q < q_hi (the mask band)
+            int q_lo, q_hi;
+            if constexpr (kBand) {
+                const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+                q_lo = key_ok ? band_query_lo(mb, key) : 0;
+                q_hi = key_ok ? band_query_hi(mb, key) : 0;   // (key_ok false: lo = 64 below)
+            } else {
+                q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+                q_hi = f.lq;
+            }
             QWalk qw = qwalk(f);
             for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
@@ -593,7 +611,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const float* nlse2 = stats + st * 256 + wg * 64;
                 const float* ndd = stats + st * 256 + 128 + wg * 64;
                 const int q0 = m * kBM + wg * 64;
-                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= q_hi;
                 const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
@@ -604,7 +622,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     pv[c + 1] = ex2_mufu(x1);
                 }
                 if (!full) {   // diagonal or ragged block: keep query columns [lo, hi) only
-                    const int lo = key_ok ? q_lo - q0 : 64, hi = f.lq - q0;
+                    const int lo = key_ok ? q_lo - q0 : 64, hi = q_hi - q0;
 #pragma unroll
                     for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
                 }
@@ -703,7 +721,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA>(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
             QWalk qw = qwalk(f);
             for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
@@ -718,13 +736,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 int* sem = nullptr;
                 if constexpr (kDet) {
                     // dQ tile (b, h, m) takes its key blocks' contributions in ascending
-                    // block order: block n waits until n blocks have added theirs. Every
-                    // block below n also sees query block m (causal or not).
+                    // block order. The key blocks that see query block m form one range
+                    // n_lo .. (the mask band), so block n waits until the n - n_lo blocks
+                    // before it have added theirs.
                     const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
                                              : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + tile;
                     if (leader) {
-                        if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
+                        int n_lo, n_hi;
+                        band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
+                                        kBN, &n_lo, &n_hi);
+                        if (sem_wait(sem, f.n - (kBand ? n_lo : 0), w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
                     }
                     ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
@@ -828,9 +850,12 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
     } else {
         using Lay = BwdLayout<HD>;
-        const bool gqa = g.group > 1;
-        auto kern = p.deterministic ? (gqa ? bwd_kernel<HD, true, true> : bwd_kernel<HD, true, false>)
-                                    : (gqa ? bwd_kernel<HD, false, true> : bwd_kernel<HD, false, false>);
+        const bool gqa = g.group > 1, band = g.win_left >= 0 || g.win_right > 0;
+        auto kern = p.deterministic
+                        ? (gqa ? (band ? bwd_kernel<HD, true, true, true> : bwd_kernel<HD, true, true, false>)
+                               : (band ? bwd_kernel<HD, true, false, true> : bwd_kernel<HD, true, false, false>))
+                        : (gqa ? (band ? bwd_kernel<HD, false, true, true> : bwd_kernel<HD, false, true, false>)
+                               : (band ? bwd_kernel<HD, false, false, true> : bwd_kernel<HD, false, false, false>));
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;

@@ -22,6 +22,7 @@
 // Q[c], dO, Q[c] -- and chunk 0 owns all of dV while chunk 1 has none.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "mask.cuh"
 #include "sched.cuh"
 
 namespace attn {
@@ -104,13 +105,15 @@ struct WideQWalk {
 };
 __device__ __forceinline__ WideQWalk qwalk(const WideBwdTile& f) { return WideQWalk{f.hq0, f.m_begin}; }
 
-__device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // Tile t: key-block tile t/2 of the d <= 128 walk (split tiles included), chunk
 // t%2 (the two chunks of a key block run at the same time on neighbouring CTAs
 // and share its loads in L2).
 // kGQA: grouped heads, as in bwd.cu's bwd_tile
-template <bool kGQA>
+__device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// kBand: as in bwd.cu's bwd_tile
+template <bool kGQA, bool kBand>
 __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
     const Geometry& g = p.g;
     const int sp = kGQA ? (t >> 1) % p.split : 0;
@@ -134,10 +137,18 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
         f.q_row0 = ti.b * g.Lq;
         f.k_row0 = ti.b * g.Lk;
     }
-    f.m_end = (f.lq + kBM - 1) / kBM;
-    f.m_begin = 0;
-    if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
-    if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
+    // the query blocks whose rows see some key of this block (the mask band;
+    // none: the tile writes zero dK/dV rows). No mask or the causal one: all
+    // blocks, or those from the one holding row n*kBN - (lk - lq) on.
+    if constexpr (kBand) {
+        band_query_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), f.n * kBN, f.n * kBN + kBN - 1, kBM,
+                          &f.m_begin, &f.m_end);
+    } else {
+        f.m_end = (f.lq + kBM - 1) / kBM;
+        f.m_begin = 0;
+        if (g.causal) f.m_begin = max(0, floor_div_w(f.n * kBN - (f.lk - f.lq), kBM));
+        if (f.n * kBN >= f.lk) f.m_end = f.m_begin;
+    }
     if constexpr (kGQA) {
         const int per = g.group / p.split;
         f.s = sp;
@@ -152,8 +163,9 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
 }
 
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
-// other path's code out of each kernel); kGQA: grouped heads
-template <int HD, int DV, bool kDet, bool kGQA>
+// other path's code out of each kernel); kGQA: grouped heads; kBand: the mask
+// has a left bound (as in bwd.cu)
+template <int HD, int DV, bool kDet, bool kGQA, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -225,7 +237,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -358,7 +370,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
             if (f.m_begin >= f.m_end) continue;
             const int pc = f.c, po = 1 - f.c;
             const bool narrow = chunk_width<HD>(f.c) == 64;
@@ -478,7 +490,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
             const int cw = chunk_width<HD>(f.c);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
@@ -513,7 +525,16 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 continue;
             }
-            const int q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+            // query q is allowed for this key iff q_lo <= q < q_hi (the mask band)
+            int q_lo, q_hi;
+            if constexpr (kBand) {
+                const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+                q_lo = key_ok ? band_query_lo(mb, key) : 0;
+                q_hi = key_ok ? band_query_hi(mb, key) : 0;   // (key_ok false: lo = 64 below)
+            } else {
+                q_lo = g.causal ? key - (f.lk - f.lq) : 0;
+                q_hi = f.lq;
+            }
             WideQWalk qw = qwalk(f);
             for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
                 const int m = qw.m;
@@ -536,7 +557,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const float* nlse2 = stats + stage * 256 + wg * 64;
                 const float* ndd = stats + stage * 256 + 128 + wg * 64;
                 const int q0 = m * kBM + wg * 64;
-                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= f.lq;
+                const bool full = key_ok && q0 >= q_lo && q0 + 64 <= q_hi;
                 const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
@@ -547,7 +568,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     pv[c + 1] = ex2_mufu(x1);
                 }
                 if (!full) {   // diagonal or ragged block: keep query columns [lo, hi) only
-                    const int lo = key_ok ? q_lo - q0 : 64, hi = f.lq - q0;
+                    const int lo = key_ok ? q_lo - q0 : 64, hi = q_hi - q0;
 #pragma unroll
                     for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
                 }
@@ -645,7 +666,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
             const int cw = chunk_width<HD>(f.c);
             const int rounds = cw / 64;
             WideQWalk qw = qwalk(f);
@@ -666,7 +687,12 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                              : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + 2 * tile + f.c;
                     if (leader) {
-                        if (sem_wait(sem, f.n, w)) fence_proxy_async_global();
+                        // the key blocks that see query block m form one range n_lo .. (the
+                        // mask band): block n waits for the n - n_lo before it
+                        int n_lo, n_hi;
+                        band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
+                                        kBN, &n_lo, &n_hi);
+                        if (sem_wait(sem, f.n - (kBand ? n_lo : 0), w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));
                     }
                     ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
@@ -744,9 +770,14 @@ cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
                            int num_sms, cudaStream_t stream) {
     using Lay = WideBwdLayout<HD, DV>;
-    const bool gqa = p.g.group > 1;
-    auto kern = p.deterministic ? (gqa ? bwd_wide_kernel<HD, DV, true, true> : bwd_wide_kernel<HD, DV, true, false>)
-                                : (gqa ? bwd_wide_kernel<HD, DV, false, true> : bwd_wide_kernel<HD, DV, false, false>);
+    const bool gqa = p.g.group > 1, band = p.g.win_left >= 0 || p.g.win_right > 0;
+    auto kern =
+        p.deterministic
+            ? (gqa ? (band ? bwd_wide_kernel<HD, DV, true, true, true> : bwd_wide_kernel<HD, DV, true, true, false>)
+                   : (band ? bwd_wide_kernel<HD, DV, true, false, true> : bwd_wide_kernel<HD, DV, true, false, false>))
+            : (gqa ? (band ? bwd_wide_kernel<HD, DV, false, true, true> : bwd_wide_kernel<HD, DV, false, true, false>)
+                   : (band ? bwd_wide_kernel<HD, DV, false, false, true>
+                           : bwd_wide_kernel<HD, DV, false, false, false>));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

@@ -22,6 +22,7 @@
 // flight, frees its tensor memory and returns.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "mask.cuh"
 #include "sched.cuh"
 
 namespace attn {
@@ -111,11 +112,19 @@ struct FwdTile {
     int lq, lk;        // sequence lengths
     int q_row0;        // packed row of the first query row of the tile
     int k_row0;        // packed row of the first key of the sequence
-    int n_kv;          // K/V blocks to visit (0: every row is fully masked); Q tile 1 visits all
-    int n_kv0;         // K/V blocks Q tile 0 visits: n_kv, or one fewer (causal: the block past
-                       // its diagonal is fully masked for it), or 0 (none of its rows sees a key)
+    // The tile streams K/V blocks kv_first .. kv_first + n_kv - 1 (n_kv = 0: no
+    // row of the tile sees a key). Q tile 0 visits stream blocks [0, n_kv0),
+    // Q tile 1 [kv_start1, n_kv): the two tiles' key ranges, 128 rows apart,
+    // differ by at most a block at either end (the causal diagonal, a local
+    // window's left edge); n_kv0 = 0 when none of tile 0's rows sees a key.
+    int kv_first, n_kv, n_kv0, kv_start1;
 };
 
+// kLeft: the mask has a left bound (a local window). Without one every row's
+// keys start at key 0, so the kernels instantiated with kLeft = false keep the
+// stream start, Q tile 1's first block and the rows' lower column bound at the
+// constant 0 (fewer live registers in the softmax loop).
+template <bool kLeft>
 __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
     const Geometry& g = p.g;
     Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0, false)
@@ -136,19 +145,26 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
         f.q_row0 = ti.b * g.Lq + ti.m * kRowsPerTile;
         f.k_row0 = ti.b * g.Lk;
     }
-    int keys = f.lk, keys0 = f.lk;
-    if (g.causal) {   // bottom-right aligned mask: row r sees keys below r + 1 + lk - lq
-        const int row_last = min(ti.m * kRowsPerTile + kRowsPerTile - 1, f.lq - 1);
-        const int row_last0 = min(ti.m * kRowsPerTile + kBM - 1, f.lq - 1);
-        keys = min(f.lk, row_last + 1 + f.lk - f.lq);
-        keys0 = min(f.lk, row_last0 + 1 + f.lk - f.lq);
+    const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+    const int r0 = ti.m * kRowsPerTile;
+    int l0, h0, l1, h1;
+    const bool has0 = band_key_blocks(mb, r0, r0 + kBM - 1, kBN, &l0, &h0);
+    bool has1 = band_key_blocks(mb, r0 + kBM, r0 + kRowsPerTile - 1, kBN, &l1, &h1);
+    if (!has1 && has0) {   // tile 1 has no row in the sequence: it shadows tile 0 (rows not stored)
+        l1 = l0;
+        h1 = h0;
+        has1 = true;
     }
-    f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
-    f.n_kv0 = keys0 > 0 ? (keys0 + kBN - 1) / kBN : 0;
+    // (tile 1's rows follow tile 0's, so with both present l0 <= l1 and h0 <= h1;
+    // tile 1 sees no key only if tile 0 sees none either)
+    f.kv_first = kLeft ? (has0 ? l0 : l1) : 0;
+    f.n_kv = has1 ? h1 - f.kv_first : 0;
+    f.n_kv0 = has0 ? h0 - f.kv_first : 0;
+    f.kv_start1 = kLeft && has1 ? l1 - f.kv_first : 0;
     return f;
 }
 
-template <int HD>
+template <int HD, bool kLeft>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -209,7 +225,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t kv_cnt = 0, it = 0, q_issued = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQEmpty), (it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -232,7 +248,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         for (int hf = 0; hf < Lay::kHalves; ++hf)
                             tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox,
                                         kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.hk,
-                                        f.k_row0 + j * kBN);
+                                        f.k_row0 + ((kLeft ? f.kv_first : 0) + j) * kBN);
                     }
                     __syncwarp();
                     ++kv_cnt;
@@ -283,9 +299,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t kv_cnt = 0, it = 0, pc0 = 0, pc1 = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
             if (f.n_kv == 0) continue;
-            const int n0 = f.n_kv0;   // Q tile 0 stops after its own last visible block
+            const int n0 = f.n_kv0, s1 = kLeft ? f.kv_start1 : 0;   // Q tile 0: [0, n0), Q tile 1: [s1, n_kv)
             ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
             if (!ok) break;
             uint32_t slot_k = kv_cnt % S;
@@ -298,8 +314,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     issue_s(0, slot_k);
                     tc_commit(bar(Lay::kSFull + 0));
                 }
-                issue_s(1, slot_k);
-                tc_commit(bar(Lay::kSFull + 1));
+                if (s1 == 0) {
+                    issue_s(1, slot_k);
+                    tc_commit(bar(Lay::kSFull + 1));
+                }
                 tc_commit(bar(Lay::kKVEmpty + slot_k));
                 if (f.n_kv == 1) tc_commit(bar(Lay::kQEmpty));   // Q is no longer read: the next tile's may land
             }
@@ -335,17 +353,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     }
                 }
                 __syncwarp();
-                // tile 1
-                ok = warp_wait(bar(Lay::kPFull + 1), pc1 & 1u, w, lane);
-                if (!ok) break;
-                ++pc1;
-                tc_fence_after_sync();
+                // tile 1 (from stream block s1 on)
+                if (j >= s1) {
+                    ok = warp_wait(bar(Lay::kPFull + 1), pc1 & 1u, w, lane);
+                    if (!ok) break;
+                    ++pc1;
+                    tc_fence_after_sync();
+                }
                 if (lane == 0) {
-                    issue_pv(1, slot_v, j > 0);
+                    if (j >= s1) issue_pv(1, slot_v, j > s1);
                     tc_commit(bar(Lay::kKVEmpty + slot_v));
                     if (more) {
-                        issue_s(1, slot_k);
-                        tc_commit(bar(Lay::kSFull + 1));
+                        if (j + 1 >= s1) {
+                            issue_s(1, slot_k);
+                            tc_commit(bar(Lay::kSFull + 1));
+                        }
                         tc_commit(bar(Lay::kKVEmpty + slot_k));
                         if (j + 2 == f.n_kv) tc_commit(bar(Lay::kQEmpty));   // that was the tile's last S
                     } else {
@@ -377,14 +399,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
             const int r = f.mp * kRowsPerTile + tq * kBM + row_in_tile;   // row inside the sequence
             const bool valid = r < f.lq;
             const long prow = (long)f.q_row0 + tq * kBM + row_in_tile;   // packed row
             __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * HD;
             float* lptr = varlen ? p.lse + (long)f.h * g.Lq + prow
                                  : p.lse + ((long)f.b * g.H + f.h) * g.Lq + r;
-            const int nkv = tq ? f.n_kv : f.n_kv0;   // blocks this Q tile visits
+            const int jb = kLeft && tq ? f.kv_start1 : 0, nkv = tq ? f.n_kv : f.n_kv0;   // stream blocks [jb, nkv)
             if (nkv == 0) {
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(optr);
@@ -394,9 +416,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 continue;
             }
-            const int col_limit = g.causal ? min(f.lk, r + 1 + f.lk - f.lq) : f.lk;
+            const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+            const int col_lo = kLeft ? band_key_lo(mb, r) : 0, col_limit = band_key_hi(mb, r);   // keys [col_lo, col_limit)
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nkv; ++j) {
+            for (int j = jb; j < nkv; ++j) {
                 ok = warp_wait(bar(Lay::kSFull + tq), sc & 1u, w, lane);
                 if (!ok) break;
                 ++sc;
@@ -408,11 +431,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) s[i] = u2f(r128[i]);
                 }
-                const int c0 = j * kBN;
-                if (c0 + kBN > col_limit) {
+                const int c0 = ((kLeft ? f.kv_first : 0) + j) * kBN;
+                if (c0 + kBN > col_limit || c0 < col_lo) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (c0 + c >= col_limit) s[c] = -INFINITY;
+                        if (c0 + c >= col_limit || c0 + c < col_lo) s[c] = -INFINITY;
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
@@ -426,7 +449,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const bool need = m_new > m_run + kTau;
                 if (__any_sync(kFullMask, need)) {
                     const float alpha = (m_new == -INFINITY) ? 1.f : ex2_mufu(m_run - m_new);
-                    if (j > 0) {   // O holds blocks 0..j-1 (their MMAs completed before S_j did)
+                    if (j > jb) {   // O holds blocks jb..j-1 (their MMAs completed before S_j did)
 #pragma unroll
                         for (int c = 0; c < HD / 32; ++c) {
                             tmem_ld32(t_o + c * 32, rr);
@@ -488,7 +511,7 @@ template <int HD>
 cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, int num_sms, cudaStream_t stream) {
     using Lay = FwdLayout<HD>;
-    auto kern = fwd_kernel<HD>;
+    auto kern = p.g.win_left >= 0 ? fwd_kernel<HD, true> : fwd_kernel<HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

@@ -19,6 +19,7 @@
 // Every wait is bounded, as in fwd.cu.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "mask.cuh"
 #include "sched.cuh"
 
 namespace attn {
@@ -62,7 +63,7 @@ struct WideTile {
     int lq, lk;
     int q_row0;      // packed row of the tile's first query row
     int k_row0;
-    int n_kv;
+    int kv_first, n_kv;   // K/V blocks kv_first .. kv_first + n_kv - 1 (n_kv = 0: no row sees a key)
 };
 
 __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
@@ -86,12 +87,11 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
         f.q_row0 = ti.b * g.Lq + ti.m * kBM;
         f.k_row0 = ti.b * g.Lk;
     }
-    int keys = f.lk;
-    if (g.causal) {
-        const int row_last = min(ti.m * kBM + kBM - 1, f.lq - 1);
-        keys = min(f.lk, row_last + 1 + f.lk - f.lq);
-    }
-    f.n_kv = keys > 0 ? (keys + kBN - 1) / kBN : 0;
+    const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+    int jlo, jhi;
+    band_key_blocks(mb, ti.m * kBM, ti.m * kBM + kBM - 1, kBN, &jlo, &jhi);
+    f.kv_first = jlo;
+    f.n_kv = jhi - jlo;
     return f;
 }
 
@@ -163,7 +163,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_expect_tx(bar(Lay::kKVFull + slot), boxes * kBox);
                 for (int hf = 0; hf < boxes; ++hf)
                     tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox, kv ? &tmV : &tmK,
-                                bar(Lay::kKVFull + slot), hf * 64, f.hk, f.k_row0 + j * kBN);
+                                bar(Lay::kKVFull + slot), hf * 64, f.hk, f.k_row0 + (f.kv_first + j) * kBN);
             }
             __syncwarp();
             ++kv_cnt;
@@ -313,7 +313,8 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 continue;
             }
-            const int col_limit = g.causal ? min(f.lk, r + 1 + f.lk - f.lq) : f.lk;
+            const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
+            const int col_lo = band_key_lo(mb, r), col_limit = band_key_hi(mb, r);   // keys [col_lo, col_limit)
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < f.n_kv; ++j) {
                 const int buf = j & 1;
@@ -329,11 +330,11 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) s[i] = u2f(r128[i]);
                 }
-                const int c0 = j * kBN;
-                if (c0 + kBN > col_limit) {
+                const int c0 = (f.kv_first + j) * kBN;
+                if (c0 + kBN > col_limit || c0 < col_lo) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (c0 + c >= col_limit) s[c] = -INFINITY;
+                        if (c0 + c >= col_limit || c0 + c < col_lo) s[c] = -INFINITY;
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll

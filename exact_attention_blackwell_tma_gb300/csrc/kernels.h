@@ -21,7 +21,9 @@ struct Geometry {
     int Hkv, group;           // key/value heads, query heads per key/value head
     const int* cu_seqlens;    // device, B+1 query offsets, or null (dense)
     const int* cu_seqlens_k;  // device, B+1 key offsets (varlen; cu_seqlens when they are shared)
-    int causal;
+    int causal;               // the mask has a right bound (win_right >= 0): longest-first walks
+    int win_left, win_right;  // mask band (mask.cuh): keys i + delta - win_left .. i + delta + win_right
+                              // of query i, -1: no bound on that side; causal is win_right = 0
     float scale;              // softmax scale (> 0)
     float scale_log2;         // scale * log2(e)
 };

@@ -46,6 +46,7 @@ class Workload:
     dv: Optional[int] = None          # head dim of v (and dO); None: the same as q and k
     hkv: Optional[int] = None         # key/value heads (grouped heads); None: H
     lengths_k: Optional[tuple] = None # varlen: per-sequence key lengths; None: the query lengths
+    window: tuple = (-1, -1)          # local window (left, right); -1: open side
 
     @property
     def scale(self) -> float:
@@ -79,15 +80,19 @@ class Workload:
 
     def pairs(self) -> int:
         """Number of unmasked (query, key) pairs summed over batch and heads
-        (causal: bottom-right aligned, j <= i + Lk - Lq)."""
+        (causal: bottom-right aligned, j <= i + Lk - Lq; a local window keeps
+        i + Lk - Lq - left <= j <= i + Lk - Lq + right)."""
+        wl, wr = self.window
+        if self.causal:
+            wr = 0
+
         def per_seq(lq, lk):
-            if not self.causal:
+            if wl < 0 and wr < 0:
                 return lq * lk
-            # row i sees min(lk, max(0, i + 1 + lk - lq)) keys
-            full = max(0, min(lq, lq - lk))          # rows before the first visible key
-            n = lq - full                             # rows that see 1 + (i - full) ... keys
-            first = lk - lq + full + 1 if n else 0
-            return n * first + n * (n - 1) // 2 if n else 0
+            i = torch.arange(lq, dtype=torch.int64)
+            lo = (i + (lk - lq) - wl).clamp(min=0) if wl >= 0 else torch.zeros_like(i)
+            hi = (i + (lk - lq) + wr + 1).clamp(max=lk) if wr >= 0 else torch.full_like(i, lk)
+            return int((hi - lo).clamp(min=0).sum())
         if self.varlen:
             return self.H * sum(per_seq(a, b) for a, b in zip(self.lengths, self.keys))
         return self.B * self.H * per_seq(self.L, self.L)

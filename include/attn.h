@@ -35,6 +35,13 @@
  *          [Tk, Hkv, d], lse fp32 [H, Tq]. Either length may be 0 for a
  *          sequence (no keys: O = 0, LSE = -inf). Both arrays on the device,
  *          same rules as cu_seqlens.
+ *   local window (attn_fwd_ex, attn_bwd_ex): window_left >= 0 drops keys
+ *          j < i + (Lk - Lq) - window_left, window_right >= 0 keys
+ *          j > i + (Lk - Lq) + window_right (per sequence for varlen); -1
+ *          leaves that side open; causal != 0 sets window_right = 0. A row
+ *          with no key left gets O = 0, LSE = -inf. The causal mask is the
+ *          band (-1, 0). (FlashAttention-4 paper, Section 4: masking
+ *          strategies compose with varlen and scheduling.)
  *   grouped heads (attn_fwd_gqa, attn_bwd_gqa): k, v, dk, dv have Hkv heads
  *          instead of H ([B, Lk, Hkv, d] or [T, Hkv, d]); H must be a
  *          multiple of Hkv, and query head h reads key/value head
@@ -149,14 +156,18 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
 /*
  * The general forward: every entry point above is this one with some
  * arguments fixed. Hkv key/value heads (grouped heads), a head dim d_v of
- * its own for v and o (d_v = d, or d = 192 with d_v = 128), and either
+ * its own for v and o (d_v = d, or d = 192 with d_v = 128), a local window
+ * (window_left, window_right; -1, -1 for none; see above), and either
  * dense tensors (cu_seqlens_q == NULL, cu_seqlens_k == NULL), packed
  * sequences with one offset array (cu_seqlens_k == NULL: Lq = Lk = T), or
  * packed sequences with key offsets of their own (Lq = Tq, Lk = Tk).
- * cu_seqlens_k without cu_seqlens_q returns ATTN_ERR_ARG.
+ * cu_seqlens_k without cu_seqlens_q, or a window bound below -1, returns
+ * ATTN_ERR_ARG. The work tiles visit only the key blocks their rows' band
+ * reaches.
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
+                int window_left, int window_right,
                 const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream);
 
 /*
@@ -175,6 +186,7 @@ size_t attn_bwd_ex_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, 
 int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 const void* dout, void* dq, void* dk, void* dv,
                 int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
+                int window_left, int window_right,
                 const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic,
                 void* workspace, size_t ws_bytes, cudaStream_t stream);
 

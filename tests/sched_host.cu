@@ -1,4 +1,5 @@
-// Host-side checks of the persistent tile scheduler (csrc/sched.cuh), compiled
+// Host-side checks of the persistent tile scheduler (csrc/sched.cuh) and of
+// the mask band's index arithmetic (csrc/mask.cuh), compiled
 // by tests/test_sched.py with nvcc and run without a GPU. The index functions
 // under test are the ones the kernels call. Prints "OK" and exits 0 when every
 // check passes; otherwise prints the first failure and exits 1.
@@ -9,6 +10,7 @@
 #include <vector>
 #include <algorithm>
 
+#include "mask.cuh"
 #include "sched.cuh"
 
 using namespace attn;
@@ -134,7 +136,55 @@ static void check_causal_balance(int B, int H, int L, int rows, bool fwd, int gr
     if (mx > mean * (1.0 + tol)) fail("causal imbalance (max/mean in percent)", (int)(100 * mx / mean), L, fwd);
 }
 
+// mask.cuh against a scan of the mask: per row and per key the range of
+// partners, and for groups of rows (keys) the blocks of keys (rows) they reach
+static void check_band(int lq, int lk, int wl, int wr) {
+    const MaskBand m = mask_band(lq, lk, wl, wr);
+    auto seen = [&](int i, int j) {   // query i sees key j: the definition, scanned
+        const int d = lk - lq;
+        if (j < 0 || j >= lk) return false;
+        if (wr >= 0 && j > i + d + wr) return false;
+        if (wl >= 0 && j < i + d - wl) return false;
+        return true;
+    };
+    for (int i = 0; i < lq; ++i) {
+        const int lo = band_key_lo(m, i), hi = band_key_hi(m, i);
+        for (int j = 0; j < lk; ++j)
+            if (seen(i, j) != (j >= lo && j < hi)) fail("band key range", i, j, wl * 1000 + wr);
+    }
+    for (int j = 0; j < lk; ++j) {
+        const int lo = band_query_lo(m, j), hi = band_query_hi(m, j);
+        for (int i = 0; i < lq; ++i)
+            if (seen(i, j) != (i >= lo && i < hi)) fail("band query range", i, j, wl * 1000 + wr);
+    }
+    for (int span : {128, 256})
+        for (int r0 = 0; r0 < lq + 256; r0 += 128) {
+            std::vector<char> blk((lk + 127) / 128 + 1, 0);
+            for (int i = r0; i < r0 + span && i < lq; ++i)
+                for (int j = 0; j < lk; ++j)
+                    if (seen(i, j)) blk[j / 128] = 1;
+            int jlo, jhi;
+            const bool any = band_key_blocks(m, r0, r0 + span - 1, 128, &jlo, &jhi);
+            for (int b = 0; b < (int)blk.size(); ++b)
+                if ((bool)blk[b] != (any && b >= jlo && b < jhi)) fail("band key blocks", r0, b, wl * 1000 + wr);
+        }
+    for (int k0 = 0; k0 < lk + 128; k0 += 128) {
+        std::vector<char> blk((lq + 127) / 128 + 1, 0);
+        for (int j = k0; j < k0 + 128 && j < lk; ++j)
+            for (int i = 0; i < lq; ++i)
+                if (seen(i, j)) blk[i / 128] = 1;
+        int mlo, mhi;
+        const bool any = band_query_blocks(m, k0, k0 + 127, 128, &mlo, &mhi);
+        for (int b = 0; b < (int)blk.size(); ++b)
+            if ((bool)blk[b] != (any && b >= mlo && b < mhi)) fail("band query blocks", k0, b, wl * 1000 + wr);
+    }
+}
+
 int main() {
+    for (int lq : {1, 130, 300, 517})
+        for (int lk : {1, 130, 300, 517})
+            for (int wl : {-1, 0, 3, 128, 200})
+                for (int wr : {-1, 0, 3, 128, 200}) check_band(lq, lk, wl, wr);
     for (int n : {1, 7, 152, 153, 1000, 1024, 4096})
         for (int grid : {1, 2, 148, 152})
             check_snake(n, grid);

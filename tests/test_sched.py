@@ -6,7 +6,10 @@ exactly one CTA in increasing order (boustrophedon hand-out); the dense
 walks (L2-section order, longest-first order) enumerate every (batch, head,
 row block) exactly once; the varlen walk covers every tile of a longest-first
 sequence map; and the per-CTA work of the benchmark's causal workloads stays
-within 3% of the mean.
+within 3% of the mean. It also checks the mask band's index arithmetic
+(csrc/mask.cuh: the keys a row sees, the rows a key is seen by, and the
+blocks a group of rows or keys reaches) against a scan of the mask for no
+mask, causal and local windows, square and rectangular.
 """
 import os
 import shutil
