@@ -36,6 +36,7 @@ _lib = None
 
 _dp = ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int)
+_bp = ctypes.POINTER(ctypes.c_ubyte)
 
 
 def build(force: bool = False) -> str:
@@ -58,13 +59,13 @@ def bind(path: str):
     lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                               ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, _bp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                _ip, _ip, _ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_bwd.restype = ctypes.c_int
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                               ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, _bp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                _ip, _ip, _ip, ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int]
     return lib
 
@@ -131,6 +132,19 @@ def _dims(q, k, cu, cuk=None):
         raise ValueError("query heads must be a multiple of key/value heads")
     return B, H, Hkv, Lq, Lk, d
 
+def _block_mask(mask, H, Lq, Lk, block):
+    """(pointer, heads, block_q, block_k) of an optional block mask [Hm, nqb, nkb]."""
+    if mask is None:
+        return None, 1, 1, 1
+    bq, bk = block
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    if m.ndim == 2:
+        m = m[None]
+    if m.shape[0] not in (1, H) or m.shape[1:] != ((Lq + bq - 1) // bq, (Lk + bk - 1) // bk):
+        raise ValueError(f"block mask of shape {m.shape} does not match H={H}, Lq={Lq}, Lk={Lk}, block={block}")
+    return m, m.shape[0], bq, bk
+
+
 def _dv(v, k):
     """Head dim of v (may differ from that of q and k); v must match k otherwise."""
     if v.shape[:-1] != k.shape[:-1]:
@@ -139,7 +153,7 @@ def _dv(v, k):
 
 
 def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthreads=None, cu_seqlens_k=None,
-        window_left: int = -1, window_right: int = -1):
+        window_left: int = -1, window_right: int = -1, block_mask=None, block=(128, 128)):
     """O and LSE (natural log) by the definition. Returns (o, lse) as float64.
 
     q and k share a head dim; v (and O) may have another one; k and v may have
@@ -147,7 +161,9 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
     batch whose key lengths differ from its query lengths. ``window_left`` /
     ``window_right``: query i sees keys i + delta - window_left ..
     i + delta + window_right (delta = Lk - Lq; -1: no bound; causal sets the
-    right bound to 0).
+    right bound to 0). ``block_mask``: dense problems only, [Hm, ceil(Lq/bq),
+    ceil(Lk/bk)] (Hm 1 or H; 2-D means Hm = 1) with ``block = (bq, bk)``; a
+    zero entry drops that block of (query, key) pairs.
     ``rows``: optional query-row indices (per sequence) to evaluate; the other
     rows of the returned arrays are NaN.
     """
@@ -157,12 +173,13 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
         raise ValueError("cu_seqlens_k needs cu_seqlens")
     B, H, Hkv, Lq, Lk, d = _dims(q, k, cu, cuk)
     dv = _dv(v, k)
+    bm, bmh, bq, bk = _block_mask(block_mask, H, Lq, Lk, block)
     o = np.full(q.shape[:-1] + (dv,), np.nan)
     lse = np.full((B, H, Lq) if cu is None else (H, q.shape[0]), np.nan)
     r = _i32(rows)
     rc = _load().oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
                             B, H, Hkv, Lq, Lk, d, dv, float(scale), int(bool(causal)),
-                            int(window_left), int(window_right),
+                            int(window_left), int(window_right), _ptr(bm, _bp), bmh, bq, bk,
                             _ptr(cu, _ip), _ptr(cuk, _ip), _ptr(r, _ip), 0 if r is None else len(r),
                             nthreads or default_threads())
     if rc != 0:
@@ -171,7 +188,8 @@ def fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None, rows=None, nthread
 
 
 def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, krows=None,
-        nthreads=None, cu_seqlens_k=None, window_left: int = -1, window_right: int = -1):
+        nthreads=None, cu_seqlens_k=None, window_left: int = -1, window_right: int = -1, block_mask=None,
+        block=(128, 128)):
     """dQ, dK, dV of L = sum(O * dO) by the definition. Returns float64 arrays.
 
     ``qrows`` / ``krows``: optional row subsets for dQ / (dK, dV); other rows NaN.
@@ -183,6 +201,7 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
         raise ValueError("cu_seqlens_k needs cu_seqlens")
     B, H, Hkv, Lq, Lk, d = _dims(q, k, cu, cuk)
     dvd = _dv(v, k)
+    bm, bmh, bq, bk = _block_mask(block_mask, H, Lq, Lk, block)
     if dout.shape != q.shape[:-1] + (dvd,):
         raise ValueError("dout must have the rows and heads of q and the head dim of v")
     dq = np.full(q.shape, np.nan)
@@ -192,7 +211,7 @@ def bwd(q, k, v, dout, scale: float, causal: bool, cu_seqlens=None, qrows=None, 
     rc = _load().oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp),
                             _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
                             B, H, Hkv, Lq, Lk, d, dvd, float(scale), int(bool(causal)),
-                            int(window_left), int(window_right), _ptr(cu, _ip),
+                            int(window_left), int(window_right), _ptr(bm, _bp), bmh, bq, bk, _ptr(cu, _ip),
                             _ptr(cuk, _ip), _ptr(qr, _ip), 0 if qr is None else len(qr),
                             _ptr(kr, _ip), 0 if kr is None else len(kr),
                             nthreads or default_threads())

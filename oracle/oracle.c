@@ -19,7 +19,12 @@
  *                     j <= i + delta + wr (wr >= 0)
  *   (a band around the bottom-right diagonal: the FlashAttention-4 paper's
  *   Section 4 lists masking strategies among the primitives its kernels
- *   compose; the band is the plainest one beyond the causal mask).
+ *   compose; the band is the plainest one beyond the causal mask),
+ *   and with a block mask (dense problems; same section: block-sparse
+ *   patterns are one of those primitives): a byte array
+ *   block_mask[mask_heads][ceil(Lq / block_q)][ceil(Lk / block_k)], mask_heads
+ *   1 (shared) or H (query head h uses its own); allowed(i, j) also needs
+ *   block_mask[h or 0][i / block_q][j / block_k] != 0.
  *     LSE_i = m_i + ln sum_j exp(s_ij - m_i),  m_i = max_j s_ij   (allowed j)
  *     P_ij  = exp(s_ij - LSE_i)
  *     O_i   = sum_j P_ij v_j
@@ -83,6 +88,8 @@ typedef struct {
     double *o, *lse, *dq, *dk, *dv;
     int B, H, Hkv, Lq, Lk, d, dvh;   /* Hkv: heads of k, v; dvh: head dim of v, o, dout, dv */
     int wl, wr;                      /* window bounds (-1: none); causal is wr = 0 */
+    const unsigned char *bmask;      /* block mask or NULL; heads bm_h, block sizes bm_q x bm_k */
+    int bm_h, bm_q, bm_k;
     double scale;
     const int *cu;          /* NULL for dense */
     const int *cuk;         /* key offsets (varlen): cu_seqlens_k, or cu */
@@ -134,12 +141,18 @@ static long stat_off(const job_t *J, int b, int h, int i) {
     return ((long)b * J->H + h) * J->Lq + i;
 }
 
-static int allowed(const job_t *J, int b, int i, int j) {
+/* does query row i of query head h see key j (batch entry / sequence b) */
+static int allowed(const job_t *J, int b, int h, int i, int j) {
     int lq = seq_lq(J, b), lk = seq_lk(J, b);
     int delta = lk - lq;
     if (j < 0 || j >= lk) return 0;
     if (J->wr >= 0 && j > i + delta + J->wr) return 0;
     if (J->wl >= 0 && j < i + delta - J->wl) return 0;
+    if (J->bmask) {
+        int rows = (lq + J->bm_q - 1) / J->bm_q, cols = (lk + J->bm_k - 1) / J->bm_k;
+        int hm = J->bm_h == 1 ? 0 : h;
+        if (!J->bmask[((long)hm * rows + i / J->bm_q) * cols + j / J->bm_k]) return 0;
+    }
     return 1;
 }
 
@@ -160,14 +173,14 @@ static double row_lse(const job_t *J, int b, int h, int i) {
     int lk = seq_lk(J, b);
     double m = -INFINITY;
     for (int j = 0; j < lk; j++)
-        if (allowed(J, b, i, j)) {
+        if (allowed(J, b, h, i, j)) {
             double s = score(J, b, h, i, j);
             if (s > m) m = s;
         }
     if (m == -INFINITY) return -INFINITY;
     double sum = 0.0;
     for (int j = 0; j < lk; j++)
-        if (allowed(J, b, i, j)) sum += exp(score(J, b, h, i, j) - m);
+        if (allowed(J, b, h, i, j)) sum += exp(score(J, b, h, i, j) - m);
     return m + log(sum);
 }
 
@@ -177,7 +190,7 @@ static void row_out(const job_t *J, int b, int h, int i, double lse, double *out
     for (int c = 0; c < dv; c++) out[c] = 0.0;
     if (lse == -INFINITY) return;
     for (int j = 0; j < lk; j++) {
-        if (!allowed(J, b, i, j)) continue;
+        if (!allowed(J, b, h, i, j)) continue;
         double p = exp(score(J, b, h, i, j) - lse);
         const double *vj = J->v + row_off_kv(J, b, j, kvh(J, h), J->Lk);
         for (int c = 0; c < dv; c++) out[c] += p * vj[c];
@@ -218,7 +231,7 @@ static void do_item(job_t *J, int b, int h, int i) {
         for (int c = 0; c < d; c++) dqi[c] = 0.0;
         if (J->lse_all[stat_off(J, b, h, i)] == -INFINITY) return;
         for (int j = 0; j < lk; j++) {
-            if (!allowed(J, b, i, j)) continue;
+            if (!allowed(J, b, h, i, j)) continue;
             double ds = dscore(J, b, h, i, j);
             const double *kj = J->k + row_off_k(J, b, j, kvh(J, h), J->Lk);
             for (int c = 0; c < d; c++) dqi[c] += ds * kj[c];
@@ -234,7 +247,7 @@ static void do_item(job_t *J, int b, int h, int i) {
         for (int c = 0; c < dv; c++) dvj[c] = 0.0;
         for (int hq = hk * g; hq < hk * g + g; hq++)
             for (int r = 0; r < lq; r++) {
-                if (!allowed(J, b, r, j)) continue;
+                if (!allowed(J, b, hq, r, j)) continue;
                 long st = stat_off(J, b, hq, r);
                 double p = exp(score(J, b, hq, r, j) - J->lse_all[st]);
                 const double *dor = J->dout + row_off_v(J, b, r, hq, J->Lq);
@@ -307,9 +320,10 @@ static int check_offsets(int B, const int *cu) {
 }
 
 static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, const int *cu, const int *cuk,
-                      int wl, int wr) {
+                      int wl, int wr, const unsigned char *bmask, int bm_h, int bm_q, int bm_k) {
     if (B < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || dv < 1) return -1;
     if (wl < -1 || wr < -1) return -1;
+    if (bmask && (cu || (bm_h != 1 && bm_h != H) || bm_q < 1 || bm_k < 1)) return -1;
     if (!cu && (Lq < 0 || Lk < 0)) return -1;
     if (cuk && !cu) return -1;
     if (cu && check_offsets(B, cu)) return -1;
@@ -319,8 +333,10 @@ static int check_args(int B, int H, int Hkv, int Lq, int Lk, int d, int dv, cons
 
 static void init_job(job_t *J, const double *q, const double *k, const double *v, const double *dout,
                      int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
-                     int wl, int wr, const int *cu, const int *cuk) {
+                     int wl, int wr, const int *cu, const int *cuk, const unsigned char *bmask, int bm_h,
+                     int bm_q, int bm_k) {
     memset(J, 0, sizeof(*J));
+    J->bmask = bmask; J->bm_h = bm_h; J->bm_q = bm_q; J->bm_k = bm_k;
     J->q = q; J->k = k; J->v = v; J->dout = dout;
     J->B = B; J->H = H; J->Hkv = Hkv; J->Lq = Lq; J->Lk = Lk; J->d = d; J->dvh = dv;
     J->scale = scale; J->wl = wl; J->wr = causal ? 0 : wr;
@@ -329,13 +345,15 @@ static void init_job(job_t *J, const double *q, const double *k, const double *v
 
 int oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dv, double scale, int causal,
-               int window_left, int window_right,
+               int window_left, int window_right, const unsigned char *block_mask, int mask_heads,
+               int block_q, int block_k,
                const int *cu_seqlens, const int *cu_seqlens_k, const int *rows, int nrows, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens, cu_seqlens_k, window_left, window_right)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dv, cu_seqlens, cu_seqlens_k, window_left, window_right, block_mask,
+                   mask_heads, block_q, block_k)) return -1;
     job_t J;
     init_job(&J, q, k, v, NULL, B, H, Hkv, Lq, Lk, d, dv, scale, causal, window_left, window_right, cu_seqlens,
-             cu_seqlens_k);
+             cu_seqlens_k, block_mask, mask_heads, block_q, block_k);
     J.o = o; J.lse = lse;
     long n;
     int *items = make_items(&J, rows, nrows, 0, &n);
@@ -348,15 +366,17 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
 int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
                double *dq, double *dk, double *dv,
                int B, int H, int Hkv, int Lq, int Lk, int d, int dvd, double scale, int causal,
-               int window_left, int window_right,
+               int window_left, int window_right, const unsigned char *block_mask, int mask_heads,
+               int block_q, int block_k,
                const int *cu_seqlens, const int *cu_seqlens_k, const int *qrows, int nqrows,
                const int *krows, int nkrows, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens, cu_seqlens_k, window_left, window_right)) return -1;
+    if (check_args(B, H, Hkv, Lq, Lk, d, dvd, cu_seqlens, cu_seqlens_k, window_left, window_right, block_mask,
+                   mask_heads, block_q, block_k)) return -1;
     if ((qrows && nqrows < 0) || (krows && nkrows < 0)) return -1;
     job_t J;
     init_job(&J, q, k, v, dout, B, H, Hkv, Lq, Lk, d, dvd, scale, causal, window_left, window_right, cu_seqlens,
-             cu_seqlens_k);
+             cu_seqlens_k, block_mask, mask_heads, block_q, block_k);
     J.dq = dq; J.dk = dk; J.dv = dv;
 
     /* longest sequence, the range of relative row indices */

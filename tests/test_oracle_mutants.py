@@ -39,6 +39,9 @@ MUTANTS = [
     ("key length of sequence b from the query offsets",
      "static int seq_lk(const job_t *J, int b) { return J->cu ? J->cuk[b + 1] - J->cuk[b] : J->Lk; }",
      "static int seq_lk(const job_t *J, int b) { return J->cu ? J->cu[b + 1] - J->cu[b] : J->Lk; }"),
+    ("block mask column from the query index", "if (!J->bmask[((long)hm * rows + i / J->bm_q) * cols + j / J->bm_k]) return 0;",
+     "if (!J->bmask[((long)hm * rows + i / J->bm_q) * cols + i / J->bm_k]) return 0;"),
+    ("block mask of head 0 for every head", "int hm = J->bm_h == 1 ? 0 : h;", "int hm = 0;"),
     ("interleaved head groups", "static int kvh(const job_t *J, int h) { return h / (J->H / J->Hkv); }",
      "static int kvh(const job_t *J, int h) { return h % J->Hkv; }"),
     ("dK/dV from the group's first query head only", "for (int hq = hk * g; hq < hk * g + g; hq++)",
@@ -78,6 +81,8 @@ BATTERY = [
     (pins.test_window_matches_textbook_band, (7, 7, 2, 0)),
     (pins.test_zero_window_returns_the_diagonal_value, ()),
     (pins.test_bwd_finite_differences_window, (2, 1)),
+    (pins.test_block_mask_matches_textbook, (True, 2, 3, True)),
+    (pins.test_bwd_finite_differences_block_mask, (True,)),
     (pins.test_bwd_finite_differences_varlen_separate_keys, (True,)),
 ]
 

@@ -344,6 +344,66 @@ def test_window_wider_than_the_sequence_is_no_window():
             np.testing.assert_array_equal(x, y)
 
 
+def expand_block_mask(bmask, Lq, Lk, bq, bk):
+    """[Hm, nqb, nkb] block mask -> [Hm, Lq, Lk] element mask (numpy repeat)."""
+    m = np.repeat(np.repeat(np.asarray(bmask, dtype=bool), bq, axis=1), bk, axis=2)
+    return m[:, :Lq, :Lk]
+
+
+def textbook_masked(q, k, v, scale, keep):
+    """softmax over the kept (query, key) pairs; keep is [Hm, Lq, Lk] (Hm 1 or H)."""
+    s = np.einsum("bihc,bjhc->bhij", q, k) * scale
+    s = np.where(keep[None], s, -np.inf)
+    with np.errstate(invalid="ignore"):
+        lse = logsumexp(s, axis=-1)
+        p = np.nan_to_num(softmax(s, axis=-1), nan=0.0)
+    return np.einsum("bhij,bjhc->bihc", p, v), lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("bq,bk", [(2, 3), (3, 2), (4, 4)])
+@pytest.mark.parametrize("per_head", [False, True])
+def test_block_mask_matches_textbook(per_head, bq, bk, causal):
+    """A block mask drops whole (query block, key block) rectangles, on top of
+    the causal mask; with one mask per head each head uses its own."""
+    Lq, Lk, H = 9, 11, 3
+    q, k, v = rnd((2, Lq, H, 4), 101), rnd((2, Lk, H, 4), 102), rnd((2, Lk, H, 4), 103)
+    nqb, nkb = -(-Lq // bq), -(-Lk // bk)
+    bm = (np.random.default_rng(104).random((H if per_head else 1, nqb, nkb)) < 0.6).astype(np.uint8)
+    bm[0, 0, :] = 0   # a query block that sees nothing
+    o, lse = oracle.fwd(q, k, v, 0.6, causal, block_mask=bm, block=(bq, bk))
+    keep = expand_block_mask(bm, Lq, Lk, bq, bk)
+    if causal:
+        keep = keep & (np.arange(Lk)[None, :] <= np.arange(Lq)[:, None] + (Lk - Lq))[None]
+    o_ref, lse_ref = textbook_masked(q, k, v, 0.6, keep)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], atol=1e-12)
+    assert np.isneginf(lse[~fin]).all() and (o[:, :bq][:, :, 0] == 0).all()
+
+
+def test_all_ones_block_mask_is_no_mask():
+    q, k, v = rnd((1, 7, 2, 3), 105), rnd((1, 7, 2, 3), 106), rnd((1, 7, 2, 3), 107)
+    for causal in (False, True):
+        a = oracle.fwd(q, k, v, 0.5, causal)
+        b = oracle.fwd(q, k, v, 0.5, causal, block_mask=np.ones((1, 4, 3), np.uint8), block=(2, 3))
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
+def test_block_mask_keeping_one_key_block_is_attention_over_it():
+    """Every query block keeping only key block c is attention over those keys."""
+    Lq, Lk, bq, bk = 8, 9, 4, 3
+    q, k, v = rnd((1, Lq, 1, 3), 108), rnd((1, Lk, 1, 3), 109), rnd((1, Lk, 1, 3), 110)
+    for c in range(3):
+        bm = np.zeros((1, 2, 3), np.uint8)
+        bm[0, :, c] = 1
+        o, lse = oracle.fwd(q, k, v, 0.7, False, block_mask=bm, block=(bq, bk))
+        o_ref, lse_ref = oracle.fwd(q, k[:, c * bk:(c + 1) * bk], v[:, c * bk:(c + 1) * bk], 0.7, False)
+        np.testing.assert_allclose(o, o_ref, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_ref, atol=1e-13)
+
+
 def test_row_subset_matches_full():
     q, k, v = rnd((2, 10, 2, 4), 36), rnd((2, 10, 2, 4), 37), rnd((2, 10, 2, 4), 38)
     full_o, full_l = oracle.fwd(q, k, v, 0.5, True)
@@ -459,6 +519,31 @@ def test_bwd_finite_differences_window(wl, wr):
             plus[which][idx] += 1e-6
             minus[which][idx] -= 1e-6
             g[idx] = (loss_w(*plus) - loss_w(*minus)) / 2e-6
+        assert np.abs(got - g).max() < 1e-7
+
+
+@pytest.mark.parametrize("per_head", [False, True])
+def test_bwd_finite_differences_block_mask(per_head):
+    H = 2
+    q, k, v, do = rnd((1, 6, H, 3), 111), rnd((1, 5, H, 3), 112), rnd((1, 5, H, 3), 113), rnd((1, 6, H, 3), 114)
+    bm = np.array([[[1, 0, 1], [0, 1, 1], [1, 1, 0]]], np.uint8)
+    if per_head:
+        bm = np.concatenate([bm, bm[:, ::-1]], axis=0)
+    dq, dk, dv = oracle.bwd(q, k, v, do, 0.8, True, block_mask=bm, block=(2, 2))
+
+    def loss_b(q_, k_, v_):
+        o, _ = oracle.fwd(q_, k_, v_, 0.8, True, block_mask=bm, block=(2, 2))
+        return float(np.sum(o * do))
+
+    for got, which in ((dq, 0), (dk, 1), (dv, 2)):
+        arrs = [q, k, v]
+        g = np.zeros_like(arrs[which])
+        for idx in np.ndindex(g.shape):
+            plus = [a.copy() for a in arrs]
+            minus = [a.copy() for a in arrs]
+            plus[which][idx] += 1e-6
+            minus[which][idx] -= 1e-6
+            g[idx] = (loss_b(*plus) - loss_b(*minus)) / 2e-6
         assert np.abs(got - g).max() < 1e-7
 
 
