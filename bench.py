@@ -49,6 +49,9 @@ WORKLOADS = {
     "b2h16l8192dqk192dv128": (inputs.HDSWEEP.with_(d=192, dv=128), (True,)),
     # causal with a local window of 4096 keys (attn_fwd_ex / attn_bwd_ex window bounds)
     "b2h16l8192d128_window4096": (inputs.HDSWEEP.with_(name="b2h16l8192d128_window4096", window=(4096, 0)), (True,)),
+    # causal with a block mask: each query block keeps its 4 nearest key blocks and every 8th
+    "b2h16l8192d128_blocksparse": (inputs.HDSWEEP.with_(name="b2h16l8192d128_blocksparse",
+                                                        block_pattern=("local_strided", 4, 8)), (True,)),
     # grouped heads: 16 query heads over 2 key/value heads
     "b2h16kv2l8192d128": (inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2), (True,)),
     "varlen32_h16d128": (inputs.VARLEN, (True,)),
@@ -138,6 +141,7 @@ class Problem:
         self.q, self.k, self.v, self.do = (t[n].to(device) for n in ("q", "k", "v", "do"))
         self.cu = t["cu_seqlens"].to(device) if w.varlen else None
         self.cuk = t["cu_seqlens_k"].to(device) if "cu_seqlens_k" in t else None
+        self.mask = inputs.block_mask(w).to(device) if w.block_pattern is not None else None
         self.o = torch.empty(self.q.shape[:-1] + (w.d_v,), dtype=self.q.dtype, device=device)
         self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
         self.Hkv = w.H_kv
@@ -160,7 +164,7 @@ class Problem:
             return
         rc = binding.attn_fwd_ex(self.q, self.k, self.v, self.o, self.lse, self.B, self.H, self.Hkv, self.Lq,
                                  self.Lk, self.d, self.w.d_v, self.w.scale, causal, self.w.window[0],
-                                 self.w.window[1], self.cu, None)
+                                 self.w.window[1], self.mask, 1, self.cu, None)
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -174,7 +178,8 @@ class Problem:
             return
         rc = binding.attn_bwd_ex(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
                                  self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.d_v, self.w.scale, causal,
-                                 self.w.window[0], self.w.window[1], self.cu, None, 0, self.ws, self.ws.numel())
+                                 self.w.window[0], self.w.window[1], self.mask, 1, self.cu, None, 0, self.ws,
+                                 self.ws.numel())
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -295,7 +300,7 @@ def oracle_sample(w, variants, nthreads=None, budget=ORACLE_SAMPLE_FLOPS):
         where = "batch 0"
 
     def sample_flops(Lp, nh=1):
-        sw = w.with_(lengths=None, lengths_k=None, hkv=None, B=1, H=nh, L=Lp)
+        sw = w.with_(lengths=None, lengths_k=None, hkv=None, B=1, H=nh, L=Lp)   # (a block pattern scales with L)
         return sum(flops(sw, c, kind) for c in variants for kind in kinds_of(w))
 
     Lp = L
@@ -311,11 +316,15 @@ def oracle_sample(w, variants, nthreads=None, budget=ORACLE_SAMPLE_FLOPS):
     kinds = kinds_of(w)
     for causal in variants:
         t0 = time.perf_counter()
+        bm = None
+        if w.block_pattern is not None:   # the leading Lp x Lp block of the mask
+            nb = -(-Lp // 128)
+            bm = inputs.block_mask(w)[:, :nb, :nb].numpy()
         oracle.fwd(f64["q"], f64["k"], f64["v"], w.scale, causal, nthreads=nthreads, window_left=w.window[0],
-                   window_right=w.window[1])
+                   window_right=w.window[1], block_mask=bm)
         if "bwd" in kinds:
             oracle.bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal, nthreads=nthreads,
-                       window_left=w.window[0], window_right=w.window[1])
+                       window_left=w.window[0], window_right=w.window[1], block_mask=bm)
         secs += time.perf_counter() - t0
     total_flops = sample_flops(Lp, nh)
     what = f"{where}" + (f", leading {Lp}x{Lp} block" if Lp < L else "") + \

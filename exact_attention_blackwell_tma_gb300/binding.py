@@ -38,13 +38,14 @@ def _declare(lib):
     lib.attn_fwd_gqa.restype = c_int
     lib.attn_fwd_gqa.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p]
     lib.attn_fwd_ex.restype = c_int
-    lib.attn_fwd_ex.argtypes = ([c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_void_p,
-                                                                  c_void_p])
+    lib.attn_fwd_ex.argtypes = ([c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_int,
+                                                                  c_void_p, c_void_p, c_void_p])
     lib.attn_bwd_ex_workspace_size.restype = c_size_t
     lib.attn_bwd_ex_workspace_size.argtypes = [c_int] * 9
     lib.attn_bwd_ex.restype = c_int
-    lib.attn_bwd_ex.argtypes = ([c_void_p] * 9 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_void_p,
-                                                                  c_int, c_void_p, c_size_t, c_void_p])
+    lib.attn_bwd_ex.argtypes = ([c_void_p] * 9 + [c_int] * 7 + [c_float, c_int, c_int, c_int, c_void_p, c_int,
+                                                                  c_void_p, c_void_p, c_int, c_void_p, c_size_t,
+                                                                  c_void_p])
     lib.attn_fwd_varlen.restype = c_int
     lib.attn_fwd_varlen.argtypes = [c_void_p] * 5 + [c_int] * 7 + [c_float, c_int, c_void_p, c_void_p, c_void_p]
     lib.attn_bwd_workspace_size.restype = c_size_t
@@ -154,10 +155,10 @@ def attn_fwd_varlen(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, cu
 
 
 def attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left=-1, window_right=-1,
-                cu_seqlens_q=None, cu_seqlens_k=None, stream=None) -> int:
+                block_mask=None, mask_heads=1, cu_seqlens_q=None, cu_seqlens_k=None, stream=None) -> int:
     return load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Lq, Lk, d, d_v, scale,
-                              int(causal), int(window_left), int(window_right), _ptr(cu_seqlens_q),
-                              _ptr(cu_seqlens_k), _stream(stream))
+                              int(causal), int(window_left), int(window_right), _ptr(block_mask), int(mask_heads),
+                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream(stream))
 
 
 def attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic) -> int:
@@ -165,11 +166,12 @@ def attn_bwd_ex_workspace_size(B, H, Hkv, Lq, Lk, d, d_v, causal, deterministic)
 
 
 def attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left,
-                window_right, cu_seqlens_q, cu_seqlens_k, deterministic, workspace, ws_bytes, stream=None) -> int:
+                window_right, block_mask, mask_heads, cu_seqlens_q, cu_seqlens_k, deterministic, workspace, ws_bytes,
+                stream=None) -> int:
     return load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                               _ptr(dv), B, H, Hkv, Lq, Lk, d, d_v, scale, int(causal), int(window_left),
-                              int(window_right), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(deterministic),
-                              _ptr(workspace), ws_bytes, _stream(stream))
+                              int(window_right), _ptr(block_mask), int(mask_heads), _ptr(cu_seqlens_q),
+                              _ptr(cu_seqlens_k), int(deterministic), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def attn_bwd_workspace_size(B, H, Lq, Lk, d, causal, deterministic) -> int:
@@ -230,6 +232,18 @@ def _dims(q, k, cu_seqlens):
     return cu_seqlens.numel() - 1, H, T, k.shape[0], d, k.shape[1]
 
 
+def _mask_heads(block_mask, H, Lq, Lk):
+    """Heads of a block mask after checking its shape [Hm, ceil(Lq/128), ceil(Lk/128)] (2-D: Hm = 1)."""
+    if block_mask is None:
+        return 1
+    shape = tuple(block_mask.shape)
+    want = (-(-Lq // 128), -(-Lk // 128))
+    if block_mask.dtype != torch.uint8 or not (shape == want or (len(shape) == 3 and shape[1:] == want
+                                                                 and shape[0] in (1, H))):
+        raise ValueError(f"block_mask must be uint8 [1 or {H}, {want[0]}, {want[1]}], got {block_mask.dtype} {shape}")
+    return 1 if len(shape) == 2 else shape[0]
+
+
 def _check_tensors(*ts):
     for t in ts:
         if t is None:
@@ -239,12 +253,14 @@ def _check_tensors(*ts):
 
 
 def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, out=None, lse=None,
-            stream=None, cu_seqlens_k=None, window=(-1, -1)):
+            stream=None, cu_seqlens_k=None, window=(-1, -1), block_mask=None):
     """O, LSE for bf16 q, k, v ([B, L, H, d], or [T, H, d] with int32 cu_seqlens).
     v (and O) may have a head dim of their own (d = 192 with 128); k and v may
     have fewer heads than q (grouped heads: query head h reads h // (H // Hkv)).
     cu_seqlens_k: key offsets of a varlen batch whose key lengths differ.
-    window: (left, right) bounds of a local window, -1 for an open side."""
+    window: (left, right) bounds of a local window, -1 for an open side.
+    block_mask: uint8 CUDA tensor [Hm, ceil(Lq/128), ceil(Lk/128)] (Hm 1 or H;
+    2-D means Hm = 1), dense problems only; zero drops a 128 x 128 block."""
     _check_tensors(q, k, v, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     dv = v.shape[-1]
@@ -253,9 +269,11 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
         out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq) if cu_seqlens is None else (H, Lq), dtype=torch.float32, device=q.device)
-    if tuple(window) != (-1, -1):
+    if tuple(window) != (-1, -1) or block_mask is not None:
+        mh = _mask_heads(block_mask, H, Lq, Lk)
+        _check_tensors(block_mask)
         _check(attn_fwd_ex(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, window[0], window[1],
-                           cu_seqlens, cu_seqlens_k, stream))
+                           block_mask, mh, cu_seqlens, cu_seqlens_k, stream))
     elif cu_seqlens_k is not None:
         _check(attn_fwd_varlen(q, k, v, out, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, cu_seqlens,
                                cu_seqlens_k, stream))
@@ -270,10 +288,10 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None, 
 
 def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu_seqlens=None,
              deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None,
-             cu_seqlens_k=None, window=(-1, -1)):
+             cu_seqlens_k=None, window=(-1, -1), block_mask=None):
     """dQ, dK, dV (bf16) for the loss sum(O * dO); k and v may have fewer heads
     than q (grouped heads), dK and dV then have theirs; v (dO, dV) may have a head
-    dim of its own (d = 192 with 128). cu_seqlens_k and window as in forward()."""
+    dim of its own (d = 192 with 128). cu_seqlens_k, window and block_mask as in forward()."""
     _check_tensors(q, k, v, o, lse, dout, cu_seqlens, cu_seqlens_k)
     B, H, Lq, Lk, d, Hkv = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -285,9 +303,12 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, cu
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = workspace.numel() * workspace.element_size()
-    if d_v != d or tuple(window) != (-1, -1):
+    if d_v != d or tuple(window) != (-1, -1) or block_mask is not None:
+        mh = _mask_heads(block_mask, H, Lq, Lk)
+        _check_tensors(block_mask)
         _check(attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window[0],
-                           window[1], cu_seqlens, cu_seqlens_k, deterministic, workspace, ws_bytes, stream))
+                           window[1], block_mask, mh, cu_seqlens, cu_seqlens_k, deterministic, workspace, ws_bytes,
+                           stream))
     elif cu_seqlens_k is not None:
         _check(attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, scale, causal, cu_seqlens,
                                cu_seqlens_k, deterministic, workspace, ws_bytes, stream))

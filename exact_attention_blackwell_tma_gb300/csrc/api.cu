@@ -151,6 +151,13 @@ int check_common(int B, int H, int Lq, int Lk, int d, float scale, const int* cu
     return ATTN_OK;
 }
 
+int check_block_mask(const unsigned char* mask, int heads, int H, const int* cu) {
+    if (!mask) return ATTN_OK;
+    if (cu) return fail(ATTN_ERR_ARG, "block masks are for dense problems (cu_seqlens must be null)");
+    if (heads != 1 && heads != H) return fail(ATTN_ERR_ARG, "block mask heads %d must be 1 or H = %d", heads, H);
+    return ATTN_OK;
+}
+
 int check_window(int wl, int wr) {
     if (wl < -1 || wr < -1) return fail(ATTN_ERR_ARG, "window bounds must be >= 0, or -1 for none (%d, %d)", wl, wr);
     return ATTN_OK;
@@ -186,8 +193,11 @@ namespace {
 // one offset array (cu_seqlens_k == cu_seqlens) or with key offsets of their own.
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Lq,
               int Lk, int d, int dv, float scale, int causal, int window_left, int window_right,
-              const int* cu_seqlens, const int* cu_seqlens_k, cudaStream_t stream) {
+              const unsigned char* block_mask, int mask_heads, const int* cu_seqlens, const int* cu_seqlens_k,
+              cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
+    if (rc) return rc;
+    rc = check_block_mask(block_mask, mask_heads, H, cu_seqlens);
     if (rc) return rc;
     rc = check_window(window_left, window_right);
     if (rc) return rc;
@@ -218,6 +228,8 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.g.scale_log2 = scale * kLog2e;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.dv = dv;
+    p.mask.ptr = block_mask;
+    p.mask.heads = mask_heads;
     p.lse = lse;
     // d <= 128: a work tile is two 128-row Q tiles; wider heads: one
     const bool wide = d > 128;
@@ -248,24 +260,24 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                             int Hkv, int Lq, int Lk, int d, int dv, float scale, int causal,
                             const int* cu_seqlens, cudaStream_t stream) {
-    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, -1, -1, cu_seqlens, cu_seqlens,
-                     stream);
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, dv, scale, causal, -1, -1, nullptr, 1, cu_seqlens,
+                     cu_seqlens, stream);
 }
 
 extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
                            int Lq, int Lk, int d, int d_v, float scale, int causal, int window_left,
-                           int window_right, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                           cudaStream_t stream) {
+                           int window_right, const unsigned char* block_mask, int mask_heads,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream) {
     if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_fwd_ex: key offsets without query offsets");
     return fwd_entry(q, k, v, o, lse, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left, window_right,
-                     cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, stream);
+                     block_mask, mask_heads, cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, stream);
 }
 
 extern "C" int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                int Hkv, int Tq, int Tk, int d, int dv, float scale, int causal,
                                const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream) {
     if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_fwd_varlen: null offsets");
-    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, -1, -1, cu_seqlens_q,
+    return fwd_entry(q, k, v, o, lse, B, H, Hkv, Tq, Tk, d, dv, scale, causal, -1, -1, nullptr, 1, cu_seqlens_q,
                      cu_seqlens_k, stream);
 }
 
@@ -331,9 +343,12 @@ namespace {
 // The backward behind every entry point (cu_seqlens_k as in fwd_entry).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
               void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale,
-              int causal, int window_left, int window_right, const int* cu_seqlens, const int* cu_seqlens_k,
-              int deterministic, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+              int causal, int window_left, int window_right, const unsigned char* block_mask, int mask_heads,
+              const int* cu_seqlens, const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
+              cudaStream_t stream) {
     int rc = check_common(B, H, Lq, Lk, d, scale, cu_seqlens, cu_seqlens_k);
+    if (rc) return rc;
+    rc = check_block_mask(block_mask, mask_heads, H, cu_seqlens);
     if (rc) return rc;
     rc = check_window(window_left, window_right);
     if (rc) return rc;
@@ -373,6 +388,8 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     set_mask(&p.g, causal, window_left, window_right);
     p.g.scale = scale;
     p.g.scale_log2 = scale * kLog2e;
+    p.mask.ptr = block_mask;
+    p.mask.heads = mask_heads;
     p.o = static_cast<const __nv_bfloat16*>(o);
     p.dout = static_cast<const __nv_bfloat16*>(dout);
     p.lse = lse;
@@ -416,19 +433,20 @@ extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const v
                             const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
                             int d, float scale, int causal, const int* cu_seqlens, int deterministic,
                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, scale, causal, -1, -1, cu_seqlens,
-                     cu_seqlens, deterministic, workspace, ws_bytes, stream);
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, scale, causal, -1, -1, nullptr, 1,
+                     cu_seqlens, cu_seqlens, deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Lq, int Lk,
                            int d, int d_v, float scale, int causal, int window_left, int window_right,
-                           const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic, void* workspace,
-                           size_t ws_bytes, cudaStream_t stream) {
+                           const unsigned char* block_mask, int mask_heads, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
     if (cu_seqlens_k && !cu_seqlens_q) return fail(ATTN_ERR_ARG, "attn_bwd_ex: key offsets without query offsets");
     return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d_v, scale, causal, window_left,
-                     window_right, cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q, deterministic,
-                     workspace, ws_bytes, stream);
+                     window_right, block_mask, mask_heads, cu_seqlens_q, cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q,
+                     deterministic, workspace, ws_bytes, stream);
 }
 
 extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -437,7 +455,7 @@ extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, cons
                                const int* cu_seqlens_k, int deterministic, void* workspace, size_t ws_bytes,
                                cudaStream_t stream) {
     if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "attn_bwd_varlen: null offsets");
-    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, d, scale, causal, -1, -1,
+    return bwd_entry(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Tq, Tk, d, d, scale, causal, -1, -1, nullptr, 1,
                      cu_seqlens_q, cu_seqlens_k, deterministic, workspace, ws_bytes, stream);
 }
 

@@ -87,6 +87,12 @@ struct BwdTile {
     int hq0;           // first query head the tile visits
     int nblk;          // query blocks the tile visits: (group / split) x (m_end - m_begin)
     int s;             // which of the key block's split tiles (0 when split == 1)
+    // block-sparse (block mask given): entry (query head h, query block m) of
+    // this key block's mask column is mcol[h * mhead + m * mstride] (mhead 0:
+    // one mask for all heads); nblk counts the kept pairs only
+    const unsigned char* mcol;
+    long mstride, mhead;
+    int nheads;          // query heads the tile visits
 };
 
 // The tile's query blocks in visiting order: every query head of its share of
@@ -106,14 +112,42 @@ struct QWalk {
 };
 __device__ __forceinline__ QWalk qwalk(const BwdTile& f) { return QWalk{f.hq0, f.m_begin}; }
 
+// Block-sparse walk: from (qw.h, qw.m) on, the first pair the block mask keeps
+// (warp-wide scans: every lane of the warp calls it alike).
+__device__ __forceinline__ void sparse_seek(const BwdTile& f, QWalk& qw, int lane) {
+    while (qw.h < f.hq0 + f.nheads) {
+        qw.m = sparse_next_col(f.mcol + qw.h * f.mhead, f.mstride, qw.m, f.m_end, lane);
+        if (qw.m < f.m_end) return;
+        ++qw.h;
+        qw.m = f.m_begin;
+    }
+}
+
+// The first pair of the tile's walk, and the next one.
+template <bool kSparse>
+__device__ __forceinline__ QWalk qwalk_start(const BwdTile& f, int lane) {
+    QWalk qw = qwalk(f);
+    if (kSparse && f.mcol) sparse_seek(f, qw, lane);
+    return qw;
+}
+template <bool kGQA, bool kSparse>
+__device__ __forceinline__ void qwalk_step(QWalk& qw, const BwdTile& f, int lane) {
+    if (kSparse && f.mcol) {
+        ++qw.m;
+        sparse_seek(f, qw, lane);
+    } else {
+        qw.next<kGQA>(f);
+    }
+}
+
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // kGQA: grouped heads (the kernels for one query head per key/value head are
 // instantiated without the group walk and the split, which keeps their code
 // and registers as small as before grouped heads existed)
-template <bool kGQA, bool kBand>
-__device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
+template <bool kGQA, bool kBand, bool kSparse>
+__device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm, int lane) {
     const Geometry& g = p.g;
     // the split tiles of one key block are neighbours in the walk, so they run
     // at the same time and share the block's K and V in L2
@@ -161,6 +195,26 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         f.s = 0;
         f.hq0 = f.h;
         f.nblk = f.m_end - f.m_begin;
+    }
+    f.mcol = nullptr;
+    if constexpr (kSparse) {
+        f.mstride = f.mhead = 0;
+        f.nheads = f.m_end > f.m_begin ? f.nblk / (f.m_end - f.m_begin) : 0;
+        if (p.mask.ptr) {   // keep the (head, query block) pairs the block mask keeps
+            f.mcol = p.mask.ptr + f.n;
+            f.mstride = mask_cols(g);
+            f.mhead = p.mask.heads == 1 ? 0 : (long)mask_rows(g) * mask_cols(g);
+            int kept = 0;
+            if (f.nheads > 0) {
+                if (f.mhead == 0) {
+                    kept = f.nheads * sparse_count_col(f.mcol, f.mstride, f.m_begin, f.m_end, lane);
+                } else {
+                    for (int x = 0; x < f.nheads; ++x)
+                        kept += sparse_count_col(f.mcol + (f.hq0 + x) * f.mhead, f.mstride, f.m_begin, f.m_end, lane);
+                }
+            }
+            f.nblk = kept;
+        }
     }
     return f;
 }
@@ -256,10 +310,12 @@ __global__ void bwd_convert(const float* __restrict__ acc, __nv_bfloat16* __rest
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
 // other path's code out of each kernel); kGQA: grouped heads (bwd_tile);
 // kBand: the mask is a local window other than the plain causal mask (a
-// left bound, or a right bound past the diagonal); the kernels for no mask
-// and the causal mask keep their closed forms (a key's query rows run from
-// its diagonal, or from 0, to the sequence's end)
-template <int HD, bool kDet, bool kGQA, bool kBand>
+// left bound, or a right bound past the diagonal) or has a block mask; the
+// kernels for no mask and the causal mask keep their closed forms (a key's
+// query rows run from its diagonal, or from 0, to the sequence's end).
+// kSparse (with kBand only): a block mask is given, the walks skip the blocks
+// it drops.
+template <int HD, bool kDet, bool kGQA, bool kBand, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -332,8 +388,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
-            if (f.m_begin >= f.m_end) continue;
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
             if (lane == 0) {
@@ -347,8 +403,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             __syncwarp();
             ++tile_it;
-            QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk && ok; ++u, qw.next<kGQA>(f)) {
+            QWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk && ok; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / NQS) & 1u) ^ 1u, w, lane);
@@ -437,8 +493,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
-            if (f.m_begin >= f.m_end) continue;
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
             if (!ok) break;
             ++tile_it;
@@ -544,7 +600,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
@@ -557,7 +613,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const long slot = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv * HD;
                 return p.dkv_part + (which ? f.s : p.split + f.s) * slot + kv_off();
             };
-            if (f.m_begin >= f.m_end) {   // no query sees this key block
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) {   // no query sees this key block
                 __nv_bfloat16* dv_ptr = p.dv + kv_off();
                 __nv_bfloat16* dk_ptr = p.dk + kv_off();
                 float* pk_ptr = partial ? part_slot(1) : nullptr;
@@ -588,8 +644,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 q_lo = g.causal ? key - (f.lk - f.lq) : 0;
                 q_hi = f.lq;
             }
-            QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
+            QWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 const uint32_t st = qc % NQS;
                 uint8_t* ds_tile = ds_tiles + (qc & 1u) * Lay::kDSBytes;   // alternate dS tiles per block
@@ -721,9 +777,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand>(t, p, vmp);
-            QWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            QWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
@@ -746,7 +802,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         int n_lo, n_hi;
                         band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
                                         kBN, &n_lo, &n_hi);
-                        if (sem_wait(sem, f.n - (kBand ? n_lo : 0), w)) fence_proxy_async_global();
+                        int before = f.n - (kBand ? n_lo : 0);   // key blocks that add to this tile before block n
+                        if (kSparse && f.mcol) {   // block-sparse: only the kept ones
+                            const unsigned char* row =
+                                p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
+                            before = 0;
+                            for (int x = n_lo; x < f.n; ++x) before += row[x] != 0;
+                        }
+                        if (sem_wait(sem, before, w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
                     }
                     ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
@@ -823,6 +886,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
 }
 
+// The instantiation for a mask: none or causal; a general band; a band with a block mask.
+template <int HD, bool kDet, bool kGQA>
+auto bwd_kernel_for(bool band, bool sparse) {
+    return sparse ? bwd_kernel<HD, kDet, kGQA, true, true>
+                  : (band ? bwd_kernel<HD, kDet, kGQA, true, false> : bwd_kernel<HD, kDet, kGQA, false, false>);
+}
+
 template <int HD>
 cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
@@ -850,12 +920,12 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
     } else {
         using Lay = BwdLayout<HD>;
-        const bool gqa = g.group > 1, band = g.win_left >= 0 || g.win_right > 0;
-        auto kern = p.deterministic
-                        ? (gqa ? (band ? bwd_kernel<HD, true, true, true> : bwd_kernel<HD, true, true, false>)
-                               : (band ? bwd_kernel<HD, true, false, true> : bwd_kernel<HD, true, false, false>))
-                        : (gqa ? (band ? bwd_kernel<HD, false, true, true> : bwd_kernel<HD, false, true, false>)
-                               : (band ? bwd_kernel<HD, false, false, true> : bwd_kernel<HD, false, false, false>));
+        const bool gqa = g.group > 1, sparse = p.mask.ptr != nullptr;
+        const bool band = sparse || g.win_left >= 0 || g.win_right > 0;
+        auto kern = p.deterministic ? (gqa ? bwd_kernel_for<HD, true, true>(band, sparse)
+                                           : bwd_kernel_for<HD, true, false>(band, sparse))
+                                    : (gqa ? bwd_kernel_for<HD, false, true>(band, sparse)
+                                           : bwd_kernel_for<HD, false, false>(band, sparse));
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;

@@ -88,6 +88,12 @@ struct WideBwdTile {
     int hq0;             // first query head the tile visits
     int nblk;            // query blocks the tile visits: (group / split) x (m_end - m_begin)
     int s;               // which of the key block's split tiles (0 when split == 1)
+    // block-sparse (block mask given): entry (query head h, query block m) of
+    // this key block's mask column is mcol[h * mhead + m * mstride] (mhead 0:
+    // one mask for all heads); nblk counts the kept pairs only
+    const unsigned char* mcol;
+    long mstride, mhead;
+    int nheads;          // query heads the tile visits
 };
 
 // The tile's query blocks in visiting order: every query head of the tile's
@@ -105,6 +111,34 @@ struct WideQWalk {
 };
 __device__ __forceinline__ WideQWalk qwalk(const WideBwdTile& f) { return WideQWalk{f.hq0, f.m_begin}; }
 
+// Block-sparse walk: from (qw.h, qw.m) on, the first pair the block mask keeps
+// (warp-wide scans: every lane of the warp calls it alike).
+__device__ __forceinline__ void sparse_seek(const WideBwdTile& f, WideQWalk& qw, int lane) {
+    while (qw.h < f.hq0 + f.nheads) {
+        qw.m = sparse_next_col(f.mcol + qw.h * f.mhead, f.mstride, qw.m, f.m_end, lane);
+        if (qw.m < f.m_end) return;
+        ++qw.h;
+        qw.m = f.m_begin;
+    }
+}
+
+// The first pair of the tile's walk, and the next one.
+template <bool kSparse>
+__device__ __forceinline__ WideQWalk qwalk_start(const WideBwdTile& f, int lane) {
+    WideQWalk qw = qwalk(f);
+    if (kSparse && f.mcol) sparse_seek(f, qw, lane);
+    return qw;
+}
+template <bool kGQA, bool kSparse>
+__device__ __forceinline__ void qwalk_step(WideQWalk& qw, const WideBwdTile& f, int lane) {
+    if (kSparse && f.mcol) {
+        ++qw.m;
+        sparse_seek(f, qw, lane);
+    } else {
+        qw.next<kGQA>(f);
+    }
+}
+
 
 // Tile t: key-block tile t/2 of the d <= 128 walk (split tiles included), chunk
 // t%2 (the two chunks of a key block run at the same time on neighbouring CTAs
@@ -112,9 +146,9 @@ __device__ __forceinline__ WideQWalk qwalk(const WideBwdTile& f) { return WideQW
 // kGQA: grouped heads, as in bwd.cu's bwd_tile
 __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
-// kBand: as in bwd.cu's bwd_tile
-template <bool kGQA, bool kBand>
-__device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm) {
+// kBand, kSparse: as in bwd.cu's bwd_tile
+template <bool kGQA, bool kBand, bool kSparse>
+__device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm, int lane) {
     const Geometry& g = p.g;
     const int sp = kGQA ? (t >> 1) % p.split : 0;
     const int u = kGQA ? (t >> 1) / p.split : t >> 1;
@@ -159,13 +193,33 @@ __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, 
         f.hq0 = f.h;
         f.nblk = f.m_end - f.m_begin;
     }
+    f.mcol = nullptr;
+    if constexpr (kSparse) {
+        f.mstride = f.mhead = 0;
+        f.nheads = f.m_end > f.m_begin ? f.nblk / (f.m_end - f.m_begin) : 0;
+        if (p.mask.ptr) {   // keep the (head, query block) pairs the block mask keeps
+            f.mcol = p.mask.ptr + f.n;
+            f.mstride = mask_cols(g);
+            f.mhead = p.mask.heads == 1 ? 0 : (long)mask_rows(g) * mask_cols(g);
+            int kept = 0;
+            if (f.nheads > 0) {
+                if (f.mhead == 0) {
+                    kept = f.nheads * sparse_count_col(f.mcol, f.mstride, f.m_begin, f.m_end, lane);
+                } else {
+                    for (int x = 0; x < f.nheads; ++x)
+                        kept += sparse_count_col(f.mcol + (f.hq0 + x) * f.mhead, f.mstride, f.m_begin, f.m_end, lane);
+                }
+            }
+            f.nblk = kept;
+        }
+    }
     return f;
 }
 
 // kDet: deterministic dQ accumulation (a separate instantiation keeps the
 // other path's code out of each kernel); kGQA: grouped heads; kBand: the mask
 // has a left bound (as in bwd.cu)
-template <int HD, int DV, bool kDet, bool kGQA, bool kBand>
+template <int HD, int DV, bool kDet, bool kGQA, bool kBand, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -237,8 +291,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
-            if (f.m_begin >= f.m_end) continue;
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
             if (lane == 0) {
@@ -253,8 +307,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             ++tile_it;
             const int pc = f.c, po = 1 - f.c;
-            WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk && ok; ++u, qw.next<kGQA>(f)) {
+            WideQWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk && ok; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 for (int item = 0; item < kItemsPerBlock; ++item) {
                     const uint32_t slot = ic % NS;
@@ -370,8 +424,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
-            if (f.m_begin >= f.m_end) continue;
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             const int pc = f.c, po = 1 - f.c;
             const bool narrow = chunk_width<HD>(f.c) == 64;
             const uint32_t id_kv = narrow ? kIdKV64 : kIdKV128;
@@ -490,7 +544,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
             const int cw = chunk_width<HD>(f.c);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
@@ -510,7 +564,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const long rows = (varlen ? (long)g.Lk : (long)g.B * g.Lk) * g.Hkv;
                 return p.dkv_part + (which ? f.s * rows * HD : (p.split * HD + f.s * DV) * rows) + kv_off(which);
             };
-            if (f.m_begin >= f.m_end) {   // no query sees this key block
+            if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) {   // no query sees this key block
                 if (key_ok) {
                     for (int which = 0; which < 2; ++which) {
                         const int cols = (which ? cw : cwv) / 2;
@@ -535,8 +589,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 q_lo = g.causal ? key - (f.lk - f.lq) : 0;
                 q_hi = f.lq;
             }
-            WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
+            WideQWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kSFull), sc & 1u, w, lane);
                 if (!ok) break;
@@ -666,11 +720,11 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand>(t, p, vmp);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
             const int cw = chunk_width<HD>(f.c);
             const int rounds = cw / 64;
-            WideQWalk qw = qwalk(f);
-            for (int u = 0; u < f.nblk; ++u, qw.next<kGQA>(f)) {
+            WideQWalk qw = qwalk_start<kSparse>(f, lane);
+            for (int u = 0; u < f.nblk; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
                 ok = warp_wait(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
@@ -692,7 +746,14 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         int n_lo, n_hi;
                         band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
                                         kBN, &n_lo, &n_hi);
-                        if (sem_wait(sem, f.n - (kBand ? n_lo : 0), w)) fence_proxy_async_global();
+                        int before = f.n - (kBand ? n_lo : 0);   // key blocks that add to this tile before block n
+                        if (kSparse && f.mcol) {   // block-sparse: only the kept ones
+                            const unsigned char* row =
+                                p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
+                            before = 0;
+                            for (int x = n_lo; x < f.n; ++x) before += row[x] != 0;
+                        }
+                        if (sem_wait(sem, before, w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));
                     }
                     ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
@@ -765,19 +826,25 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
+// The instantiation for a mask: none or causal; a general band; a band with a block mask.
+template <int HD, int DV, bool kDet, bool kGQA>
+auto wide_kernel_for(bool band, bool sparse) {
+    return sparse ? bwd_wide_kernel<HD, DV, kDet, kGQA, true, true>
+                  : (band ? bwd_wide_kernel<HD, DV, kDet, kGQA, true, false>
+                          : bwd_wide_kernel<HD, DV, kDet, kGQA, false, false>);
+}
+
 template <int HD, int DV>
 cudaError_t launch_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, const VarlenMap* vm,
                            int num_sms, cudaStream_t stream) {
     using Lay = WideBwdLayout<HD, DV>;
-    const bool gqa = p.g.group > 1, band = p.g.win_left >= 0 || p.g.win_right > 0;
-    auto kern =
-        p.deterministic
-            ? (gqa ? (band ? bwd_wide_kernel<HD, DV, true, true, true> : bwd_wide_kernel<HD, DV, true, true, false>)
-                   : (band ? bwd_wide_kernel<HD, DV, true, false, true> : bwd_wide_kernel<HD, DV, true, false, false>))
-            : (gqa ? (band ? bwd_wide_kernel<HD, DV, false, true, true> : bwd_wide_kernel<HD, DV, false, true, false>)
-                   : (band ? bwd_wide_kernel<HD, DV, false, false, true>
-                           : bwd_wide_kernel<HD, DV, false, false, false>));
+    const bool gqa = p.g.group > 1, sparse = p.mask.ptr != nullptr;
+    const bool band = sparse || p.g.win_left >= 0 || p.g.win_right > 0;
+    auto kern = p.deterministic ? (gqa ? wide_kernel_for<HD, DV, true, true>(band, sparse)
+                                       : wide_kernel_for<HD, DV, true, false>(band, sparse))
+                                : (gqa ? wide_kernel_for<HD, DV, false, true>(band, sparse)
+                                       : wide_kernel_for<HD, DV, false, false>(band, sparse));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

@@ -118,14 +118,24 @@ struct FwdTile {
     // differ by at most a block at either end (the causal diagonal, a local
     // window's left edge); n_kv0 = 0 when none of tile 0's rows sees a key.
     int kv_first, n_kv, n_kv0, kv_start1;
+    // block-sparse (block mask given): the stream is the blocks in
+    // [kv_first, kb_end) active in either Q tile's mask row (mrow1 null: tile
+    // 1 has no row block); both Q tiles walk all of it (n_kv0 = n_kv,
+    // kv_start1 = 0) and mask the blocks their own row drops
+    const unsigned char* mrow0;
+    const unsigned char* mrow1;
+    int kb_end;
 };
 
-// kLeft: the mask has a left bound (a local window). Without one every row's
-// keys start at key 0, so the kernels instantiated with kLeft = false keep the
-// stream start, Q tile 1's first block and the rows' lower column bound at the
-// constant 0 (fewer live registers in the softmax loop).
-template <bool kLeft>
-__device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
+// kGeneral: the mask has a left bound (a local window) or a block mask.
+// Without either every row's keys start at key 0 and every block in range is
+// visited, so the kernels instantiated with kGeneral = false keep the stream
+// start, Q tile 1's first block and the rows' lower column bound at the
+// constant 0 and contain no mask scans (fewer live registers in the softmax
+// loop). kSparse (with kGeneral only): a block mask is given. lane: the
+// calling warp's lane (the block-mask scans are warp-wide).
+template <bool kGeneral, bool kSparse>
+__device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen, int lane) {
     const Geometry& g = p.g;
     Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kRowsPerTile, p.head_section, g.causal != 0, false)
                      : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, true) : sched_dense(t, g.H, p.nm, p.head_section, false));
@@ -157,14 +167,26 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
     }
     // (tile 1's rows follow tile 0's, so with both present l0 <= l1 and h0 <= h1;
     // tile 1 sees no key only if tile 0 sees none either)
-    f.kv_first = kLeft ? (has0 ? l0 : l1) : 0;
+    f.kv_first = kGeneral ? (has0 ? l0 : l1) : 0;
     f.n_kv = has1 ? h1 - f.kv_first : 0;
     f.n_kv0 = has0 ? h0 - f.kv_first : 0;
-    f.kv_start1 = kLeft && has1 ? l1 - f.kv_first : 0;
+    f.kv_start1 = kGeneral && has1 ? l1 - f.kv_first : 0;
+    f.mrow0 = f.mrow1 = nullptr;
+    f.kb_end = f.kv_first + f.n_kv;
+    if constexpr (kSparse) {
+        if (p.mask.ptr) {
+            const int mh = p.mask.heads == 1 ? 0 : ti.h, qb = 2 * ti.m;
+            f.mrow0 = p.mask.ptr + ((long)mh * mask_rows(g) + qb) * mask_cols(g);
+            f.mrow1 = qb + 1 < mask_rows(g) ? f.mrow0 + mask_cols(g) : nullptr;
+            f.n_kv = f.n_kv > 0 ? sparse_count(f.mrow0, f.mrow1, f.kv_first, f.kb_end, lane) : 0;
+            f.n_kv0 = f.n_kv;
+            f.kv_start1 = 0;
+        }
+    }
     return f;
 }
 
-template <int HD, bool kLeft>
+template <int HD, bool kGeneral, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -225,7 +247,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t kv_cnt = 0, it = 0, q_issued = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kGeneral, kSparse>(t, p, vm, varlen, lane);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQEmpty), (it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -238,6 +260,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             __syncwarp();
             ++q_issued;
+            const bool sparse = kSparse && f.mrow0 != nullptr;
+            int kb = kGeneral ? f.kv_first : 0;   // key block of stream block j
+            if (sparse) kb = sparse_next(f.mrow0, f.mrow1, kb, f.kb_end, lane);
             for (int j = 0; j < f.n_kv && ok; ++j) {
                 for (int kv = 0; kv < 2; ++kv) {
                     const uint32_t slot = kv_cnt % S, ph = (kv_cnt / S) & 1u;
@@ -248,11 +273,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         for (int hf = 0; hf < Lay::kHalves; ++hf)
                             tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox,
                                         kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.hk,
-                                        f.k_row0 + ((kLeft ? f.kv_first : 0) + j) * kBN);
+                                        f.k_row0 + (kGeneral ? kb : j) * kBN);
                     }
                     __syncwarp();
                     ++kv_cnt;
                 }
+                if constexpr (kGeneral) kb = sparse ? sparse_next(f.mrow0, f.mrow1, kb + 1, f.kb_end, lane) : kb + 1;
             }
             ++it;
         }
@@ -299,9 +325,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t kv_cnt = 0, it = 0, pc0 = 0, pc1 = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kGeneral, kSparse>(t, p, vm, varlen, lane);
             if (f.n_kv == 0) continue;
-            const int n0 = f.n_kv0, s1 = kLeft ? f.kv_start1 : 0;   // Q tile 0: [0, n0), Q tile 1: [s1, n_kv)
+            const int n0 = f.n_kv0, s1 = kGeneral ? f.kv_start1 : 0;   // Q tile 0: [0, n0), Q tile 1: [s1, n_kv)
             ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
             if (!ok) break;
             uint32_t slot_k = kv_cnt % S;
@@ -399,14 +425,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const FwdTile f = fwd_tile<kLeft>(t, p, vm, varlen);
+            const FwdTile f = fwd_tile<kGeneral, kSparse>(t, p, vm, varlen, lane);
             const int r = f.mp * kRowsPerTile + tq * kBM + row_in_tile;   // row inside the sequence
             const bool valid = r < f.lq;
             const long prow = (long)f.q_row0 + tq * kBM + row_in_tile;   // packed row
             __nv_bfloat16* optr = p.o + (prow * g.H + f.h) * HD;
             float* lptr = varlen ? p.lse + (long)f.h * g.Lq + prow
                                  : p.lse + ((long)f.b * g.H + f.h) * g.Lq + r;
-            const int jb = kLeft && tq ? f.kv_start1 : 0, nkv = tq ? f.n_kv : f.n_kv0;   // stream blocks [jb, nkv)
+            const int jb = kGeneral && tq ? f.kv_start1 : 0, nkv = tq ? f.n_kv : f.n_kv0;   // stream blocks [jb, nkv)
             if (nkv == 0) {
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(optr);
@@ -417,7 +443,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 continue;
             }
             const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
-            const int col_lo = kLeft ? band_key_lo(mb, r) : 0, col_limit = band_key_hi(mb, r);   // keys [col_lo, col_limit)
+            const int col_lo = kGeneral ? band_key_lo(mb, r) : 0, col_limit = band_key_hi(mb, r);   // keys [col_lo, col_limit)
+            // block-sparse: this Q tile's mask row (null: its row block is past the mask, no row is stored)
+            const bool sparse = kSparse && f.mrow0 != nullptr;
+            const unsigned char* mrow = tq ? f.mrow1 : f.mrow0;
+            int kb = (kGeneral ? f.kv_first : 0) + jb;   // key block of stream block j
+            if (sparse) kb = sparse_next(f.mrow0, f.mrow1, f.kv_first, f.kb_end, lane);
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = jb; j < nkv; ++j) {
                 ok = warp_wait(bar(Lay::kSFull + tq), sc & 1u, w, lane);
@@ -431,12 +462,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) s[i] = u2f(r128[i]);
                 }
-                const int c0 = ((kLeft ? f.kv_first : 0) + j) * kBN;
-                if (c0 + kBN > col_limit || c0 < col_lo) {
+                const int c0 = (kGeneral ? kb : j) * kBN;
+                const bool dropped = sparse && (mrow == nullptr || mrow[kb] == 0);   // the block mask drops it here
+                if (dropped || c0 + kBN > col_limit || c0 < col_lo) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (c0 + c >= col_limit || c0 + c < col_lo) s[c] = -INFINITY;
+                        if (dropped || c0 + c >= col_limit || c0 + c < col_lo) s[c] = -INFINITY;
                 }
+                if constexpr (kGeneral) kb = sparse ? sparse_next(f.mrow0, f.mrow1, kb + 1, f.kb_end, lane) : kb + 1;
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
                 for (int c = 4; c < kBN; c += 4) {
@@ -511,7 +544,8 @@ template <int HD>
 cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, int num_sms, cudaStream_t stream) {
     using Lay = FwdLayout<HD>;
-    auto kern = p.g.win_left >= 0 ? fwd_kernel<HD, true> : fwd_kernel<HD, false>;
+    auto kern = p.mask.ptr ? fwd_kernel<HD, true, true>
+                           : (p.g.win_left >= 0 ? fwd_kernel<HD, true, false> : fwd_kernel<HD, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;

@@ -64,9 +64,15 @@ struct WideTile {
     int q_row0;      // packed row of the tile's first query row
     int k_row0;
     int kv_first, n_kv;   // K/V blocks kv_first .. kv_first + n_kv - 1 (n_kv = 0: no row sees a key)
+    // block-sparse (block mask given): the n_kv blocks in [kv_first, kb_end)
+    // that the tile's mask row keeps
+    const unsigned char* mrow;
+    int kb_end;
 };
 
-__device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen) {
+// kSparse: a block mask may be given (the kernels without one contain no mask scans)
+template <bool kSparse>
+__device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const VarlenMap& vm, bool varlen, int lane) {
     const Geometry& g = p.g;
     Tile ti = varlen ? sched_varlen(vm, t, g.B, g.H, kBM, p.head_section, g.causal != 0, false)
                      : (g.causal ? sched_dense_lpt(t, g.B, g.H, p.nm, true)
@@ -92,10 +98,19 @@ __device__ __forceinline__ WideTile wide_tile(int t, const FwdParams& p, const V
     band_key_blocks(mb, ti.m * kBM, ti.m * kBM + kBM - 1, kBN, &jlo, &jhi);
     f.kv_first = jlo;
     f.n_kv = jhi - jlo;
+    f.kb_end = jhi;
+    f.mrow = nullptr;
+    if constexpr (kSparse) {
+        if (p.mask.ptr) {
+            const int mh = p.mask.heads == 1 ? 0 : ti.h;
+            f.mrow = p.mask.ptr + ((long)mh * mask_rows(g) + ti.m) * mask_cols(g);
+            f.n_kv = f.n_kv > 0 ? sparse_count(f.mrow, nullptr, jlo, jhi, lane) : 0;
+        }
+    }
     return f;
 }
 
-template <int HD, int DV>
+template <int HD, int DV, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -154,8 +169,8 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ TMA producer
         uint32_t kv_cnt = 0, it = 0, q_issued = 0;
         bool ok = true;
-        // one tile of K (kv = 0) or V (kv = 1), block j, into the next ring slot
-        auto load_kv = [&](const WideTile& f, int kv, int j) -> bool {
+        // one tile of K (kv = 0) or V (kv = 1) of key block kb, into the next ring slot
+        auto load_kv = [&](const WideTile& f, int kv, int kb) -> bool {
             const uint32_t slot = kv_cnt % S, ph = (kv_cnt / S) & 1u;
             if (!warp_wait(bar(Lay::kKVEmpty + slot), ph ^ 1u, w, lane)) return false;
             if (lane == 0) {
@@ -163,14 +178,14 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_expect_tx(bar(Lay::kKVFull + slot), boxes * kBox);
                 for (int hf = 0; hf < boxes; ++hf)
                     tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox, kv ? &tmV : &tmK,
-                                bar(Lay::kKVFull + slot), hf * 64, f.hk, f.k_row0 + (f.kv_first + j) * kBN);
+                                bar(Lay::kKVFull + slot), hf * 64, f.hk, f.k_row0 + kb * kBN);
             }
             __syncwarp();
             ++kv_cnt;
             return true;
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideTile f = wide_tile(t, p, vm, varlen);
+            const WideTile f = wide_tile<kSparse>(t, p, vm, varlen, lane);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQEmpty), (it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -181,11 +196,24 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             __syncwarp();
             ++q_issued;
-            // consumption order: K0, K1, then V_j, K_{j+2} for each block j
-            ok = load_kv(f, 0, 0) && (f.n_kv < 2 || load_kv(f, 0, 1));
+            // consumption order: K0, K1, then V_j, K_{j+2} for each block j; the K and
+            // V cursors walk the tile's key blocks (block-sparse: the kept ones)
+            const bool sparse = kSparse && f.mrow != nullptr;
+            auto kept = [&](int kb) { return sparse ? sparse_next(f.mrow, nullptr, kb, f.kb_end, lane) : kb; };
+            int kb_k = kept(f.kv_first), kb_v = kb_k;
+            ok = load_kv(f, 0, kb_k);
+            kb_k = kept(kb_k + 1);
+            if (ok && f.n_kv >= 2) {
+                ok = load_kv(f, 0, kb_k);
+                kb_k = kept(kb_k + 1);
+            }
             for (int j = 0; j < f.n_kv && ok; ++j) {
-                ok = load_kv(f, 1, j);
-                if (ok && j + 2 < f.n_kv) ok = load_kv(f, 0, j + 2);
+                ok = load_kv(f, 1, kb_v);
+                kb_v = kept(kb_v + 1);
+                if (ok && j + 2 < f.n_kv) {
+                    ok = load_kv(f, 0, kb_k);
+                    kb_k = kept(kb_k + 1);
+                }
             }
             ++it;
         }
@@ -226,7 +254,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_commit(bar(Lay::kKVEmpty + slot));
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideTile f = wide_tile(t, p, vm, varlen);
+            const WideTile f = wide_tile<kSparse>(t, p, vm, varlen, lane);
             if (f.n_kv == 0) continue;
             ok = warp_wait(bar(Lay::kQFull), it & 1u, w, lane);
             if (!ok) break;
@@ -298,7 +326,7 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideTile f = wide_tile(t, p, vm, varlen);
+            const WideTile f = wide_tile<kSparse>(t, p, vm, varlen, lane);
             const int r = f.m * kBM + row_in_tile;
             const bool valid = r < f.lq;
             const long prow = (long)f.q_row0 + row_in_tile;
@@ -315,6 +343,8 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             const MaskBand mb = mask_band(f.lq, f.lk, g.win_left, g.win_right);
             const int col_lo = band_key_lo(mb, r), col_limit = band_key_hi(mb, r);   // keys [col_lo, col_limit)
+            const bool sparse = kSparse && f.mrow != nullptr;
+            int kb = sparse ? sparse_next(f.mrow, nullptr, f.kv_first, f.kb_end, lane) : f.kv_first;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < f.n_kv; ++j) {
                 const int buf = j & 1;
@@ -330,7 +360,8 @@ fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) s[i] = u2f(r128[i]);
                 }
-                const int c0 = (f.kv_first + j) * kBN;
+                const int c0 = kb * kBN;
+                kb = sparse ? sparse_next(f.mrow, nullptr, kb + 1, f.kb_end, lane) : kb + 1;
                 if (c0 + kBN > col_limit || c0 < col_lo) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
@@ -425,7 +456,7 @@ template <int HD, int DV>
 cudaError_t launch_fwd_wide_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const FwdParams& p, int num_sms, cudaStream_t stream) {
     using Lay = WideLayout<HD, DV>;
-    auto kern = fwd_wide_kernel<HD, DV>;
+    auto kern = p.mask.ptr ? fwd_wide_kernel<HD, DV, true> : fwd_wide_kernel<HD, DV, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.g.cu_seqlens ? num_sms : min(p.n_tiles, num_sms);

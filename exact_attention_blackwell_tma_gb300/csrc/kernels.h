@@ -19,26 +19,40 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct Geometry {
     int B, H, Lq, Lk, d;      // dense: sizes; varlen: Lq, Lk = packed query and key rows
     int Hkv, group;           // key/value heads, query heads per key/value head
-    const int* cu_seqlens;    // device, B+1 query offsets, or null (dense)
-    const int* cu_seqlens_k;  // device, B+1 key offsets (varlen; cu_seqlens when they are shared)
     int causal;               // the mask has a right bound (win_right >= 0): longest-first walks
     int win_left, win_right;  // mask band (mask.cuh): keys i + delta - win_left .. i + delta + win_right
                               // of query i, -1: no bound on that side; causal is win_right = 0
     float scale;              // softmax scale (> 0)
     float scale_log2;         // scale * log2(e)
+    const int* cu_seqlens;    // device, B+1 query offsets, or null (dense)
+    const int* cu_seqlens_k;  // device, B+1 key offsets (varlen; cu_seqlens when they are shared)
 };
 
+// A block mask (dense problems): bytes [heads][ceil(Lq/128)][ceil(Lk/128)],
+// heads 1 (shared) or H; a zero byte drops that 128 x 128 block (mask.cuh).
+// ptr null: none.
+struct BlockMask {
+    const unsigned char* ptr;
+    int heads;
+};
+__host__ __device__ inline int mask_rows(const Geometry& g) { return (g.Lq + 127) / 128; }
+__host__ __device__ inline int mask_cols(const Geometry& g) { return (g.Lk + 127) / 128; }
+
+// The fields are ordered to leave no padding: with more than 128 bytes of
+// parameters the forward kernel's register allocation spilled more.
 struct FwdParams {
     Geometry g;
     __nv_bfloat16* o;         // rows and heads of q, head dim dv
-    int dv;                   // head dim of v and o (g.d for q and k)
     float* lse;               // dense [B, H, Lq]; varlen [H, T]
+    int* status;
+    uint64_t wait_budget_ns;
+    int dv;                   // head dim of v and o (g.d for q and k)
     int n_tiles;              // dense: exact count; varlen: computed on device
     int nm;                   // dense: query blocks per (b, h): 256 rows (d <= 128) or 128 rows
     int head_section;         // heads per L2 section (LPT walk)
-    int* status;
-    uint64_t wait_budget_ns;
+    BlockMask mask;
 };
+static_assert(sizeof(FwdParams) <= 128, "forward parameters");
 
 struct BwdParams {
     Geometry g;
@@ -62,6 +76,7 @@ struct BwdParams {
     int head_section;
     int* status;
     uint64_t wait_budget_ns;
+    BlockMask mask;
 };
 
 // Semaphores of the deterministic backward: two per dQ tile (one per dQ column

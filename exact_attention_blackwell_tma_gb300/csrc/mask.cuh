@@ -73,3 +73,57 @@ __host__ __device__ __forceinline__ bool band_query_blocks(const MaskBand& m, in
     *mhi = (hi + bm - 1) / bm;
     return true;
 }
+
+// ---------------------------------------------------------------------------
+// Block masks (dense problems): a byte per (query block, key block) of 128 x
+// 128, block_mask[mask_head][qb][kb] != 0 keeps the block (FlashAttention-4
+// paper, Section 4: block-sparse patterns are one of the composable
+// primitives). The scans below are warp-cooperative: every lane of the calling
+// warp must call them with the same arguments, and every lane gets the result.
+#ifdef __CUDACC__
+// The first block kb' in [kb, hi) with row0[kb'] or row1[kb'] nonzero (row1
+// may be null), or hi.
+__device__ __forceinline__ int sparse_next(const unsigned char* row0, const unsigned char* row1, int kb, int hi,
+                                           int lane) {
+    for (int base = kb; base < hi; base += 32) {
+        const int c = base + lane;
+        const bool a = c < hi && (row0[c] | (row1 ? row1[c] : 0));
+        const unsigned m = __ballot_sync(0xffffffffu, a);
+        if (m) return base + __ffs(m) - 1;
+    }
+    return hi;
+}
+
+// Number of blocks kb' in [lo, hi) with row0[kb'] or row1[kb'] nonzero.
+__device__ __forceinline__ int sparse_count(const unsigned char* row0, const unsigned char* row1, int lo, int hi,
+                                            int lane) {
+    int n = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int c = base + lane;
+        const bool a = c < hi && (row0[c] | (row1 ? row1[c] : 0));
+        n += __popc(__ballot_sync(0xffffffffu, a));
+    }
+    return n;
+}
+
+// Column scans (the backward's query blocks of one key block): entries
+// col[m * stride] for m in [m, hi).
+__device__ __forceinline__ int sparse_next_col(const unsigned char* col, long stride, int m, int hi, int lane) {
+    for (int base = m; base < hi; base += 32) {
+        const int r = base + lane;
+        const bool a = r < hi && col[(long)r * stride];
+        const unsigned msk = __ballot_sync(0xffffffffu, a);
+        if (msk) return base + __ffs(msk) - 1;
+    }
+    return hi;
+}
+
+__device__ __forceinline__ int sparse_count_col(const unsigned char* col, long stride, int lo, int hi, int lane) {
+    int n = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int r = base + lane;
+        n += __popc(__ballot_sync(0xffffffffu, r < hi && col[(long)r * stride]));
+    }
+    return n;
+}
+#endif

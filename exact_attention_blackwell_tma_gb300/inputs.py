@@ -47,6 +47,7 @@ class Workload:
     hkv: Optional[int] = None         # key/value heads (grouped heads); None: H
     lengths_k: Optional[tuple] = None # varlen: per-sequence key lengths; None: the query lengths
     window: tuple = (-1, -1)          # local window (left, right); -1: open side
+    block_pattern: Optional[tuple] = None   # ("local_strided", local, stride): block mask pattern
 
     @property
     def scale(self) -> float:
@@ -95,6 +96,8 @@ class Workload:
             return int((hi - lo).clamp(min=0).sum())
         if self.varlen:
             return self.H * sum(per_seq(a, b) for a, b in zip(self.lengths, self.keys))
+        if self.block_pattern is not None:
+            return self.B * self.H * _pairs_in_blocks(block_mask(self)[0], self.L, self.L, wl, wr)
         return self.B * self.H * per_seq(self.L, self.L)
 
     def fwd_flops(self) -> int:
@@ -108,6 +111,30 @@ class Workload:
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
+
+
+def block_mask(w: Workload):
+    """The workload's block mask, uint8 [1, ceil(L/128), ceil(L/128)], from its
+    pattern: ("local_strided", a, s) keeps, for query block q, key blocks
+    q-a+1 .. q and every key block k with k % s == s - 1."""
+    kind, a, st = w.block_pattern
+    assert kind == "local_strided"
+    n = -(-w.L // 128)
+    qb = torch.arange(n)[:, None]
+    kb = torch.arange(n)[None, :]
+    keep = ((qb - kb >= 0) & (qb - kb < a)) | (kb % st == st - 1)
+    return keep.to(torch.uint8)[None]
+
+
+def _pairs_in_blocks(mask2d, lq, lk, wl, wr) -> int:
+    """Pairs a block mask keeps inside the band (for the FLOP count)."""
+    i = torch.arange(lq, dtype=torch.int64)
+    lo = (i + (lk - lq) - wl).clamp(min=0) if wl >= 0 else torch.zeros_like(i)
+    hi = (i + (lk - lq) + wr + 1).clamp(max=lk) if wr >= 0 else torch.full_like(i, lk)
+    rows = mask2d[(i // 128)].to(torch.bool)                        # [lq, nkb]
+    k0 = torch.arange(mask2d.shape[1], dtype=torch.int64)[None, :] * 128
+    cnt = (torch.minimum(hi[:, None], (k0 + 128).clamp(max=lk)) - torch.maximum(lo[:, None], k0)).clamp(min=0)
+    return int((cnt * rows).sum())
 
 
 def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:

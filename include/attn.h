@@ -42,6 +42,12 @@
  *          with no key left gets O = 0, LSE = -inf. The causal mask is the
  *          band (-1, 0). (FlashAttention-4 paper, Section 4: masking
  *          strategies compose with varlen and scheduling.)
+ *   block mask (attn_fwd_ex, attn_bwd_ex; dense problems only): a DEVICE
+ *          byte array [mask_heads][ceil(Lq/128)][ceil(Lk/128)], mask_heads 1
+ *          (one mask for every head) or H (query head h uses its own); a zero
+ *          byte drops all pairs of that 128-query x 128-key block, on top of
+ *          the causal or window mask (FlashAttention-4 paper, Section 4:
+ *          block-sparse patterns). Work tiles skip dropped blocks.
  *   grouped heads (attn_fwd_gqa, attn_bwd_gqa): k, v, dk, dv have Hkv heads
  *          instead of H ([B, Lk, Hkv, d] or [T, Hkv, d]); H must be a
  *          multiple of Hkv, and query head h reads key/value head
@@ -157,17 +163,18 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
  * The general forward: every entry point above is this one with some
  * arguments fixed. Hkv key/value heads (grouped heads), a head dim d_v of
  * its own for v and o (d_v = d, or d = 192 with d_v = 128), a local window
- * (window_left, window_right; -1, -1 for none; see above), and either
+ * (window_left, window_right; -1, -1 for none; see above), a block mask
+ * (block_mask, mask_heads; NULL for none; see above), and either
  * dense tensors (cu_seqlens_q == NULL, cu_seqlens_k == NULL), packed
  * sequences with one offset array (cu_seqlens_k == NULL: Lq = Lk = T), or
  * packed sequences with key offsets of their own (Lq = Tq, Lk = Tk).
- * cu_seqlens_k without cu_seqlens_q, or a window bound below -1, returns
- * ATTN_ERR_ARG. The work tiles visit only the key blocks their rows' band
+ * cu_seqlens_k without cu_seqlens_q, a window bound below -1, or a block
+ * mask with offsets or mask_heads not 1 or H, returns ATTN_ERR_ARG. The work tiles visit only the key blocks their rows' band
  * reaches.
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
-                int window_left, int window_right,
+                int window_left, int window_right, const unsigned char* block_mask, int mask_heads,
                 const int* cu_seqlens_q, const int* cu_seqlens_k, cudaStream_t stream);
 
 /*
@@ -186,7 +193,7 @@ size_t attn_bwd_ex_workspace_size(int B, int H, int Hkv, int Lq, int Lk, int d, 
 int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 const void* dout, void* dq, void* dk, void* dv,
                 int B, int H, int Hkv, int Lq, int Lk, int d, int d_v, float scale, int causal,
-                int window_left, int window_right,
+                int window_left, int window_right, const unsigned char* block_mask, int mask_heads,
                 const int* cu_seqlens_q, const int* cu_seqlens_k, int deterministic,
                 void* workspace, size_t ws_bytes, cudaStream_t stream);
 

@@ -96,6 +96,14 @@ def test_argument_errors_need_no_gpu(built):
     assert lib.attn_fwd_gqa(dummy, dummy, dummy, dummy, dummy, 1, 2, 4, 128, 128, 128, 128, 0.1, 0, None,
                             None) == -1
     assert lib.attn_bwd_gqa(*([dummy] * 9), 1, 8, 3, 128, 128, 64, 0.1, 0, None, 0, dummy, 1 << 30, None) == -1
+    # block masks: dense problems only, one mask or one per query head
+    assert lib.attn_fwd_ex(dummy, dummy, dummy, dummy, dummy, 2, 4, 4, 256, 256, 64, 64, 0.1, 1, -1, -1, dummy, 1,
+                           dummy, None, None) == -1
+    assert "dense" in binding.last_error()
+    assert lib.attn_fwd_ex(dummy, dummy, dummy, dummy, dummy, 1, 4, 4, 256, 256, 64, 64, 0.1, 1, -1, -1, dummy, 3,
+                           None, None, None) == -1
+    assert lib.attn_fwd_ex(dummy, dummy, dummy, dummy, dummy, 1, 4, 4, 256, 256, 64, 64, 0.1, 1, -2, -1, None, 1,
+                           None, None, None) == -1
     # backward: workspace too small
     ws = lib.attn_bwd_workspace_size(1, 1, 128, 128, 64, 0, 0)
     assert ws > 0
