@@ -146,7 +146,12 @@ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b :
 // kGQA: grouped heads (the kernels for one query head per key/value head are
 // instantiated without the group walk and the split, which keeps their code
 // and registers as small as before grouped heads existed)
-template <bool kGQA, bool kBand, bool kSparse>
+// kSpt (the deterministic kernels): with a right mask bound, key blocks are
+// walked shortest first -- the last key block of a (batch, head) first -- so
+// that, with each dQ tile's contributions serialised from its highest key
+// block down, no work tile waits at its first dQ write (FlashAttention-4
+// paper, Section 3.2.4, SPT order).
+template <bool kGQA, bool kBand, bool kSparse, bool kSpt>
 __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const VarlenMap* vm, int lane) {
     const Geometry& g = p.g;
     // the split tiles of one key block are neighbours in the walk, so they run
@@ -156,8 +161,9 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
         sp = t % p.split;
         t /= p.split;
     }
-    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, false, true)
-                 : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, false)
+    const bool spt = kSpt && g.causal;
+    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, spt, true)
+                 : (g.causal ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, spt)
                              : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
     BwdTile f;
     f.b = ti.b;
@@ -388,7 +394,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -493,7 +499,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVFull), tile_it & 1u, w, lane);
             if (!ok) break;
@@ -600,7 +606,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
             const long krow = (long)f.k_row0 + key;
@@ -777,7 +783,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const BwdTile f = bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const BwdTile f = bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             QWalk qw = qwalk_start<kSparse>(f, lane);
             for (int u = 0; u < f.nblk; ++u, qwalk_step<kGQA, kSparse>(qw, f, lane)) {
                 const int m = qw.m;
@@ -791,10 +797,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 tc_fence_after_sync();
                 int* sem = nullptr;
                 if constexpr (kDet) {
-                    // dQ tile (b, h, m) takes its key blocks' contributions in ascending
-                    // block order. The key blocks that see query block m form one range
-                    // n_lo .. (the mask band), so block n waits until the n - n_lo blocks
-                    // before it have added theirs.
+                    // dQ tile (b, h, m) takes its key blocks' contributions in a fixed order:
+                    // from the highest key block down with a right mask bound (SPT), else
+                    // ascending. The key blocks that see query block m form one range
+                    // [n_lo, n_hi) (the mask band), so block n waits until the blocks before
+                    // it in that order have added theirs.
                     const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
                                              : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + tile;
@@ -802,12 +809,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         int n_lo, n_hi;
                         band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
                                         kBN, &n_lo, &n_hi);
-                        int before = f.n - (kBand ? n_lo : 0);   // key blocks that add to this tile before block n
+                        // key blocks that add to this tile before block n: those below it, or with
+                        // a right mask bound (SPT order) those above it up to n_hi - 1
+                        const bool spt = g.causal != 0;
+                        int before = spt ? n_hi - 1 - f.n : f.n - (kBand ? n_lo : 0);
                         if (kSparse && f.mcol) {   // block-sparse: only the kept ones
                             const unsigned char* row =
                                 p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
                             before = 0;
-                            for (int x = n_lo; x < f.n; ++x) before += row[x] != 0;
+                            for (int x = spt ? f.n + 1 : n_lo; x < (spt ? n_hi : f.n); ++x) before += row[x] != 0;
                         }
                         if (sem_wait(sem, before, w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells

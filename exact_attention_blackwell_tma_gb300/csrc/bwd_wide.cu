@@ -147,13 +147,19 @@ __device__ __forceinline__ void qwalk_step(WideQWalk& qw, const WideBwdTile& f, 
 __device__ __forceinline__ int floor_div_w(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // kBand, kSparse: as in bwd.cu's bwd_tile
-template <bool kGQA, bool kBand, bool kSparse>
+// kSpt (the deterministic kernels): with a right mask bound, key blocks are
+// walked shortest first -- the last key block of a (batch, head) first -- so
+// that, with each dQ tile's contributions serialised from its highest key
+// block down, no work tile waits at its first dQ write (FlashAttention-4
+// paper, Section 3.2.4, SPT order).
+template <bool kGQA, bool kBand, bool kSparse, bool kSpt>
 __device__ __forceinline__ WideBwdTile wide_bwd_tile(int t, const BwdParams& p, const VarlenMap* vm, int lane) {
     const Geometry& g = p.g;
     const int sp = kGQA ? (t >> 1) % p.split : 0;
     const int u = kGQA ? (t >> 1) / p.split : t >> 1;
-    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, false, true)
-                 : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, false)
+    const bool spt = kSpt && g.causal;
+    Tile ti = vm ? sched_varlen(*vm, u, g.B, g.Hkv, kBN, p.head_section, spt, true)
+                 : (g.causal ? sched_dense_lpt(u, g.B, g.Hkv, p.nm, spt)
                              : sched_dense(u, g.Hkv, p.nm, p.head_section, false));
     WideBwdTile f;
     f.b = ti.b;
@@ -291,7 +297,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             ok = warp_wait(bar(Lay::kKVEmpty), (tile_it & 1u) ^ 1u, w, lane);
             if (!ok) break;
@@ -424,7 +430,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             if (kSparse ? f.nblk == 0 : f.m_begin >= f.m_end) continue;
             const int pc = f.c, po = 1 - f.c;
             const bool narrow = chunk_width<HD>(f.c) == 64;
@@ -544,7 +550,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             const int cw = chunk_width<HD>(f.c);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
@@ -720,7 +726,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
-            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse>(t, p, vmp, lane);
+            const WideBwdTile f = wide_bwd_tile<kGQA, kBand, kSparse, kDet>(t, p, vmp, lane);
             const int cw = chunk_width<HD>(f.c);
             const int rounds = cw / 64;
             WideQWalk qw = qwalk_start<kSparse>(f, lane);
@@ -735,8 +741,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after_sync();
                 int* sem = nullptr;
                 if constexpr (kDet) {
-                    // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in
-                    // ascending block order under its own semaphore
+                    // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in the
+                    // order of bwd.cu (SPT with a right mask bound) under its own semaphore
                     const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
                                              : ((long)f.b * g.H + qw.h) * p.nq + m;
                     sem = p.semaphores + 2 * tile + f.c;
@@ -746,12 +752,15 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         int n_lo, n_hi;
                         band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
                                         kBN, &n_lo, &n_hi);
-                        int before = f.n - (kBand ? n_lo : 0);   // key blocks that add to this tile before block n
+                        // key blocks that add to this tile before block n: those below it, or with
+                        // a right mask bound (SPT order) those above it up to n_hi - 1
+                        const bool spt = g.causal != 0;
+                        int before = spt ? n_hi - 1 - f.n : f.n - (kBand ? n_lo : 0);
                         if (kSparse && f.mcol) {   // block-sparse: only the kept ones
                             const unsigned char* row =
                                 p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
                             before = 0;
-                            for (int x = n_lo; x < f.n; ++x) before += row[x] != 0;
+                            for (int x = spt ? f.n + 1 : n_lo; x < (spt ? n_hi : f.n); ++x) before += row[x] != 0;
                         }
                         if (sem_wait(sem, before, w)) fence_proxy_async_global();
                         mbar_arrive(bar(Lay::kSemGo));
