@@ -199,6 +199,72 @@ class Problem:
             raise binding.AttnError(rc, binding.last_error())
 
 
+class E2EPipeline:
+    """Steps through the C ABI from pinned host buffers: every step copies its
+    inputs to the device and every mask variant's results back. The copies of
+    neighbouring steps overlap the computation: two buffer sets (by step
+    parity; outputs also by variant), host-to-device copies on one stream and
+    device-to-host copies on another, ordered against the computation by
+    events. After run(), outs[parity][variant] hold that step's results."""
+
+    def __init__(self, prob, variants, kinds):
+        self.variants, self.kinds = variants, kinds
+        ins = ("q", "k", "v", "do") if "bwd" in kinds else ("q", "k", "v")
+        self.host = {n: prob.host[n].pin_memory() for n in ins}
+        out_names = ("o", "lse", "dq", "dk", "dv") if "bwd" in kinds else ("o", "lse")
+        self.base = [prob, prob.clone()]
+        self.sets = [[self.base[p] if vi == 0 else self.base[p].clone(inputs_from=self.base[p])
+                      for vi in range(len(variants))] for p in range(2)]
+        self.outs = [[{n: torch.empty(getattr(s_, n).shape, dtype=getattr(s_, n).dtype, pin_memory=True)
+                       for n in out_names} for s_ in row] for row in self.sets]
+        self.h2d_bytes = sum(x.numel() * x.element_size() for x in self.host.values())
+        self.d2h_bytes = sum(x.numel() * x.element_size() for x in self.outs[0][0].values()) * len(variants)
+        self.up, self.down = torch.cuda.Stream(), torch.cuda.Stream()
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.in_free = [torch.cuda.Event() for _ in range(2)]
+        self.done = [[torch.cuda.Event() for _ in variants] for _ in range(2)]
+        self.out_free = [[torch.cuda.Event() for _ in variants] for _ in range(2)]
+
+    def _upload(self, i):
+        p = i % 2
+        self.up.wait_event(self.in_free[p])          # the step before that used this set has computed
+        with torch.cuda.stream(self.up):
+            for n, src in self.host.items():
+                getattr(self.base[p], n).copy_(src, non_blocking=True)
+        self.in_ready[p].record(self.up)
+
+    def _compute_and_download(self, i):
+        p = i % 2
+        main = torch.cuda.current_stream()
+        main.wait_event(self.in_ready[p])
+        for vi, c in enumerate(self.variants):
+            s_ = self.sets[p][vi]
+            main.wait_event(self.out_free[p][vi])   # this set's previous results are on the host
+            for kind in self.kinds:
+                s_.fwd(c) if kind == "fwd" else s_.bwd(c)
+            self.done[p][vi].record(main)
+            self.down.wait_event(self.done[p][vi])
+            with torch.cuda.stream(self.down):
+                for n, dst in self.outs[p][vi].items():
+                    dst.copy_(getattr(s_, n), non_blocking=True)
+            self.out_free[p][vi].record(self.down)
+        self.in_free[p].record(main)
+
+    def run(self, nsteps, start=None):
+        """Enqueue nsteps steps; the current stream then waits for every copy."""
+        if start is not None:
+            self.up.wait_event(start)
+        self._upload(0)
+        for i in range(nsteps):
+            if i + 1 < nsteps:
+                self._upload(i + 1)
+            self._compute_and_download(i)
+        main = torch.cuda.current_stream()
+        for p in range(2):
+            for vi in range(len(self.variants)):
+                main.wait_event(self.out_free[p][vi])
+
+
 def flops(w, causal, which):
     ww = w.with_(causal=causal)
     return ww.fwd_flops() if which == "fwd" else ww.bwd_flops()
@@ -434,76 +500,19 @@ def run_ours(args, world, rank, local, dist):
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the main kernel, per launch"}
 
     # ---- end to end through the C ABI with host buffers
-    # Every step copies its inputs from pinned host memory and every mask
-    # variant's results back, inside the timed region. The copies of
-    # neighbouring steps overlap the computation: two buffer sets, host-to-
-    # device copies on one stream and device-to-host copies on another, ordered
-    # against the computation by events.
     e2e = None
     if not args.no_e2e:
-        ins = ("q", "k", "v", "do") if "bwd" in kinds else ("q", "k", "v")
-        host = {n: prob.host[n].pin_memory() for n in ins}
-        out_names = ("o", "lse", "dq", "dk", "dv") if "bwd" in kinds else ("o", "lse")
-        base = [prob, prob.clone()]                                   # input sets, by step parity
-        sets = [[base[p] if vi == 0 else base[p].clone(inputs_from=base[p]) for vi in range(len(variants))]
-                for p in range(2)]                                    # output sets, by parity and variant
-        outs = [[{n: torch.empty(getattr(s_, n).shape, dtype=getattr(s_, n).dtype, pin_memory=True)
-                  for n in out_names} for s_ in row] for row in sets]
-        h2d = sum(x.numel() * x.element_size() for x in host.values())
-        d2h = sum(x.numel() * x.element_size() for x in outs[0][0].values()) * len(variants)
-        main = torch.cuda.current_stream()
-        up, down = torch.cuda.Stream(), torch.cuda.Stream()
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        in_free = [torch.cuda.Event() for _ in range(2)]
-        done = [[torch.cuda.Event() for _ in variants] for _ in range(2)]
-        out_free = [[torch.cuda.Event() for _ in variants] for _ in range(2)]
-
-        def upload(i):
-            p = i % 2
-            up.wait_event(in_free[p])          # the step before that used this set has computed
-            with torch.cuda.stream(up):
-                for n, src in host.items():
-                    getattr(base[p], n).copy_(src, non_blocking=True)
-            in_ready[p].record(up)
-
-        def compute_and_download(i):
-            p = i % 2
-            main.wait_event(in_ready[p])
-            for vi, c in enumerate(variants):
-                s_ = sets[p][vi]
-                main.wait_event(out_free[p][vi])   # this set's previous results are on the host
-                for kind in kinds:
-                    s_.fwd(c) if kind == "fwd" else s_.bwd(c)
-                done[p][vi].record(main)
-                down.wait_event(done[p][vi])
-                with torch.cuda.stream(down):
-                    for n, dst in outs[p][vi].items():
-                        dst.copy_(getattr(s_, n), non_blocking=True)
-                out_free[p][vi].record(down)
-            in_free[p].record(main)
-
-        def run(nsteps, start=None):
-            if start is not None:
-                up.wait_event(start)
-            upload(0)
-            for i in range(nsteps):
-                if i + 1 < nsteps:
-                    upload(i + 1)
-                compute_and_download(i)
-            for p in range(2):
-                for vi in range(len(variants)):
-                    main.wait_event(out_free[p][vi])
-
-        run(2)
+        pipe = E2EPipeline(prob, variants, kinds)
+        pipe.run(2)
         barrier(dist)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        run(args.steps, start=a)
+        pipe.run(args.steps, start=a)
         b.record()
         barrier(dist)
         e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist)
         e2e = {"value": world * step_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
                "overlap": "two buffer sets; host-to-device and device-to-host copies on their own streams"}
 
     # ---- oracle on the host cores (rank 0, N=1 only)
