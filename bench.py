@@ -320,23 +320,30 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
 
 
-def dist_setup():
+def dist_setup(backend="nccl"):
+    """World size, rank, local rank and the process group module (None for one
+    process). Independent replicas: the group only carries the barrier and the
+    max over ranks of the timed region, never data."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if backend == "nccl":
+        torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
         return world, rank, local, dist
-    torch.cuda.set_device(local)
     return 1, 0, local, None
+
+
+def _device_of(dist):
+    return "cuda" if dist is None or dist.get_backend() == "nccl" else "cpu"
 
 
 def max_over_ranks(x, dist):
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_device_of(dist))
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -344,7 +351,8 @@ def max_over_ranks(x, dist):
 def barrier(dist):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if _device_of(dist) == "cuda":
+        torch.cuda.synchronize()
 
 
 # ------------------------------------------------------------------------------------------ oracle
