@@ -75,11 +75,11 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 813.537e6 + 474.775e6,
+        "bytes": 821.898e6 + 479.444e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "277a9a4695e065384ad1d89d3aeb372104a6662a07306e774a194ba26c2c96c4",
+                "cf0222d843378704a67406e8d76e0f380e202570ad1b0ba7141d447987a0c328",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
@@ -91,11 +91,11 @@ NCU_TRAFFIC = {
         },
     },
     ("b4h16l4096d128", "bwd", True): {
-        "bytes": 1906.274e6 + 973.202e6,
+        "bytes": 1887.251e6 + 967.382e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "277a9a4695e065384ad1d89d3aeb372104a6662a07306e774a194ba26c2c96c4",
+                "cf0222d843378704a67406e8d76e0f380e202570ad1b0ba7141d447987a0c328",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
