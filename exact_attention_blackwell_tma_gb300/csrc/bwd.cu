@@ -22,6 +22,7 @@
 #include "ptx.cuh"
 #include "mask.cuh"
 #include "sched.cuh"
+#include "dq_order.cuh"
 
 namespace attn {
 namespace {
@@ -65,7 +66,7 @@ struct BwdLayout {
                          kSFull = kDOEmpty + kDOStages, kDPFull = kSFull + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,   // two
                          kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
-                         kSemGo = kDKVFull + 1, kStageReady = kSemGo + 1,
+                         kStageReady = kDKVFull + 1,
                          kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -360,7 +361,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
-        mbar_init(bar(Lay::kSemGo), 1);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -774,13 +774,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // block's dQ MMA has read) in 128-row x 32-column swizzled boxes and added
         // by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic mode:
         // the same reduce-adds under the tile's semaphore, in key-block order,
-        // each block's completing before the next block's start.
+        // each block's completing before the next block's start. Only the leader
+        // thread, which issues the reduce-adds, waits on the semaphore, and only
+        // once the first round is staged: the dQ row leaves tensor memory before
+        // the wait, so the next query block's dP^T and dQ go ahead while this
+        // block queues for its turn.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -796,40 +800,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
-                int* sem = nullptr;
-                if constexpr (kDet) {
-                    // dQ tile (b, h, m) takes its key blocks' contributions in a fixed order:
-                    // from the highest key block down with a right mask bound (SPT), else
-                    // ascending. The key blocks that see query block m form one range
-                    // [n_lo, n_hi) (the mask band), so block n waits until the blocks before
-                    // it in that order have added theirs.
-                    const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + qw.h) * p.nq + m;
-                    sem = p.semaphores + tile;
-                    if (leader) {
-                        int n_lo, n_hi;
-                        band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
-                                        kBN, &n_lo, &n_hi);
-                        // key blocks that add to this tile before block n: those below it, or with
-                        // a right mask bound (SPT order) those above it up to n_hi - 1
-                        const bool spt = g.causal != 0;
-                        int before = spt ? n_hi - 1 - f.n : f.n - (kBand ? n_lo : 0);
-                        if (kSparse && f.mcol) {   // block-sparse: only the kept ones
-                            const unsigned char* row =
-                                p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
-                            before = 0;
-                            for (int x = spt ? f.n + 1 : n_lo; x < (spt ? n_hi : f.n); ++x) before += row[x] != 0;
-                        }
-                        if (sem_wait(sem, before, w)) fence_proxy_async_global();
-                        mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
-                    }
-                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
-                    ++sgo;
-                    ok = ok && !*abort_flag;
-                    if (!ok) break;
-                }
                 // the whole dQ row leaves tensor memory at once, so the next dP^T can start
-                // (deterministic mode: once the semaphore has let this block in)
                 uint32_t row[HD];
                 if constexpr (HD == 128) {
                     tmem_ld128(tmem + lane_off + Lay::kTDP, row);
@@ -843,6 +814,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
+                int* sem = nullptr;   // deterministic mode (leader): the dQ tile's semaphore
+                bool sem_ok = true;
 #pragma unroll
                 for (int rnd = 0; rnd < HD / 64; ++rnd) {
                     const bool last = rnd == HD / 64 - 1;
@@ -865,18 +838,27 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     mbar_arrive(bar(Lay::kStageReady));
                     if (leader) {
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            // rows past the query block's sequence carry exact zeros (P = 0 there)
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
-                                                  f.q_row0 + m * kBM);
-                            bulk_commit_group();
-                            if (kDet && last) {
-                                // every reduce-add of this block is complete before the next block's start
-                                bulk_wait_group0();
-                                fence_proxy_async_global();
-                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                            } else {
-                                bulk_wait_group_read0();
+                            if constexpr (kDet) {
+                                if (rnd == 0) {   // this block's turn at the dQ tile
+                                    sem = p.semaphores + dq_semaphore(p, f, qw.h, m, varlen);
+                                    sem_ok = sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w);
+                                    if (sem_ok) fence_proxy_async_global();
+                                }
+                            }
+                            if (sem_ok) {
+                                // rows past the query block's sequence carry exact zeros (P = 0 there)
+                                for (int c2 = 0; c2 < 2; ++c2)
+                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
+                                                      f.q_row0 + m * kBM);
+                                bulk_commit_group();
+                                if (kDet && last) {
+                                    // every reduce-add of this block is complete before the next block's start
+                                    bulk_wait_group0();
+                                    fence_proxy_async_global();
+                                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                                } else {
+                                    bulk_wait_group_read0();
+                                }
                             }
                         }
                         mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));

@@ -24,6 +24,7 @@
 #include "ptx.cuh"
 #include "mask.cuh"
 #include "sched.cuh"
+#include "dq_order.cuh"
 
 namespace attn {
 namespace {
@@ -63,8 +64,8 @@ struct WideBwdLayout {
     static constexpr int kKVFull = 0, kKVEmpty = 1, kRFull = 2, kREmpty = 2 + kSlots, kStatFull = 2 + 2 * kSlots,
                          kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
                          kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1,
-                         kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1,
-                         kStageReady = kSemGo + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
+                         kDKVFull = kDQFree + 1,
+                         kStageReady = kDKVFull + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
                          kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -263,7 +264,6 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
-        mbar_init(bar(Lay::kSemGo), 1);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -716,13 +716,14 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // As in bwd.cu, for one column chunk: TMA reduce-adds of 128-row x
         // 32-column boxes staged through this block's dS tile; deterministic
         // mode: the same reduce-adds under the chunk's semaphore, each key block's
-        // completing before the next one's start.
+        // completing before the next one's start (the leader waits for the turn
+        // once the first round is staged and the chunk has left tensor memory).
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -739,37 +740,6 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
-                int* sem = nullptr;
-                if constexpr (kDet) {
-                    // chunk c of dQ tile (b, h, m) takes its key blocks' contributions in the
-                    // order of bwd.cu (SPT with a right mask bound) under its own semaphore
-                    const long tile = varlen ? (long)qw.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + qw.h) * p.nq + m;
-                    sem = p.semaphores + 2 * tile + f.c;
-                    if (leader) {
-                        // the key blocks that see query block m form one range n_lo .. (the
-                        // mask band): block n waits for the n - n_lo before it
-                        int n_lo, n_hi;
-                        band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * kBM, m * kBM + kBM - 1,
-                                        kBN, &n_lo, &n_hi);
-                        // key blocks that add to this tile before block n: those below it, or with
-                        // a right mask bound (SPT order) those above it up to n_hi - 1
-                        const bool spt = g.causal != 0;
-                        int before = spt ? n_hi - 1 - f.n : f.n - (kBand ? n_lo : 0);
-                        if (kSparse && f.mcol) {   // block-sparse: only the kept ones
-                            const unsigned char* row =
-                                p.mask.ptr + ((p.mask.heads == 1 ? 0 : (long)qw.h) * mask_rows(g) + m) * mask_cols(g);
-                            before = 0;
-                            for (int x = spt ? f.n + 1 : n_lo; x < (spt ? n_hi : f.n); ++x) before += row[x] != 0;
-                        }
-                        if (sem_wait(sem, before, w)) fence_proxy_async_global();
-                        mbar_arrive(bar(Lay::kSemGo));
-                    }
-                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
-                    ++sgo;
-                    ok = ok && !*abort_flag;
-                    if (!ok) break;
-                }
                 uint32_t row[128];
                 if (rounds == 2) {
                     tmem_ld128(tmem + lane_off + Lay::kTDP, row);
@@ -783,6 +753,8 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
+                int* sem = nullptr;   // deterministic mode (leader): the dQ chunk's semaphore
+                bool sem_ok = true;
 #pragma unroll
                 for (int rnd = 0; rnd < 2; ++rnd) {
                     if (rnd >= rounds) break;
@@ -806,16 +778,25 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     mbar_arrive(bar(Lay::kStageReady));
                     if (leader) {
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
-                                                  qw.h, f.q_row0 + m * kBM);
-                            bulk_commit_group();
-                            if (kDet && last) {
-                                bulk_wait_group0();
-                                fence_proxy_async_global();
-                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                            } else {
-                                bulk_wait_group_read0();
+                            if constexpr (kDet) {
+                                if (rnd == 0) {   // this block's turn at chunk c of the dQ tile
+                                    sem = p.semaphores + 2 * dq_semaphore(p, f, qw.h, m, varlen) + f.c;
+                                    sem_ok = sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w);
+                                    if (sem_ok) fence_proxy_async_global();
+                                }
+                            }
+                            if (sem_ok) {
+                                for (int c2 = 0; c2 < 2; ++c2)
+                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
+                                                      qw.h, f.q_row0 + m * kBM);
+                                bulk_commit_group();
+                                if (kDet && last) {
+                                    bulk_wait_group0();
+                                    fence_proxy_async_global();
+                                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                                } else {
+                                    bulk_wait_group_read0();
+                                }
                             }
                         }
                         mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
