@@ -75,35 +75,39 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 821.898e6 + 479.444e6,
+        "bytes": 823.151e6 + 480.989e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "cf0222d843378704a67406e8d76e0f380e202570ad1b0ba7141d447987a0c328",
+                "50f9505e8b85432ecff730d8665fb99b7ebc304e269b2c80e7314bf42cc6566a",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
+                "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
                 "03d6c4f342d65da22060e6d69d9f490978d56ded7dca12337f5845aecf433e43",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
+                "3ba6d27d9c01f9761a7158c8f093d35d28186c953f6e844fe30c75baf35034d6",
         },
     },
     ("b4h16l4096d128", "bwd", True): {
-        "bytes": 1887.251e6 + 967.382e6,
+        "bytes": 1870.324e6 + 961.560e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "cf0222d843378704a67406e8d76e0f380e202570ad1b0ba7141d447987a0c328",
+                "50f9505e8b85432ecff730d8665fb99b7ebc304e269b2c80e7314bf42cc6566a",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "0a43aa2da9f8cc10d2e3ddf84019ec2e9a76ae596702a99139145d83346a82a5",
+                "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
                 "03d6c4f342d65da22060e6d69d9f490978d56ded7dca12337f5845aecf433e43",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
+                "3ba6d27d9c01f9761a7158c8f093d35d28186c953f6e844fe30c75baf35034d6",
         },
     },
 }
