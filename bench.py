@@ -89,7 +89,7 @@ NCU_TRAFFIC = {
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
-                "3ba6d27d9c01f9761a7158c8f093d35d28186c953f6e844fe30c75baf35034d6",
+                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
         },
     },
     ("b4h16l4096d128", "bwd", True): {
@@ -107,7 +107,7 @@ NCU_TRAFFIC = {
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
-                "3ba6d27d9c01f9761a7158c8f093d35d28186c953f6e844fe30c75baf35034d6",
+                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
         },
     },
 }

@@ -8,7 +8,9 @@
 // A key block waits until the count equals the number of blocks ahead of it,
 // adds its contribution, waits for the adds to complete and increments the
 // count: the sum is taken in the same order on every run (FlashAttention-4
-// paper, Section 3.2.4).
+// paper, Section 3.2.4). The functions are also compiled for the host, where
+// tests/sched_host.cu checks that the turns of every dQ tile's contributors
+// are 0, 1, ..., K - 1 (a gap or a repeat would leave a block waiting).
 #pragma once
 
 #include "kernels.h"
@@ -20,7 +22,7 @@ namespace attn {
 // per head, sequence b's blocks from q_row0 / 128 + b on, which leaves room for
 // every sequence's ragged last block).
 template <class Tile>
-__device__ __forceinline__ long dq_semaphore(const BwdParams& p, const Tile& f, int h, int m, bool varlen) {
+__host__ __device__ __forceinline__ long dq_semaphore(const BwdParams& p, const Tile& f, int h, int m, bool varlen) {
     const Geometry& g = p.g;
     return varlen ? (long)h * (g.Lq / 128 + g.B + 1) + f.q_row0 / 128 + f.b + m : ((long)f.b * g.H + h) * p.nq + m;
 }
@@ -31,7 +33,7 @@ __device__ __forceinline__ long dq_semaphore(const BwdParams& p, const Tile& f, 
 // blocks that see query block m form one range [n_lo, n_hi) (the mask band);
 // with a block mask only the kept ones count.
 template <bool kBand, bool kSparse, class Tile>
-__device__ __forceinline__ int dq_turn(const BwdParams& p, const Tile& f, int h, int m) {
+__host__ __device__ __forceinline__ int dq_turn(const BwdParams& p, const Tile& f, int h, int m) {
     const Geometry& g = p.g;
     int n_lo, n_hi;
     band_key_blocks(mask_band(f.lq, f.lk, g.win_left, g.win_right), m * 128, m * 128 + 127, 128, &n_lo, &n_hi);

@@ -1,5 +1,6 @@
-// Host-side checks of the persistent tile scheduler (csrc/sched.cuh) and of
-// the mask band's index arithmetic (csrc/mask.cuh), compiled
+// Host-side checks of the persistent tile scheduler (csrc/sched.cuh), of
+// the mask band's index arithmetic (csrc/mask.cuh) and of the deterministic
+// backward's dQ order (csrc/dq_order.cuh), compiled
 // by tests/test_sched.py with nvcc and run without a GPU. The index functions
 // under test are the ones the kernels call. Prints "OK" and exits 0 when every
 // check passes; otherwise prints the first failure and exits 1.
@@ -12,6 +13,7 @@
 
 #include "mask.cuh"
 #include "sched.cuh"
+#include "dq_order.cuh"
 
 using namespace attn;
 
@@ -180,11 +182,78 @@ static void check_band(int lq, int lk, int wl, int wr) {
     }
 }
 
+
+// The deterministic backward's dQ order (dq_order.cuh): for every dQ tile, the
+// key blocks that contribute to it -- those whose rows see some row of the
+// query block (a scan of the mask) and, with a block mask, whose block it
+// keeps -- get the turns 0, 1, ..., K - 1, each once. kBand = false is the
+// instantiation for no mask and the causal one.
+struct HostTile {
+    int b, n, lq, lk, q_row0;
+    const unsigned char* mcol;
+};
+
+template <bool kBand, bool kSparse>
+static void check_dq_turns(int lq, int lk, int wl, int wr, const std::vector<unsigned char>* mask) {
+    BwdParams p{};
+    p.g.B = 1;
+    p.g.H = p.g.Hkv = p.g.group = 1;
+    p.g.Lq = lq;
+    p.g.Lk = lk;
+    p.g.causal = wr >= 0;
+    p.g.win_left = wl;
+    p.g.win_right = wr;
+    p.nq = (lq + 127) / 128;
+    p.mask = BlockMask{mask ? mask->data() : nullptr, 1};
+    const int nq = (lq + 127) / 128, nk = (lk + 127) / 128;
+    auto sees = [&](int i, int j) {
+        const int d = lk - lq;
+        return !(wr >= 0 && j > i + d + wr) && !(wl >= 0 && j < i + d - wl);
+    };
+    for (int m = 0; m < nq; ++m) {
+        std::vector<int> turns;
+        for (int n = 0; n < nk; ++n) {
+            bool any = false;
+            for (int i = m * 128; i < std::min(lq, m * 128 + 128) && !any; ++i)
+                for (int j = n * 128; j < std::min(lk, n * 128 + 128) && !any; ++j) any = sees(i, j);
+            if (mask && !(*mask)[(size_t)m * nk + n]) any = false;
+            if (!any) continue;
+            const HostTile f{0, n, lq, lk, 0, mask ? mask->data() + n : nullptr};
+            turns.push_back(dq_turn<kBand, kSparse>(p, f, 0, m));
+            if (dq_semaphore(p, f, 0, m, false) != m) fail("dq semaphore index", lq, lk, m);
+        }
+        std::sort(turns.begin(), turns.end());
+        for (int k = 0; k < (int)turns.size(); ++k)
+            if (turns[k] != k) fail("dq turns not 0..K-1", m, k, wl * 100000 + wr * 100 + lq % 100);
+    }
+}
+
+static void check_dq_order() {
+    unsigned seed = 12345;
+    for (int lq : {1, 130, 300, 517, 1000})
+        for (int lk : {1, 130, 300, 517, 1000}) {
+            check_dq_turns<false, false>(lq, lk, -1, -1, nullptr);
+            check_dq_turns<false, false>(lq, lk, -1, 0, nullptr);
+            for (int wl : {-1, 0, 3, 128, 200})
+                for (int wr : {-1, 0, 3, 128, 200}) {
+                    check_dq_turns<true, false>(lq, lk, wl, wr, nullptr);
+                    const int nq = (lq + 127) / 128, nk = (lk + 127) / 128;
+                    std::vector<unsigned char> mask((size_t)nq * nk);
+                    for (auto& x : mask) {
+                        seed = seed * 1103515245u + 12345u;
+                        x = (seed >> 16) % 3 != 0;
+                    }
+                    check_dq_turns<true, true>(lq, lk, wl, wr, &mask);
+                }
+        }
+}
+
 int main() {
     for (int lq : {1, 130, 300, 517})
         for (int lk : {1, 130, 300, 517})
             for (int wl : {-1, 0, 3, 128, 200})
                 for (int wr : {-1, 0, 3, 128, 200}) check_band(lq, lk, wl, wr);
+    check_dq_order();
     for (int n : {1, 7, 152, 153, 1000, 1024, 4096})
         for (int grid : {1, 2, 148, 152})
             check_snake(n, grid);

@@ -9,7 +9,10 @@ sequence map; and the per-CTA work of the benchmark's causal workloads stays
 within 3% of the mean. It also checks the mask band's index arithmetic
 (csrc/mask.cuh: the keys a row sees, the rows a key is seen by, and the
 blocks a group of rows or keys reaches) against a scan of the mask for no
-mask, causal and local windows, square and rectangular.
+mask, causal and local windows, square and rectangular; and the
+deterministic backward's dQ order (csrc/dq_order.cuh): for every dQ tile the
+key blocks that contribute to it, found by scanning the mask (and a block
+mask), get the turns 0 .. K-1 once each.
 """
 import os
 import shutil
