@@ -75,11 +75,11 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 823.151e6 + 480.989e6,
+        "bytes": 821.898e6 + 479.444e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "50f9505e8b85432ecff730d8665fb99b7ebc304e269b2c80e7314bf42cc6566a",
+                "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
@@ -93,11 +93,11 @@ NCU_TRAFFIC = {
         },
     },
     ("b4h16l4096d128", "bwd", True): {
-        "bytes": 1870.324e6 + 961.560e6,
+        "bytes": 1887.251e6 + 967.382e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "50f9505e8b85432ecff730d8665fb99b7ebc304e269b2c80e7314bf42cc6566a",
+                "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":

@@ -66,7 +66,7 @@ struct BwdLayout {
                          kSFull = kDOEmpty + kDOStages, kDPFull = kSFull + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,   // two
                          kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
-                         kStageReady = kDKVFull + 1,
+                         kSemGo = kDKVFull + 1, kStageReady = kSemGo + 1,
                          kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -228,37 +228,60 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
 
 // ----------------------------------------------------------------------------
 // Preprocess: D = rowsum(dO * O), zero the dQ accumulator and semaphores,
-// build the varlen map (block 0). One thread per (row, head).
+// build the varlen map (block 0). D: eight lanes per (row, head), lane l
+// reading 16-byte pieces l, l + 8, ... of the row's O and dO (128-byte runs,
+// all loads of a lane issued together), summed by shuffles within the eight.
+// The loop runs warp by warp, four rows per warp and step, so every shuffle
+// has the whole warp.
 __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc4, int n_sem) {
     const Geometry& g = p.g;
     const long stride = (long)gridDim.x * blockDim.x;
     const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int dv = p.d_v;   // O and dO have the head dim of v
-    for (long i = tid; i < rows_q * g.H; i += stride) {
-        const long row = i / g.H;
-        const int h = (int)(i - row * g.H);
-        const uint4* o4 = reinterpret_cast<const uint4*>(p.o + i * dv);
-        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + i * dv);
+    const int dv = p.d_v;   // O and dO have the head dim of v: 64 .. 256, 4 pieces of 8 lanes at most
+    const int pieces = dv / 64;
+    const int lane = threadIdx.x & 31, l8 = lane & 7;
+    const long n_rows = rows_q * g.H;
+    const long warps = stride / 32;
+    for (long r0 = tid / 32 * 4; r0 < n_rows; r0 += warps * 4) {
+        const long i = r0 + (lane >> 3);   // (row, head) of this lane's group
+        const bool valid = i < n_rows;
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.o + (valid ? i : 0) * dv);
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + (valid ? i : 0) * dv);
+        uint4 a[4], b[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (valid && j < pieces) {
+                a[j] = o4[j * 8 + l8];
+                b[j] = d4[j * 8 + l8];
+            }
         float acc = 0.f;
-        for (int c = 0; c < dv / 8; ++c) {
-            uint4 a = o4[c], b = d4[c];
-            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!valid || j >= pieces) continue;
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[j]);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[j]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
+                const float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
                 acc = fmaf(fa.x, fb.x, acc);
                 acc = fmaf(fa.y, fb.y, acc);
             }
         }
-        long di;
-        if (g.cu_seqlens) {
-            di = (long)h * g.Lq + row;
-        } else {
-            const long b = row / g.Lq, r = row - b * g.Lq;
-            di = (b * g.H + h) * g.Lq + r;
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (valid && l8 == 0) {
+            const long row = i / g.H;
+            const int h = (int)(i - row * g.H);
+            long di;
+            if (g.cu_seqlens) {
+                di = (long)h * g.Lq + row;
+            } else {
+                const long b = row / g.Lq, r = row - b * g.Lq;
+                di = (b * g.H + h) * g.Lq + r;
+            }
+            p.delta[di] = acc;
         }
-        p.delta[di] = acc;
     }
     float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
     for (long i = tid; i < n_acc4; i += stride) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -361,6 +384,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
+        mbar_init(bar(Lay::kSemGo), 1);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -774,17 +798,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // block's dQ MMA has read) in 128-row x 32-column swizzled boxes and added
         // by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic mode:
         // the same reduce-adds under the tile's semaphore, in key-block order,
-        // each block's completing before the next block's start. Only the leader
-        // thread, which issues the reduce-adds, waits on the semaphore, and only
-        // once the first round is staged: the dQ row leaves tensor memory before
-        // the wait, so the next query block's dP^T and dQ go ahead while this
-        // block queues for its turn.
+        // each block's completing before the next block's start.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -800,7 +820,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
+                int* sem = nullptr;
+                if constexpr (kDet) {
+                    // this block's turn at the dQ tile: the leader waits for it and tells the warpgroup
+                    sem = p.semaphores + dq_semaphore(p, f, qw.h, m, varlen);
+                    if (leader) {
+                        if (sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w)) fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kSemGo));   // arrive even after a failure; abort_flag tells
+                    }
+                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                    ++sgo;
+                    ok = ok && !*abort_flag;
+                    if (!ok) break;
+                }
                 // the whole dQ row leaves tensor memory at once, so the next dP^T can start
+                // (deterministic mode: once the semaphore has let this block in)
                 uint32_t row[HD];
                 if constexpr (HD == 128) {
                     tmem_ld128(tmem + lane_off + Lay::kTDP, row);
@@ -814,8 +848,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-                int* sem = nullptr;   // deterministic mode (leader): the dQ tile's semaphore
-                bool sem_ok = true;
 #pragma unroll
                 for (int rnd = 0; rnd < HD / 64; ++rnd) {
                     const bool last = rnd == HD / 64 - 1;
@@ -838,27 +870,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     mbar_arrive(bar(Lay::kStageReady));
                     if (leader) {
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            if constexpr (kDet) {
-                                if (rnd == 0) {   // this block's turn at the dQ tile
-                                    sem = p.semaphores + dq_semaphore(p, f, qw.h, m, varlen);
-                                    sem_ok = sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w);
-                                    if (sem_ok) fence_proxy_async_global();
-                                }
-                            }
-                            if (sem_ok) {
-                                // rows past the query block's sequence carry exact zeros (P = 0 there)
-                                for (int c2 = 0; c2 < 2; ++c2)
-                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
-                                                      f.q_row0 + m * kBM);
-                                bulk_commit_group();
-                                if (kDet && last) {
-                                    // every reduce-add of this block is complete before the next block's start
-                                    bulk_wait_group0();
-                                    fence_proxy_async_global();
-                                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                                } else {
-                                    bulk_wait_group_read0();
-                                }
+                            // rows past the query block's sequence carry exact zeros (P = 0 there)
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
+                                                  f.q_row0 + m * kBM);
+                            bulk_commit_group();
+                            if (kDet && last) {
+                                // every reduce-add of this block is complete before the next block's start
+                                bulk_wait_group0();
+                                fence_proxy_async_global();
+                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                            } else {
+                                bulk_wait_group_read0();
                             }
                         }
                         mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
@@ -899,7 +922,7 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     VarlenMap* vm = reinterpret_cast<VarlenMap*>(
         reinterpret_cast<char*>(p.semaphores) + (((size_t)n_sem * sizeof(int) + 255) & ~(size_t)255));
     {
-        const long work = rows_q * g.H;
+        const long work = rows_q * g.H * 8;   // eight lanes per (row, head)
         int blocks = (int)((work + 255) / 256);
         if (blocks > 8 * num_sms) blocks = 8 * num_sms;
         if (blocks < 1) blocks = 1;

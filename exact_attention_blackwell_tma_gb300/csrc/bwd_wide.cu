@@ -64,8 +64,8 @@ struct WideBwdLayout {
     static constexpr int kKVFull = 0, kKVEmpty = 1, kRFull = 2, kREmpty = 2 + kSlots, kStatFull = 2 + 2 * kSlots,
                          kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
                          kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1,
-                         kDKVFull = kDQFree + 1,
-                         kStageReady = kDKVFull + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
+                         kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1,
+                         kStageReady = kSemGo + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
                          kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -264,6 +264,7 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
+        mbar_init(bar(Lay::kSemGo), 1);
         mbar_init(bar(Lay::kStageReady), 128);
         mbar_init(bar(Lay::kStageFree), 1);
         mbar_init(bar(Lay::kDrain), 1);
@@ -716,14 +717,13 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // As in bwd.cu, for one column chunk: TMA reduce-adds of 128-row x
         // 32-column boxes staged through this block's dS tile; deterministic
         // mode: the same reduce-adds under the chunk's semaphore, each key block's
-        // completing before the next one's start (the leader waits for the turn
-        // once the first round is staged and the chunk has left tensor memory).
+        // completing before the next one's start.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -740,6 +740,20 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint32_t stage_s = base + Lay::kDSOff + dsb * Lay::kDSBytes;
                 ++dqc;
                 tc_fence_after_sync();
+                int* sem = nullptr;
+                if constexpr (kDet) {
+                    // this block's turn at chunk c of the dQ tile (the order of bwd.cu, one
+                    // semaphore per chunk): the leader waits for it and tells the warpgroup
+                    sem = p.semaphores + 2 * dq_semaphore(p, f, qw.h, m, varlen) + f.c;
+                    if (leader) {
+                        if (sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w)) fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kSemGo));
+                    }
+                    ok = warp_wait(bar(Lay::kSemGo), sgo & 1u, w, lane);
+                    ++sgo;
+                    ok = ok && !*abort_flag;
+                    if (!ok) break;
+                }
                 uint32_t row[128];
                 if (rounds == 2) {
                     tmem_ld128(tmem + lane_off + Lay::kTDP, row);
@@ -753,8 +767,6 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-                int* sem = nullptr;   // deterministic mode (leader): the dQ chunk's semaphore
-                bool sem_ok = true;
 #pragma unroll
                 for (int rnd = 0; rnd < 2; ++rnd) {
                     if (rnd >= rounds) break;
@@ -778,25 +790,16 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     mbar_arrive(bar(Lay::kStageReady));
                     if (leader) {
                         if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            if constexpr (kDet) {
-                                if (rnd == 0) {   // this block's turn at chunk c of the dQ tile
-                                    sem = p.semaphores + 2 * dq_semaphore(p, f, qw.h, m, varlen) + f.c;
-                                    sem_ok = sem_wait(sem, dq_turn<kBand, kSparse>(p, f, qw.h, m), w);
-                                    if (sem_ok) fence_proxy_async_global();
-                                }
-                            }
-                            if (sem_ok) {
-                                for (int c2 = 0; c2 < 2; ++c2)
-                                    tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
-                                                      qw.h, f.q_row0 + m * kBM);
-                                bulk_commit_group();
-                                if (kDet && last) {
-                                    bulk_wait_group0();
-                                    fence_proxy_async_global();
-                                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                                } else {
-                                    bulk_wait_group_read0();
-                                }
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
+                                                  qw.h, f.q_row0 + m * kBM);
+                            bulk_commit_group();
+                            if (kDet && last) {
+                                bulk_wait_group0();
+                                fence_proxy_async_global();
+                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                            } else {
+                                bulk_wait_group_read0();
                             }
                         }
                         mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
