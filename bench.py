@@ -81,7 +81,7 @@ NCU_TRAFFIC = {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
                 "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
+                "88be7192335af7bd9df50bd519e6da2e23c72f3a3a263d4ef33d2f5abac13898",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
@@ -99,7 +99,7 @@ NCU_TRAFFIC = {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
                 "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "a6d901cb9926474faaee65b06ed19314d942fef581f4b4cbfe49e16614b3eb3f",
+                "88be7192335af7bd9df50bd519e6da2e23c72f3a3a263d4ef33d2f5abac13898",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
