@@ -1,6 +1,7 @@
 """The benchmark's reference arm (the fp64 oracle on the host cores) prints one
-JSON line with the keys the benchmark contract asks for. Runs without a GPU:
-the reference arm touches no CUDA code."""
+JSON line with the keys the benchmark contract asks for, and the recorded ncu
+traffic figures are reported only while the kernel sources they were taken
+from are unchanged. Runs without a GPU: neither touches CUDA code."""
 import json
 import os
 import subprocess
@@ -27,3 +28,45 @@ def test_reference_arm_json_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def _bench_module():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_traffic_records_name_their_profile_and_sources():
+    """Every recorded DRAM traffic figure points at a committed ncu summary and
+    at the kernel sources whose hashes key it."""
+    bench = _bench_module()
+    assert bench.NCU_TRAFFIC
+    for key, rec in bench.NCU_TRAFFIC.items():
+        assert rec["bytes"] > 0, key
+        assert os.path.isfile(os.path.join(ROOT, rec["profile"])), rec["profile"]
+        assert rec["sources"], key
+        for rel, digest in rec["sources"].items():
+            assert os.path.isfile(os.path.join(ROOT, rel)), rel
+            assert len(digest) == 64 and int(digest, 16) >= 0, rel
+
+
+def test_traffic_is_null_once_a_source_changes(monkeypatch):
+    """The figure is reported while every keyed source still has the hash it
+    had at the capture, and null as soon as one differs."""
+    bench = _bench_module()
+    key = next(iter(bench.NCU_TRAFFIC))
+    rec = bench.NCU_TRAFFIC[key]
+    import hashlib
+    current = {rel: hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest()
+               for rel in rec["sources"]}
+    matching = dict(rec, sources=current)
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, matching)
+    assert bench.ncu_traffic(*key) == rec["bytes"]
+    rel = next(iter(current))
+    stale = dict(rec, sources=dict(current, **{rel: "0" * 64}))
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, stale)
+    assert bench.ncu_traffic(*key) is None
+    missing = dict(rec, sources=dict(current, **{"no/such/file.cu": "0" * 64}))
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, missing)
+    assert bench.ncu_traffic(*key) is None
+    assert bench.ncu_traffic("no-such-workload", "bwd", False) is None
