@@ -228,6 +228,36 @@ static void check_dq_turns(int lq, int lk, int wl, int wr, const std::vector<uns
     }
 }
 
+// Every dQ semaphore the kernels address lies inside the array the host
+// sizes (bwd_semaphore_count): dense and packed layouts, including the wide
+// kernel's second column chunk (index 2 * tile + 1). Distinct dQ tiles get
+// distinct semaphores.
+static void check_dq_semaphore_bounds(const std::vector<int>& lens, int H, bool varlen) {
+    BwdParams p{};
+    const int B = (int)lens.size();
+    int T = 0;
+    for (int L : lens) T += L;
+    const int Lq = varlen ? T : lens[0];
+    p.g.B = B;
+    p.g.H = H;
+    p.g.Lq = Lq;
+    p.nq = (Lq + 127) / 128;
+    const long count = bwd_semaphore_count(B, H, Lq, varlen);
+    std::set<long> seen;
+    int row0 = 0;
+    for (int b = 0; b < B; ++b) {
+        const int lq = varlen ? lens[b] : Lq;
+        const HostTile f{b, 0, lq, lq, varlen ? row0 : b * Lq, nullptr};
+        for (int h = 0; h < H; ++h)
+            for (int m = 0; m < (lq + 127) / 128; ++m) {
+                const long idx = dq_semaphore(p, f, h, m, varlen);
+                if (idx < 0 || 2 * idx + 1 >= count) fail("dq semaphore out of range", b, h, m);
+                if (!seen.insert(idx).second) fail("dq semaphore shared", b, h, m);
+            }
+        row0 += lq;
+    }
+}
+
 static void check_dq_order() {
     unsigned seed = 12345;
     for (int lq : {1, 130, 300, 517, 1000})
@@ -254,6 +284,12 @@ int main() {
             for (int wl : {-1, 0, 3, 128, 200})
                 for (int wr : {-1, 0, 3, 128, 200}) check_band(lq, lk, wl, wr);
     check_dq_order();
+    check_dq_semaphore_bounds({4096, 4096, 4096, 4096}, 16, false);
+    check_dq_semaphore_bounds({1, 1, 1}, 3, false);
+    check_dq_semaphore_bounds({300, 300}, 5, false);
+    check_dq_semaphore_bounds({1, 128, 129, 0, 255, 256, 257, 1000, 1}, 4, true);
+    check_dq_semaphore_bounds({127, 127, 127, 127, 127, 127, 127}, 2, true);
+    check_dq_semaphore_bounds({16384, 256, 300, 4096, 1}, 16, true);
     for (int n : {1, 7, 152, 153, 1000, 1024, 4096})
         for (int grid : {1, 2, 148, 152})
             check_snake(n, grid);

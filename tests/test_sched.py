@@ -12,7 +12,9 @@ blocks a group of rows or keys reaches) against a scan of the mask for no
 mask, causal and local windows, square and rectangular; and the
 deterministic backward's dQ order (csrc/dq_order.cuh): for every dQ tile the
 key blocks that contribute to it, found by scanning the mask (and a block
-mask), get the turns 0 .. K-1 once each.
+mask), get the turns 0 .. K-1 once each, and every dQ tile's semaphore (both
+column chunks in the wide kernel) is its own and lies inside the array the
+host sizes, for dense and packed layouts.
 """
 import os
 import shutil
