@@ -139,3 +139,18 @@ def test_grouped_split_policy(built, B, H, Hkv, L, d, split):
     got = lib.attn_bwd_gqa_workspace_size(B, H, Hkv, L, L, d, 1, 0)
     part = 2 * split * B * L * Hkv * d * 4 if split > 1 else 0
     assert got - base == (part + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("B,H,T,d,dv", [(3, 4, 1000, 64, 64), (32, 16, 200000, 128, 128), (7, 2, 129, 192, 128),
+                                        (1, 1, 1, 256, 256)])
+def test_workspace_holds_every_part(built, B, H, T, d, dv):
+    """A lower bound built from the parts the backward keeps in the workspace,
+    for a packed batch of T rows (the largest layout): the fp32 dQ
+    accumulator, D, two semaphores per dQ tile of each sequence (a sequence's
+    ragged last block included: H * (T / 128 + B + 1) tiles), and the sequence
+    map (four arrays of about 1024 ints)."""
+    lib = binding.load()
+    got = lib.attn_bwd_ex_workspace_size(B, H, H, T, T, d, dv, 1, 1)
+    need = 4 * T * H * d + 4 * T * H + 4 * 2 * H * (T // 128 + B + 1) + 4 * 4 * 1024
+    assert got >= need
+    assert got % 256 == 0
