@@ -82,6 +82,12 @@ def test_argument_errors_need_no_gpu(built):
     assert lib.attn_fwd(dummy + 2, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 64, 0.1, 0, None, None) == -2
     # varlen requires Lq == Lk (both the packed row count)
     assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 2, 1, 128, 64, 64, 0.1, 0, dummy, None) == -1
+    # varlen batches: 1 .. 1024 sequences (the sequence map's capacity)
+    assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 1025, 1, 4096, 4096, 64, 0.1, 0, dummy, None) == -1
+    assert "1024" in binding.last_error()
+    assert lib.attn_fwd(dummy, dummy, dummy, dummy, dummy, 0, 1, 4096, 4096, 64, 0.1, 0, dummy, None) == -1
+    assert lib.attn_fwd_varlen(dummy, dummy, dummy, dummy, dummy, 1025, 1, 1, 4096, 4096, 64, 64, 0.1, 0, dummy,
+                               dummy, None) == -1
     # separate value head dim: only (192, 128) besides dv = d
     assert lib.attn_fwd_hdim(dummy, dummy, dummy, dummy, dummy, 1, 1, 128, 128, 128, 64, 0.1, 0, None, None) == -1
     assert "dv=64" in binding.last_error()
