@@ -63,6 +63,10 @@ def _declare(lib):
                                                                       c_void_p, c_size_t, c_void_p])
     lib.attn_bwd_noalloc.restype = c_int
     lib.attn_bwd_noalloc.argtypes = [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_void_p, c_int, c_void_p]
+    lib.attn_set_backward_cta_pairs.restype = c_int
+    lib.attn_set_backward_cta_pairs.argtypes = [c_int]
+    lib.attn_set_exp2_emulation.restype = c_int
+    lib.attn_set_exp2_emulation.argtypes = [c_int, c_int]
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_last_error.argtypes = []
     lib.attn_check_status.restype = c_int
@@ -211,6 +215,18 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, 
     return load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                    _ptr(dk), _ptr(dv), B, H, Lq, Lk, d, scale, int(causal), _ptr(cu_seqlens),
                                    int(deterministic), _stream(stream))
+
+
+def attn_set_backward_cta_pairs(enable) -> int:
+    """Backward main kernel on CTA pairs (2-CTA tensor cores) where it applies;
+    returns the previous setting."""
+    return load().attn_set_backward_cta_pairs(int(bool(enable)))
+
+
+def attn_set_exp2_emulation(d, every) -> int:
+    """Forward exp2 emulation for head dim d: one column pair in `every` (0, 4, 8)
+    by the FMA polynomial; returns the previous setting (or a negative code)."""
+    return load().attn_set_exp2_emulation(int(d), int(every))
 
 
 def attn_last_error() -> str:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 
 LIBS = {
-    "libattn.so": ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide.cu"],
+    "libattn.so": ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide.cu", "bwd_pair.cu"],
     "libattn_selftest.so": ["selftest.cu"],
 }
 HEADERS = ["ptx.cuh", "sched.cuh", "kernels.h", "mask.cuh", "dq_order.cuh"]

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -53,15 +54,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [rows, H, d] bf16 viewed as 3-D (d innermost); boxes of 128 rows x 1 head x
-// 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect.
-// Rows past `rows` read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d) {
+// [rows, H, d] bf16 viewed as 3-D (d innermost); boxes of box_rows rows x 1
+// head x 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors
+// expect. Rows past `rows` read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d, int box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -69,14 +70,15 @@ bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d) {
     return r == CUDA_SUCCESS;
 }
 
-// The fp32 dQ accumulator [rows, H, d] for TMA reduce-adds: boxes of 128 rows x
-// 32 columns (128 bytes) with the 128-byte swizzle. Rows past `rows` are skipped.
-bool make_map_f32(CUtensorMap* m, void* ptr, long rows, int H, int d) {
+// The fp32 dQ accumulator [rows, H, d] for TMA reduce-adds: boxes of box_rows
+// rows x 32 columns (128 bytes) with the 128-byte swizzle. Rows past `rows` are
+// skipped.
+bool make_map_f32(CUtensorMap* m, void* ptr, long rows, int H, int d, int box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
-    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -119,6 +121,16 @@ uint64_t wait_budget_ns() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// exp2 emulation of the forward kernel per head dim (index 0: d = 64, 1: d =
+// 128): 0 = MUFU only, 8 or 4 = one score-column pair in every 8 or 4 by the
+// FMA polynomial. Set by attn_set_exp2_emulation; the defaults are the faster
+// setting measured on GB300 for each head dim.
+std::atomic<int> g_poly_every[2] = {{0}, {0}};
+
+// Backward main kernel on CTA pairs (2-CTA tensor cores) where it applies; set
+// by attn_set_backward_cta_pairs; the default is the faster one measured on GB300.
+std::atomic<int> g_bwd_pairs{0};
 
 // Heads per L2 section for the LPT walk: the two bf16 tensors every tile of a
 // head streams (K and V in the forward, Q and dO in the backward) should fit
@@ -250,7 +262,9 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     if (!make_map(&tq, q, rows_q, H, d) || !make_map(&tk, kp, krows, Hkv, d) ||
         !make_map(&tv, vp, krows, Hkv, rows_k > 0 ? dv : d))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream) : launch_fwd(tq, tk, tv, p, di.sms, stream);
+    const int poly = d == 64 ? g_poly_every[0].load() : (d == 128 ? g_poly_every[1].load() : 0);
+    cudaError_t e = wide ? launch_fwd_wide(tq, tk, tv, p, di.sms, stream)
+                         : launch_fwd(tq, tk, tv, p, poly, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -412,17 +426,21 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();
     CUtensorMap tq, tk, tv, tdo, tdq;
+    PairMaps pm;
     const long qrows = rows_q > 0 ? rows_q : rows_k;
     const long krows = rows_k > 0 ? rows_k : rows_q;
     // Without query rows (or keys) the matching descriptors are never used; they
     // view the other tensor, with the heads of the smaller one so they stay in bounds.
     const int hq_map = rows_q > 0 ? H : Hkv;
+    const void* qsrc = rows_q > 0 ? q : k;
+    const void* dosrc = rows_q > 0 ? dout : k;
     // (v and dO are d_v <= d wide, so a fallback view of q or k with that width stays in bounds too)
-    if (!make_map(&tq, rows_q > 0 ? q : k, qrows, hq_map, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, Hkv, d) ||
-        !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d_v) ||
-        !make_map(&tdo, rows_q > 0 ? dout : k, qrows, hq_map, d_v) || !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d))
+    if (!make_map(&tq, qsrc, qrows, hq_map, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, Hkv, d) ||
+        !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d_v) || !make_map(&tdo, dosrc, qrows, hq_map, d_v) ||
+        !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d) || !make_map(&pm.q64, qsrc, qrows, hq_map, d, 64) ||
+        !make_map(&pm.do64, dosrc, qrows, hq_map, d_v, 64) || !make_map_f32(&pm.dq64, p.dq_acc, qrows, hq_map, d, 64))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, p, di.sms, stream);
+    cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, pm, g_bwd_pairs.load() != 0, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -520,6 +538,15 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
     // the backward's preprocess kernel zeroes the accumulator and the semaphores on every call
     return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, d, scale, causal, cu_seqlens, deterministic,
                     scratch, (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int attn_set_backward_cta_pairs(int enable) { return g_bwd_pairs.exchange(enable ? 1 : 0); }
+
+extern "C" int attn_set_exp2_emulation(int d, int every) {
+    if (d != 64 && d != 128) return fail(ATTN_ERR_ARG, "exp2 emulation applies to head dims 64 and 128, not %d", d);
+    if (every != 0 && every != 4 && every != 8)
+        return fail(ATTN_ERR_ARG, "exp2 emulation: one pair in 0 (off), 4 or 8, not %d", every);
+    return g_poly_every[d == 64 ? 0 : 1].exchange(every);
 }
 
 extern "C" const char* attn_last_error(void) { return g_err; }

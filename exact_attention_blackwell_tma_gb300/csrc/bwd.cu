@@ -233,7 +233,7 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
 // all loads of a lane issued together), summed by shuffles within the eight.
 // The loop runs warp by warp, four rows per warp and step, so every shuffle
 // has the whole warp.
-__global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc4, int n_sem) {
+__global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc4, int n_sem, int keys_per_tile) {
     const Geometry& g = p.g;
     const long stride = (long)gridDim.x * blockDim.x;
     const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -288,8 +288,9 @@ __global__ void bwd_prep(BwdParams p, VarlenMap* vm_out, long rows_q, long n_acc
     for (long i = tid; i < n_sem; i += stride) p.semaphores[i] = 0;
     if (g.cu_seqlens && blockIdx.x == 0) {
         // longest-first map of the sequences (FlashAttention-4 paper, Section 3.3,
-        // varlen LPT); work tiles are key blocks of key/value heads
-        sched_varlen_build(*vm_out, g.cu_seqlens, g.cu_seqlens_k, g.B, g.Hkv, kBN, true, threadIdx.x, blockDim.x);
+        // varlen LPT); work tiles are key blocks (or key-block pairs) of key/value heads
+        sched_varlen_build(*vm_out, g.cu_seqlens, g.cu_seqlens_k, g.B, g.Hkv, keys_per_tile, true, threadIdx.x,
+                           blockDim.x);
     }
 }
 
@@ -911,8 +912,8 @@ auto bwd_kernel_for(bool band, bool sparse) {
 
 template <int HD>
 cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const PairMaps& pm, bool pair,
+                          const BwdParams& p, int num_sms, cudaStream_t stream) {
     const Geometry& g = p.g;
     const bool varlen = g.cu_seqlens != nullptr;
     const long rows_q = varlen ? (long)g.Lq : (long)g.B * g.Lq;
@@ -926,12 +927,18 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         int blocks = (int)((work + 255) / 256);
         if (blocks > 8 * num_sms) blocks = 8 * num_sms;
         if (blocks < 1) blocks = 1;
-        bwd_prep<<<blocks, 256, 0, stream>>>(p, vm, rows_q, n_acc4, n_sem);
+        bwd_prep<<<blocks, 256, 0, stream>>>(p, vm, rows_q, n_acc4, n_sem, pair ? 2 * kBN : kBN);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaSuccess;
-    if constexpr (HD > 128) {
+    if (pair) {
+        BwdParams pp = p;   // work tiles are key-block pairs
+        pp.nm = bwd_pair_tiles_per_head(g.Lk);
+        pp.n_tiles = varlen ? 0 : g.B * g.H * pp.nm;
+        e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq64, pp, vm, num_sms, stream);
+        if (e != cudaSuccess) return e;
+    } else if constexpr (HD > 128) {
         e = launch_bwd_wide(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else {
@@ -982,13 +989,14 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 size_t bwd_varlen_map_bytes() { return sizeof(VarlenMap); }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int num_sms,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const PairMaps& pm, bool pair,
+                       const BwdParams& p, int num_sms, cudaStream_t stream) {
+    pair = pair && bwd_pair_supported(p);
     switch (p.g.d) {
-        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
-        case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
-        case 192: return launch_bwd_hd<192>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
-        case 256: return launch_bwd_hd<256>(tq, tk, tv, tdo, tdq, p, num_sms, stream);
+        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);
+        case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, tdq, pm, pair, p, num_sms, stream);
+        case 192: return launch_bwd_hd<192>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);
+        case 256: return launch_bwd_hd<256>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

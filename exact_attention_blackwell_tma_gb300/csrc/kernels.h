@@ -111,15 +111,34 @@ inline size_t bwd_partial_bytes(int split, long rows_k, int Hkv, int d, int dv) 
 }
 
 // Launchers (return cudaSuccess or the launch error).
+// poly_every: exp2 emulation of the plain kernel (no left window bound, no
+// block mask): 0 (MUFU only), 8 or 4 (one column pair in every 8 or 4 by the
+// FMA polynomial).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int num_sms, cudaStream_t stream);
+                       const FwdParams& p, int poly_every, int num_sms, cudaStream_t stream);
 // Head dims 192 and 256 (and d_qk = 192 with d_v = 128): one 128-row Q tile per
 // work tile (nm counts 128-row blocks).
 cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_sms, cudaStream_t stream);
+// Tensor maps with 64-row boxes (q, dO: 64 rows x 64 columns bf16; the dQ
+// accumulator: 64 rows x 32 columns fp32), used by the CTA-pair backward.
+struct PairMaps {
+    CUtensorMap q64, do64, dq64;
+};
+// pair: run the main kernel on CTA pairs when bwd_pair_supported(p) holds.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p, int num_sms,
-                       cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const PairMaps& pm, bool pair,
+                       const BwdParams& p, int num_sms, cudaStream_t stream);
+
+// The backward's main kernel on CTA pairs (2-CTA tensor cores, bwd_pair.cu):
+// head dim 128 (q, k, v), one query head per key/value head, no window beyond
+// the causal mask, no block mask; dense or packed, deterministic or not.
+bool bwd_pair_supported(const BwdParams& p);
+// key-block pairs per (batch, head) of Lk keys
+int bwd_pair_tiles_per_head(int Lk);
+cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo64, const CUtensorMap& tdq64, const BwdParams& p,
+                            const void* varlen_map, int num_sms, cudaStream_t stream);
 
 // Main kernel of the backward for head dims 192 and 256 (preprocess and dQ
 // conversion are shared with the d <= 128 path). varlen_map: the VarlenMap the

@@ -266,6 +266,41 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int B, int H, int Lq, int Lk, int d, float scale, int causal,
                      const int* cu_seqlens, int deterministic, cudaStream_t stream);
 
+/*
+ * Partial emulation of the forward's exponentials (FlashAttention-4 paper,
+ * Section 3.1.3, "partial emulation"; FA4 blog, "关键实现技术"): for head dim d
+ * (64 or 128), `every` = 8 or 4 computes one score-column pair in every 8 or 4
+ * (12.5% or 25% of the entries) with a degree-3 Cody-Waite + Horner polynomial
+ * on the FMA pipes instead of the MUFU ex2 unit, except on each row's last K/V
+ * block; 0 uses MUFU for all. Results differ from MUFU's by at most one bf16
+ * ulp of P. It applies to the plain forward kernel (no left window bound, no
+ * block mask). The setting is process-wide (all threads, all devices) and
+ * takes effect at the next forward call; the default per head dim is the one
+ * measured faster on GB300.
+ * Returns the previous setting (>= 0), or ATTN_ERR_ARG for another d or
+ * `every` value.
+ */
+int attn_set_exp2_emulation(int d, int every);
+
+/*
+ * Backward on CTA pairs (FlashAttention-4 paper, Section 3.2.3 "2-CTA backward
+ * pass"; Section 2.2 "2-CTA tensor cores"): with `enable` != 0 the backward's
+ * main kernel runs on clusters of two CTAs whose tensor cores work as one
+ * (tcgen05 .cta_group::2): each pair owns 256 keys, the S^T, dP^T, dV and dK
+ * products run with M = 256 and each CTA stages half of operand B, and dQ is
+ * summed over the pair's 256 keys by the MMA itself, so each CTA adds a
+ * 64-row dQ tile per query block (half the global reduce-adds of single
+ * CTAs). It applies where supported: head dim 128 for q, k and v, one query
+ * head per key/value head, no window beyond the causal mask, no block mask
+ * (dense or packed, deterministic or not); other problems run on single CTAs.
+ * Results agree with the single-CTA kernels to rounding (the order of the fp32
+ * sums differs); the deterministic mode stays bit-identical run to run. The
+ * setting is process-wide and takes effect at the next backward call; the
+ * default is the one measured faster on GB300.
+ * Returns the previous setting (0 or 1).
+ */
+int attn_set_backward_cta_pairs(int enable);
+
 /* Message for the last nonzero return code on this thread ("" if none). */
 const char* attn_last_error(void);
 
