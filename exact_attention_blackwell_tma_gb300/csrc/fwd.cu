@@ -63,20 +63,16 @@ struct FwdLayout {
     static_assert(256 + 2 * HD <= (int)kTmemCols, "tensor memory budget");
 };
 
-// Partial exp2 emulation (FlashAttention-4 paper, Section 3.1.3): one pair of
-// score columns in every kPolyEvery is exponentiated by the FMA polynomial
-// instead of the MUFU unit, off on the last K/V block of each row (FA4 blog,
-// "关键实现技术"). 0 disables it, which is the default on GB300: its MUFU unit
-// runs ex2 at twice the B200 rate (31.6/clk/SM measured), and in this kernel
-// one pair in 8 emulated was 2-4% slower, one in 4 was 8-11% slower.
-#ifndef ATTN_POLY_EVERY
-#define ATTN_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = ATTN_POLY_EVERY;
-
+// Partial exp2 emulation (FlashAttention-4 paper, Section 3.1.3): with kPoly > 0,
+// one pair of score columns in every kPoly is exponentiated by the FMA
+// polynomial instead of the MUFU unit (kPoly = 8: 12.5% of the entries, 4: 25%;
+// the paper emulates 10-25%), never on a row's last K/V block (FA4 blog,
+// "关键实现技术"). kPoly = 0: MUFU only. The launcher picks the kernel from the
+// per-head-dim setting of attn_set_exp2_emulation.
+//
 // P = 2^(s * sl2 - m) for one 128-column row, packed to bf16 pairs into tensor
 // memory at t_p (64 columns); the fp32 sum goes to l0 + l1.
-template <bool kEmulate>
+template <int kPoly>
 __device__ __forceinline__ void exp_row_to_tmem(const float (&s)[128], float sl2, float neg_m, uint32_t t_p,
                                                 float& l0, float& l1) {
     // x = s * sl2 - m and the running sum on packed fp32 pairs: half the FMA/add
@@ -91,7 +87,7 @@ __device__ __forceinline__ void exp_row_to_tmem(const float (&s)[128], float sl2
         for (int i = 0; i < 32; ++i) {
             float x0, x1;
             f32x2_split(ffma2(f32x2(s[64 * hf + 2 * i], s[64 * hf + 2 * i + 1]), sc2, nm2), x0, x1);
-            const bool poly = kEmulate && kPolyEvery > 0 && (i % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
+            const bool poly = kPoly > 0 && (i % (kPoly > 0 ? kPoly : 1)) == kPoly - 1;
             const float p0 = poly ? ex2_poly3(x0) : ex2_mufu(x0);
             const float p1 = poly ? ex2_poly3(x1) : ex2_mufu(x1);
             if (i & 1) acc_b = fadd2(acc_b, f32x2(p0, p1));
@@ -186,7 +182,7 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdParams& p, const Var
     return f;
 }
 
-template <int HD, bool kGeneral, bool kSparse>
+template <int HD, bool kGeneral, bool kSparse, int kPoly>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -496,11 +492,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float l0 = 0.f, l1 = 0.f;
-                if constexpr (kPolyEvery > 0) {
-                    if (j + 1 < nkv) exp_row_to_tmem<true>(s, sl2, neg_m, t_s, l0, l1);
-                    else exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
+                if constexpr (kPoly > 0) {
+                    if (j + 1 < nkv) exp_row_to_tmem<kPoly>(s, sl2, neg_m, t_s, l0, l1);
+                    else exp_row_to_tmem<0>(s, sl2, neg_m, t_s, l0, l1);   // last block: MUFU only
                 } else {
-                    exp_row_to_tmem<false>(s, sl2, neg_m, t_s, l0, l1);   // one copy of the loop in the code
+                    exp_row_to_tmem<0>(s, sl2, neg_m, t_s, l0, l1);   // one copy of the loop in the code
                 }
                 l_run += l0 + l1;
                 tmem_st_wait();
@@ -540,12 +536,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
 }
 
+// The kernel for a problem: the general one for a left window bound or a block
+// mask (MUFU only), else the plain one with the requested exp2 emulation.
+template <int HD>
+auto fwd_kernel_for(const FwdParams& p, int poly_every) {
+    if (p.mask.ptr) return fwd_kernel<HD, true, true, 0>;
+    if (p.g.win_left >= 0) return fwd_kernel<HD, true, false, 0>;
+    return poly_every == 8 ? fwd_kernel<HD, false, false, 8>
+                           : (poly_every == 4 ? fwd_kernel<HD, false, false, 4> : fwd_kernel<HD, false, false, 0>);
+}
+
 template <int HD>
 cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const FwdParams& p, int num_sms, cudaStream_t stream) {
+                          const FwdParams& p, int poly_every, int num_sms, cudaStream_t stream) {
     using Lay = FwdLayout<HD>;
-    auto kern = p.mask.ptr ? fwd_kernel<HD, true, true>
-                           : (p.g.win_left >= 0 ? fwd_kernel<HD, true, false> : fwd_kernel<HD, false, false>);
+    auto kern = fwd_kernel_for<HD>(p, poly_every);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
@@ -562,10 +567,10 @@ cudaError_t launch_fwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int num_sms, cudaStream_t stream) {
+                       const FwdParams& p, int poly_every, int num_sms, cudaStream_t stream) {
     switch (p.g.d) {
-        case 64: return launch_fwd_hd<64>(tq, tk, tv, p, num_sms, stream);
-        case 128: return launch_fwd_hd<128>(tq, tk, tv, p, num_sms, stream);
+        case 64: return launch_fwd_hd<64>(tq, tk, tv, p, poly_every, num_sms, stream);
+        case 128: return launch_fwd_hd<128>(tq, tk, tv, p, poly_every, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

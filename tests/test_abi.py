@@ -160,3 +160,16 @@ def test_workspace_holds_every_part(built, B, H, T, d, dv):
     need = 4 * T * H * d + 4 * T * H + 4 * 2 * H * (T // 128 + B + 1) + 4 * 4 * 1024
     assert got >= need
     assert got % 256 == 0
+
+
+def test_exp2_emulation_setting(built):
+    """attn_set_exp2_emulation: head dims 64 and 128, one pair in 0, 4 or 8;
+    returns the previous setting; anything else is an argument error."""
+    lib = binding.load()
+    prev = lib.attn_set_exp2_emulation(128, 8)
+    assert prev in (0, 4, 8)
+    assert lib.attn_set_exp2_emulation(128, 4) == 8
+    assert lib.attn_set_exp2_emulation(128, prev) == 4
+    assert lib.attn_set_exp2_emulation(192, 8) == binding.ATTN_ERR_ARG
+    assert lib.attn_set_exp2_emulation(64, 3) == binding.ATTN_ERR_ARG
+    assert "0 (off), 4 or 8" in binding.last_error()

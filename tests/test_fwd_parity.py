@@ -187,3 +187,61 @@ def test_workload_varlen():
         og = to64(o[a:a + L][rows][:, [0, 9]])[None]
         lg = to64(lse[[0, 9]][:, a:a + L][:, rows])[None]
         assert_fwd_close(og, lg, o_ref[:, rows], lse_ref[:, :, rows], f"varlen seq {b} (L={L})")
+
+
+# ------------------------------------------------------------------ partial exp2 emulation
+
+class _exp2_emulation:
+    """Set the forward's exp2 emulation for head dim d for the duration of a block."""
+
+    def __init__(self, d, every):
+        self.d, self.every = d, every
+
+    def __enter__(self):
+        self.prev = binding.attn_set_exp2_emulation(self.d, self.every)
+        assert self.prev >= 0, binding.last_error()
+
+    def __exit__(self, *exc):
+        binding.attn_set_exp2_emulation(self.d, self.prev)
+        return False
+
+
+@pytest.mark.parametrize("every", [4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [77, 300, 640])
+def test_exp2_emulation_full(L, causal, d, every):
+    """The kernels with one column pair in 4 or 8 exponentiated by the FMA
+    polynomial (FlashAttention-4 paper, Section 3.1.3): every element against
+    the oracle, with growing scores so that rescaling runs too; and against the
+    MUFU-only kernel, from which P differs by at most one bf16 ulp."""
+    t = inputs.small(B=2, H=2, L=L, d=d, seed=12)
+    ramp = torch.linspace(0.2, 4.0, L).view(1, L, 1, 1)
+    t["k"] = (t["k"].float() * ramp).to(torch.bfloat16)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    with _exp2_emulation(d, 0):
+        o_mufu, lse_mufu = run_dense(t, causal, scale)
+    with _exp2_emulation(d, every):
+        o, lse = run_dense(t, causal, scale)
+    o_ref, lse_ref = oracle_fwd_subset(t, scale, causal, heads=[0, 1])
+    what = f"poly 1/{every} L={L} causal={causal} d={d}"
+    assert_fwd_close(to64(o), to64(lse), o_ref, lse_ref, what)
+    assert float((o.float() - o_mufu.float()).abs().max()) <= 2e-2, what
+    assert float((lse - lse_mufu).abs().max()) <= 1e-3, what
+
+
+@pytest.mark.parametrize("every", [4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_exp2_emulation_workload(d, every):
+    """B2 H16 L8192 causal with spiky K (the head-dim sweep workload), sampled rows."""
+    w = inputs.HDSWEEP.with_(d=d)
+    t = inputs.make(w)
+    with _exp2_emulation(d, every):
+        o, lse = run_dense(t, True, w.scale)
+    rows = sorted({0, 1, 127, 128, 255, 256, 4095, 4096, w.L - 129, w.L - 1} |
+                  set(np.random.default_rng(5).choice(w.L, 12, replace=False).tolist()))
+    bsel = [0, w.B - 1]
+    sub = {n: t[n][bsel] for n in ("q", "k", "v")}
+    o_ref, lse_ref = oracle_fwd_subset(sub, w.scale, True, heads=[5], rows=rows)
+    assert_fwd_close(to64(o[bsel][:, rows][:, :, [5]]), to64(lse[bsel][:, [5]][:, :, rows]),
+                     o_ref[:, rows], lse_ref[:, :, rows], f"{w.name} poly 1/{every}")

@@ -75,7 +75,9 @@ def test_poly_exp2_accuracy_and_agreement_with_mufu():
     bp = yp[:2_000_001].to(torch.bfloat16).view(torch.int16).int().cpu().numpy()
     bm = ym[:2_000_001].to(torch.bfloat16).view(torch.int16).int().cpu().numpy()
     assert np.abs(bp - bm).max() <= 1
-    assert np.mean(bp == bm) >= 0.98
+    rate = float(np.mean(bp == bm))
+    print(f"poly-exp2 vs MUFU: bf16 results equal on {rate:.4%} of the sweep")
+    assert rate >= 0.98
     # Disagreements after bf16 rounding may only occur where exact 2^x lies within
     # the two approximations' error (poly fit 8.6e-5, MUFU ~2 fp32 ulp) of a
     # bf16 rounding midpoint.
