@@ -4,9 +4,10 @@ fp64 oracle, plus the deterministic mode's bit-reproducibility.
 The backward consumes the forward's O and LSE from the CUDA path (as a user
 would); the oracle recomputes everything from q, k, v, dO by the definition.
 Small problems are compared over every element; the workload shapes on
-sampled query rows (dQ) and key rows (dK, dV), and over whole tensors through
-two identities that hold at any size: sum_j dV_j = sum_i dO_i and
-sum_j dK_j = 0 (rows of P sum to one; rows of dS sum to zero).
+sampled query rows (dQ) and key rows (dK, dV) drawn over the whole sequence,
+in the default and the deterministic mode, and over whole tensors through two
+identities that hold at any size: sum_j dV_j = sum_i dO_i and sum_j dK_j = 0
+(rows of P sum to one; rows of dS sum to zero).
 """
 import numpy as np
 import pytest
@@ -145,12 +146,10 @@ def test_value_head_dim_deterministic_is_bit_identical():
 
 # ------------------------------------------------------------------ workload shapes
 
-def _rows(L, n, seed, tail=None):
+def _rows(L, n, seed):
+    """n seeded rows of [0, L) plus both edges of the first block boundary and the last row."""
     rng = np.random.default_rng(seed)
-    if tail is None:
-        rows = set(rng.choice(L, size=min(n, L), replace=False).tolist()) | {0, 127, 128, L - 1}
-    else:
-        rows = set((L - 1 - rng.choice(tail, size=min(n, tail), replace=False)).tolist()) | {L - 1, L - tail}
+    rows = set(rng.choice(L, size=min(n, L), replace=False).tolist()) | {0, 127, 128, L - 1}
     return sorted(r for r in rows if 0 <= r < L)
 
 
@@ -166,18 +165,17 @@ def _identities(t, dk, dv, what):
     assert ratio < 5e-2, f"{what}: |sum dK| / |dK| = {ratio:.3e}"
 
 
-def _workload_check(w, causal, heads, deterministic=False, tail_keys=None, kv_rows=True):
+def _workload_check(w, causal, heads, deterministic=False):
     t = inputs.make(w)
     dq, dk, dv = run_dense(t, causal, w.scale, deterministic)
     qrows = _rows(w.L, 16, w.seed)
-    krows = _rows(w.L, 12, w.seed + 1, tail=tail_keys) if kv_rows else []
+    krows = _rows(w.L, 12, w.seed + 1)
     bsel = sorted({0, w.B - 1})   # first and last batch entries
     sub = {n: t[n][bsel] for n in ("q", "k", "v", "do")}
     rq, rk, rv = oracle_bwd_subset(sub, w.scale, causal, heads=heads, qrows=qrows, krows=krows)
     assert_grad_close(to64(dq[bsel][:, qrows][:, :, heads]), rq[:, qrows], f"{w.name} dQ")
-    if kv_rows:
-        assert_grad_close(to64(dk[bsel][:, krows][:, :, heads]), rk[:, krows], f"{w.name} dK")
-        assert_grad_close(to64(dv[bsel][:, krows][:, :, heads]), rv[:, krows], f"{w.name} dV")
+    assert_grad_close(to64(dk[bsel][:, krows][:, :, heads]), rk[:, krows], f"{w.name} dK")
+    assert_grad_close(to64(dv[bsel][:, krows][:, :, heads]), rv[:, krows], f"{w.name} dV")
     _identities(t, dk, dv, w.name)
 
 
@@ -197,39 +195,60 @@ def test_workload_hdsweep_value_head_dim():
     _workload_check(inputs.HDSWEEP.with_(d=192, dv=128), True, heads=[3])
 
 
+@pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
-def test_workload_long(causal):
-    # causal: dK/dV sampled among the last 256 keys (cheap for the oracle);
-    # non-causal: dQ rows exactly, dK/dV through the identities over all keys
-    _workload_check(inputs.LONG, causal, heads=[7], tail_keys=256 if causal else None, kv_rows=causal)
-
-
-def test_workload_long_deterministic_repeatable():
+def test_workload_long(causal, deterministic):
+    """B1 H32 L32768: dQ rows and dK/dV rows sampled over the whole sequence
+    (key blocks 0 and 1 included: with a causal mask they see every query
+    block, and in the deterministic mode they take the most semaphore turns),
+    against the fp64 oracle on one head; deterministic runs also repeat bit
+    for bit."""
     w = inputs.LONG
     t = inputs.make(w)
-    a = run_dense(t, True, w.scale, deterministic=True)
-    b = run_dense(t, True, w.scale, deterministic=True)
-    for x, y in zip(a, b):
-        assert torch.equal(x, y)
+    got = run_dense(t, causal, w.scale, deterministic)
+    if deterministic:
+        again = run_dense(t, causal, w.scale, deterministic)
+        for x, y in zip(got, again):
+            assert torch.equal(x, y)
+    dq, dk, dv = got
+    heads = [7]
+    qrows = _rows(w.L, 16, w.seed)
+    krows = sorted(set(_rows(w.L, 12, w.seed + 1)) | {1, 64, 200, w.L // 2, w.L // 2 + 77})
+    rq, rk, rv = oracle_bwd_subset(t, w.scale, causal, heads=heads, qrows=qrows, krows=krows)
+    what = f"{w.name} causal={causal} det={deterministic}"
+    assert_grad_close(to64(dq[:, qrows][:, :, heads]), rq[:, qrows], f"{what} dQ")
+    assert_grad_close(to64(dk[:, krows][:, :, heads]), rk[:, krows], f"{what} dK")
+    assert_grad_close(to64(dv[:, krows][:, :, heads]), rv[:, krows], f"{what} dV")
+    _identities(t, dk, dv, what)
 
 
-def test_workload_varlen():
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_workload_varlen(deterministic):
     w = inputs.VARLEN
     t = inputs.make(w)
     cu = t["cu_seqlens"]
     q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "do"))
     cud = cu.cuda()
     o, lse = binding.forward(q, k, v, causal=True, scale=w.scale, cu_seqlens=cud)
-    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=True, scale=w.scale, cu_seqlens=cud)
+    dq, dk, dv = binding.backward(q, k, v, o, lse, do, causal=True, scale=w.scale, cu_seqlens=cud,
+                                  deterministic=deterministic)
     binding.check_status()
+    if deterministic:
+        again = binding.backward(q, k, v, o, lse, do, causal=True, scale=w.scale, cu_seqlens=cud,
+                                 deterministic=True)
+        binding.check_status()
+        for x, y in zip((dq, dk, dv), again):
+            assert torch.equal(x, y)
     lens = np.diff(cu.numpy())
     order = np.argsort(lens)
     for b in [int(order[0]), int(order[-1]), 5]:
         a, L = int(cu[b]), int(lens[b])
         sub = {n: t[n][a:a + L].unsqueeze(0) for n in ("q", "k", "v", "do")}
         qrows = _rows(L, 10, b)
-        krows = _rows(L, 8, b + 1, tail=min(256, L))
+        # key rows over the whole sequence: the first ones see every query row
+        krows = _rows(L, 8, b + 1)
         rq, rk, rv = oracle_bwd_subset(sub, w.scale, True, heads=[0, 9], qrows=qrows, krows=krows)
-        assert_grad_close(to64(dq[a:a + L][qrows][:, [0, 9]])[None], rq[:, qrows], f"varlen seq {b} dQ")
-        assert_grad_close(to64(dk[a:a + L][krows][:, [0, 9]])[None], rk[:, krows], f"varlen seq {b} dK")
-        assert_grad_close(to64(dv[a:a + L][krows][:, [0, 9]])[None], rv[:, krows], f"varlen seq {b} dV")
+        what = f"varlen seq {b} det={deterministic}"
+        assert_grad_close(to64(dq[a:a + L][qrows][:, [0, 9]])[None], rq[:, qrows], f"{what} dQ")
+        assert_grad_close(to64(dk[a:a + L][krows][:, [0, 9]])[None], rk[:, krows], f"{what} dK")
+        assert_grad_close(to64(dv[a:a + L][krows][:, [0, 9]])[None], rv[:, krows], f"{what} dV")
