@@ -5,10 +5,16 @@ A step is one pass of the whole path over one batch of synthetic input: for
 each mask variant of the workload, the forward and the backward (preprocess,
 main kernel, dQ conversion), called through the general entry points
 attn_fwd_ex / attn_bwd_ex (attn_fwd_varlen / attn_bwd_varlen for the
-prefill/decode mix). The default workload is B=4, H=16, L=4096, d=128
-(bf16), causal and non-causal. Throughput is algorithmic FLOPs / time:
-forward 2*(d + d_v) per unmasked (query, key) pair, backward 2*(3d + 2d_v)
-(2.5x the forward when d_v = d).
+prefill/decode mix). The default workload is the long-context one,
+B=1, H=32, L=32768, d=128 (bf16), causal and non-causal: the largest
+configuration of the five the parity tests cover. Throughput is algorithmic
+FLOPs / time: forward 2*(d + d_v) per unmasked (query, key) pair, backward
+2*(3d + 2d_v) (2.5x the forward when d_v = d).
+
+Beside the step, the same run times two single calls with their own roofline
+fraction: the causal forward at B=2, H=16, L=8192, d=128 (the workload whose
+forward has a stated goal of 55% of the dense BF16 peak), and the
+deterministic causal backward of the default workload.
 
   python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -61,7 +67,9 @@ WORKLOADS = {
     "mix32_prefill_decode_h16kv4d128": (inputs.PREFILL_DECODE, (True,)),
     "b1h32l32768d128": (inputs.LONG, (True, False)),
 }
-DEFAULT_WORKLOAD = "b4h16l4096d128"
+DEFAULT_WORKLOAD = "b1h32l32768d128"
+# the causal forward at d = 128, L = 8192 must reach this fraction of the dense BF16 peak
+TARGET_WORKLOAD, TARGET_FRAC = "b2h16l8192d128", 0.55
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -187,18 +195,18 @@ class Problem:
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
-    def bwd(self, causal):
+    def bwd(self, causal, deterministic=0):
         if self.cuk is not None:
             rc = binding.attn_bwd_varlen(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk,
                                          self.dv, self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.scale,
-                                         causal, self.cu, self.cuk, 0, self.ws, self.ws.numel())
+                                         causal, self.cu, self.cuk, deterministic, self.ws, self.ws.numel())
             if rc:
                 raise binding.AttnError(rc, binding.last_error())
             return
         rc = binding.attn_bwd_ex(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
                                  self.B, self.H, self.Hkv, self.Lq, self.Lk, self.d, self.w.d_v, self.w.scale, causal,
-                                 self.w.window[0], self.w.window[1], self.mask, 1, self.cu, None, 0, self.ws,
-                                 self.ws.numel())
+                                 self.w.window[0], self.w.window[1], self.mask, 1, self.cu, None, deterministic,
+                                 self.ws, self.ws.numel())
         if rc:
             raise binding.AttnError(rc, binding.last_error())
 
@@ -359,6 +367,53 @@ def barrier(dist):
         torch.cuda.synchronize()
 
 
+def time_single(prob, call, steps, warmup):
+    """Mean CUDA-event time (ms) of one call, on the stream it is launched on,
+    over `steps` back-to-back runs after `warmup` untimed ones."""
+    for _ in range(max(warmup, 3)):
+        call(prob)
+    binding.check_status()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record()
+        call(prob)
+        b.record()
+    torch.cuda.synchronize()
+    binding.check_status()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def single_call_records(args, pk, dev, main_prob):
+    """The goal row (causal forward, d = 128, L = 8192) and the deterministic
+    causal backward of the long-context workload, each with its own fraction
+    of the measured dense BF16 peak."""
+    out = {}
+    w, _ = WORKLOADS[TARGET_WORKLOAD]
+    prob = main_prob if args.workload == TARGET_WORKLOAD else Problem(w, dev)
+    t_ms = time_single(prob, lambda p_: p_.fwd(True), args.steps, args.warmup)
+    fl = flops(w, True, "fwd")
+    ach = fl / (t_ms * 1e-3) / 1e12
+    out["target"] = {"workload": TARGET_WORKLOAD, "call": "attn_fwd (causal)", "ms": t_ms, "achieved": ach,
+                     "unit": UNIT, "peak": pk["bf16"], "frac": ach / pk["bf16"], "goal_frac": TARGET_FRAC,
+                     "met": ach / pk["bf16"] >= TARGET_FRAC,
+                     "l2": "inputs 192 MiB > 129 MiB L2; no flush between calls"}
+    if prob is not main_prob:
+        del prob
+        torch.cuda.empty_cache()
+    wl, _ = WORKLOADS["b1h32l32768d128"]
+    prob = main_prob if args.workload == "b1h32l32768d128" else None
+    if prob is not None:
+        prob.fwd(True)
+        t_ms = time_single(prob, lambda p_: p_.bwd(True, deterministic=1), args.steps, args.warmup)
+        fl = flops(wl, True, "bwd")
+        ach = fl / (t_ms * 1e-3) / 1e12
+        out["deterministic"] = {"workload": "b1h32l32768d128", "call": "attn_bwd (causal, deterministic)",
+                                "ms": t_ms, "achieved": ach, "unit": UNIT, "peak": pk["bf16"],
+                                "frac": ach / pk["bf16"]}
+    return out
+
+
 # ------------------------------------------------------------------------------------------ oracle
 # About 10 s of the oracle on 16 host cores (it runs near 0.027 TFLOP/s there).
 ORACLE_SAMPLE_FLOPS = 3e11
@@ -511,6 +566,9 @@ def run_ours(args, world, rank, local, dist):
                 "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the main kernel, per launch"}
 
+    # ---- the goal row and the deterministic backward, one call each
+    extra = {} if args.no_extra else single_call_records(args, pk, dev, prob)
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -546,7 +604,7 @@ def run_ours(args, world, rank, local, dist):
                            "l2": f"inputs {input_bytes / 2**20:.0f} MiB > 129 MiB L2; no flush between steps",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
                 "frac_of_peak": value / world / pk["bf16"],
-                "roofline": roofline, "roofline_calls": rooflines,
+                "roofline": roofline, "roofline_calls": rooflines, **extra,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps * len(variants) * (4 if "bwd" in kinds else 1),
                 "clocks": clk.summary()}
@@ -563,6 +621,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the goal-row and deterministic single-call timings")
     args = ap.parse_args()
     world, rank, local, dist = dist_setup() if args.impl == "ours" else (
         int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None)
