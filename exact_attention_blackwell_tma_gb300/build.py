@@ -22,7 +22,7 @@ LIBS = {
     "libattn.so": ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide.cu", "bwd_pair.cu"],
     "libattn_selftest.so": ["selftest.cu"],
 }
-HEADERS = ["ptx.cuh", "sched.cuh", "kernels.h", "mask.cuh", "dq_order.cuh"]
+HEADERS = ["ptx.cuh", "sched.cuh", "kernels.h", "mask.cuh", "dq_order.cuh", "dq_reduce.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

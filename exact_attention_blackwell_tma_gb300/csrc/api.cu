@@ -438,7 +438,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     if (!make_map(&tq, qsrc, qrows, hq_map, d) || !make_map(&tk, rows_k > 0 ? k : q, krows, Hkv, d) ||
         !make_map(&tv, rows_k > 0 ? v : q, krows, Hkv, d_v) || !make_map(&tdo, dosrc, qrows, hq_map, d_v) ||
         !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d) || !make_map(&pm.q64, qsrc, qrows, hq_map, d, 64) ||
-        !make_map(&pm.do64, dosrc, qrows, hq_map, d_v, 64) || !make_map_f32(&pm.dq64, p.dq_acc, qrows, hq_map, d, 64))
+        !make_map(&pm.do64, dosrc, qrows, hq_map, d_v, 64) || !make_map_f32(&pm.dq32, p.dq_acc, qrows, hq_map, d, 32))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, pm, g_bwd_pairs.load() != 0, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));

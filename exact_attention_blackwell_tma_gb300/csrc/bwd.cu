@@ -23,6 +23,7 @@
 #include "mask.cuh"
 #include "sched.cuh"
 #include "dq_order.cuh"
+#include "dq_reduce.cuh"
 
 namespace attn {
 namespace {
@@ -66,8 +67,8 @@ struct BwdLayout {
                          kSFull = kDOEmpty + kDOStages, kDPFull = kSFull + 1,
                          kPFull = kDPFull + 1, kDSFull = kPFull + 1, kDSEmpty = kDSFull + 1,   // two
                          kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1, kDKVFull = kDQFree + 1,
-                         kSemGo = kDKVFull + 1, kStageReady = kSemGo + 1,
-                         kStageFree = kStageReady + 1, kDrain = kStageFree + 1, kNumBars = kDrain + 1;
+                         kSemGo = kDKVFull + 1, kRedDone = kSemGo + 1, kDrain = kRedDone + 1,
+                         kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory columns. Compute warpgroup wg owns query columns
@@ -350,7 +351,7 @@ template <int HD, bool kDet, bool kGQA, bool kBand, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-           const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, const VarlenMap* vm) {
+           const __grid_constant__ CUtensorMap tmDQ32, const BwdParams p, const VarlenMap* vm) {
     using Lay = BwdLayout<HD>;
     constexpr int NQS = Lay::kQStages, NDS = Lay::kDOStages;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -380,14 +381,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(Lay::kDPFull), 1);
         mbar_init(bar(Lay::kPFull), 256);
         mbar_init(bar(Lay::kDSFull), 256);
-        mbar_init(bar(Lay::kDSEmpty + 0), 1);
-        mbar_init(bar(Lay::kDSEmpty + 1), 1);
+        mbar_init(bar(Lay::kDSEmpty + 0), 4);   // each dQ warp releases its rows of the stage
+        mbar_init(bar(Lay::kDSEmpty + 1), 4);
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
-        mbar_init(bar(Lay::kStageReady), 128);
-        mbar_init(bar(Lay::kStageFree), 1);
+        mbar_init(bar(Lay::kRedDone), 4);       // deterministic: each dQ warp's adds are complete
         mbar_init(bar(Lay::kDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -397,7 +397,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO);
-        tma_prefetch_desc(&tmDQ);
+        tma_prefetch_desc(&tmDQ32);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -796,16 +796,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // ------------------------------------------------------------ dQ read-out warpgroup
         // Each dQ tile (128 query rows x d, fp32) goes from tensor memory to the
         // global accumulator: staged through shared memory (the dS^T tile this
-        // block's dQ MMA has read) in 128-row x 32-column swizzled boxes and added
-        // by TMA bulk reduce-adds, d/64 rounds of two boxes. Deterministic mode:
-        // the same reduce-adds under the tile's semaphore, in key-block order,
-        // each block's completing before the next block's start.
+        // block's dQ MMA has read) and added by TMA reduce-adds, each warp its own
+        // 32 rows (dq_reduce.cuh). Deterministic mode: the same reduce-adds under
+        // the tile's semaphore, in key-block order, every warp's completing before
+        // the next block's start.
         const int quarter = warp & 3;
-        const int rq = quarter * 32 + lane;        // query row inside the block
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, rdc = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -849,50 +848,27 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-#pragma unroll
-                for (int rnd = 0; rnd < HD / 64; ++rnd) {
-                    const bool last = rnd == HD / 64 - 1;
-                    if (rnd > 0) {
-                        ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
-                        ++sfree;
-                        if (!ok) break;
+                dq_warp_reduce(&tmDQ32, stage, stage_s, row, HD / 64, 0, qw.h, f.q_row0 + m * kBM, quarter, lane);
+                if (lane == 0) {
+                    if constexpr (kDet) {
+                        bulk_wait_group0();   // this warp's adds are complete
+                        fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kRedDone));
+                    } else {
+                        bulk_wait_group_read0();
                     }
-#pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
-                        const int c0 = rnd * 64 + c2 * 32;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)   // 128-byte swizzle: chunk j at j ^ (row % 8)
-                            *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
-                                make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
-                                           row[c0 + 4 * j + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(Lay::kStageReady));
-                    if (leader) {
-                        if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            // rows past the query block's sequence carry exact zeros (P = 0 there)
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, rnd * 64 + c2 * 32, qw.h,
-                                                  f.q_row0 + m * kBM);
-                            bulk_commit_group();
-                            if (kDet && last) {
-                                // every reduce-add of this block is complete before the next block's start
-                                bulk_wait_group0();
-                                fence_proxy_async_global();
-                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                            } else {
-                                bulk_wait_group_read0();
-                            }
-                        }
-                        mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
-                    }
-                    ++srdy;
+                    mbar_arrive(bar(Lay::kDSEmpty + dsb));   // this warp's rows of the stage are read
                 }
-                if (!ok) break;
+                if constexpr (kDet) {
+                    // every warp's adds of this block are complete: the next block's turn
+                    if (leader && mbar_wait(bar(Lay::kRedDone), rdc & 1u, w))
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                    ++rdc;
+                }
+                __syncwarp();
             }
         }
-        if (leader) bulk_wait_group0();   // the last reduce-adds complete before the CTA exits
+        if (lane == 0) bulk_wait_group0();   // the last reduce-adds complete before the CTA exits
     }
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
@@ -936,10 +912,10 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         BwdParams pp = p;   // work tiles are key-block pairs
         pp.nm = bwd_pair_tiles_per_head(g.Lk);
         pp.n_tiles = varlen ? 0 : g.B * g.H * pp.nm;
-        e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq64, pp, vm, num_sms, stream);
+        e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq32, pp, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else if constexpr (HD > 128) {
-        e = launch_bwd_wide(tq, tk, tv, tdo, tdq, p, vm, num_sms, stream);
+        e = launch_bwd_wide(tq, tk, tv, tdo, pm.dq32, p, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else {
         using Lay = BwdLayout<HD>;
@@ -958,7 +934,7 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
         const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
         if (grid > 0) {
-            kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p, vm);
+            kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, pm.dq32, p, vm);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }

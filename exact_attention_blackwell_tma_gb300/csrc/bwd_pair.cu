@@ -76,7 +76,7 @@ struct Lay {
                          kKVEmpty = kDQFree + 1, kQEmpty = kKVEmpty + 1, kStatFull = kQEmpty + kQStages,
                          kDOEmpty = kStatFull + kQStages, kSFull = kDOEmpty + 1, kDPFull = kSFull + 1,
                          kDSEmpty = kDPFull + 1, kDQFull = kDSEmpty + 1, kDKVFull = kDQFull + 1,
-                         kSemGo = kDKVFull + 1, kStageReady = kSemGo + 1, kDrain = kStageReady + 1,
+                         kSemGo = kDKVFull + 1, kRedDone = kSemGo + 1, kDrain = kRedDone + 1,
                          kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -140,7 +140,7 @@ template <bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO64,
-                const __grid_constant__ CUtensorMap tmDQ64, const BwdParams p, const VarlenMap* vm) {
+                const __grid_constant__ CUtensorMap tmDQ32, const BwdParams p, const VarlenMap* vm) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -162,7 +162,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         mbar_init(bar(Lay::kKVFull), 1);
         for (int s = 0; s < Lay::kQStages; ++s) {
             mbar_init(bar(Lay::kQFull + s), 1);
-            mbar_init(bar(Lay::kQEmpty + s), 1);
+            mbar_init(bar(Lay::kQEmpty + s), 4);   // each dQ warp: its rows of the staged dQ are read
             mbar_init(bar(Lay::kStatFull + s), 1);
         }
         mbar_init(bar(Lay::kDOFull), 1);
@@ -177,7 +177,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
-        mbar_init(bar(Lay::kStageReady), 128);
+        mbar_init(bar(Lay::kRedDone), 4);      // deterministic: each dQ warp's adds are complete
         mbar_init(bar(Lay::kDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -187,7 +187,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO64);
-        tma_prefetch_desc(&tmDQ64);
+        tma_prefetch_desc(&tmDQ32);
     }
     if (warp == 1) {   // both CTAs allocate: the pair gets the same columns in each
         tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
@@ -550,9 +550,11 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         // This CTA's 64 queries of the block x 128 columns, summed over the pair's
         // 256 keys by the MMA: tensor-memory lanes 0-63 hold columns 0-63 of query
         // rows 0-63 and lanes 64-127 columns 64-127 of the same rows. Staged through
-        // the Q stage the block's dK product has finished reading, in four 64-row x
-        // 32-column swizzled boxes, and added with TMA reduce-adds; deterministic
-        // mode: under the semaphore of this query-row half, pairs in a fixed order.
+        // the Q stage the block's dK product has finished reading, as four 64-row x
+        // 32-column swizzled boxes; each warp adds its own 32 rows x 64 columns with
+        // TMA reduce-adds issued by its lane 0 (two 32-row boxes). Deterministic
+        // mode: under the semaphore of this query-row half, pairs in a fixed order,
+        // every warp's adds complete before the next pair's turn.
         const int q4 = warp - 12;
         const int qr = (q4 & 1) * 32 + lane;      // query row inside this CTA's 64
         const int half = q4 >> 1;                 // columns [64 half, 64 half + 64)
@@ -560,7 +562,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
         const uint32_t dqfree = lbar(Lay::kDQFree);
-        uint32_t dqc = 0, sgo = 0, srdy = 0;
+        uint32_t dqc = 0, sgo = 0, rdc = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = cl; t < n_tiles && ok; t = snake_tile(cl, ++k, ncl)) {
@@ -607,28 +609,31 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                                        row[bx * 32 + 4 * j + 3]);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(bar(Lay::kStageReady));
-                if (leader) {
-                    if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                        // rows past the sequence carry exact zeros (P = 0 there)
-                        for (int bx = 0; bx < 4; ++bx)
-                            tma_reduce_add_3d(&tmDQ64, stage_s + bx * kQuad, bx * 32, f.h,
-                                              f.q_row0 + m * kBM + 64 * (int)rank);
-                        bulk_commit_group();
-                        if (kDet) {
-                            bulk_wait_group0();
-                            fence_proxy_async_global();
-                            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                        } else {
-                            bulk_wait_group_read0();
-                        }
+                __syncwarp();
+                if (lane == 0) {
+                    // this warp's 32 rows (rows past the sequence carry exact zeros: P = 0 there)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_reduce_add_3d(&tmDQ32, stage_s + (2 * half + bx) * kQuad + (q4 & 1) * 4096,
+                                          (2 * half + bx) * 32, f.h, f.q_row0 + m * kBM + 64 * (int)rank + (q4 & 1) * 32);
+                    bulk_commit_group();
+                    if constexpr (kDet) {
+                        bulk_wait_group0();
+                        fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kRedDone));
+                    } else {
+                        bulk_wait_group_read0();
                     }
-                    mbar_arrive(bar(Lay::kQEmpty + st));   // the stage may take the next Q block
+                    mbar_arrive(bar(Lay::kQEmpty + st));   // this warp's rows of the stage are read
                 }
-                ++srdy;
+                if constexpr (kDet) {
+                    if (leader && mbar_wait(bar(Lay::kRedDone), rdc & 1u, w))
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                    ++rdc;
+                }
+                __syncwarp();
             }
         }
-        if (leader) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
     }
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
@@ -652,7 +657,7 @@ bool bwd_pair_supported(const BwdParams& p) {
 int bwd_pair_tiles_per_head(int Lk) { return (Lk + 2 * kBN - 1) / (2 * kBN); }
 
 cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo64, const CUtensorMap& tdq64, const BwdParams& p,
+                            const CUtensorMap& tdo64, const CUtensorMap& tdq32, const BwdParams& p,
                             const void* varlen_map, int num_sms, cudaStream_t stream) {
     auto kern = p.deterministic ? bwd_pair_kernel<true> : bwd_pair_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
@@ -683,7 +688,7 @@ cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, cons
     const int clusters = varlen ? max_clusters : min(p.n_tiles, max_clusters);
     if (clusters <= 0) return cudaSuccess;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, kern, tq64, tk, tv, tdo64, tdq64, p,
+    return cudaLaunchKernelEx(&cfg, kern, tq64, tk, tv, tdo64, tdq32, p,
                               static_cast<const VarlenMap*>(varlen_map));
 }
 

@@ -25,6 +25,7 @@
 #include "mask.cuh"
 #include "sched.cuh"
 #include "dq_order.cuh"
+#include "dq_reduce.cuh"
 
 namespace attn {
 namespace {
@@ -65,7 +66,7 @@ struct WideBwdLayout {
                          kSFull = kStatFull + 2, kDPFull = kSFull + 1, kPFull = kDPFull + 1, kDSFull = kPFull + 1,
                          kDSEmpty = kDSFull + 1, kDQFull = kDSEmpty + 2, kDQFree = kDQFull + 1,
                          kDKVFull = kDQFree + 1, kSemGo = kDKVFull + 1,
-                         kStageReady = kSemGo + 1, kStageFree = kStageReady + 1, kDrain = kStageFree + 1,
+                         kRedDone = kSemGo + 1, kDrain = kRedDone + 1,
                          kNumBars = kDrain + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16;
@@ -259,14 +260,13 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(Lay::kDPFull), 1);
         mbar_init(bar(Lay::kPFull), 256);
         mbar_init(bar(Lay::kDSFull), 256);
-        mbar_init(bar(Lay::kDSEmpty + 0), 1);
-        mbar_init(bar(Lay::kDSEmpty + 1), 1);
+        mbar_init(bar(Lay::kDSEmpty + 0), 4);   // each dQ warp releases its rows of the stage
+        mbar_init(bar(Lay::kDSEmpty + 1), 4);
         mbar_init(bar(Lay::kDQFull), 1);
         mbar_init(bar(Lay::kDQFree), 128);
         mbar_init(bar(Lay::kDKVFull), 1);
         mbar_init(bar(Lay::kSemGo), 1);
-        mbar_init(bar(Lay::kStageReady), 128);
-        mbar_init(bar(Lay::kStageFree), 1);
+        mbar_init(bar(Lay::kRedDone), 4);       // deterministic: each dQ warp's adds are complete
         mbar_init(bar(Lay::kDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -714,16 +714,15 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ dQ read-out warpgroup
-        // As in bwd.cu, for one column chunk: TMA reduce-adds of 128-row x
-        // 32-column boxes staged through this block's dS tile; deterministic
-        // mode: the same reduce-adds under the chunk's semaphore, each key block's
-        // completing before the next one's start.
+        // As in bwd.cu, for one column chunk: each warp adds its own 32 rows with
+        // TMA reduce-adds staged through this block's dS tile (dq_reduce.cuh);
+        // deterministic mode: the same reduce-adds under the chunk's semaphore,
+        // every warp's completing before the next key block's start.
         const int quarter = warp & 3;
-        const int rq = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
-        uint32_t dqc = 0, sgo = 0, srdy = 0, sfree = 0;
+        uint32_t dqc = 0, sgo = 0, rdc = 0;
         bool ok = true;
         uint32_t rr[32];
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -767,49 +766,27 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 tc_fence_before_sync();
                 mbar_arrive(bar(Lay::kDQFree));
-#pragma unroll
-                for (int rnd = 0; rnd < 2; ++rnd) {
-                    if (rnd >= rounds) break;
-                    const bool last = rnd == rounds - 1;
-                    if (rnd > 0) {
-                        ok = warp_wait(bar(Lay::kStageFree), sfree & 1u, w, lane);
-                        ++sfree;
-                        if (!ok) break;
+                dq_warp_reduce(&tmDQ, stage, stage_s, row, rounds, 128 * f.c, qw.h, f.q_row0 + m * kBM, quarter,
+                               lane);
+                if (lane == 0) {
+                    if constexpr (kDet) {
+                        bulk_wait_group0();   // this warp's adds are complete
+                        fence_proxy_async_global();
+                        mbar_arrive(bar(Lay::kRedDone));
+                    } else {
+                        bulk_wait_group_read0();
                     }
-#pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        uint8_t* srow = stage + c2 * kBox + (rq >> 3) * 1024 + (rq & 7) * 128;
-                        const int c0 = rnd * 64 + c2 * 32;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4*>(srow + ((j ^ (rq & 7)) << 4)) =
-                                make_uint4(row[c0 + 4 * j], row[c0 + 4 * j + 1], row[c0 + 4 * j + 2],
-                                           row[c0 + 4 * j + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(Lay::kStageReady));
-                    if (leader) {
-                        if (mbar_wait(bar(Lay::kStageReady), srdy & 1u, w)) {
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                tma_reduce_add_3d(&tmDQ, stage_s + c2 * kBox, 128 * f.c + rnd * 64 + c2 * 32,
-                                                  qw.h, f.q_row0 + m * kBM);
-                            bulk_commit_group();
-                            if (kDet && last) {
-                                bulk_wait_group0();
-                                fence_proxy_async_global();
-                                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-                            } else {
-                                bulk_wait_group_read0();
-                            }
-                        }
-                        mbar_arrive(bar(last ? Lay::kDSEmpty + dsb : Lay::kStageFree));
-                    }
-                    ++srdy;
+                    mbar_arrive(bar(Lay::kDSEmpty + dsb));   // this warp's rows of the stage are read
                 }
-                if (!ok) break;
+                if constexpr (kDet) {
+                    if (leader && mbar_wait(bar(Lay::kRedDone), rdc & 1u, w))
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+                    ++rdc;
+                }
+                __syncwarp();
             }
         }
-        if (leader) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
     }
     tc_fence_before_sync();
     __syncthreads();

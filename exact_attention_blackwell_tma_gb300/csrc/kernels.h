@@ -120,10 +120,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // work tile (nm counts 128-row blocks).
 cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_sms, cudaStream_t stream);
-// Tensor maps with 64-row boxes (q, dO: 64 rows x 64 columns bf16; the dQ
-// accumulator: 64 rows x 32 columns fp32), used by the CTA-pair backward.
+// Tensor maps with boxes of fewer rows: q and dO in 64-row x 64-column bf16
+// boxes (the CTA-pair backward), and the dQ accumulator in 32-row x 32-column
+// fp32 boxes (each dQ warp adds its own 32 rows, dq_reduce.cuh).
 struct PairMaps {
-    CUtensorMap q64, do64, dq64;
+    CUtensorMap q64, do64, dq32;
 };
 // pair: run the main kernel on CTA pairs when bwd_pair_supported(p) holds.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -137,12 +138,13 @@ bool bwd_pair_supported(const BwdParams& p);
 // key-block pairs per (batch, head) of Lk keys
 int bwd_pair_tiles_per_head(int Lk);
 cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo64, const CUtensorMap& tdq64, const BwdParams& p,
+                            const CUtensorMap& tdo64, const CUtensorMap& tdq32, const BwdParams& p,
                             const void* varlen_map, int num_sms, cudaStream_t stream);
 
 // Main kernel of the backward for head dims 192 and 256 (preprocess and dQ
-// conversion are shared with the d <= 128 path). varlen_map: the VarlenMap the
-// preprocess kernel builds in the workspace (read only for varlen problems).
+// conversion are shared with the d <= 128 path). tdq_acc: the dQ accumulator in
+// 32-row x 32-column boxes. varlen_map: the VarlenMap the preprocess kernel
+// builds in the workspace (read only for varlen problems).
 cudaError_t launch_bwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdParams& p,
                             const void* varlen_map, int num_sms, cudaStream_t stream);
