@@ -83,39 +83,43 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 821.898e6 + 479.444e6,
+        "bytes": 813.827e6 + 476.064e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
+                "4f102ff15eac13f2afe75a480aaf4adf7a1d3029907b9d650f107f5b00796356",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "88be7192335af7bd9df50bd519e6da2e23c72f3a3a263d4ef33d2f5abac13898",
+                "5611492efba67473908868e7e95af02995ec2acabe1500b8104d04459416985b",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "03d6c4f342d65da22060e6d69d9f490978d56ded7dca12337f5845aecf433e43",
+                "f8bc257a612049ccb342efadbcd5376c275b39b89f5a9e48e810f89b3378c5e6",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
                 "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
+                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
         },
     },
     ("b4h16l4096d128", "bwd", True): {
-        "bytes": 1887.251e6 + 967.382e6,
+        "bytes": 1833.847e6 + 944.477e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "7b169e6e94e5ca6e0db54e96282f8c43b49808f5ee0df46cf6d0ce4451a16b4e",
+                "4f102ff15eac13f2afe75a480aaf4adf7a1d3029907b9d650f107f5b00796356",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "88be7192335af7bd9df50bd519e6da2e23c72f3a3a263d4ef33d2f5abac13898",
+                "5611492efba67473908868e7e95af02995ec2acabe1500b8104d04459416985b",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "03d6c4f342d65da22060e6d69d9f490978d56ded7dca12337f5845aecf433e43",
+                "f8bc257a612049ccb342efadbcd5376c275b39b89f5a9e48e810f89b3378c5e6",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
                 "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
+                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
         },
     },
 }
