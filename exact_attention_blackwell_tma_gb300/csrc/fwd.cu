@@ -260,15 +260,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             int kb = kGeneral ? f.kv_first : 0;   // key block of stream block j
             if (sparse) kb = sparse_next(f.mrow0, f.mrow1, kb, f.kb_end, lane);
             for (int j = 0; j < f.n_kv && ok; ++j) {
+                // K and V of a block complete on the K slot's barrier (one wait for both)
+                const uint32_t slot_k = kv_cnt % S;
                 for (int kv = 0; kv < 2; ++kv) {
                     const uint32_t slot = kv_cnt % S, ph = (kv_cnt / S) & 1u;
                     ok = warp_wait(bar(Lay::kKVEmpty + slot), ph ^ 1u, w, lane);
                     if (!ok) break;
                     if (lane == 0) {
-                        mbar_expect_tx(bar(Lay::kKVFull + slot), Lay::kTileBytes);
+                        if (kv == 0) mbar_expect_tx(bar(Lay::kKVFull + slot_k), 2 * Lay::kTileBytes);
                         for (int hf = 0; hf < Lay::kHalves; ++hf)
                             tma_load_3d(base + Lay::kKVOff + slot * Lay::kTileBytes + hf * kBox,
-                                        kv ? &tmV : &tmK, bar(Lay::kKVFull + slot), hf * 64, f.hk,
+                                        kv ? &tmV : &tmK, bar(Lay::kKVFull + slot_k), hf * 64, f.hk,
                                         f.k_row0 + (kGeneral ? kb : j) * kBN);
                     }
                     __syncwarp();
@@ -282,7 +284,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (q_issued) drain_wait(bar(Lay::kQFull), (q_issued - 1) & 1u, p.wait_budget_ns);
             for (uint32_t i = 0; i < (uint32_t)S && i < kv_cnt; ++i) {
                 const uint32_t n = kv_cnt - 1 - i;
-                drain_wait(bar(Lay::kKVFull + n % S), (n / S) & 1u, p.wait_budget_ns);
+                if ((n & 1u) == 0) drain_wait(bar(Lay::kKVFull + n % S), (n / S) & 1u, p.wait_budget_ns);
             }
         }
         __syncwarp();
@@ -345,9 +347,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             __syncwarp();
             for (int j = 0; j < f.n_kv; ++j) {
-                const uint32_t slot_v = kv_cnt % S;
-                ok = warp_wait(bar(Lay::kKVFull + slot_v), (kv_cnt / S) & 1u, w, lane);
-                if (!ok) break;
+                const uint32_t slot_v = kv_cnt % S;   // arrived with the block's K
                 ++kv_cnt;
                 const bool more = j + 1 < f.n_kv;
                 // tile 0: PV for block j, then S for block j+1 (while it sees them)
