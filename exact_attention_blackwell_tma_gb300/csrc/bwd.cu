@@ -166,12 +166,14 @@ __device__ __forceinline__ BwdTile bwd_tile(int t, const BwdParams& p, const Var
     // Dense problems walk the heads in L2-sized sections, longest key blocks first
     // within a section (FlashAttention-4 paper, Section 3.3): a section's Q, dO and
     // dQ accumulator stay in L2 (B1 H32 L32768 causal: 43 -> 9.5 GB of DRAM traffic
-    // per launch, 975 -> 1045 TF/s). The deterministic kernels keep one global
-    // order of levels instead, shortest first (SPT), which their dQ turns need.
+    // per launch, 975 -> 1045 TF/s). Causal problems whose sections would leave the
+    // CTAs unbalanced keep one global longest-first order (p.sections, chosen on
+    // the host by sched_sections_pay); the deterministic kernels keep one global
+    // order too, shortest first (SPT), which their dQ turns need.
     const bool spt = kSpt && g.causal;
     Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, kBN, p.head_section, spt, true)
-                 : (spt ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, true)
-                        : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
+                 : ((g.causal && (spt || !p.sections)) ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, spt)
+                                                        : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
     BwdTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -913,10 +915,13 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaSuccess;
+    // Q and dO bytes of every query head: the working set of a global walk
+    const double ws_bytes = 2.0 * 2.0 * (double)rows_q * g.H * HD;
     if (pair) {
         BwdParams pp = p;   // work tiles are key-block pairs
         pp.nm = bwd_pair_tiles_per_head(g.Lk);
         pp.n_tiles = varlen ? 0 : g.B * g.H * pp.nm;
+        pp.sections = sched_sections_pay(g.B, g.H, pp.nm, p.head_section, 1, num_sms / 2, ws_bytes) ? 1 : 0;
         e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq32, pp, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else if constexpr (HD > 128) {
@@ -938,8 +943,10 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         // the register split re-distributes exactly the registers the CTA launches with
         if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
         const int grid = varlen ? num_sms : min(p.n_tiles, num_sms);
+        BwdParams pk = p;
+        pk.sections = sched_sections_pay(g.B, g.Hkv, p.nm, p.head_section, gqa ? p.split : 1, grid, ws_bytes) ? 1 : 0;
         if (grid > 0) {
-            kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, pm.dq32, p, vm);
+            kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, pm.dq32, pk, vm);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }

@@ -101,11 +101,12 @@ template <bool kSpt>
 __device__ __forceinline__ PairTile pair_tile(int t, const BwdParams& p, const VarlenMap* vm, uint32_t rank) {
     const Geometry& g = p.g;
     const bool spt = kSpt && g.causal;
-    // heads in L2-sized sections, longest pairs first within a section; the
-    // deterministic kernel keeps one global order of levels, shortest first
+    // heads in L2-sized sections, longest pairs first within a section, where
+    // that pays (p.sections, as in bwd.cu); the deterministic kernel keeps one
+    // global order of levels, shortest first
     Tile ti = vm ? sched_varlen(*vm, t, g.B, g.H, 2 * kBN, p.head_section, spt, true)
-                 : (spt ? sched_dense_lpt(t, g.B, g.H, p.nm, true)
-                        : sched_dense(t, g.H, p.nm, p.head_section, false));
+                 : ((g.causal && (spt || !p.sections)) ? sched_dense_lpt(t, g.B, g.H, p.nm, spt)
+                                                        : sched_dense(t, g.H, p.nm, p.head_section, false));
     PairTile f;
     f.b = ti.b;
     f.h = ti.h;

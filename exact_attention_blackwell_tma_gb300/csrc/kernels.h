@@ -74,6 +74,7 @@ struct BwdParams {
     int nm;                   // dense: 128-row K/V blocks per (b, h)
     int nq;                   // dense: 128-row Q blocks per (b, h)
     int head_section;
+    int sections;             // causal dense, default mode: walk heads in sections (sched_sections_pay)
     int* status;
     uint64_t wait_budget_ns;
     BlockMask mask;

@@ -79,6 +79,43 @@ __host__ __device__ __forceinline__ Tile sched_dense(int t, int H, int nm, int h
     return ti;
 }
 
+// Whether a causal dense backward (default mode) should walk its heads in
+// L2-sized sections (sched_dense) rather than in one global longest-first order
+// (sched_dense_lpt). Sections keep a section's Q, dO and dQ accumulator in L2;
+// their tile lengths form a sawtooth (longest first within each section), which
+// the boustrophedon hand-out balances less well. Measured on GB300 (d = 128
+// unless stated): B1 H32 L32768 gained 10% (a 537 MB working set of Q and dO,
+// 7% imbalance), B4 H16 L4096 11% (134 MB, 4%), B2 H16 L8192 lost 2% (134 MB,
+// 10.5%; d = 64 lost 11%). So: sections when the heads' Q and dO exceed three
+// L2s, or when the sectioned order leaves the busiest CTA under 5% above the
+// mean (host simulation of the hand-out below). units: key blocks (or pairs)
+// per (b, h); nkv: key/value heads; split: tiles per key block; grid: CTAs (or
+// clusters) of the launch; ws_bytes: Q and dO bytes of all query heads.
+inline bool sched_sections_pay(int B, int nkv, int units, int hs, int split, int grid, double ws_bytes) {
+    if (ws_bytes > 3.0 * 129.0e6) return true;
+    const long n = (long)B * nkv * units * split;
+    if (grid <= 0 || n <= grid || hs >= nkv * B) return false;
+    double total = 0, worst = 0;
+    for (int cta = 0; cta < grid; ++cta) {
+        double load = 0;
+        for (int k = 0;; ++k) {
+            const int t = snake_tile(cta, k, grid);
+            if (t >= n) break;
+            // tile t of the sectioned order: the key block's level inside its section
+            const int u = t / split;
+            const int per_b = nkv * units;
+            const int rem = u % per_b;
+            const int s = rem / (hs * units), h0 = s * hs;
+            const int sec_h = hs < nkv - h0 ? hs : nkv - h0;
+            const int level = (rem - s * hs * units) / sec_h;
+            load += units - level;   // causal: the key block at level l sees units - l query blocks
+        }
+        total += load;
+        worst = load > worst ? load : worst;
+    }
+    return worst < 1.05 * total / grid;
+}
+
 // Tables for a varlen problem (shared memory in the forward, the workspace in
 // the backward).
 struct VarlenMap {

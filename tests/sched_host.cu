@@ -278,7 +278,21 @@ static void check_dq_order() {
         }
 }
 
+// The backward's choice of tile order for causal dense problems
+// (sched_sections_pay) on the benchmark's workloads, as measured on GB300:
+// sections for B4 H16 L4096 and B1 H32 L32768, one global order for B2 H16
+// L8192 (d = 64 and 128); never sections when every tile fits one round.
+static void check_sections_choice() {
+    auto ws = [](double B, double H, double L, double d) { return 4.0 * B * L * H * d; };
+    if (!sched_sections_pay(4, 16, 32, 16, 1, 152, ws(4, 16, 4096, 128))) fail("sections B4 H16 L4096", 4, 16, 4096);
+    if (!sched_sections_pay(1, 32, 256, 3, 1, 152, ws(1, 32, 32768, 128))) fail("sections B1 H32 L32768", 1, 32, 32768);
+    if (sched_sections_pay(2, 16, 64, 16, 1, 152, ws(2, 16, 8192, 128))) fail("global B2 H16 L8192 d128", 2, 16, 8192);
+    if (sched_sections_pay(2, 16, 64, 16, 1, 152, ws(2, 16, 8192, 64))) fail("global B2 H16 L8192 d64", 2, 16, 8192);
+    if (sched_sections_pay(1, 2, 8, 1, 1, 152, ws(1, 2, 1024, 128))) fail("one round", 1, 2, 1024);
+}
+
 int main() {
+    check_sections_choice();
     for (int lq : {1, 130, 300, 517})
         for (int lk : {1, 130, 300, 517})
             for (int wl : {-1, 0, 3, 128, 200})
