@@ -643,8 +643,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     ++qc;
                     st = st_next;
                 }
-                continue;
-            }
+            } else {
             for (int u = 0; u < f.nblk; ++u) {
                 const uint32_t sd = qc % NDS, dsb = qc & 1u;   // dO stage, dS tile of this block
                 const SmemDesc do_km = at_stage(do_km0, sd), do_mn = at_stage(do_mn0, sd);
@@ -701,11 +700,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (lane == 0) {
 #pragma unroll
                     for (int k = 0; k < kBM / 16; ++k)
-                        mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(k),
+                        mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDS + packed_col(k),
                                q_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k)
-                        mma_ss(tmem + Lay::kTDP, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
+                        mma_ss(tmem + Lay::kTDQ, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
                                k > 0 ? 1u : 0u);
                     tc_commit(bar(Lay::kDQFull));
                     tc_commit(bar(Lay::kQEmpty + st));
@@ -717,6 +716,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 __syncwarp();
                 ++qc;
                 st = st_next;
+            }
             }
         }
         if (lane == 0) {
@@ -869,7 +869,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     tmem_st32(tmem + lane_off + Lay::kTDS + wg * 32, ds2);
                 } else {
                     // dS^T also into tensor memory (over this warpgroup's dP^T columns, already read) for dK
-                    tmem_st32(tmem + lane_off + Lay::kTDP + wg * 64, ds2);
+                    tmem_st32(tmem + lane_off + Lay::kTDS + wg * 64, ds2);
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
