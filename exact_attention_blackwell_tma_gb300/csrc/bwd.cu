@@ -540,6 +540,33 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 mma_ss(d_tmem, a, off, b, off, kIdSq, k > 0);
             }
         };
+        // The d = 64 order issues from the whole warp (one elected lane) in the default
+        // mode (B2 H16 L8192 d64: causal 667 -> 726 TF/s, non-causal 714 -> 791) and
+        // from lane 0 in the deterministic mode, where the converged issue measured
+        // slower (469 -> 401). The d = 128 order issues from lane 0 (converged issue
+        // measured 15-35% slower there, for reasons not found).
+        auto ss = [&](uint32_t d_tmem, SmemDesc a, uint32_t a_step, SmemDesc b, uint32_t b_step, uint32_t id,
+                      uint32_t acc) {
+            if constexpr (kDet) {
+                if (lane == 0) mma_ss(d_tmem, a, a_step, b, b_step, id, acc);
+            } else {
+                mma_ss_w(d_tmem, a, a_step, b, b_step, id, acc);
+            }
+        };
+        auto ts = [&](uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t b_step, uint32_t id, uint32_t acc) {
+            if constexpr (kDet) {
+                if (lane == 0) mma_ts(d_tmem, a_tmem, b, b_step, id, acc);
+            } else {
+                mma_ts_w(d_tmem, a_tmem, b, b_step, id, acc);
+            }
+        };
+        auto nt = [&](uint32_t d_tmem, SmemDesc a, SmemDesc b) {
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {
+                const uint32_t off = desc_step((k >> 2) * kBox + (k & 3) * 32);
+                ss(d_tmem, a, off, b, off, kIdSq, k > 0);
+            }
+        };
         uint32_t tile_it = 0, qc = 0, pc = 0, dsc = 0, dqf = 0;
         bool ok = true;
         for (int k = 0, t = blockIdx.x; t < n_tiles && ok; t = snake_tile(blockIdx.x, ++k, gridDim.x)) {
@@ -563,9 +590,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 ok = warp_wait(bar(Lay::kDOFull + sd0), (qc / NDS) & 1u, w, lane);
                 if (!ok) break;
                 tc_fence_after_sync();
-                if (lane == 0) {
-                    mma_nt(tmem + Lay::kTDP, v_km, at_stage(do_km0, sd0));
-                    tc_commit(bar(Lay::kDPFull));
+                {
+                    nt(tmem + Lay::kTDP, v_km, at_stage(do_km0, sd0));
+                    if (lane == 0) tc_commit(bar(Lay::kDPFull));
                 }
                 __syncwarp();
                 for (int u = 0; u < f.nblk; ++u) {
@@ -578,13 +605,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     if (!ok) break;
                     ++pc;
                     tc_fence_after_sync();
-                    if (lane == 0) {
+                    {
                         const SmemDesc do_mn = at_stage(do_mn0, sd);
 #pragma unroll
                         for (int k = 0; k < kBM / 16; ++k)
-                            mma_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
-                                   do_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
-                        tc_commit(bar(Lay::kDOEmpty + sd));   // dO is no longer read
+                            ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(k),
+                               do_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
+                        if (lane == 0) tc_commit(bar(Lay::kDOEmpty + sd));   // dO is no longer read
                     }
                     __syncwarp();
                     const bool more = u + 1 < f.nblk;
@@ -593,9 +620,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         ok = warp_wait(bar(Lay::kQFull + st_next), ((qc + 1) / NQS) & 1u, w, lane);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        if (lane == 0) {
-                            mma_nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next));
-                            tc_commit(bar(Lay::kSFull));
+                        {
+                            nt(tmem + Lay::kTS, k_km, at_stage(q_km0, st_next));
+                            if (lane == 0) tc_commit(bar(Lay::kSFull));
                         }
                         __syncwarp();
                     }
@@ -609,17 +636,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         if (!ok) break;
                     }
                     tc_fence_after_sync();
-                    if (lane == 0) {
+                    {
                         if (more) {
-                            mma_nt(tmem + Lay::kTDP, v_km, at_stage(do_km0, (qc + 1) % NDS));
-                            tc_commit(bar(Lay::kDPFull));
+                            nt(tmem + Lay::kTDP, v_km, at_stage(do_km0, (qc + 1) % NDS));
+                            if (lane == 0) tc_commit(bar(Lay::kDPFull));
                         }
                         // dK += dS^T Q (dS^T from its own tensor-memory columns)
 #pragma unroll
                         for (int k = 0; k < kBM / 16; ++k)
-                            mma_ts(tmem + Lay::kTDK, tmem + Lay::kTDS + packed_col_ds(k),
-                                   q_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
-                        tc_commit(bar(Lay::kTDSFree));
+                            ts(tmem + Lay::kTDK, tmem + Lay::kTDS + packed_col_ds(k),
+                               q_mn, desc_step(k * 2048), kIdKV, (u > 0 || k > 0) ? 1u : 0u);
+                        if (lane == 0) tc_commit(bar(Lay::kTDSFree));
                     }
                     __syncwarp();
                     // dQ = dS K into its own columns once the previous dQ tile has left them
@@ -627,16 +654,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     if (!ok) break;
                     ++dqf;
                     tc_fence_after_sync();
-                    if (lane == 0) {
+                    {
 #pragma unroll
                         for (int k = 0; k < kBN / 16; ++k)
-                            mma_ss(tmem + Lay::kTDQ, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
-                                   k > 0 ? 1u : 0u);
-                        tc_commit(bar(Lay::kDQFull));
-                        tc_commit(bar(Lay::kQEmpty + st));
+                            ss(tmem + Lay::kTDQ, ds_mn, desc_step(k * 2048), k_mn, desc_step(k * 2048), kIdDQ,
+                               k > 0 ? 1u : 0u);
+                        if (lane == 0) tc_commit(bar(Lay::kDQFull));
+                        if (lane == 0) tc_commit(bar(Lay::kQEmpty + st));
                         if (!more) {
-                            tc_commit(bar(Lay::kDKVFull));
-                            tc_commit(bar(Lay::kKVEmpty));
+                            if (lane == 0) tc_commit(bar(Lay::kDKVFull));
+                            if (lane == 0) tc_commit(bar(Lay::kKVEmpty));
                         }
                     }
                     __syncwarp();

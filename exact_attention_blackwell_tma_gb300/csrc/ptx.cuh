@@ -264,6 +264,35 @@ __host__ __device__ __forceinline__ SmemDesc sdesc_sw128_split(uint32_t saddr, u
 // Byte offset -> low-half increment.
 __host__ __device__ constexpr uint32_t desc_step(uint32_t bytes) { return bytes >> 4; }
 
+// Warp-converged MMA issue: every lane of the warp executes the call with the
+// same operands and one lane, chosen by elect.sync, issues the instruction.
+// In isolation an MMA sequence issued this way keeps its rate (65 cycles per
+// 128 x 128 x 16 MMA on GB300) while ten other warps of the SM run exp/FMA
+// code at full issue rate; issued from a one-lane branch of a warp that runs
+// the loop, the same sequence took 231 cycles per MMA under that load.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, SmemDesc a, uint32_t a_step, SmemDesc b, uint32_t b_step,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo + a_step), "r"(a.hi), "r"(b.lo + b_step), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t b_step,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo + b_step), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, SmemDesc a, uint32_t a_step, SmemDesc b, uint32_t b_step,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
