@@ -82,18 +82,58 @@ def kinds_of(w):
 # profile. It holds only for the kernel sources it was taken on: their SHA-256
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
+    ("b1h32l32768d128", "bwd", False): {
+        "bytes": 8726.112e6 + 4563.768e6,
+        "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
+        "sources": {
+            "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
+                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
+            "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
+                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
+            "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
+                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
+            "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
+                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
+            "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
+                "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
+                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
+                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
+        },
+    },
+    ("b1h32l32768d128", "bwd", True): {
+        "bytes": 6241.267e6 + 3554.771e6,
+        "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
+        "sources": {
+            "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
+                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
+            "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
+                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
+            "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
+                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
+            "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
+                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
+            "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
+                "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
+                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
+            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
+                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
+        },
+    },
     ("b4h16l4096d128", "bwd", False): {
-        "bytes": 813.827e6 + 476.064e6,
+        "bytes": 822.964e6 + 475.964e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "4f102ff15eac13f2afe75a480aaf4adf7a1d3029907b9d650f107f5b00796356",
+                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "5611492efba67473908868e7e95af02995ec2acabe1500b8104d04459416985b",
+                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
-                "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
+                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "f8bc257a612049ccb342efadbcd5376c275b39b89f5a9e48e810f89b3378c5e6",
+                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
@@ -103,17 +143,17 @@ NCU_TRAFFIC = {
         },
     },
     ("b4h16l4096d128", "bwd", True): {
-        "bytes": 1833.847e6 + 944.477e6,
+        "bytes": 472.444e6 + 255.855e6,
         "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "4f102ff15eac13f2afe75a480aaf4adf7a1d3029907b9d650f107f5b00796356",
+                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "5611492efba67473908868e7e95af02995ec2acabe1500b8104d04459416985b",
+                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
-                "bcdf1040f57b0516d473e0a1c35e303d0b43dc4415b7790d0b7543e0ee7d329c",
+                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "f8bc257a612049ccb342efadbcd5376c275b39b89f5a9e48e810f89b3378c5e6",
+                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
