@@ -190,6 +190,20 @@ def test_workload_hdsweep(d):
     _workload_check(inputs.HDSWEEP.with_(d=d), True, heads=[3])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_workload_hdsweep_deterministic(d):
+    """B2 H16 L8192 causal, spiky K, deterministic mode: sampled rows against the
+    oracle and two runs bit-identical (d = 64 runs the order with dQ and dS^T in
+    tensor-memory columns of their own, issued from lane 0 in this mode)."""
+    w = inputs.HDSWEEP.with_(d=d)
+    _workload_check(w, True, heads=[3], deterministic=True)
+    t = inputs.make(w)
+    a = run_dense(t, True, w.scale, True)
+    b = run_dense(t, True, w.scale, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_workload_hdsweep_value_head_dim():
     """B2 H16 L8192, q/k head dim 192, v head dim 128, causal, spiky K."""
     _workload_check(inputs.HDSWEEP.with_(d=192, dv=128), True, heads=[3])
