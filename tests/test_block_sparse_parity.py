@@ -62,15 +62,18 @@ def test_block_mask_full(d, causal, per_head):
     _full_check(t, causal, float(np.float32(1 / np.sqrt(d))), mask, f"d={d} causal={causal} per_head={per_head}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Lq,Lk", [(300, 900), (900, 300), (129, 1)])
-def test_block_mask_rectangular(Lq, Lk):
-    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=128, seed=83)
-    _full_check(t, True, 0.1, random_mask(2, Lq, Lk, 84, 0.7), f"Lq={Lq} Lk={Lk}")
+def test_block_mask_rectangular(Lq, Lk, d):
+    """Odd query-block counts leave the last 256-row tile one 128-row block."""
+    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=d, seed=83)
+    _full_check(t, True, 0.1, random_mask(2, Lq, Lk, 84, 0.7), f"Lq={Lq} Lk={Lk} d={d}")
 
 
-def test_block_mask_with_window():
-    t = inputs.small(B=1, H=2, L=1000, d=128, seed=85)
-    _full_check(t, True, 0.09, random_mask(1, 1000, 1000, 86, 0.6), "mask + window", window=(300, 0))
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_mask_with_window(d):
+    t = inputs.small(B=1, H=2, L=1000, d=d, seed=85)
+    _full_check(t, True, 0.09, random_mask(1, 1000, 1000, 86, 0.6), f"mask + window d={d}", window=(300, 0))
 
 
 @pytest.mark.parametrize("deterministic", [False, True])
