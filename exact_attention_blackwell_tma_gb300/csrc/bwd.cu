@@ -1070,8 +1070,8 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (pair) {
         BwdParams pp = p;   // work tiles are key-block pairs
         pp.nm = bwd_pair_tiles_per_head(g.Lk);
-        pp.n_tiles = varlen ? 0 : g.B * g.H * pp.nm;
-        pp.sections = sched_sections_pay(g.B, g.H, pp.nm, p.head_section, 1, num_sms / 2, ws_bytes) ? 1 : 0;
+        pp.n_tiles = varlen ? 0 : g.B * g.Hkv * pp.nm;   // a tile walks every query head of its group
+        pp.sections = sched_sections_pay(g.B, g.Hkv, pp.nm, p.head_section, 1, num_sms / 2, ws_bytes) ? 1 : 0;
         e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq32, pp, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else if constexpr (HD > 128) {
@@ -1101,7 +1101,7 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
             if (e != cudaSuccess) return e;
         }
     }
-    if (p.split > 1) {
+    if (p.split > 1 && !pair) {   // (the pair kernel writes dK and dV of the whole group itself)
         const long rows_k = varlen ? (long)g.Lk : (long)g.B * g.Lk;
         const long n4k = rows_k * g.Hkv * HD / 4, n4v = rows_k * g.Hkv * p.d_v / 4;
         int blocks = (int)((n4k + n4v + 255) / 256);

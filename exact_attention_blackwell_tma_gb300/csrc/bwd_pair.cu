@@ -11,9 +11,10 @@
 // a kernel that uses the pair mode uses it for every tensor-memory and
 // tensor-core instruction.
 //
-// Work tile: one key-block pair (256 keys) of one (batch, head); CTA r of the
-// cluster owns key block 2p + r. Both walk the query blocks either key block
-// sees, in the same order. Per query block (128 queries) the even CTA's MMA
+// Work tile: one key-block pair (256 keys) of one (batch, key/value head); CTA
+// r of the cluster owns key block 2p + r. Both walk the query blocks either key
+// block sees, for every query head of the key/value head's group (grouped
+// heads), in the same order; dK and dV sum over the group in the tile. Per query block (128 queries) the even CTA's MMA
 // thread issues:
 //   S^T  = K Q^T     M = 256 (keys), N = 128 (queries); B = Q split by query halves
 //   dP^T = V dO^T    M = 256, N = 128;                  B = dO split by query halves
@@ -85,11 +86,14 @@ struct Lay {
 };
 
 struct PairTile {
-    int b, h, p;       // batch, head, key-block pair
+    int b, h, p;       // batch, key/value head, key-block pair
     int n;             // this CTA's key block (2p + rank)
     int lq, lk;
     int q_row0, k_row0;
     int m_begin, m_end;   // query blocks either key block of the pair sees
+    // the tile walks every query head of the group (hq0 .. hq0 + group - 1), each
+    // over [m_begin, m_end): step u is query head hq0 + u / nm, block m_begin + u % nm
+    int hq0, nm, nblk;
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
@@ -104,9 +108,9 @@ __device__ __forceinline__ PairTile pair_tile(int t, const BwdParams& p, const V
     // heads in L2-sized sections, longest pairs first within a section, where
     // that pays (p.sections, as in bwd.cu); the deterministic kernel keeps one
     // global order of levels, shortest first
-    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.H, 2 * kBN, p.head_section, spt, true)
-                 : ((g.causal && (spt || !p.sections)) ? sched_dense_lpt(t, g.B, g.H, p.nm, spt)
-                                                        : sched_dense(t, g.H, p.nm, p.head_section, false));
+    Tile ti = vm ? sched_varlen(*vm, t, g.B, g.Hkv, 2 * kBN, p.head_section, spt, true)
+                 : ((g.causal && (spt || !p.sections)) ? sched_dense_lpt(t, g.B, g.Hkv, p.nm, spt)
+                                                        : sched_dense(t, g.Hkv, p.nm, p.head_section, false));
     PairTile f;
     f.b = ti.b;
     f.h = ti.h;
@@ -127,6 +131,9 @@ __device__ __forceinline__ PairTile pair_tile(int t, const BwdParams& p, const V
     f.m_end = (f.lq + kBM - 1) / kBM;
     f.m_begin = g.causal ? max(0, floor_div(n0 * kBN - (f.lk - f.lq), kBM)) : 0;
     if (n0 * kBN >= f.lk || f.m_begin > f.m_end) f.m_begin = f.m_end;
+    f.hq0 = f.h * g.group;
+    f.nm = f.m_end - f.m_begin;
+    f.nblk = g.group * f.nm;
     return f;
 }
 
@@ -232,7 +239,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             }
             __syncwarp();
             ++tile_it;
-            for (int u = 0, m = f.m_begin; m < f.m_end && ok; ++u, ++m) {
+            for (int u = 0; u < f.nblk && ok; ++u) {
+                const int hq = f.hq0 + u / f.nm, m = f.m_begin + u % f.nm;
                 const uint32_t st = qc % Lay::kQStages;
                 ok = warp_wait(bar(Lay::kQEmpty + st), ((qc / Lay::kQStages) & 1u) ^ 1u, w, lane);
                 if (!ok) break;
@@ -242,10 +250,10 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                     // [tau0 tau1]: queries 0-63 / 64-127, this CTA's 64 columns (B of dK)
                     const uint32_t full = lbar(Lay::kQFull + st), dst = base + Lay::kQOff + st * Lay::kStageBytes;
                     if (leader_cta) mbar_expect_tx(bar(Lay::kQFull + st), 2u * Lay::kStageBytes);
-                    tma_load_3d_pair(dst, &tmQ64, full, 0, f.h, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + kQuad, &tmQ64, full, 64, f.h, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + 2 * kQuad, &tmQ64, full, 64 * (int)rank, f.h, qrow);
-                    tma_load_3d_pair(dst + 3 * kQuad, &tmQ64, full, 64 * (int)rank, f.h, qrow + 64);
+                    tma_load_3d_pair(dst, &tmQ64, full, 0, hq, qrow + 64 * (int)rank);
+                    tma_load_3d_pair(dst + kQuad, &tmQ64, full, 64, hq, qrow + 64 * (int)rank);
+                    tma_load_3d_pair(dst + 2 * kQuad, &tmQ64, full, 64 * (int)rank, hq, qrow);
+                    tma_load_3d_pair(dst + 3 * kQuad, &tmQ64, full, 64 * (int)rank, hq, qrow + 64);
                 }
                 // row statistics of the query block, negated: -lse (log2 units), -D
                 float* nlse2 = stats + st * 256;
@@ -255,7 +263,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                     const int r = m * kBM + lane * 4 + e;
                     float lv = -INFINITY, dv = 0.f;
                     if (r < f.lq) {
-                        const long si = varlen ? (long)f.h * g.Lq + f.q_row0 + r : ((long)f.b * g.H + f.h) * g.Lq + r;
+                        const long si = varlen ? (long)hq * g.Lq + f.q_row0 + r : ((long)f.b * g.H + hq) * g.Lq + r;
                         lv = -p.lse[si] * kLog2e;
                         dv = -p.delta[si];
                     }
@@ -270,10 +278,10 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 if (lane == 0) {
                     const uint32_t full = lbar(Lay::kDOFull), dst = base + Lay::kDOOff;
                     if (leader_cta) mbar_expect_tx(bar(Lay::kDOFull), 2u * Lay::kStageBytes);
-                    tma_load_3d_pair(dst, &tmDO64, full, 0, f.h, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + kQuad, &tmDO64, full, 64, f.h, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + 2 * kQuad, &tmDO64, full, 64 * (int)rank, f.h, qrow);
-                    tma_load_3d_pair(dst + 3 * kQuad, &tmDO64, full, 64 * (int)rank, f.h, qrow + 64);
+                    tma_load_3d_pair(dst, &tmDO64, full, 0, hq, qrow + 64 * (int)rank);
+                    tma_load_3d_pair(dst + kQuad, &tmDO64, full, 64, hq, qrow + 64 * (int)rank);
+                    tma_load_3d_pair(dst + 2 * kQuad, &tmDO64, full, 64 * (int)rank, hq, qrow);
+                    tma_load_3d_pair(dst + 3 * kQuad, &tmDO64, full, 64 * (int)rank, hq, qrow + 64);
                 }
                 __syncwarp();
                 ++qc;
@@ -321,7 +329,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             for (int k = 0, t = cl; t < n_tiles && ok; t = snake_tile(cl, ++k, ncl)) {
                 const PairTile f = pair_tile<kDet>(t, p, vmp, rank);
                 if (f.m_begin >= f.m_end) continue;
-                const int nblk = f.m_end - f.m_begin;
+                const int nblk = f.nblk;
                 ok = warp_wait_cluster(bar(Lay::kKVFull), tile_it & 1u, w, lane);
                 if (!ok) break;
                 ++tile_it;
@@ -424,8 +432,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             const PairTile f = pair_tile<kDet>(t, p, vmp, rank);
             const int key = f.n * kBN + r;
             const bool key_ok = key < f.lk;
-            const long kv_off = (((long)f.k_row0 + key) * g.H + f.h) * HD + wg * (HD / 2);
-            if (f.m_begin >= f.m_end) {   // no query sees the pair's keys
+            const long kv_off = (((long)f.k_row0 + key) * g.Hkv + f.h) * HD + wg * (HD / 2);
+            if (f.nblk == 0) {   // no query sees the pair's keys
                 if (key_ok) {
 #pragma unroll
                     for (int c = 0; c < HD / 16; ++c) {
@@ -439,7 +447,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             // sequence (the pair's odd block at its end) sees none
             const int q_lo = key_ok ? (g.causal ? key - (f.lk - f.lq) : 0) : f.lq;
             const int q_hi = f.lq;
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            for (int u = 0; u < f.nblk; ++u) {
+                const int m = f.m_begin + u % f.nm;
                 const uint32_t st = qc % Lay::kQStages;
                 ok = warp_wait_cluster(bar(Lay::kSFull), sc & 1u, w, lane);
                 if (!ok) break;
@@ -570,7 +579,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         uint32_t rr[32];
         for (int k = 0, t = cl; t < n_tiles && ok; t = snake_tile(cl, ++k, ncl)) {
             const PairTile f = pair_tile<kDet>(t, p, vmp, rank);
-            for (int m = f.m_begin; m < f.m_end; ++m) {
+            for (int u = 0; u < f.nblk; ++u) {
+                const int hq = f.hq0 + u / f.nm, m = f.m_begin + u % f.nm;
                 const uint32_t st = dqc % Lay::kQStages;
                 ok = warp_wait_cluster(bar(Lay::kDQFull), dqc & 1u, w, lane);
                 if (!ok) break;
@@ -578,8 +588,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 tc_fence_after_sync();
                 int* sem = nullptr;
                 if constexpr (kDet) {
-                    const long tile = varlen ? (long)f.h * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
-                                             : ((long)f.b * g.H + f.h) * p.nq + m;
+                    const long tile = varlen ? (long)hq * (g.Lq / kBM + g.B + 1) + f.q_row0 / kBM + f.b + m
+                                             : ((long)f.b * g.H + hq) * p.nq + m;
                     sem = p.semaphores + 2 * tile + rank;
                     if (leader) {
                         if (sem_wait(sem, pair_dq_turn(p, f, m), w)) fence_proxy_async_global();
@@ -617,7 +627,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                     // this warp's 32 rows (rows past the sequence carry exact zeros: P = 0 there)
                     for (int bx = 0; bx < 2; ++bx)
                         tma_reduce_add_3d(&tmDQ32, stage_s + (2 * half + bx) * kQuad + (q4 & 1) * 4096,
-                                          (2 * half + bx) * 32, f.h, f.q_row0 + m * kBM + 64 * (int)rank + (q4 & 1) * 32);
+                                          (2 * half + bx) * 32, hq, f.q_row0 + m * kBM + 64 * (int)rank + (q4 & 1) * 32);
                     bulk_commit_group();
                     if constexpr (kDet) {
                         bulk_wait_group0();
@@ -653,7 +663,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
 
 bool bwd_pair_supported(const BwdParams& p) {
     const Geometry& g = p.g;
-    return g.d == HD && p.d_v == HD && g.group == 1 && g.win_left < 0 && (g.win_right < 0 || g.win_right == 0) &&
+    return g.d == HD && p.d_v == HD && g.win_left < 0 && (g.win_right < 0 || g.win_right == 0) &&
            p.mask.ptr == nullptr;
 }
 

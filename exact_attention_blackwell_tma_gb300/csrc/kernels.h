@@ -133,8 +133,9 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const BwdParams& p, int num_sms, cudaStream_t stream);
 
 // The backward's main kernel on CTA pairs (2-CTA tensor cores, bwd_pair.cu):
-// head dim 128 (q, k, v), one query head per key/value head, no window beyond
-// the causal mask, no block mask; dense or packed, deterministic or not.
+// head dim 128 (q, k, v), grouped heads (a tile walks the query heads of its
+// key/value head's group), no window beyond the causal mask, no block mask;
+// dense or packed, deterministic or not.
 bool bwd_pair_supported(const BwdParams& p);
 // key-block pairs per (batch, head) of Lk keys
 int bwd_pair_tiles_per_head(int Lk);

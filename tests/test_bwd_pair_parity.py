@@ -4,9 +4,9 @@ the fp64 oracle.
 FlashAttention-4 paper, Section 3.2.3: the two CTAs of a cluster run the
 backward's MMAs together with M = 256 (each stages half of operand B), and the
 pair sums dQ over its 256 keys before one reduce-add pass. The kernel covers
-head dim 128, one query head per key/value head, no mask beyond the causal
-one and no block mask, dense or packed, in both modes; attn_set_backward_cta_pairs
-switches it on. These tests switch it on and compare every element with the
+head dim 128, grouped heads (a work tile walks every query head of its
+key/value head's group), no mask beyond the causal one and no block mask,
+dense or packed, in both modes; attn_set_backward_cta_pairs switches it on. These tests switch it on and compare every element with the
 oracle (ragged lengths that leave the pair's second key block partly or wholly
 past the keys, Lq != Lk, packed batches with one or two offset arrays), check
 that the deterministic mode repeats bit for bit, that problems the pair kernel
@@ -111,23 +111,52 @@ def test_pair_agrees_with_single_ctas():
         assert_grad_close(to64(a), to64(b), f"pair vs single {name}")
 
 
-@pytest.mark.parametrize("what", ["gqa", "window", "blockmask", "d64", "d192"])
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 1), (8, 2)])
+@pytest.mark.parametrize("L", [77, 300, 513])
+def test_pair_grouped_heads(L, H, Hkv, causal, deterministic):
+    """Grouped heads on CTA pairs: a tile's key blocks see every query head of
+    the group, and dK/dV sum over them in the tile."""
+    t = inputs.small(B=2, H=H, L=L, d=128, seed=48, Hkv=Hkv)
+    _check(t, causal, 0.088, f"pair gqa L={L} H={H}/{Hkv} causal={causal} det={deterministic}", deterministic)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_pair_grouped_heads_varlen(deterministic):
+    lens = [1, 128, 200, 513, 77, 256, 0, 129]
+    cu = inputs.cu_seqlens(lens)
+    g = torch.Generator("cpu").manual_seed(49)
+    T = int(cu[-1])
+    t = {"q": torch.randn(T, 6, 128, generator=g).to(torch.bfloat16),
+         "k": torch.randn(T, 2, 128, generator=g).to(torch.bfloat16),
+         "v": torch.randn(T, 2, 128, generator=g).to(torch.bfloat16),
+         "do": torch.randn(T, 6, 128, generator=g).to(torch.bfloat16)}
+    _check(t, True, 0.09, f"pair gqa varlen det={deterministic}", deterministic, cu=cu)
+
+
+def test_pair_grouped_deterministic_is_bit_identical():
+    t = inputs.small(B=1, H=8, L=1200, d=128, seed=50, Hkv=2)
+    ref = _grads(t, True, 0.088, deterministic=True)
+    for _ in range(3):
+        again = _grads(t, True, 0.088, deterministic=True)
+        for a, b in zip(ref, again):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("what", ["window", "blockmask", "d64", "d192"])
 def test_pair_switch_leaves_other_problems_correct(what):
     """With the switch on, problems outside the pair kernel run on single CTAs."""
     import oracle
-    if what == "gqa":
-        t = inputs.small(B=1, H=4, L=300, d=128, seed=47, Hkv=2)
-        kw, okw = {}, {}
-    else:
-        d = {"d64": 64, "d192": 192}.get(what, 128)
-        t = inputs.small(B=1, H=2, L=300, d=d, seed=47)
-        kw, okw = {}, {}
-        if what == "window":
-            kw, okw = {"window": (100, -1)}, {"window_left": 100, "window_right": -1}
-        if what == "blockmask":
-            m = np.ones((1, 3, 3), np.uint8)
-            m[0, 2, 1] = 0
-            kw, okw = {"block_mask": torch.from_numpy(m).cuda()}, {"block_mask": m}
+    d = {"d64": 64, "d192": 192}.get(what, 128)
+    t = inputs.small(B=1, H=2, L=300, d=d, seed=47)
+    kw, okw = {}, {}
+    if what == "window":
+        kw, okw = {"window": (100, -1)}, {"window_left": 100, "window_right": -1}
+    if what == "blockmask":
+        m = np.ones((1, 3, 3), np.uint8)
+        m[0, 2, 1] = 0
+        kw, okw = {"block_mask": torch.from_numpy(m).cuda()}, {"block_mask": m}
     dq, dk, dv = _grads(t, True, 0.1, **kw)
     rq, rk, rv = oracle.bwd(*(to64(t[n]) for n in ("q", "k", "v", "do")), 0.1, True, **okw)
     for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), (rq, rk, rv)):
@@ -156,3 +185,29 @@ def test_pair_workloads(wname, causal, deterministic):
     assert_grad_close(to64(dq[bsel][:, qrows][:, :, head]), rq[:, qrows], f"{what} dQ")
     assert_grad_close(to64(dk[bsel][:, krows][:, :, head]), rk[:, krows], f"{what} dK")
     assert_grad_close(to64(dv[bsel][:, krows][:, :, head]), rv[:, krows], f"{what} dV")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_pair_workload_grouped(deterministic):
+    """B2 H16 over 2 key/value heads, L8192 d128, causal, spiky K, on CTA pairs:
+    dQ rows of query heads 3 and 12 against the oracle with their key/value
+    heads; dK/dV rows of key/value head 1 against the oracle on its whole group."""
+    import oracle
+    w = inputs.HDSWEEP.with_(name="b2h16kv2l8192d128", hkv=2)
+    t = inputs.make(w)
+    dq, dk, dv = _grads(t, True, w.scale, deterministic)
+    G = w.H // w.H_kv
+    bsel = [0, w.B - 1]
+    qrows, krows = _rows(w.L, 12, 5), _rows(w.L, 8, 6)
+    qh = [3, 12]
+    sub = {n: to64(t[n][bsel][:, :, qh]) for n in ("q", "do")}
+    sub.update({n: to64(t[n][bsel][:, :, [h // G for h in qh]]) for n in ("k", "v")})
+    rq, _, _ = oracle.bwd(sub["q"], sub["k"], sub["v"], sub["do"], w.scale, True, qrows=qrows, krows=[])
+    assert_grad_close(to64(dq[bsel][:, qrows][:, :, qh]), rq[:, qrows], f"pair grouped workload det={deterministic} dQ")
+    kh = 1
+    grp = list(range(kh * G, kh * G + G))
+    full = {n: to64(t[n][bsel][:, :, grp]) for n in ("q", "do")}
+    full.update({n: to64(t[n][bsel][:, :, [kh]]) for n in ("k", "v")})
+    _, rk, rv = oracle.bwd(full["q"], full["k"], full["v"], full["do"], w.scale, True, qrows=[], krows=krows)
+    assert_grad_close(to64(dk[bsel][:, krows][:, :, [kh]]), rk[:, krows], f"pair grouped workload det={deterministic} dK")
+    assert_grad_close(to64(dv[bsel][:, krows][:, :, [kh]]), rv[:, krows], f"pair grouped workload det={deterministic} dV")
