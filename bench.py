@@ -83,17 +83,17 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b1h32l32768d128", "bwd", False): {
-        "bytes": 8726.112e6 + 4563.768e6,
+        "bytes": 8723.587e6 + 4563.228e6,
         "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
+                "8ac6affa50ea489ab0fbfb4a34b618f0f1f718f4789ae548fcf77b69713cdd57",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
+                "1daa08742d3a36e404cda987b2cee61572e6d3ce0b888e1d7d7b922da00d3fec",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
@@ -103,57 +103,17 @@ NCU_TRAFFIC = {
         },
     },
     ("b1h32l32768d128", "bwd", True): {
-        "bytes": 6241.267e6 + 3554.771e6,
+        "bytes": 6415.699e6 + 3665.171e6,
         "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
+                "8ac6affa50ea489ab0fbfb4a34b618f0f1f718f4789ae548fcf77b69713cdd57",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
                 "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
-            "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
-                "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
-            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
-                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
-            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
-                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
-        },
-    },
-    ("b4h16l4096d128", "bwd", False): {
-        "bytes": 822.964e6 + 475.964e6,
-        "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
-        "sources": {
-            "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
-            "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
-            "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
-                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
-            "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
-            "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
-                "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
-            "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
-                "d3268cfe95ac87277ec035e806c4ac4c57c17361d3c6b4c9c26b3e80fa94ac40",
-            "exact_attention_blackwell_tma_gb300/csrc/dq_reduce.cuh":
-                "7ddedbe18fcca40f3a3e932502abeb8096da330d02b5731aeb6314e8dafeb072",
-        },
-    },
-    ("b4h16l4096d128", "bwd", True): {
-        "bytes": 472.444e6 + 255.855e6,
-        "profile": "profiles/bwd_kernel_b4h16l4096d128.md",
-        "sources": {
-            "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "43fdb2a0b8eca6f360eea39f6a024f44529f6ec87ce5734b89b319e914f346c2",
-            "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
-            "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
-                "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
-            "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "e3b6dea6dadd3631bb63035c5dcca74539d0fd6589bcd617c85f0596be777c17",
+                "1daa08742d3a36e404cda987b2cee61572e6d3ce0b888e1d7d7b922da00d3fec",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
