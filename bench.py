@@ -83,17 +83,17 @@ def kinds_of(w):
 # is checked at run time and the field is reported as null after any change.
 NCU_TRAFFIC = {
     ("b1h32l32768d128", "bwd", False): {
-        "bytes": 8723.587e6 + 4563.228e6,
+        "bytes": 8728.203e6 + 4564.870e6,
         "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "8ac6affa50ea489ab0fbfb4a34b618f0f1f718f4789ae548fcf77b69713cdd57",
+                "60bc2511e502cc06be6d193c1279504a2fdce162ce618fc40e08004425c032ba",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
+                "3c0283284f2342dd722773b9195bbfdc67274aa16994dbb143983c848529bf9c",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "1daa08742d3a36e404cda987b2cee61572e6d3ce0b888e1d7d7b922da00d3fec",
+                "5affc1850bc7073eafc4f405d84928b0a015bd41fe555c117e9c97cdf3d90f72",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":
@@ -103,17 +103,17 @@ NCU_TRAFFIC = {
         },
     },
     ("b1h32l32768d128", "bwd", True): {
-        "bytes": 6415.699e6 + 3665.171e6,
+        "bytes": 6605.666e6 + 3768.216e6,
         "profile": "profiles/bwd_kernel_b1h32l32768d128_traffic.md",
         "sources": {
             "exact_attention_blackwell_tma_gb300/csrc/bwd.cu":
-                "8ac6affa50ea489ab0fbfb4a34b618f0f1f718f4789ae548fcf77b69713cdd57",
+                "60bc2511e502cc06be6d193c1279504a2fdce162ce618fc40e08004425c032ba",
             "exact_attention_blackwell_tma_gb300/csrc/ptx.cuh":
-                "363df0116a5afdf9d3934973a09bc776dac39149d3a352555cec5f4e5dc4a53f",
+                "3c0283284f2342dd722773b9195bbfdc67274aa16994dbb143983c848529bf9c",
             "exact_attention_blackwell_tma_gb300/csrc/sched.cuh":
                 "0328db7053351282b31375c9f4ccf44236a648824c9e57efab5f143fdd22abd6",
             "exact_attention_blackwell_tma_gb300/csrc/kernels.h":
-                "1daa08742d3a36e404cda987b2cee61572e6d3ce0b888e1d7d7b922da00d3fec",
+                "5affc1850bc7073eafc4f405d84928b0a015bd41fe555c117e9c97cdf3d90f72",
             "exact_attention_blackwell_tma_gb300/csrc/mask.cuh":
                 "a8db3e42b70e326e0df86ce85e11cf81134dc7f609b7d0006d9f1a409692beee",
             "exact_attention_blackwell_tma_gb300/csrc/dq_order.cuh":

@@ -56,16 +56,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [rows, H, d] bf16 viewed as 3-D (d innermost); boxes of box_rows rows x 1
 // head x 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors
-// expect. Rows past `rows` read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d, int box_rows = 128) {
+// expect, or (narrow) 32 columns (64 bytes) with the 64-byte swizzle. Rows past
+// `rows` read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, long rows, int H, int d, int box_rows = 128, bool narrow = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t box[3] = {narrow ? 32u : 64u, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -426,7 +427,8 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.status = di.status;
     p.wait_budget_ns = wait_budget_ns();
     CUtensorMap tq, tk, tv, tdo, tdq;
-    PairMaps pm;
+    PairMaps pm = {};
+    const bool pairs = g_bwd_pairs.load() != 0;
     const long qrows = rows_q > 0 ? rows_q : rows_k;
     const long krows = rows_k > 0 ? rows_k : rows_q;
     // Without query rows (or keys) the matching descriptors are never used; they
@@ -440,7 +442,12 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
         !make_map_f32(&tdq, p.dq_acc, qrows, hq_map, d) || !make_map(&pm.q64, qsrc, qrows, hq_map, d, 64) ||
         !make_map(&pm.do64, dosrc, qrows, hq_map, d_v, 64) || !make_map_f32(&pm.dq32, p.dq_acc, qrows, hq_map, d, 32))
         return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, pm, g_bwd_pairs.load() != 0, p, di.sms, stream);
+    // the pair backward's 32-column halves at head dim 64
+    if (pairs && d == 64 && d_v == 64 &&
+        (!make_map(&pm.q32, qsrc, qrows, hq_map, d, 128, true) || !make_map(&pm.do32, dosrc, qrows, hq_map, d, 128, true) ||
+         !make_map(&pm.k32, rows_k > 0 ? k : q, krows, Hkv, d, 128, true)))
+        return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    cudaError_t e = launch_bwd(tq, tk, tv, tdo, tdq, pm, pairs, p, di.sms, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

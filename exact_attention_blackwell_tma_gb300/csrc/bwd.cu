@@ -1072,7 +1072,7 @@ cudaError_t launch_bwd_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         pp.nm = bwd_pair_tiles_per_head(g.Lk);
         pp.n_tiles = varlen ? 0 : g.B * g.Hkv * pp.nm;   // a tile walks every query head of its group
         pp.sections = sched_sections_pay(g.B, g.Hkv, pp.nm, p.head_section, 1, num_sms / 2, ws_bytes) ? 1 : 0;
-        e = launch_bwd_pair(pm.q64, tk, tv, pm.do64, pm.dq32, pp, vm, num_sms, stream);
+        e = launch_bwd_pair(pm, tk, tv, pp, vm, num_sms, stream);
         if (e != cudaSuccess) return e;
     } else if constexpr (HD > 128) {
         e = launch_bwd_wide(tq, tk, tv, tdo, pm.dq32, p, vm, num_sms, stream);
@@ -1131,7 +1131,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const BwdParams& p, int num_sms, cudaStream_t stream) {
     pair = pair && bwd_pair_supported(p);
     switch (p.g.d) {
-        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);
+        case 64: return launch_bwd_hd<64>(tq, tk, tv, tdo, tdq, pm, pair, p, num_sms, stream);
         case 128: return launch_bwd_hd<128>(tq, tk, tv, tdo, tdq, pm, pair, p, num_sms, stream);
         case 192: return launch_bwd_hd<192>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);
         case 256: return launch_bwd_hd<256>(tq, tk, tv, tdo, tdq, pm, false, p, num_sms, stream);

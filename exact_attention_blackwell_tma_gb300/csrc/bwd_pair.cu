@@ -1,5 +1,5 @@
 // Backward pass on CTA pairs: the main kernel of dQ, dK, dV with 2-CTA tensor
-// cores (tcgen05 .cta_group::2), head dim 128.
+// cores (tcgen05 .cta_group::2), head dims 64 and 128.
 //
 // FlashAttention-4 paper, Section 3.2.3 "2-CTA backward pass": with M = 256
 // the two CTAs of a cluster act as one larger tile -- each stages half of
@@ -18,16 +18,20 @@
 // thread issues:
 //   S^T  = K Q^T     M = 256 (keys), N = 128 (queries); B = Q split by query halves
 //   dP^T = V dO^T    M = 256, N = 128;                  B = dO split by query halves
-//   dV  += P^T dO    M = 256, N = 128 (d);  A = P^T from each CTA's tensor memory,
-//                                           B = dO split by column halves
-//   dK  += dS^T Q    M = 256, N = 128 (d);  A = dS^T from tensor memory, B = Q split
-//                                           by column halves
-//   dQ   = dS K      M = 128 (queries: 64 per CTA), N = 128 (d), K = the pair's 256
+//   dV  += P^T dO    M = 256, N = d;  A = P^T from each CTA's tensor memory,
+//                                     B = dO split by column halves
+//   dK  += dS^T Q    M = 256, N = d;  A = dS^T from tensor memory, B = Q split
+//                                     by column halves
+//   dQ   = dS K      M = 128 (queries: 64 per CTA), N = d, K = the pair's 256
 //                    keys; A = dS of this CTA's 64 queries over both key blocks (the
 //                    peer writes its half into this CTA's shared memory), B = K of the
-//                    256 keys, this CTA's 64 columns
-// so each CTA adds a 64 x 128 dQ tile per query block to the fp32 accumulator:
+//                    256 keys, this CTA's d/2 columns
+// so each CTA adds a 64 x d dQ tile per query block to the fp32 accumulator:
 // per pair one reduce-add pass per 256 keys instead of two.
+//
+// The column halves of B (the MN-major operands of dV, dK, dQ) are 64 columns
+// with the 128-byte swizzle at d = 128 and 32 columns (64 bytes a row) with the
+// 64-byte swizzle at d = 64; everything else is the same at both head dims.
 //
 // Roles per CTA (512 threads): warp 0 loads (TMA; the pair's loads of one MMA
 // complete on the even CTA's barrier), warp 1 issues the MMAs (even CTA only),
@@ -45,7 +49,6 @@
 namespace attn {
 namespace {
 
-constexpr int HD = 128;
 constexpr int kBM = 128;              // query rows per query block
 constexpr int kBN = 128;              // keys per key block (one CTA)
 constexpr int kThreads = 512;
@@ -58,13 +61,25 @@ static_assert((kRegsLoadMma + 2 * kRegsCompute + kRegsDq) * 128 <= kLaunchRegs *
 
 __device__ __forceinline__ uint32_t packed_col(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
 
-struct Lay {
+template <int HD>
+struct PairLay {
+    static constexpr bool kNarrow = HD == 64;   // column halves of 32: the 64-byte swizzle
     static constexpr int kQStages = 2;
-    static constexpr int kStageBytes = 4 * kQuad;                // [sig0 sig1 tau0 tau1]
-    static constexpr int kKOff = 0;                              // own key block, 2 boxes
-    static constexpr int kVOff = kKOff + 2 * kBox;
-    static constexpr int kKXOff = kVOff + 2 * kBox;              // K of the pair's 256 keys, this CTA's 64 columns
-    static constexpr int kQOff = kKXOff + 2 * kBox;              // Q ring (stage = dQ staging after dK)
+    // A Q (dO) stage is [sig | tau]. sig: this CTA's 64 queries, every column,
+    // K-major (HD/64 quadrants of 64 rows x 64 columns): B of S^T (dP^T). tau: the
+    // block's 128 queries, this CTA's HD/2 columns, MN-major: B of dK (dV); two
+    // 64-row quadrants at d = 128, one 128-row x 32-column box at d = 64.
+    static constexpr int kSigBytes = (HD / 64) * kQuad;
+    static constexpr int kTauBytes = 128 * HD;                   // 128 rows x HD/2 bf16
+    static constexpr int kStageBytes = kSigBytes + kTauBytes;
+    static constexpr int kKBytes = 256 * HD;                     // 128 keys x HD bf16
+    static constexpr int kKXBytes = 256 * HD;                    // 256 keys x HD/2 bf16
+    // bytes per 16 rows along K of an MN-major column half (two 8-row atoms)
+    static constexpr uint32_t kMnStep16 = kNarrow ? 1024 : 2048;
+    static constexpr int kKOff = 0;                              // own key block, HD/64 boxes
+    static constexpr int kVOff = kKOff + kKBytes;
+    static constexpr int kKXOff = kVOff + kKBytes;               // K of the pair's 256 keys, this CTA's HD/2 columns
+    static constexpr int kQOff = kKXOff + kKXBytes;              // Q ring (stage = dQ staging after dK)
     static constexpr int kDOOff = kQOff + kQStages * kStageBytes;
     static constexpr int kDSOff = kDOOff + kStageBytes;          // dS: 256 key rows x 64 queries
     static constexpr int kDSBytes = 256 * 128;
@@ -83,6 +98,9 @@ struct Lay {
     static constexpr int kSmemBytes = kMiscOff + 16;
     static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + HD;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kStageBytes >= 64 * HD * 4, "a Q stage holds the CTA's 64 x HD fp32 dQ tile");
+    static_assert(kKXOff % 1024 == 0 && kQOff % 1024 == 0 && kStageBytes % 1024 == 0 && kDSOff % 1024 == 0,
+                  "swizzle atoms aligned");
 };
 
 struct PairTile {
@@ -146,11 +164,18 @@ __device__ __forceinline__ int pair_dq_turn(const BwdParams& p, const PairTile& 
     return p.g.causal ? (n_hi + 1) / 2 - 1 - f.p : f.p - n_lo / 2;
 }
 
-template <bool kDet>
+// tmQ64, tmDO64: 64-row x 64-column boxes; tmQ32, tmDO32, tmK32: 128-row x
+// 32-column boxes with the 64-byte swizzle (d = 64 only); tmDQ32: the fp32 dQ
+// accumulator in 32-row x 32-column boxes.
+template <int HD, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO64,
-                const __grid_constant__ CUtensorMap tmDQ32, const BwdParams p, const VarlenMap* vm) {
+                const __grid_constant__ CUtensorMap tmDQ32, const __grid_constant__ CUtensorMap tmQ32,
+                const __grid_constant__ CUtensorMap tmDO32, const __grid_constant__ CUtensorMap tmK32,
+                const BwdParams p, const VarlenMap* vm) {
+    using Lay = PairLay<HD>;
+    constexpr bool kNarrow = Lay::kNarrow;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -198,6 +223,11 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO64);
         tma_prefetch_desc(&tmDQ32);
+        if constexpr (kNarrow) {
+            tma_prefetch_desc(&tmQ32);
+            tma_prefetch_desc(&tmDO32);
+            tma_prefetch_desc(&tmK32);
+        }
     }
     if (warp == 1) {   // both CTAs allocate: the pair gets the same columns in each
         tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
@@ -220,6 +250,19 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         uint32_t tile_it = 0, qc = 0;
         bool ok = true;
         float* stats = reinterpret_cast<float*>(smem + Lay::kStatOff);
+        // one Q (dO) stage of query block rows [qrow, qrow + 128): sig = this CTA's
+        // 64 queries, every column; tau = the 128 queries, this CTA's HD/2 columns
+        auto load_stage = [&](uint32_t dst, const CUtensorMap* m64, const CUtensorMap* m32, uint32_t full, int hq,
+                              int qrow) {
+            for (int c = 0; c < HD / 64; ++c)
+                tma_load_3d_pair(dst + c * kQuad, m64, full, c * 64, hq, qrow + 64 * (int)rank);
+            if constexpr (kNarrow) {
+                tma_load_3d_pair(dst + Lay::kSigBytes, m32, full, 32 * (int)rank, hq, qrow);
+            } else {
+                tma_load_3d_pair(dst + Lay::kSigBytes, m64, full, 64 * (int)rank, hq, qrow);
+                tma_load_3d_pair(dst + Lay::kSigBytes + kQuad, m64, full, 64 * (int)rank, hq, qrow + 64);
+            }
+        };
         for (int k = 0, t = cl; t < n_tiles && ok; t = snake_tile(cl, ++k, ncl)) {
             const PairTile f = pair_tile<kDet>(t, p, vmp, rank);
             if (f.m_begin >= f.m_end) continue;
@@ -227,14 +270,21 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             if (!ok) break;
             if (lane == 0) {
                 const uint32_t full = lbar(Lay::kKVFull);
-                if (leader_cta) mbar_expect_tx(bar(Lay::kKVFull), 2u * 6u * kBox);   // K, V, KX of both CTAs
+                // K, V, KX of both CTAs
+                if (leader_cta) mbar_expect_tx(bar(Lay::kKVFull), 2u * (2u * Lay::kKBytes + Lay::kKXBytes));
                 const int krow = f.k_row0 + f.n * kBN, krow0 = f.k_row0 + 2 * f.p * kBN;
+                for (int c = 0; c < HD / 64; ++c) {
+                    tma_load_3d_pair(base + Lay::kKOff + c * kBox, &tmK, full, c * 64, f.h, krow);
+                    tma_load_3d_pair(base + Lay::kVOff + c * kBox, &tmV, full, c * 64, f.h, krow);
+                }
+                // the pair's 256 keys, this CTA's HD/2 columns of K (B of the dQ product)
                 for (int hf = 0; hf < 2; ++hf) {
-                    tma_load_3d_pair(base + Lay::kKOff + hf * kBox, &tmK, full, hf * 64, f.h, krow);
-                    tma_load_3d_pair(base + Lay::kVOff + hf * kBox, &tmV, full, hf * 64, f.h, krow);
-                    // the pair's 256 keys, this CTA's 64 columns of K (B of the dQ product)
-                    tma_load_3d_pair(base + Lay::kKXOff + hf * kBox, &tmK, full, (int)rank * 64, f.h,
-                                     krow0 + hf * kBN);
+                    if constexpr (kNarrow)
+                        tma_load_3d_pair(base + Lay::kKXOff + hf * (Lay::kKXBytes / 2), &tmK32, full, (int)rank * 32,
+                                         f.h, krow0 + hf * kBN);
+                    else
+                        tma_load_3d_pair(base + Lay::kKXOff + hf * kBox, &tmK, full, (int)rank * 64, f.h,
+                                         krow0 + hf * kBN);
                 }
             }
             __syncwarp();
@@ -246,14 +296,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 if (!ok) break;
                 const int qrow = f.q_row0 + m * kBM;
                 if (lane == 0) {
-                    // [sig0 sig1]: this CTA's 64 queries, columns 0-63 / 64-127 (B of S^T);
-                    // [tau0 tau1]: queries 0-63 / 64-127, this CTA's 64 columns (B of dK)
                     const uint32_t full = lbar(Lay::kQFull + st), dst = base + Lay::kQOff + st * Lay::kStageBytes;
                     if (leader_cta) mbar_expect_tx(bar(Lay::kQFull + st), 2u * Lay::kStageBytes);
-                    tma_load_3d_pair(dst, &tmQ64, full, 0, hq, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + kQuad, &tmQ64, full, 64, hq, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + 2 * kQuad, &tmQ64, full, 64 * (int)rank, hq, qrow);
-                    tma_load_3d_pair(dst + 3 * kQuad, &tmQ64, full, 64 * (int)rank, hq, qrow + 64);
+                    load_stage(dst, &tmQ64, &tmQ32, full, hq, qrow);
                 }
                 // row statistics of the query block, negated: -lse (log2 units), -D
                 float* nlse2 = stats + st * 256;
@@ -278,10 +323,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 if (lane == 0) {
                     const uint32_t full = lbar(Lay::kDOFull), dst = base + Lay::kDOOff;
                     if (leader_cta) mbar_expect_tx(bar(Lay::kDOFull), 2u * Lay::kStageBytes);
-                    tma_load_3d_pair(dst, &tmDO64, full, 0, hq, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + kQuad, &tmDO64, full, 64, hq, qrow + 64 * (int)rank);
-                    tma_load_3d_pair(dst + 2 * kQuad, &tmDO64, full, 64 * (int)rank, hq, qrow);
-                    tma_load_3d_pair(dst + 3 * kQuad, &tmDO64, full, 64 * (int)rank, hq, qrow + 64);
+                    load_stage(dst, &tmDO64, &tmDO32, full, hq, qrow);
                 }
                 __syncwarp();
                 ++qc;
@@ -306,12 +348,16 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
             constexpr uint32_t kIdDQ = idesc_bf16_f32(kBM, HD, true, true);         // dQ: 128 x d
             const SmemDesc k_km = sdesc_sw128_split(base + Lay::kKOff, 16, 1024);
             const SmemDesc v_km = sdesc_sw128_split(base + Lay::kVOff, 16, 1024);
-            const SmemDesc kx_mn = sdesc_sw128_split(base + Lay::kKXOff, kBox, 1024);
+            // MN-major column halves: 64-byte swizzle at d = 64, 128-byte at d = 128
+            auto mn_half = [&](uint32_t off) {
+                return kNarrow ? sdesc_sw64_split(base + off, 16384, 512) : sdesc_sw128_split(base + off, kBox, 1024);
+            };
+            const SmemDesc kx_mn = mn_half(Lay::kKXOff);
             const SmemDesc ds_mn = sdesc_sw128_split(base + Lay::kDSOff, kBox, 1024);
             const SmemDesc q_km0 = sdesc_sw128_split(base + Lay::kQOff, 16, 1024);
-            const SmemDesc q_mn0 = sdesc_sw128_split(base + Lay::kQOff + 2 * kQuad, kBox, 1024);
+            const SmemDesc q_mn0 = mn_half(Lay::kQOff + Lay::kSigBytes);
             const SmemDesc do_km = sdesc_sw128_split(base + Lay::kDOOff, 16, 1024);
-            const SmemDesc do_mn = sdesc_sw128_split(base + Lay::kDOOff + 2 * kQuad, kBox, 1024);
+            const SmemDesc do_mn = mn_half(Lay::kDOOff + Lay::kSigBytes);
             auto at_stage = [&](SmemDesc d, uint32_t stage) {
                 d.lo += stage * desc_step(Lay::kStageBytes);
                 return d;
@@ -363,7 +409,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
 #pragma unroll
                         for (int kk = 0; kk < kBM / 16; ++kk)
                             mma_pair_ts(tmem + Lay::kTDV, tmem + Lay::kTS + packed_col(kk), do_mn,
-                                        desc_step(kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
+                                        desc_step(kk * Lay::kMnStep16), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
                         tc_commit_pair(bar(Lay::kDOEmpty), 3);
                     }
                     __syncwarp();
@@ -387,12 +433,12 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
 #pragma unroll
                         for (int kk = 0; kk < kBM / 16; ++kk)
                             mma_pair_ts(tmem + Lay::kTDK, tmem + Lay::kTDP + packed_col(kk), q_mn,
-                                        desc_step(kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
+                                        desc_step(kk * Lay::kMnStep16), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
                         // dQ over the pair's 256 keys: key rows 0-127 are the even CTA's block
 #pragma unroll
                         for (int kk = 0; kk < 2 * kBN / 16; ++kk)
-                            mma_pair_ss(tmem + Lay::kTDP, ds_mn, desc_step(kk * 2048), kx_mn, desc_step(kk * 2048),
-                                        kIdDQ, kk > 0 ? 1u : 0u);
+                            mma_pair_ss(tmem + Lay::kTDP, ds_mn, desc_step(kk * 2048), kx_mn,
+                                        desc_step(kk * Lay::kMnStep16), kIdDQ, kk > 0 ? 1u : 0u);
                         tc_commit_pair(bar(Lay::kDQFull), 3);
                         tc_commit_pair(bar(Lay::kDSEmpty), 3);
                         if (!more) {
@@ -559,17 +605,17 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
         }
     } else {
         // ------------------------------------------------------------ dQ warpgroup (both CTAs)
-        // This CTA's 64 queries of the block x 128 columns, summed over the pair's
-        // 256 keys by the MMA: tensor-memory lanes 0-63 hold columns 0-63 of query
-        // rows 0-63 and lanes 64-127 columns 64-127 of the same rows. Staged through
-        // the Q stage the block's dK product has finished reading, as four 64-row x
-        // 32-column swizzled boxes; each warp adds its own 32 rows x 64 columns with
-        // TMA reduce-adds issued by its lane 0 (two 32-row boxes). Deterministic
+        // This CTA's 64 queries of the block x HD columns, summed over the pair's
+        // 256 keys by the MMA: tensor-memory lanes 0-63 hold columns 0 .. HD/2-1 of
+        // query rows 0-63 and lanes 64-127 columns HD/2 .. HD-1 of the same rows.
+        // Staged through the Q stage the block's dK product has finished reading, as
+        // HD/32 64-row x 32-column swizzled boxes; each warp adds its own 32 rows x
+        // HD/2 columns with TMA reduce-adds issued by its lane 0. Deterministic
         // mode: under the semaphore of this query-row half, pairs in a fixed order,
         // every warp's adds complete before the next pair's turn.
         const int q4 = warp - 12;
         const int qr = (q4 & 1) * 32 + lane;      // query row inside this CTA's 64
-        const int half = q4 >> 1;                 // columns [64 half, 64 half + 64)
+        const int half = q4 >> 1;                 // columns [HD/2 half, HD/2 half + HD/2)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         setmaxnreg_inc<kRegsDq>();
         const bool leader = warp == 12 && lane == 0;
@@ -600,9 +646,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                     ok = ok && !*abort_flag;
                     if (!ok) break;
                 }
-                uint32_t row[64];
+                uint32_t row[HD / 2];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < HD / 64; ++c) {
                     tmem_ld32(tmem + lane_off + Lay::kTDP + c * 32, rr);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) row[c * 32 + i] = rr[i];
@@ -613,8 +659,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 uint8_t* stage = smem + Lay::kQOff + st * Lay::kStageBytes;
                 const uint32_t stage_s = base + Lay::kQOff + st * Lay::kStageBytes;
 #pragma unroll
-                for (int bx = 0; bx < 2; ++bx) {   // boxes 2 half, 2 half + 1: 32 columns each
-                    uint8_t* srow = stage + (2 * half + bx) * kQuad + (qr >> 3) * 1024 + (qr & 7) * 128;
+                for (int bx = 0; bx < HD / 64; ++bx) {   // this half's boxes: 32 columns each
+                    uint8_t* srow = stage + ((HD / 64) * half + bx) * kQuad + (qr >> 3) * 1024 + (qr & 7) * 128;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         *reinterpret_cast<uint4*>(srow + ((j ^ (qr & 7)) << 4)) =
@@ -625,9 +671,11 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
                 __syncwarp();
                 if (lane == 0) {
                     // this warp's 32 rows (rows past the sequence carry exact zeros: P = 0 there)
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_reduce_add_3d(&tmDQ32, stage_s + (2 * half + bx) * kQuad + (q4 & 1) * 4096,
-                                          (2 * half + bx) * 32, hq, f.q_row0 + m * kBM + 64 * (int)rank + (q4 & 1) * 32);
+                    for (int bx = 0; bx < HD / 64; ++bx) {
+                        const int box = (HD / 64) * half + bx;
+                        tma_reduce_add_3d(&tmDQ32, stage_s + box * kQuad + (q4 & 1) * 4096, box * 32, hq,
+                                          f.q_row0 + m * kBM + 64 * (int)rank + (q4 & 1) * 32);
+                    }
                     bulk_commit_group();
                     if constexpr (kDet) {
                         bulk_wait_group0();
@@ -663,16 +711,19 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant
 
 bool bwd_pair_supported(const BwdParams& p) {
     const Geometry& g = p.g;
-    return g.d == HD && p.d_v == HD && g.win_left < 0 && (g.win_right < 0 || g.win_right == 0) &&
+    return (g.d == 64 || g.d == 128) && p.d_v == g.d && g.win_left < 0 && (g.win_right < 0 || g.win_right == 0) &&
            p.mask.ptr == nullptr;
 }
 
 int bwd_pair_tiles_per_head(int Lk) { return (Lk + 2 * kBN - 1) / (2 * kBN); }
 
-cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo64, const CUtensorMap& tdq32, const BwdParams& p,
-                            const void* varlen_map, int num_sms, cudaStream_t stream) {
-    auto kern = p.deterministic ? bwd_pair_kernel<true> : bwd_pair_kernel<false>;
+namespace {
+
+template <int HD>
+cudaError_t launch_pair_hd(const PairMaps& pm, const CUtensorMap& tk, const CUtensorMap& tv, const BwdParams& p,
+                           const void* varlen_map, int num_sms, cudaStream_t stream) {
+    using Lay = PairLay<HD>;
+    auto kern = p.deterministic ? bwd_pair_kernel<HD, true> : bwd_pair_kernel<HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
@@ -701,8 +752,19 @@ cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, cons
     const int clusters = varlen ? max_clusters : min(p.n_tiles, max_clusters);
     if (clusters <= 0) return cudaSuccess;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, kern, tq64, tk, tv, tdo64, tdq32, p,
+    return cudaLaunchKernelEx(&cfg, kern, pm.q64, tk, tv, pm.do64, pm.dq32, pm.q32, pm.do32, pm.k32, p,
                               static_cast<const VarlenMap*>(varlen_map));
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pair(const PairMaps& pm, const CUtensorMap& tk, const CUtensorMap& tv, const BwdParams& p,
+                            const void* varlen_map, int num_sms, cudaStream_t stream) {
+    switch (p.g.d) {
+        case 64: return launch_pair_hd<64>(pm, tk, tv, p, varlen_map, num_sms, stream);
+        case 128: return launch_pair_hd<128>(pm, tk, tv, p, varlen_map, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace attn

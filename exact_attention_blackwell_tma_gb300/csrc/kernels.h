@@ -121,11 +121,14 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // work tile (nm counts 128-row blocks).
 cudaError_t launch_fwd_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_sms, cudaStream_t stream);
-// Tensor maps with boxes of fewer rows: q and dO in 64-row x 64-column bf16
-// boxes (the CTA-pair backward), and the dQ accumulator in 32-row x 32-column
-// fp32 boxes (each dQ warp adds its own 32 rows, dq_reduce.cuh).
+// Tensor maps with boxes of fewer rows or columns: q and dO in 64-row x
+// 64-column bf16 boxes (the CTA-pair backward), and the dQ accumulator in 32-row
+// x 32-column fp32 boxes (each dQ warp adds its own 32 rows, dq_reduce.cuh).
+// q32, do32, k32: 128-row x 32-column bf16 boxes with the 64-byte swizzle, the
+// pair backward's column halves at head dim 64 (encoded for that case only).
 struct PairMaps {
     CUtensorMap q64, do64, dq32;
+    CUtensorMap q32, do32, k32;
 };
 // pair: run the main kernel on CTA pairs when bwd_pair_supported(p) holds.
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -133,14 +136,13 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const BwdParams& p, int num_sms, cudaStream_t stream);
 
 // The backward's main kernel on CTA pairs (2-CTA tensor cores, bwd_pair.cu):
-// head dim 128 (q, k, v), grouped heads (a tile walks the query heads of its
-// key/value head's group), no window beyond the causal mask, no block mask;
-// dense or packed, deterministic or not.
+// head dim 64 or 128 (q, k, v alike), grouped heads (a tile walks the query
+// heads of its key/value head's group), no window beyond the causal mask, no
+// block mask; dense or packed, deterministic or not.
 bool bwd_pair_supported(const BwdParams& p);
 // key-block pairs per (batch, head) of Lk keys
 int bwd_pair_tiles_per_head(int Lk);
-cudaError_t launch_bwd_pair(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo64, const CUtensorMap& tdq32, const BwdParams& p,
+cudaError_t launch_bwd_pair(const PairMaps& pm, const CUtensorMap& tk, const CUtensorMap& tv, const BwdParams& p,
                             const void* varlen_map, int num_sms, cudaStream_t stream);
 
 // Main kernel of the backward for head dims 192 and 256 (preprocess and dQ

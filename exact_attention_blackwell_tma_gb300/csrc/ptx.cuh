@@ -261,6 +261,18 @@ __host__ __device__ __forceinline__ SmemDesc sdesc_sw128_split(uint32_t saddr, u
     d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
     return d;
 }
+// The same for a 64-byte-swizzled MN-major operand (the CTA-pair backward's
+// 32-column halves at head dim 64): rows of 32 bf16 (64 B) along M/N, 8 rows
+// along K per 512-byte atom; lbo = distance between 32-element column groups,
+// sbo = distance between 8-row groups along K. The atom base must be 512-byte
+// aligned. This is the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_64B and a
+// 64-byte inner box writes.
+__host__ __device__ __forceinline__ SmemDesc sdesc_sw64_split(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    SmemDesc d;
+    d.lo = ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+    d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+    return d;
+}
 // Byte offset -> low-half increment.
 __host__ __device__ constexpr uint32_t desc_step(uint32_t bytes) { return bytes >> 4; }
 

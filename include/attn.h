@@ -290,8 +290,8 @@ int attn_set_exp2_emulation(int d, int every);
  * products run with M = 256 and each CTA stages half of operand B, and dQ is
  * summed over the pair's 256 keys by the MMA itself, so each CTA adds a
  * 64-row dQ tile per query block (half the global reduce-adds of single
- * CTAs). It applies where supported: head dim 128 for q, k and v, grouped
- * heads or not, no window beyond the causal mask, no block mask (dense or
+ * CTAs). It applies where supported: head dim 64 or 128, the same for q, k
+ * and v, grouped heads or not, no window beyond the causal mask, no block mask (dense or
  * packed, deterministic or not); other problems run on single CTAs.
  * Results agree with the single-CTA kernels to rounding (the order of the fp32
  * sums differs); the deterministic mode stays bit-identical run to run. The

@@ -4,10 +4,12 @@ the fp64 oracle.
 FlashAttention-4 paper, Section 3.2.3: the two CTAs of a cluster run the
 backward's MMAs together with M = 256 (each stages half of operand B), and the
 pair sums dQ over its 256 keys before one reduce-add pass. The kernel covers
-head dim 128, grouped heads (a work tile walks every query head of its
+grouped heads (a work tile walks every query head of its
 key/value head's group), no mask beyond the causal one and no block mask,
-dense or packed, in both modes; attn_set_backward_cta_pairs switches it on. These tests switch it on and compare every element with the
-oracle (ragged lengths that leave the pair's second key block partly or wholly
+dense or packed, in both modes, head dims 64 and 128 (at 64 the column halves
+of operand B are 32 columns with the 64-byte swizzle);
+attn_set_backward_cta_pairs switches it on. These tests switch it on and
+compare every element with the oracle (ragged lengths that leave the pair's second key block partly or wholly
 past the keys, Lq != Lk, packed batches with one or two offset arrays), check
 that the deterministic mode repeats bit for bit, that problems the pair kernel
 does not cover still come out right with the switch on, and the workload
@@ -52,47 +54,52 @@ def _check(t, causal, scale, what, deterministic=False, cu=None, cuk=None):
     assert_grad_close(to64(dv), rv, f"{what} dV")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("L", [1, 77, 128, 129, 256, 300, 513, 1000])
-def test_pair_ragged_full(L, causal, deterministic):
-    t = inputs.small(B=2, H=2, L=L, d=128, seed=41)
-    _check(t, causal, 0.088, f"pair L={L} causal={causal} det={deterministic}", deterministic)
+def test_pair_ragged_full(L, causal, deterministic, d):
+    t = inputs.small(B=2, H=2, L=L, d=d, seed=41)
+    _check(t, causal, 0.088, f"pair d={d} L={L} causal={causal} det={deterministic}", deterministic)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Lq,Lk", [(200, 77), (77, 300), (384, 129), (129, 640), (640, 256)])
-def test_pair_rectangular(Lq, Lk, causal):
-    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=128, seed=42)
-    _check(t, causal, 0.088, f"pair Lq={Lq} Lk={Lk} causal={causal}")
+def test_pair_rectangular(Lq, Lk, causal, d):
+    t = inputs.small(B=1, H=2, L=Lq, Lk=Lk, d=d, seed=42)
+    _check(t, causal, 0.088, f"pair d={d} Lq={Lq} Lk={Lk} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
-def test_pair_varlen(causal, deterministic):
+def test_pair_varlen(causal, deterministic, d):
     lens = [1, 128, 200, 513, 77, 256, 384, 0, 129]
     cu = inputs.cu_seqlens(lens)
     g = torch.Generator("cpu").manual_seed(43)
     T = int(cu[-1])
-    t = {n: torch.randn(T, 3, 128, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
-    _check(t, causal, 0.09, f"pair varlen causal={causal} det={deterministic}", deterministic, cu=cu)
+    t = {n: torch.randn(T, 3, d, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
+    _check(t, causal, 0.09, f"pair d={d} varlen causal={causal} det={deterministic}", deterministic, cu=cu)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_pair_varlen_separate_key_offsets(causal):
+def test_pair_varlen_separate_key_offsets(causal, d):
     lq, lk = [1, 128, 200, 513, 0, 300], [300, 1, 200, 129, 77, 256]
     cu, cuk = inputs.cu_seqlens(lq), inputs.cu_seqlens(lk)
     g = torch.Generator("cpu").manual_seed(44)
-    t = {"q": torch.randn(int(cu[-1]), 2, 128, generator=g).to(torch.bfloat16),
-         "k": torch.randn(int(cuk[-1]), 2, 128, generator=g).to(torch.bfloat16),
-         "v": torch.randn(int(cuk[-1]), 2, 128, generator=g).to(torch.bfloat16),
-         "do": torch.randn(int(cu[-1]), 2, 128, generator=g).to(torch.bfloat16)}
-    _check(t, causal, 0.09, f"pair varlen q/k offsets causal={causal}", cu=cu, cuk=cuk)
+    t = {"q": torch.randn(int(cu[-1]), 2, d, generator=g).to(torch.bfloat16),
+         "k": torch.randn(int(cuk[-1]), 2, d, generator=g).to(torch.bfloat16),
+         "v": torch.randn(int(cuk[-1]), 2, d, generator=g).to(torch.bfloat16),
+         "do": torch.randn(int(cu[-1]), 2, d, generator=g).to(torch.bfloat16)}
+    _check(t, causal, 0.09, f"pair d={d} varlen q/k offsets causal={causal}", cu=cu, cuk=cuk)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_pair_deterministic_is_bit_identical(causal):
-    t = inputs.small(B=2, H=4, L=1500, d=128, seed=45)
+def test_pair_deterministic_is_bit_identical(causal, d):
+    t = inputs.small(B=2, H=4, L=1500, d=d, seed=45)
     ref = _grads(t, causal, 0.088, deterministic=True)
     for _ in range(3):
         again = _grads(t, causal, 0.088, deterministic=True)
@@ -100,10 +107,11 @@ def test_pair_deterministic_is_bit_identical(causal):
             assert torch.equal(a, b)
 
 
-def test_pair_agrees_with_single_ctas():
+@pytest.mark.parametrize("d", [64, 128])
+def test_pair_agrees_with_single_ctas(d):
     """The same problem on CTA pairs and on single CTAs: dQ sums in another
     order, so the two agree to rounding, both within tolerance of each other."""
-    t = inputs.small(B=2, H=3, L=900, d=128, seed=46)
+    t = inputs.small(B=2, H=3, L=900, d=d, seed=46)
     pair = _grads(t, True, 0.088)
     binding.attn_set_backward_cta_pairs(0)
     single = _grads(t, True, 0.088)
@@ -114,29 +122,31 @@ def test_pair_agrees_with_single_ctas():
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 1), (8, 2)])
-@pytest.mark.parametrize("L", [77, 300, 513])
-def test_pair_grouped_heads(L, H, Hkv, causal, deterministic):
+@pytest.mark.parametrize("L,d", [(77, 128), (300, 128), (513, 128), (77, 64), (513, 64)])
+def test_pair_grouped_heads(L, d, H, Hkv, causal, deterministic):
     """Grouped heads on CTA pairs: a tile's key blocks see every query head of
     the group, and dK/dV sum over them in the tile."""
-    t = inputs.small(B=2, H=H, L=L, d=128, seed=48, Hkv=Hkv)
-    _check(t, causal, 0.088, f"pair gqa L={L} H={H}/{Hkv} causal={causal} det={deterministic}", deterministic)
+    t = inputs.small(B=2, H=H, L=L, d=d, seed=48, Hkv=Hkv)
+    _check(t, causal, 0.088, f"pair gqa d={d} L={L} H={H}/{Hkv} causal={causal} det={deterministic}", deterministic)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("deterministic", [False, True])
-def test_pair_grouped_heads_varlen(deterministic):
+def test_pair_grouped_heads_varlen(deterministic, d):
     lens = [1, 128, 200, 513, 77, 256, 0, 129]
     cu = inputs.cu_seqlens(lens)
     g = torch.Generator("cpu").manual_seed(49)
     T = int(cu[-1])
-    t = {"q": torch.randn(T, 6, 128, generator=g).to(torch.bfloat16),
-         "k": torch.randn(T, 2, 128, generator=g).to(torch.bfloat16),
-         "v": torch.randn(T, 2, 128, generator=g).to(torch.bfloat16),
-         "do": torch.randn(T, 6, 128, generator=g).to(torch.bfloat16)}
-    _check(t, True, 0.09, f"pair gqa varlen det={deterministic}", deterministic, cu=cu)
+    t = {"q": torch.randn(T, 6, d, generator=g).to(torch.bfloat16),
+         "k": torch.randn(T, 2, d, generator=g).to(torch.bfloat16),
+         "v": torch.randn(T, 2, d, generator=g).to(torch.bfloat16),
+         "do": torch.randn(T, 6, d, generator=g).to(torch.bfloat16)}
+    _check(t, True, 0.09, f"pair gqa d={d} varlen det={deterministic}", deterministic, cu=cu)
 
 
-def test_pair_grouped_deterministic_is_bit_identical():
-    t = inputs.small(B=1, H=8, L=1200, d=128, seed=50, Hkv=2)
+@pytest.mark.parametrize("d", [64, 128])
+def test_pair_grouped_deterministic_is_bit_identical(d):
+    t = inputs.small(B=1, H=8, L=1200, d=d, seed=50, Hkv=2)
     ref = _grads(t, True, 0.088, deterministic=True)
     for _ in range(3):
         again = _grads(t, True, 0.088, deterministic=True)
@@ -144,14 +154,14 @@ def test_pair_grouped_deterministic_is_bit_identical():
             assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("what", ["window", "blockmask", "d64", "d192"])
+@pytest.mark.parametrize("what", ["window", "blockmask", "d64window", "d192"])
 def test_pair_switch_leaves_other_problems_correct(what):
     """With the switch on, problems outside the pair kernel run on single CTAs."""
     import oracle
-    d = {"d64": 64, "d192": 192}.get(what, 128)
+    d = {"d64window": 64, "d192": 192}.get(what, 128)
     t = inputs.small(B=1, H=2, L=300, d=d, seed=47)
     kw, okw = {}, {}
-    if what == "window":
+    if what in ("window", "d64window"):
         kw, okw = {"window": (100, -1)}, {"window_left": 100, "window_right": -1}
     if what == "blockmask":
         m = np.ones((1, 3, 3), np.uint8)
@@ -211,3 +221,22 @@ def test_pair_workload_grouped(deterministic):
     _, rk, rv = oracle.bwd(full["q"], full["k"], full["v"], full["do"], w.scale, True, qrows=[], krows=krows)
     assert_grad_close(to64(dk[bsel][:, krows][:, :, [kh]]), rk[:, krows], f"pair grouped workload det={deterministic} dK")
     assert_grad_close(to64(dv[bsel][:, krows][:, :, [kh]]), rv[:, krows], f"pair grouped workload det={deterministic} dV")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_pair_workload_d64(deterministic):
+    """B2 H16 L8192 d64, causal, spiky K, on CTA pairs (64-byte-swizzled column
+    halves): sampled dQ rows and dK/dV rows over the whole sequence against the
+    oracle on one head of each batch entry."""
+    w = inputs.HDSWEEP.with_(d=64)
+    t = inputs.make(w)
+    dq, dk, dv = _grads(t, True, w.scale, deterministic)
+    head = [9]
+    qrows, krows = _rows(w.L, 12, 7), _rows(w.L, 12, 8)
+    what = f"pair {w.name} det={deterministic}"
+    for b in range(w.B):
+        sub = {n: t[n][[b]] for n in ("q", "k", "v", "do")}
+        rq, rk, rv = oracle_bwd_subset(sub, w.scale, True, heads=head, qrows=qrows, krows=krows)
+        assert_grad_close(to64(dq[[b]][:, qrows][:, :, head]), rq[:, qrows], f"{what} b={b} dQ")
+        assert_grad_close(to64(dk[[b]][:, krows][:, :, head]), rk[:, krows], f"{what} b={b} dK")
+        assert_grad_close(to64(dv[[b]][:, krows][:, :, head]), rv[:, krows], f"{what} b={b} dV")
