@@ -374,6 +374,11 @@ def barrier(dist):
 def time_single(prob, call, steps, warmup):
     """Mean CUDA-event time (ms) of one call, on the stream it is launched on,
     over `steps` back-to-back runs after `warmup` untimed ones."""
+    return time_single_stats(prob, call, steps, warmup)[0]
+
+
+def time_single_stats(prob, call, steps, warmup):
+    """(mean, median) CUDA-event time (ms) of one call, as time_single."""
     for _ in range(max(warmup, 3)):
         call(prob)
     binding.check_status()
@@ -385,7 +390,8 @@ def time_single(prob, call, steps, warmup):
         b.record()
     torch.cuda.synchronize()
     binding.check_status()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ts = [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(ts), statistics.median(ts)
 
 
 def single_call_records(args, pk, dev, main_prob):
@@ -395,10 +401,11 @@ def single_call_records(args, pk, dev, main_prob):
     out = {}
     w, _ = WORKLOADS[TARGET_WORKLOAD]
     prob = main_prob if args.workload == TARGET_WORKLOAD else Problem(w, dev)
-    t_ms = time_single(prob, lambda p_: p_.fwd(True), args.steps, args.warmup)
+    t_ms, t_med = time_single_stats(prob, lambda p_: p_.fwd(True), args.steps, args.warmup)
     fl = flops(w, True, "fwd")
     ach = fl / (t_ms * 1e-3) / 1e12
-    out["target"] = {"workload": TARGET_WORKLOAD, "call": "attn_fwd (causal)", "ms": t_ms, "achieved": ach,
+    out["target"] = {"workload": TARGET_WORKLOAD, "call": "attn_fwd (causal)", "ms": t_ms, "median_ms": t_med,
+                     "achieved": ach,
                      "unit": UNIT, "peak": pk["bf16"], "frac": ach / pk["bf16"], "goal_frac": TARGET_FRAC,
                      "met": ach / pk["bf16"] >= TARGET_FRAC,
                      "l2": "inputs 192 MiB > 129 MiB L2; no flush between calls"}
@@ -409,11 +416,11 @@ def single_call_records(args, pk, dev, main_prob):
     prob = main_prob if args.workload == "b1h32l32768d128" else None
     if prob is not None:
         prob.fwd(True)
-        t_ms = time_single(prob, lambda p_: p_.bwd(True, deterministic=1), args.steps, args.warmup)
+        t_ms, t_med = time_single_stats(prob, lambda p_: p_.bwd(True, deterministic=1), args.steps, args.warmup)
         fl = flops(wl, True, "bwd")
         ach = fl / (t_ms * 1e-3) / 1e12
         out["deterministic"] = {"workload": "b1h32l32768d128", "call": "attn_bwd (causal, deterministic)",
-                                "ms": t_ms, "achieved": ach, "unit": UNIT, "peak": pk["bf16"],
+                                "ms": t_ms, "median_ms": t_med, "achieved": ach, "unit": UNIT, "peak": pk["bf16"],
                                 "frac": ach / pk["bf16"]}
     return out
 
@@ -551,15 +558,18 @@ def run_ours(args, world, rank, local, dist):
     value = world * step_flops / (ms * 1e-3) / 1e12
 
     # per-kernel-call durations -> rooflines
-    per_call = {}
+    per_call, per_call_median = {}, {}
     for key in evs[0]:
-        per_call[key] = statistics.mean(e[key][0].elapsed_time(e[key][1]) for e in evs)
+        ts = [e[key][0].elapsed_time(e[key][1]) for e in evs]
+        per_call[key] = statistics.mean(ts)
+        per_call_median[key] = statistics.median(ts)
     rooflines = []
     for (kind, c), t_ms in per_call.items():
         fl = flops(w, c, kind)
         ach = fl / (t_ms * 1e-3) / 1e12
         rooflines.append({"kernel": f"attn_{kind}", "variant": "causal" if c else "non-causal",
-                          "ms": t_ms, "achieved": ach, "bound": "tensor", "unit": "TFLOP/s",
+                          "ms": t_ms, "median_ms": per_call_median[(kind, c)], "achieved": ach,
+                          "bound": "tensor", "unit": "TFLOP/s",
                           "peak": pk["bf16"], "frac": ach / pk["bf16"], "traffic": None})
     for r in rooflines:
         r["traffic"] = ncu_traffic(w.name, r["kernel"][5:], r["variant"] == "causal")
